@@ -1,0 +1,443 @@
+"""Pins of the CPU oracle against things other than itself: library conversions, error bounds,
+brute force on tiny inputs, invariants, textbook special cases and values printed on the pages.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _ulp32(x):
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(x, np.finfo(np.float32).tiny)))
+    return np.exp2(e - 23)
+
+
+# ------------------------------------------------------------------------------------------
+# Number formats
+# ------------------------------------------------------------------------------------------
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal(200000).astype(np.float32) * np.float32(3.0)
+    # exact ties: bf16 value plus half an ulp, both parities
+    base = torch.from_numpy(v[:1000]).to(torch.bfloat16).float().numpy()
+    ties = (base.view(np.uint32) + np.uint32(0x8000)).view(np.float32)
+    v = np.concatenate([v, ties, np.float32([0.0, -0.0, 1e-40, -1e-40, 3.4e38])])
+    ours = oracle.f32_to_bf16(v)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_decode_matches_torch_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_to_f32(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert nan.sum() == 2 and ours[0x7e] == 448.0 and ours[0x01] == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    rng = np.random.default_rng(2)
+    v = np.concatenate([
+        rng.uniform(-448, 448, 100000), rng.standard_normal(100000) * 0.01,
+        rng.standard_normal(50000) * 1e-3]).astype(np.float32)
+    # midpoints between neighbouring finite codes exercise ties-to-even
+    vals = np.sort(oracle.e4m3_to_f32(np.arange(0, 0x7f, dtype=np.uint8)))
+    mids = ((vals[1:].astype(np.float64) + vals[:-1]) / 2).astype(np.float32)
+    v = np.concatenate([v, mids, -mids, np.float32([0.0, -0.0, 448.0, -448.0])])
+    ours = oracle.f32_to_e4m3(v)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_saturates_and_round_trips():
+    big = np.float32([449.0, 464.0, 1e6, -500.0, np.inf, -np.inf])
+    q = oracle.f32_to_e4m3(big)
+    assert list(q) == [0x7e, 0x7e, 0x7e, 0xfe, 0x7e, 0xfe]
+    finite = np.array([c for c in range(256) if (c & 0x7f) != 0x7f], dtype=np.uint8)
+    assert np.array_equal(oracle.f32_to_e4m3(oracle.e4m3_to_f32(finite)), finite)
+
+
+def test_exp_within_two_ulp_of_fp64():
+    z = np.linspace(-87.0, 87.0, 400001, dtype=np.float64).astype(np.float32)
+    ours = oracle.exp(z).astype(np.float64)
+    ref = np.exp(z.astype(np.float64))
+    err = np.abs(ours - ref) / _ulp32(ref)
+    assert err.max() <= 2.0, err.max()
+    assert oracle.exp(np.float32([0.0]))[0] == 1.0
+
+
+def test_sigmoid_within_three_ulp_of_fp64():
+    z = np.linspace(-30.0, 30.0, 200001).astype(np.float32)
+    ours = oracle.sigmoid(z).astype(np.float64)
+    ref = 1.0 / (1.0 + np.exp(-z.astype(np.float64)))
+    err = np.abs(ours - ref) / _ulp32(ref)
+    assert err.max() <= 3.0, err.max()
+    assert oracle.sigmoid(np.float32([0.0]))[0] == 0.5
+
+
+# ------------------------------------------------------------------------------------------
+# Router: logits, selection, weights
+# ------------------------------------------------------------------------------------------
+def test_logit_within_fp32_dot_error_bound():
+    cfg = synth.CONFIGS["dsv3_decode"]
+    x = synth.bf16_bits(synth.normal_bf16(11, synth.TAG_X, (4, cfg.d), 1.0))
+    w = synth.normal_f32(11, synth.TAG_WGATE, (8, cfg.d), 0.02).numpy()
+    u = 2.0 ** -24
+    gamma = cfg.d * u / (1 - cfg.d * u)
+    xf = oracle.bf16_to_f32(x).astype(np.float64)
+    for t in range(4):
+        for e in range(8):
+            z = oracle.logit(x[t], w[e])
+            ref = float(xf[t] @ w[e].astype(np.float64))
+            assert abs(z - ref) <= gamma * float(np.abs(xf[t] * w[e]).sum()) + 1e-30
+
+
+def test_logit_picks_the_right_operands():
+    d = 256
+    w = np.arange(d, dtype=np.float32) * np.float32(0.5) + np.float32(1.0)
+    for j in (0, 15, 16, 100, 255):       # one-hot x selects one weight exactly
+        x = np.zeros(d, dtype=np.float32)
+        x[j] = 1.0
+        assert oracle.logit(oracle.f32_to_bf16(x), w) == w[j]
+    ones = oracle.f32_to_bf16(np.ones(d, dtype=np.float32))
+    assert oracle.logit(ones, np.full(d, 0.25, dtype=np.float32)) == 64.0
+
+
+def _brute_force_route(s, bias, k, n_group, topk_group, scale):
+    """Selection by enumeration: the kept groups and chosen experts are the unique subsets
+    whose every member ranks before every non-member ((key desc, index asc) order)."""
+    E = s.size
+    gs = E // n_group
+    v = (s + bias).astype(np.float32)
+
+    def before(a, ia, b, ib):
+        return a > b or (a == b and ia < ib)
+
+    gscore = []
+    for g in range(n_group):
+        vals = sorted(v[g * gs:(g + 1) * gs].tolist(), reverse=True)
+        gscore.append(np.float32(vals[0]) + np.float32(vals[1]) if gs > 1 else np.float32(vals[0]))
+    kept = [S for S in itertools.combinations(range(n_group), topk_group)
+            if all(before(gscore[a], a, gscore[b], b)
+                   for a in S for b in range(n_group) if b not in S)]
+    assert len(kept) == 1
+    elig = [e for e in range(E) if e // gs in kept[0]]
+    chosen = [S for S in itertools.combinations(elig, k)
+              if all(before(v[a], a, v[b], b) for a in S for b in elig if b not in S)]
+    assert len(chosen) == 1
+    order = sorted(chosen[0], key=lambda e: (-float(v[e]), e))
+    tot = np.float32(0.0)
+    for e in order:
+        tot = np.float32(tot + s[e])
+    w = [np.float32(np.float32(s[e] / tot) * np.float32(scale)) for e in order]
+    return order, w
+
+
+@pytest.mark.parametrize("E,k,n_group,topk_group", [(8, 3, 4, 2), (16, 4, 4, 2), (12, 2, 3, 1),
+                                                    (16, 5, 8, 3), (10, 3, 1, 1)])
+def test_route_matches_brute_force(E, k, n_group, topk_group):
+    d = 64
+    for seed in range(6):
+        x = synth.bf16_bits(synth.normal_bf16(seed, synth.TAG_X, (5, d), 1.0))
+        wg = synth.normal_f32(seed, synth.TAG_WGATE, (E, d), 0.1).numpy()
+        b = synth.uniform_sym_f32(seed, synth.TAG_BIAS, E, 0.3).numpy()
+        if seed == 5:   # force exact ties: duplicate gate rows and bias
+            wg[E - 1] = wg[0]
+            b[E - 1] = b[0]
+            wg[1] = wg[2]
+            b[1] = b[2]
+        idx, w, z, s = oracle.route(x, wg, b, k, n_group, topk_group, 2.5, want_scores=True)
+        for t in range(5):
+            order, ww = _brute_force_route(s[t], b, k, n_group, topk_group, 2.5)
+            assert list(idx[t]) == order
+            assert np.array_equal(w[t], np.array(ww, dtype=np.float32))
+
+
+def test_route_single_group_is_plain_topk_and_weights_sum_to_scale():
+    cfg = synth.CONFIGS["tiny"]
+    inp = synth.make_router_inputs(cfg)
+    x = synth.bf16_bits(inp["x"])
+    idx, w, z, s = oracle.route(x, inp["w_gate"].numpy(), inp["bias"].numpy(), cfg.k, 1, 1,
+                                cfg.route_scale, want_scores=True)
+    v = s + inp["bias"].numpy()
+    for t in range(cfg.T):
+        ref = np.lexsort((np.arange(cfg.E), -v[t]))[:cfg.k]   # independent sort
+        assert list(idx[t]) == list(ref)
+    assert np.allclose(w.sum(1), cfg.route_scale, rtol=1e-6, atol=0)
+    # the bias steers selection: a large bias forces an expert in for every token
+    b2 = inp["bias"].numpy().copy()
+    b2[5] = 10.0
+    idx2, _ = oracle.route(x, inp["w_gate"].numpy(), b2, cfg.k, 1, 1, 1.0)
+    assert (idx2[:, 0] == 5).all()
+
+
+def test_route_weights_use_raw_scores_not_bias():
+    d, E = 32, 8
+    x = synth.bf16_bits(synth.normal_bf16(3, synth.TAG_X, (3, d), 1.0))
+    wg = synth.normal_f32(3, synth.TAG_WGATE, (E, d), 0.1).numpy()
+    b0 = np.zeros(E, dtype=np.float32)
+    b1 = np.full(E, 0.05, dtype=np.float32)      # uniform shift: same selection, same weights
+    i0, w0 = oracle.route(x, wg, b0, 2, 1, 1, 1.0)
+    i1, w1 = oracle.route(x, wg, b1, 2, 1, 1, 1.0)
+    assert np.array_equal(i0, i1) and np.array_equal(w0, w1)
+
+
+def test_route_rejects_bad_shapes():
+    with pytest.raises(ValueError):
+        oracle.route(np.zeros((1, 24), np.uint16), np.zeros((8, 24), np.float32),
+                     np.zeros(8, np.float32), 2, 1, 1, 1.0)      # d % 16 != 0
+    with pytest.raises(ValueError):
+        oracle.route(np.zeros((1, 32), np.uint16), np.zeros((8, 32), np.float32),
+                     np.zeros(8, np.float32), 5, 4, 2, 1.0)      # k > topk_group * E/n_group
+
+
+# ------------------------------------------------------------------------------------------
+# Dispatch
+# ------------------------------------------------------------------------------------------
+def _random_topk(T, E, k, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,E,k,R", [(16, 16, 2, 2), (24, 12, 3, 4), (64, 256, 8, 8), (8, 8, 8, 8),
+                                     (6, 4, 1, 1)])
+def test_dispatch_index_matches_sorted_enumeration(T, E, k, R):
+    ti = _random_topk(T, E, k, T * 7 + E)
+    counts, offsets, row_of, src_tok = oracle.dispatch_index(ti, E, R)
+    Ts, Er = T // R, E // R
+    cap = Ts * min(k, Er)
+    # enumeration: sort (dest rank, source rank, expert, token) and lay rows out segment by segment
+    entries = sorted(((int(e) // Er, t // Ts, int(e), t, i) for t in range(T)
+                      for i, e in enumerate(ti[t])))
+    fill = {}
+    for r, s, e, t, i in entries:
+        n = fill.get((r, s), 0)
+        assert row_of[t, i] == (r * R + s) * cap + n
+        fill[(r, s)] = n + 1
+    # invariants
+    assert counts.sum() == T * k
+    assert len(set(row_of.reshape(-1).tolist())) == T * k            # injective
+    for t in range(T):
+        for i in range(k):
+            assert src_tok[row_of[t, i]] == t
+    assert (src_tok >= 0).sum() == T * k
+    assert max(fill.values()) <= cap
+    # per-destination send counts equal a bincount of destination ranks per source
+    for s in range(R):
+        dst = (ti[s * Ts:(s + 1) * Ts].reshape(-1) // Er)
+        assert np.array_equal(counts[s].reshape(R, Er).sum(1), np.bincount(dst, minlength=R))
+    # offsets are exclusive sums inside each destination rank
+    for s in range(R):
+        for r in range(R):
+            c = counts[s, r * Er:(r + 1) * Er]
+            assert np.array_equal(offsets[s, r * Er:(r + 1) * Er], np.cumsum(c) - c)
+
+
+def test_dispatch_payload_bf16_and_fp8():
+    T, d, E, k, R = 16, 256, 16, 2, 2
+    x = synth.bf16_bits(synth.normal_bf16(5, synth.TAG_X, (T, d), 1.0))
+    ti = _random_topk(T, E, k, 9)
+    _, _, row_of, src_tok = oracle.dispatch_index(ti, E, R)
+    n_rows = src_tok.size
+    recv, _ = oracle.dispatch_payload(x, row_of, n_rows)
+    for r in range(n_rows):
+        if src_tok[r] >= 0:
+            assert np.array_equal(recv[r], x[src_tok[r]])
+    q, sc = oracle.dispatch_payload(x, row_of, n_rows, fp8=True)
+    xf = oracle.bf16_to_f32(x)
+    for t in range(T):
+        blk = xf[t].reshape(d // 128, 128)
+        scale = (np.abs(blk).max(1) / np.float32(448.0)).astype(np.float32)
+        ref = torch.from_numpy((blk / scale[:, None]).astype(np.float32)).to(
+            torch.float8_e4m3fn).view(torch.uint8).numpy().reshape(-1)
+        for i in range(k):
+            assert np.array_equal(q[row_of[t, i]], ref)
+            assert np.array_equal(sc[row_of[t, i]], scale)
+
+
+# ------------------------------------------------------------------------------------------
+# Experts and combine
+# ------------------------------------------------------------------------------------------
+def _torch_swiglu(x, w13, w2, F):
+    """Dense SwiGLU MLP in fp64 torch ops with the same bf16 rounding points."""
+    g = x @ w13[:F].T
+    u = x @ w13[F:].T
+    h = (torch.nn.functional.silu(g) * u).float().to(torch.bfloat16).double()
+    return (h @ w2.T).float().to(torch.bfloat16), h
+
+
+def test_swiglu_bf16_is_a_dense_mlp_when_one_expert():
+    d, F = 256, 128
+    x = synth.normal_bf16(7, synth.TAG_X, (6, d), 1.0)
+    w13 = synth.normal_bf16(7, synth.TAG_W13, (2 * F, d), 0.05)
+    w2 = synth.normal_bf16(7, synth.TAG_W2, (d, F), 0.05)
+    ref, href = _torch_swiglu(x.double(), w13.double(), w2.double(), F)
+    ref = synth.bf16_bits(ref)
+    mism = 0
+    for t in range(6):
+        out, h = oracle.swiglu_row_bf16(synth.bf16_bits(x[t]), synth.bf16_bits(w13), synth.bf16_bits(w2))
+        assert np.allclose(h, href[t].numpy(), rtol=2 ** -8, atol=0)
+        diff = np.abs(out.astype(np.int32) - ref[t].astype(np.int32))
+        assert diff.max() <= 1
+        mism += int((diff > 0).sum())
+    assert mism <= 3
+
+
+def test_swiglu_bf16_gate_and_up_are_not_swapped():
+    d, F = 128, 128
+    x = np.full(d, 0x3f80, dtype=np.uint16)            # ones
+    w13 = np.zeros((2 * F, d), dtype=np.uint16)
+    w13[:F] = 0x3f80      # gate rows: 1.0 -> g = d
+    w13[F:] = 0x0000      # up rows: 0 -> h = 0 regardless of g
+    w2 = np.full((d, F), 0x3f80, dtype=np.uint16)
+    out, h = oracle.swiglu_row_bf16(x, w13, w2)
+    assert not h.any() and not out.any()
+    w13[:F], w13[F:] = 0, 0x3f80                        # gate 0 -> silu(0) = 0
+    out, h = oracle.swiglu_row_bf16(x, w13, w2)
+    assert not h.any()
+
+
+def test_swiglu_fp8_matches_torch_dequantised_mlp():
+    cfg = synth.MoEConfig("t", T=4, d=256, E=2, k=1, n_group=1, topk_group=1, d_ff=256,
+                          d_ff_shared=0, R=1, route_scale=1.0, act="fp8", w="fp8", seed=3)
+    W = synth.expert_weight_slice(cfg, 1)
+    x = synth.normal_bf16(3, synth.TAG_X, (4, cfg.d), 1.0)
+    xq, xs = oracle.quant_rows_e4m3(oracle.bf16_to_f32(synth.bf16_bits(x)))
+    F, d = cfg.d_ff, cfg.d
+
+    def deq(q, s):
+        v = torch.from_numpy(q.numpy() if torch.is_tensor(q) else q).view(torch.float8_e4m3fn).double()
+        s = torch.as_tensor(s).double()
+        return v * s.repeat_interleave(128, 0).repeat_interleave(128, 1)
+
+    w13 = deq(W["w13"], W["w13_s"])
+    w2 = deq(W["w2"], W["w2_s"])
+    for t in range(4):
+        xv = torch.from_numpy(xq[t]).view(torch.float8_e4m3fn).double() * \
+            torch.from_numpy(xs[t]).double().repeat_interleave(128)
+        g = w13[:F] @ xv
+        u = w13[F:] @ xv
+        hf = (torch.nn.functional.silu(g) * u).float()
+        blk = hf.view(F // 128, 128)
+        sc = blk.abs().amax(1) / 448.0
+        hq = (blk / sc[:, None]).to(torch.float8_e4m3fn).double() * sc[:, None].double()
+        ref = (w2 @ hq.reshape(-1)).float()
+        out, h = oracle.swiglu_row_fp8(xq[t], xs[t], W["w13"].numpy(), W["w13_s"].numpy(),
+                                       W["w2"].numpy(), W["w2_s"].numpy())
+        o = oracle.bf16_to_f32(out)
+        assert np.abs(o - ref.numpy()).max() <= 2 ** -7 * np.abs(ref.numpy()).max() + 1e-6
+
+
+def test_combine_identity_experts_return_scaled_x():
+    """Dispatch followed by identity experts and the combine gives route_scale * x."""
+    cfg = synth.CONFIGS["tiny"]
+    inp = synth.make_router_inputs(cfg)
+    x = synth.bf16_bits(inp["x"])
+    idx, w = oracle.route(x, inp["w_gate"].numpy(), inp["bias"].numpy(), cfg.k, cfg.n_group,
+                          cfg.topk_group, 1.75)
+    _, _, row_of, src_tok = oracle.dispatch_index(idx, cfg.E, cfg.R)
+    recv, _ = oracle.dispatch_payload(x, row_of, src_tok.size)
+    y = oracle.combine(recv, row_of, w)
+    ref = oracle.bf16_to_f32(x).astype(np.float64) * 1.75
+    yf = oracle.bf16_to_f32(y)
+    assert np.all(np.abs(yf - ref) <= 2 ** -8 * np.abs(ref) + 1e-30)
+
+
+def test_combine_matches_numpy_weighted_sum():
+    rng = np.random.default_rng(4)
+    T, d, k, n = 5, 128, 3, 20
+    eb = oracle.f32_to_bf16(rng.standard_normal((n, d)).astype(np.float32))
+    sh = oracle.f32_to_bf16(rng.standard_normal((T, d)).astype(np.float32))
+    ro = rng.permutation(n)[:T * k].reshape(T, k).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    y = oracle.combine(eb, ro, w, sh)
+    ref = np.einsum("tk,tkd->td", w.astype(np.float64), oracle.bf16_to_f32(eb)[ro].astype(np.float64))
+    ref += oracle.bf16_to_f32(sh)
+    refb = torch.from_numpy(ref).float().to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.abs(y.astype(np.int32) - refb.astype(np.int32)).max() <= 1
+
+
+# ------------------------------------------------------------------------------------------
+# The pages' metrics
+# ------------------------------------------------------------------------------------------
+def test_imbalance_factor_exercise_three():
+    g = _golden("exercise3_imbalance.json")
+    c = np.array(g["expert_counts"])
+    assert oracle.imbalance_factor(c, g["G"]) == g["imbalance_factor"]
+    assert list(c.reshape(g["G"], -1).sum(1)) == g["rank_loads"]
+
+
+def test_imbalance_factor_demo_ranges():
+    g = _golden("skew_demo.json")
+    rng = np.random.default_rng(12)
+    E, G, T, k = g["E"], g["G"], g["T"], g["k"]
+    uni = np.bincount(rng.integers(0, E, size=T * k), minlength=E)
+    assert 1.0 <= oracle.imbalance_factor(uni, G) <= 1.15
+    p = np.ones(E)
+    p[g["hot_experts"]] *= g["hot_weight"]
+    p /= p.sum()
+    sk = np.bincount(rng.choice(E, size=T * k, p=p), minlength=E)
+    assert oracle.imbalance_factor(sk, G) > g["skewed_if_above"]
+
+
+def test_distinct_experts_closed_form():
+    g = _golden("distinct_experts.json")
+    E, k, B = g["E"], g["k"], g["B"]
+    closed = E * (1 - (1 - k / E) ** B)
+    assert round(closed) == g["printed_value"]
+    assert abs(closed / E - g["printed_fraction"]) < 0.005
+    trials = [oracle.distinct_experts(_random_topk(B, E, k, 100 + s)) for s in range(64)]
+    assert abs(np.mean(trials) - closed) <= 3 * 4.58 / math.sqrt(64)
+
+
+def test_router_touches_about_the_closed_form_count():
+    """With no bias, sigmoid routing on random weights is uniform over experts, so a batch of
+    64 touches about E(1-(1-k/E)^B) = 222 experts. With the workload's U(-0.1, 0.1) bias the
+    bias dominates the near-saturated top scores and fewer experts are touched."""
+    cfg = synth.CONFIGS["dsv3_decode"]
+    inp = synth.make_router_inputs(cfg)
+    x = synth.bf16_bits(inp["x"])
+    closed = cfg.E * (1 - (1 - cfg.k / cfg.E) ** cfg.T)
+    idx0, _ = oracle.route(x, inp["w_gate"].numpy(), np.zeros(cfg.E, np.float32), cfg.k,
+                           cfg.n_group, cfg.topk_group, cfg.route_scale)
+    assert abs(oracle.distinct_experts(idx0) - closed) <= 0.1 * closed
+    idx, _ = oracle.route(x, inp["w_gate"].numpy(), inp["bias"].numpy(), cfg.k, cfg.n_group,
+                          cfg.topk_group, cfg.route_scale)
+    assert oracle.distinct_experts(idx) < oracle.distinct_experts(idx0)
+
+
+def test_layer_tokens_composes_route_experts_combine():
+    cfg = synth.CONFIGS["tiny"]
+    inp = synth.make_router_inputs(cfg)
+    W = synth.make_expert_weights(cfg)
+    w13 = synth.bf16_bits(W["w13"])
+    w2 = synth.bf16_bits(W["w2"])
+    x = synth.bf16_bits(inp["x"])
+    out = oracle.layer_tokens(cfg, x, inp["w_gate"].numpy(), inp["bias"].numpy(),
+                              lambda e: dict(w13=w13[e], w2=w2[e]), None, [3, 0, 15])
+    idx, w = oracle.route(x, inp["w_gate"].numpy(), inp["bias"].numpy(), cfg.k, 1, 1, 1.0)
+    assert np.array_equal(out["topk_idx"], idx[[3, 0, 15]])
+    t = 15
+    ref = np.zeros(cfg.d)
+    for i in range(cfg.k):
+        o, _ = oracle.swiglu_row_bf16(x[t], w13[idx[t, i]], w2[idx[t, i]])
+        ref += float(w[t, i]) * oracle.bf16_to_f32(o)
+    yb = torch.from_numpy(ref).float().to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.abs(out["y"][2].astype(np.int32) - yb.astype(np.int32)).max() <= 1
