@@ -1,0 +1,394 @@
+"""Benchmark of the MoE layer hot path on GB300.
+
+One step = one pass of the whole layer (router -> dispatch -> expert FFNs -> combine) over one
+batch of seeded synthetic input with resident random-init weights. Default workload: the
+DeepSeek-V3-shaped decode layer (T=64 tokens, d=7168, 256 routed experts of d_ff 2048 + one
+shared expert, top-8 of 8 groups keeping 4, 8 logical ranks), bf16.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0). Under torchrun (N > 1) every rank runs an independent replica
+of the layer on its own batch (no collective on the data path: the expert-parallel ranks of
+this method are logical partitions of one GPU), and the timing is the max over ranks.
+--impl reference times the CPU oracle (the plain C definition of the method) on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer µs & tokens/s vs tokens (1–16K); % of HBM / tensor roofline"
+KERNELS_PER_STEP = 8   # route x2, dispatch x2, ffn schedule, gate/up GEMM, down GEMM, combine
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="dsv3_decode")
+    p.add_argument("--T", type=int, default=0, help="override the token count (sweep points)")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=0, help="tokens in the oracle sample")
+    return p.parse_args()
+
+
+def workload(args):
+    cfg = synth.CONFIGS[args.workload]
+    if args.T:
+        cfg = cfg.with_T(args.T)
+    return cfg
+
+
+def describe(cfg):
+    return {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
+            "n_group": cfg.n_group, "topk_group": cfg.topk_group, "d_ff": cfg.d_ff,
+            "d_ff_shared": cfg.d_ff_shared, "R_logical": cfg.R, "route_scale": cfg.route_scale,
+            "act": cfg.act, "weights": cfg.w, "bias": cfg.bias}
+
+
+# ------------------------------------------------------------------------------------------
+# Algorithmic bytes / flops per stage (what the method must move; expert counts are the
+# routing's own)
+# ------------------------------------------------------------------------------------------
+def algorithmic(cfg, counts):
+    T, d, E, k, F, Fs = cfg.T, cfg.d, cfg.E, cfg.k, cfg.d_ff, cfg.d_ff_shared
+    bw = 1 if cfg.w == "fp8" else 2
+    ba = 1 if cfg.act == "fp8" else 2
+    tk = T * k
+    touched = int((counts.sum(0) > 0).sum())
+    sc_w13 = (2 * F // 128) * (d // 128) * 4 if cfg.w == "fp8" else 0
+    sc_w2 = (d // 128) * (F // 128) * 4 if cfg.w == "fp8" else 0
+    sc_act = (d // 128) * 4 if cfg.act == "fp8" else 0
+    sc_h = (F // 128) * 4 if cfg.act == "fp8" else 0
+    rows_sh = T if Fs else 0
+    b = {}
+    b["route"] = 2 * T * d + 4 * E * d + 4 * E + 8 * tk
+    b["dispatch"] = 2 * T * d + tk * (d * ba + sc_act) + 12 * tk
+    b["ffn_gate_up"] = (touched * (2 * F * d * bw + sc_w13) + (2 * Fs * d * bw + sc_w13 if Fs else 0)
+                        + (tk + rows_sh) * (d * ba + sc_act) + (tk + rows_sh) * (F * ba + sc_h))
+    b["ffn_down"] = (touched * (d * F * bw + sc_w2) + (d * Fs * bw + sc_w2 if Fs else 0)
+                     + (tk + rows_sh) * (F * ba + sc_h) + (tk + rows_sh) * d * 2)
+    b["combine"] = tk * d * 2 + (T * d * 2 if Fs else 0) + T * d * 2 + 8 * tk
+    f = {"route": 2 * T * d * E, "ffn_gate_up": 2 * (tk + rows_sh) * 2 * F * d,
+         "ffn_down": 2 * (tk + rows_sh) * F * d}
+    return b, f, touched
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm": float(p["hbm_gbs"]), "bf16": float(p["bf16_tflops"]),
+                "bf16_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def measured_traffic(kernel, workload_name):
+    """DRAM bytes per launch from the committed ncu summary, or None when absent or when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            tab = json.load(fh)
+        ent = tab[f"{kernel}@{workload_name}"]
+        src = os.path.join(ROOT, ent["source"])
+        with open(src, "rb") as fh:
+            if hashlib.sha256(fh.read()).hexdigest()[:16] != ent["source_sha256_16"]:
+                return None
+        return int(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------------------------------
+# Clocks during the timed region
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------------
+# Our arm
+# ------------------------------------------------------------------------------------------
+def run_ours(args, cfg, rank, world, local_rank):
+    import combine_grouped_gemm_gb300 as moe
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    # every rank: same weights, its own batch of tokens
+    inp = synth.make_router_inputs(cfg, dev)
+    if world > 1:
+        inp["x"] = synth.normal_bf16(cfg.seed + 7919 * rank, synth.TAG_X, (cfg.T, cfg.d),
+                                     cfg.x_std, dev)
+    W = synth.make_expert_weights(cfg, dev)
+    weights = dict(w13=W["w13"], w13_s=W["w13_s"], w2=W["w2"], w2_s=W["w2_s"], ws13=W["ws13"],
+                   ws13_s=W["ws13_s"], ws2=W["ws2"], ws2_s=W["ws2_s"])
+    lay = moe.MoELayer(cfg, inp["w_gate"], inp["bias"], weights, dev)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_LAYER_EVENTS)]
+           for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        lay(inp["x"], y)
+    torch.cuda.synchronize(dev)
+    moe.clear_status(lay.bufs["ws"])
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        lay(inp["x"], y, events=evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop() if clocks else None
+    ms = t0.elapsed_time(t1) / args.steps
+    status = moe.read_status(lay.bufs["ws"])
+    if status:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    stage_ms = {n: 0.0 for n in moe.STAGE_NAMES}
+    for row in evs:
+        for j, n in enumerate(moe.STAGE_NAMES):
+            stage_ms[n] += row[j].elapsed_time(row[j + 1]) / args.steps
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # end to end through the public API: pinned host buffers, copies inside the timed region
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    for _ in range(2):
+        lay.run_host(x_host, y_host, stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        lay.run_host(x_host, y_host, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    counts = lay.bufs["counts"].cpu().numpy()
+    return dict(ms=ms_max, ms_local=ms, stage_ms=stage_ms, clocks=clk, ms_e2e=ms_e2e,
+                counts=counts, inp=inp, W=W, lay=lay)
+
+
+def oracle_sample(cfg, inp, W, tokens):
+    """Times oracle.layer_tokens on the given tokens; weight slices are copied to the host
+    before the clock starts."""
+    import oracle
+
+    def bits(t):
+        t = t.detach().cpu().contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    x = bits(inp["x"])
+    wg = inp["w_gate"].cpu().numpy()
+    b = inp["bias"].cpu().numpy()
+    idx, _ = oracle.route(x[tokens], wg, b, cfg.k, cfg.n_group, cfg.topk_group, cfg.route_scale)
+    fp8 = cfg.w == "fp8"
+    experts = {}
+    for e in np.unique(idx):
+        e = int(e)
+        experts[e] = dict(w13=bits(W["w13"][e]), w2=bits(W["w2"][e]))
+        if fp8:
+            experts[e]["w13_s"] = W["w13_s"][e].cpu().numpy()
+            experts[e]["w2_s"] = W["w2_s"][e].cpu().numpy()
+    shared = None
+    if cfg.d_ff_shared:
+        shared = dict(ws13=bits(W["ws13"]), ws2=bits(W["ws2"]))
+        if fp8:
+            shared["ws13_s"] = W["ws13_s"].cpu().numpy()
+            shared["ws2_s"] = W["ws2_s"].cpu().numpy()
+    t = time.perf_counter()
+    oracle.layer_tokens(cfg, x, wg, b, lambda e: experts[e], shared, tokens)
+    return time.perf_counter() - t
+
+
+def main():
+    args = parse()
+    cfg = workload(args)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus > 1 and world == 1:
+        print(json.dumps({"error": "--gpus > 1 needs torchrun (one process per GPU)"}))
+        return 2
+
+    if args.impl == "reference":
+        return run_reference(args, cfg, rank, world, local_rank)
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    r = run_ours(args, cfg, rank, world, local_rank)
+    if rank == 0:
+        b, f, touched = algorithmic(cfg, r["counts"])
+        pk = peaks()
+        dom = max(r["stage_ms"], key=lambda n: r["stage_ms"][n])
+        dom_ms = r["stage_ms"][dom]
+        achieved = b[dom] / (dom_ms * 1e-3) / 1e9
+        roof = {"kernel": {"ffn_gate_up": "ffn_gemm_bf16_kernel<0>",
+                           "ffn_down": "ffn_gemm_bf16_kernel<1>"}.get(dom, dom),
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
+                "peak_source": f"{pk['source']} hbm_gbs",
+                "traffic": measured_traffic(dom, cfg.name),
+                "algorithmic_bytes_per_launch": b[dom], "launch_ms": round(dom_ms, 4)}
+        layer_bytes = sum(b.values())
+        tokens_per_s = cfg.T * world / (r["ms"] * 1e-3)
+        out = {
+            "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(r["ms"], 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": cfg.act,
+            "data": "synthetic: seeded counter-based generator, random-init weights",
+            "config": {**describe(cfg), "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: ~%.1f GB of expert weights streamed per "
+                             "step vs 129 MB L2" % (b["ffn_gate_up"] / 1e9 + b["ffn_down"] / 1e9)},
+            "layer_us": round(r["ms"] * 1e3, 2),
+            "stages_us": {n: round(v * 1e3, 2) for n, v in r["stage_ms"].items()},
+            "layer_hbm_frac": round(layer_bytes / (r["ms"] * 1e-3) / 1e9 / pk["hbm"], 4),
+            "experts_touched": touched,
+            "imbalance_factor": round(float(np.bincount(
+                np.repeat(np.arange(cfg.E), r["counts"].sum(0)), minlength=cfg.E)
+                .reshape(cfg.R, -1).sum(1).max() / (cfg.T * cfg.k / cfg.R)), 4),
+            "roofline": roof,
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": r["clocks"],
+            "e2e": {"value": round(cfg.T * world / (r["ms_e2e"] * 1e-3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
+                    "ms_per_step": round(r["ms_e2e"], 5)},
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            n = args.cpu_sample or min(cfg.T, 8)
+            rng = np.random.default_rng(0)
+            tokens = np.sort(rng.choice(cfg.T, n, replace=False))
+            sec = oracle_sample(cfg, r["inp"], r["W"], tokens)
+            out["cpu_baseline"] = {"value": round(n / sec, 4), "unit": "tokens/s", "cores": 1,
+                                   "kind": "oracle",
+                                   "sample": f"{n} of {cfg.T} tokens of {cfg.name}: route + "
+                                             f"k experts + shared + combine per token, "
+                                             f"{sec:.1f} s single-threaded"}
+        else:
+            out["cpu_baseline"] = None
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_reference(args, cfg, rank, world, local_rank):
+    """The reference arm: the CPU oracle timed on this host's cores, each step a bounded
+    sample (one token of the workload through the whole layer)."""
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local_rank) if torch.cuda.is_available() else torch.device("cpu")
+    inp = synth.make_router_inputs(cfg, dev)
+    W = synth.make_expert_weights(cfg, dev)
+    rng = np.random.default_rng(1)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, inp, W, rng.choice(cfg.T, 1))
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_sample(cfg, inp, W, rng.choice(cfg.T, 1))
+    v = args.steps / total
+    out = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tokens/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": cfg.act,
+           "data": "synthetic: seeded counter-based generator, random-init weights",
+           "config": {**describe(cfg), "parallelism": "cpu oracle, 1 thread"},
+           "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": 1,
+                            "kind": "oracle",
+                            "sample": f"1 token of {cfg.name} per step through the whole layer"},
+           "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

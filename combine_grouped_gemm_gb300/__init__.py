@@ -1,0 +1,254 @@
+"""Python binding of libmoe, the GB300 (sm_103a) MoE-layer hot path.
+
+Argument marshalling only: every function below passes device pointers of torch CUDA tensors
+and the current CUDA stream to the C ABI declared in include/moe.h, and raises MoEError on a
+non-zero return code. All the work runs in the library's CUDA kernels; there is no fallback.
+If the shared library is missing, importing this package raises at once: build it with
+``python -m combine_grouped_gemm_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmoe.so")
+
+MOE_BF16, MOE_FP8_E4M3 = 0, 1
+MOE_DEV_TIMEOUT, MOE_DEV_BOUNDS = 1, 2
+MOE_LAYER_EVENTS = 7
+STAGE_NAMES = ["route", "dispatch", "ffn_setup", "ffn_gate_up", "ffn_down", "combine"]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn, code, msg, cuda_err=0):
+        super().__init__(f"{fn}: {msg} (code {code}" + (f", cudaError {cuda_err})" if cuda_err else ")"))
+        self.code = code
+        self.cuda_error = cuda_err
+
+
+class Cfg(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("n_group", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("d_ff_shared", ctypes.c_int32), ("R", ctypes.c_int32),
+                ("route_scale", ctypes.c_float), ("act_dtype", ctypes.c_int32),
+                ("w_dtype", ctypes.c_int32)]
+
+
+class Sizes(ctypes.Structure):
+    _fields_ = [("recv_rows", ctypes.c_int64), ("cap", ctypes.c_int32),
+                ("recv_bytes", ctypes.c_size_t), ("recv_scale_bytes", ctypes.c_size_t),
+                ("ebuf_bytes", ctypes.c_size_t), ("ws_bytes", ctypes.c_size_t)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w13", "w13_scales", "w2", "w2_scales", "ws13", "ws13_scales", "ws2",
+                 "ws2_scales")]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmoe.so not found at {LIB_PATH}; build it with "
+                          "`python -m combine_grouped_gemm_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+    sigs = {
+        "moe_validate": [P],
+        "moe_query_sizes": [P, P],
+        "moe_route": [P, P, P, P, P, P, P, S],
+        "moe_dispatch": [P, P, P, P, P, P, P, P, S],
+        "moe_expert_ffn": [P, P, P, P, P, P, P, P, P, S],
+        "moe_combine": [P, P, P, P, P, P, S],
+        "moe_layer": [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P],
+        "moe_clear_status": [P, S],
+        "moe_read_status": [P, P, S],
+        "moe_strerror": [I],
+        "moe_abi_version": [],
+        "moe_last_cuda_error": [],
+    }
+    for name, args in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "moe_strerror" else ctypes.c_int
+    return L
+
+
+_lib = _load()
+
+EXPORTED = ["moe_validate", "moe_query_sizes", "moe_route", "moe_dispatch", "moe_expert_ffn",
+            "moe_combine", "moe_layer", "moe_clear_status", "moe_read_status", "moe_strerror",
+            "moe_abi_version", "moe_last_cuda_error"]
+
+
+def _check(fn, rc):
+    if rc != 0:
+        err = _lib.moe_last_cuda_error() if rc == 4 else 0
+        raise MoEError(fn, rc, _lib.moe_strerror(rc).decode(), err)
+
+
+def _dtype_code(v):
+    if isinstance(v, str):
+        return MOE_FP8_E4M3 if v in ("fp8", "e4m3") else MOE_BF16
+    return int(v)
+
+
+def make_cfg(c) -> Cfg:
+    """Cfg from any object with the moe_cfg fields (act / w may be "bf16" / "fp8")."""
+    act = getattr(c, "act_dtype", getattr(c, "act", MOE_BF16))
+    w = getattr(c, "w_dtype", getattr(c, "w", act))
+    return Cfg(c.T, c.d, c.E, c.k, c.n_group, c.topk_group, c.d_ff, c.d_ff_shared, c.R,
+               float(c.route_scale), _dtype_code(act), _dtype_code(w))
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        return int(t)
+    if not t.is_cuda:
+        raise ValueError("libmoe takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libmoe takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+_WEIGHT_KEYS = ("w13", "w13_s", "w2", "w2_s", "ws13", "ws13_s", "ws2", "ws2_s")
+
+
+def _weights(w: dict) -> Weights:
+    """moe_weights from a dict with keys w13, w13_s, w2, w2_s, ws13, ws13_s, ws2, ws2_s."""
+    return Weights(*[_p(w.get(n)) for n in _WEIGHT_KEYS])
+
+
+def validate(cfg) -> int:
+    return _lib.moe_validate(ctypes.byref(make_cfg(cfg)))
+
+
+def query_sizes(cfg) -> dict:
+    s = Sizes()
+    _check("moe_query_sizes", _lib.moe_query_sizes(ctypes.byref(make_cfg(cfg)), ctypes.byref(s)))
+    return {n: getattr(s, n) for n, _ in Sizes._fields_}
+
+
+def route(cfg, x, w_gate, bias, topk_idx, topk_w, ws, stream=None):
+    _check("moe_route", _lib.moe_route(ctypes.byref(make_cfg(cfg)), _p(x), _p(w_gate), _p(bias),
+                                       _p(topk_idx), _p(topk_w), _p(ws), _s(stream)))
+
+
+def dispatch(cfg, x, topk_idx, recv, recv_scales, counts, row_of, src_tok=None, stream=None):
+    _check("moe_dispatch", _lib.moe_dispatch(ctypes.byref(make_cfg(cfg)), _p(x), _p(topk_idx),
+                                             _p(recv), _p(recv_scales), _p(counts), _p(row_of),
+                                             _p(src_tok), _s(stream)))
+
+
+def expert_ffn(cfg, recv, recv_scales, counts, x, weights: dict, ebuf, shared_out, ws,
+               stream=None):
+    w = _weights(weights)
+    _check("moe_expert_ffn", _lib.moe_expert_ffn(ctypes.byref(make_cfg(cfg)), _p(recv),
+                                                 _p(recv_scales), _p(counts), _p(x),
+                                                 ctypes.byref(w), _p(ebuf), _p(shared_out),
+                                                 _p(ws), _s(stream)))
+
+
+def combine(cfg, ebuf, row_of, topk_w, shared_out, y, stream=None):
+    _check("moe_combine", _lib.moe_combine(ctypes.byref(make_cfg(cfg)), _p(ebuf), _p(row_of),
+                                           _p(topk_w), _p(shared_out), _p(y), _s(stream)))
+
+
+def layer(cfg, x, w_gate, bias, weights: dict, bufs: dict, y, stream=None, events=None):
+    """The whole layer. bufs holds topk_idx, topk_w, recv, recv_scales, counts, row_of, ebuf,
+    shared_out and ws (see Buffers). events: None or MOE_LAYER_EVENTS torch.cuda.Event that
+    have been recorded once (so their handles exist)."""
+    w = _weights(weights)
+    ev = None
+    if events is not None:
+        arr = (ctypes.c_void_p * MOE_LAYER_EVENTS)(*[e.cuda_event for e in events])
+        ev = ctypes.cast(arr, ctypes.c_void_p)
+    b = bufs
+    _check("moe_layer", _lib.moe_layer(ctypes.byref(make_cfg(cfg)), _p(x), _p(w_gate), _p(bias),
+                                       ctypes.byref(w), _p(b["topk_idx"]), _p(b["topk_w"]),
+                                       _p(b["recv"]), _p(b.get("recv_scales")), _p(b["counts"]),
+                                       _p(b["row_of"]), _p(b["ebuf"]), _p(b.get("shared_out")),
+                                       _p(y), _p(b["ws"]), _s(stream), ev))
+
+
+def clear_status(ws, stream=None):
+    _check("moe_clear_status", _lib.moe_clear_status(_p(ws), _s(stream)))
+
+
+def read_status(ws, stream=None) -> int:
+    st = ctypes.c_uint32(0)
+    _check("moe_read_status", _lib.moe_read_status(_p(ws), ctypes.byref(st), _s(stream)))
+    return st.value
+
+
+def abi_version() -> int:
+    return _lib.moe_abi_version()
+
+
+class Buffers(dict):
+    """Device buffers of one layer configuration, allocated once with torch (the library itself
+    allocates nothing)."""
+
+    def __init__(self, cfg, device="cuda"):
+        super().__init__()
+        s = query_sizes(cfg)
+        T, k, d, R, E = cfg.T, cfg.k, cfg.d, cfg.R, cfg.E
+        self.sizes = s
+        fp8 = make_cfg(cfg).act_dtype == MOE_FP8_E4M3
+        self["topk_idx"] = torch.empty((T, k), dtype=torch.int32, device=device)
+        self["topk_w"] = torch.empty((T, k), dtype=torch.float32, device=device)
+        self["recv"] = torch.empty((s["recv_rows"], d),
+                                   dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
+        self["recv_scales"] = (torch.empty((s["recv_rows"], d // 128), dtype=torch.float32,
+                                           device=device) if fp8 else None)
+        self["counts"] = torch.empty((R, E), dtype=torch.int32, device=device)
+        self["row_of"] = torch.empty((T, k), dtype=torch.int32, device=device)
+        self["ebuf"] = torch.empty((s["recv_rows"], d), dtype=torch.bfloat16, device=device)
+        self["shared_out"] = (torch.empty((T, d), dtype=torch.bfloat16, device=device)
+                              if cfg.d_ff_shared else None)
+        self["ws"] = torch.zeros(s["ws_bytes"], dtype=torch.uint8, device=device)
+
+
+class MoELayer:
+    """One MoE layer with resident weights: ``y = layer(x)`` runs router, dispatch, expert
+    FFNs and combine on the current stream through ``moe_layer``."""
+
+    def __init__(self, cfg, w_gate, bias, weights: dict, device="cuda"):
+        self.cfg = cfg
+        self.w_gate = w_gate
+        self.bias = bias
+        self.weights = weights
+        self.bufs = Buffers(cfg, device)
+
+    def __call__(self, x, y=None, stream=None, events=None):
+        if y is None:
+            y = torch.empty((self.cfg.T, self.cfg.d), dtype=torch.bfloat16, device=x.device)
+        layer(self.cfg, x, self.w_gate, self.bias, self.weights, self.bufs, y, stream, events)
+        return y
+
+    def run_host(self, x_host, y_host, stream=None):
+        """Host-to-host call: copies x_host (pinned bf16 [T][d]) to the device, runs the layer
+        and copies the output back into y_host (pinned), all enqueued on the stream. The caller
+        synchronises before reading y_host."""
+        if not hasattr(self, "_x_dev"):
+            self._x_dev = torch.empty((self.cfg.T, self.cfg.d), dtype=torch.bfloat16,
+                                      device=self.w_gate.device)
+            self._y_dev = torch.empty_like(self._x_dev)
+        s = stream or torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            self._x_dev.copy_(x_host, non_blocking=True)
+            layer(self.cfg, self._x_dev, self.w_gate, self.bias, self.weights, self.bufs,
+                  self._y_dev, s)
+            y_host.copy_(self._y_dev, non_blocking=True)
+        return y_host

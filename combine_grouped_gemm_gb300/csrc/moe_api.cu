@@ -1,0 +1,291 @@
+// C ABI of libmoe (declared in include/moe.h): argument checks, workspace layout, and the
+// launch sequence router -> dispatch -> expert FFN (schedule, gate/up GEMM, down GEMM) ->
+// combine on the caller's stream. Nothing here allocates memory or waits for the device,
+// except moe_read_status.
+#include <math.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return MOE_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+}  // namespace
+
+int validate(const moe_cfg& c) {
+  if (c.T < 1 || c.d < 1 || c.E < 1 || c.k < 1 || c.n_group < 1 || c.topk_group < 1 ||
+      c.d_ff < 1 || c.d_ff_shared < 0 || c.R < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (c.T % c.R || c.E % c.R || c.E % c.n_group) return MOE_ERR_INVALID_ARG;
+  if (c.topk_group > c.n_group || c.k > c.topk_group * (c.E / c.n_group))
+    return MOE_ERR_INVALID_ARG;
+  if ((c.act_dtype != MOE_BF16 && c.act_dtype != MOE_FP8_E4M3) ||
+      (c.w_dtype != MOE_BF16 && c.w_dtype != MOE_FP8_E4M3))
+    return MOE_ERR_INVALID_ARG;
+  if (!isfinite(c.route_scale)) return MOE_ERR_INVALID_ARG;
+  // limits of these kernels
+  if (c.d % 128 || c.d_ff % 128 || c.d_ff_shared % 128) return MOE_ERR_UNSUPPORTED;
+  if (c.E > 1024 || c.k > 32 || c.n_group > 64 || c.R > 64) return MOE_ERR_UNSUPPORTED;
+  if (c.act_dtype != c.w_dtype) return MOE_ERR_UNSUPPORTED;
+  if (c.d_ff_shared != 0 && c.d_ff_shared != c.d_ff) return MOE_ERR_UNSUPPORTED;
+  const long long rows = (long long)c.R * c.R * cap_of(c);
+  if (rows >= (1ll << 31) || (long long)c.T * c.k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+WsLayout ws_layout(const moe_cfg& c) {
+  WsLayout L{};
+  const size_t tk = (size_t)c.T * c.k;
+  const size_t ab = act_bytes(c);
+  const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
+  L.bn = (tk >= (size_t)64 * c.E) ? 128 : 64;
+  L.max_tiles = c.E + (int)((tk + L.bn - 1) / L.bn);
+  size_t o = 0;
+  L.status = o;     o = up256(o + 16);
+  L.partials = o;   o = up256(o + sizeof(float) * kRouteChunks * (size_t)c.T * c.E);
+  L.grp_n = o;      o = up256(o + sizeof(int32_t) * c.E);
+  L.grp_off = o;    o = up256(o + sizeof(int32_t) * c.E);
+  L.n_tiles = o;    o = up256(o + sizeof(int32_t));
+  L.tiles = o;      o = up256(o + sizeof(Tile) * (size_t)L.max_tiles);
+  L.row_list = o;   o = up256(o + sizeof(int32_t) * tk);
+  L.h = o;          o = up256(o + ab * tk * c.d_ff);
+  L.h_scales = o;   o = up256(o + (fp8 ? sizeof(float) * tk * (c.d_ff / 128) : 0));
+  L.hs = o;         o = up256(o + ab * (size_t)c.T * c.d_ff_shared);
+  L.hs_scales = o;  o = up256(o + (fp8 ? sizeof(float) * (size_t)c.T * (c.d_ff_shared / 128) : 0));
+  L.xq = o;         o = up256(o + (fp8 && c.d_ff_shared ? (size_t)c.T * c.d : 0));
+  L.xq_scales = o;  o = up256(o + (fp8 && c.d_ff_shared ? sizeof(float) * (size_t)c.T * (c.d / 128) : 0));
+  L.total = o;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define MOE_CHECK_CFG(cfg)                      \
+  do {                                          \
+    if (!(cfg)) return MOE_ERR_INVALID_ARG;     \
+    const int rc_ = validate(*(cfg));           \
+    if (rc_ != MOE_OK) return rc_;              \
+  } while (0)
+
+#define MOE_NEED(p)                              \
+  do {                                           \
+    if (!(p)) return MOE_ERR_INVALID_ARG;        \
+    if (!aligned16(p)) return MOE_ERR_MISALIGNED; \
+  } while (0)
+
+#define MOE_OPT(p)                                      \
+  do {                                                  \
+    if ((p) && !aligned16(p)) return MOE_ERR_MISALIGNED; \
+  } while (0)
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (shape constraint or NULL pointer)";
+    case MOE_ERR_UNSUPPORTED: return "shape not supported by these kernels";
+    case MOE_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA call or kernel launch failed";
+    default: return "unknown error code";
+  }
+}
+
+int moe_validate(const moe_cfg* cfg) {
+  MOE_CHECK_CFG(cfg);
+  return MOE_OK;
+}
+
+int moe_query_sizes(const moe_cfg* cfg, moe_sizes* out) {
+  MOE_CHECK_CFG(cfg);
+  if (!out) return MOE_ERR_INVALID_ARG;
+  const moe_cfg& c = *cfg;
+  const int cap = cap_of(c);
+  out->cap = cap;
+  out->recv_rows = (int64_t)c.R * c.R * cap;
+  out->recv_bytes = (size_t)out->recv_rows * c.d * act_bytes(c);
+  out->recv_scale_bytes =
+      c.act_dtype == MOE_FP8_E4M3 ? (size_t)out->recv_rows * (c.d / 128) * sizeof(float) : 0;
+  out->ebuf_bytes = (size_t)out->recv_rows * c.d * 2;
+  out->ws_bytes = ws_layout(c).total;
+  return MOE_OK;
+}
+
+int moe_route(const moe_cfg* cfg, const void* x, const float* w_gate, const float* bias,
+              int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_NEED(x);
+  MOE_NEED(w_gate);
+  MOE_NEED(bias);
+  MOE_NEED(topk_idx);
+  MOE_NEED(topk_w);
+  MOE_NEED(ws);
+  const WsLayout L = ws_layout(*cfg);
+  char* w = static_cast<char*>(ws);
+  cudaError_t e = launch_route(*cfg, x, w_gate, bias, topk_idx, topk_w,
+                               reinterpret_cast<float*>(w + L.partials),
+                               reinterpret_cast<uint32_t*>(w + L.status), stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+int moe_dispatch(const moe_cfg* cfg, const void* x, const int32_t* topk_idx, void* recv,
+                 float* recv_scales, int32_t* counts, int32_t* row_of, int32_t* src_tok,
+                 cudaStream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_NEED(x);
+  MOE_NEED(topk_idx);
+  MOE_NEED(recv);
+  MOE_NEED(counts);
+  MOE_NEED(row_of);
+  MOE_OPT(src_tok);
+  if (cfg->act_dtype == MOE_FP8_E4M3) MOE_NEED(recv_scales);
+  cudaError_t e = launch_dispatch(*cfg, x, topk_idx, recv, recv_scales, counts, row_of, src_tok,
+                                  stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+int moe_expert_ffn(const moe_cfg* cfg, const void* recv, const float* recv_scales,
+                   const int32_t* counts, const void* x, const moe_weights* w, void* ebuf,
+                   void* shared_out, void* ws, cudaStream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  const moe_cfg& c = *cfg;
+  MOE_NEED(recv);
+  MOE_NEED(counts);
+  MOE_NEED(ebuf);
+  MOE_NEED(ws);
+  if (!w) return MOE_ERR_INVALID_ARG;
+  MOE_NEED(w->w13);
+  MOE_NEED(w->w2);
+  const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
+  if (fp8) {
+    MOE_NEED(recv_scales);
+    MOE_NEED(w->w13_scales);
+    MOE_NEED(w->w2_scales);
+  }
+  if (c.d_ff_shared) {
+    MOE_NEED(x);
+    MOE_NEED(w->ws13);
+    MOE_NEED(w->ws2);
+    MOE_NEED(shared_out);
+    if (fp8) {
+      MOE_NEED(w->ws13_scales);
+      MOE_NEED(w->ws2_scales);
+    }
+  }
+  if (fp8) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(c);
+  char* wsp = static_cast<char*>(ws);
+  cudaError_t e = launch_ffn_setup(c, L, counts, x, wsp, stream);
+  if (e == cudaSuccess)
+    e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream);
+  if (e == cudaSuccess)
+    e = launch_ffn_gemm(c, L, 1, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+int moe_combine(const moe_cfg* cfg, const void* ebuf, const int32_t* row_of,
+                const float* topk_w, const void* shared_out, void* y, cudaStream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_NEED(ebuf);
+  MOE_NEED(row_of);
+  MOE_NEED(topk_w);
+  MOE_OPT(shared_out);
+  MOE_NEED(y);
+  cudaError_t e = launch_combine(*cfg, ebuf, row_of, topk_w, shared_out, y, stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const float* bias,
+              const moe_weights* w, int32_t* topk_idx, float* topk_w, void* recv,
+              float* recv_scales, int32_t* counts, int32_t* row_of, void* ebuf,
+              void* shared_out, void* y, void* ws, cudaStream_t stream,
+              const cudaEvent_t* events) {
+  MOE_CHECK_CFG(cfg);
+  const moe_cfg& c = *cfg;
+  MOE_NEED(x);
+  MOE_NEED(w_gate);
+  MOE_NEED(bias);
+  MOE_NEED(topk_idx);
+  MOE_NEED(topk_w);
+  MOE_NEED(recv);
+  MOE_NEED(counts);
+  MOE_NEED(row_of);
+  MOE_NEED(ebuf);
+  MOE_NEED(y);
+  MOE_NEED(ws);
+  if (!w) return MOE_ERR_INVALID_ARG;
+  MOE_NEED(w->w13);
+  MOE_NEED(w->w2);
+  const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
+  if (fp8) {
+    MOE_NEED(recv_scales);
+    MOE_NEED(w->w13_scales);
+    MOE_NEED(w->w2_scales);
+  }
+  if (c.d_ff_shared) {
+    MOE_NEED(w->ws13);
+    MOE_NEED(w->ws2);
+    MOE_NEED(shared_out);
+    if (fp8) {
+      MOE_NEED(w->ws13_scales);
+      MOE_NEED(w->ws2_scales);
+    }
+  }
+  if (fp8) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(c);
+  char* wsp = static_cast<char*>(ws);
+  auto rec = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(events[i], stream) : cudaSuccess;
+  };
+  cudaError_t e = rec(0);
+  if (e == cudaSuccess)
+    e = launch_route(c, x, w_gate, bias, topk_idx, topk_w,
+                     reinterpret_cast<float*>(wsp + L.partials),
+                     reinterpret_cast<uint32_t*>(wsp + L.status), stream);
+  if (e == cudaSuccess) e = rec(1);
+  if (e == cudaSuccess)
+    e = launch_dispatch(c, x, topk_idx, recv, recv_scales, counts, row_of, nullptr, stream);
+  if (e == cudaSuccess) e = rec(2);
+  if (e == cudaSuccess) e = launch_ffn_setup(c, L, counts, x, wsp, stream);
+  if (e == cudaSuccess) e = rec(3);
+  if (e == cudaSuccess)
+    e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream);
+  if (e == cudaSuccess) e = rec(4);
+  if (e == cudaSuccess)
+    e = launch_ffn_gemm(c, L, 1, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream);
+  if (e == cudaSuccess) e = rec(5);
+  if (e == cudaSuccess)
+    e = launch_combine(c, ebuf, row_of, topk_w, c.d_ff_shared ? shared_out : nullptr, y, stream);
+  if (e == cudaSuccess) e = rec(6);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+int moe_clear_status(void* ws, cudaStream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+int moe_read_status(const void* ws, uint32_t* status, cudaStream_t stream) {
+  if (!ws || !status) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpy(status, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+}  // extern "C"

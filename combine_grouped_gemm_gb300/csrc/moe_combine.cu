@@ -1,0 +1,85 @@
+// Combine kernel: weighted gather-sum of each token's k expert-output rows back to token order,
+// plus the shared expert's row, in fp32, rounded once to bf16.
+//
+// Method: "7.13 Serving Mixture-of-Experts" (llm-stack-book), Expert Parallelism Mechanics,
+// combine step (a token's k partial results weighted-summed by its gate weights); DeepEP
+// section (the combine stays in BF16).
+#include "moe_device.cuh"
+
+namespace moe {
+namespace {
+
+// Block (token t, column slice), 128 threads, one 16-byte vector (8 columns) per thread per
+// iteration: k gathered row vectors and the shared row, fp32 FMAs in selection order.
+__global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ ebuf,
+                                                      const int32_t* __restrict__ row_of,
+                                                      const float* __restrict__ topk_w,
+                                                      const uint4* __restrict__ shared_out,
+                                                      uint4* __restrict__ y, int d, int k,
+                                                      int slice_vecs) {
+  __shared__ int32_t rows[32];
+  __shared__ float wts[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+    wts[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  const int vpr = d / 8;
+  const int v0 = blockIdx.y * slice_vecs, v1 = min(vpr, v0 + slice_vecs);
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int i = 0; i < k; ++i) {
+      const int row = rows[i];
+      if (row < 0) continue;
+      const uint4 e = __ldg(ebuf + (size_t)row * vpr + v);
+      const float w = wts[i];
+      acc[0] = __fmaf_rn(w, bf16_lo(e.x), acc[0]);
+      acc[1] = __fmaf_rn(w, bf16_hi(e.x), acc[1]);
+      acc[2] = __fmaf_rn(w, bf16_lo(e.y), acc[2]);
+      acc[3] = __fmaf_rn(w, bf16_hi(e.y), acc[3]);
+      acc[4] = __fmaf_rn(w, bf16_lo(e.z), acc[4]);
+      acc[5] = __fmaf_rn(w, bf16_hi(e.z), acc[5]);
+      acc[6] = __fmaf_rn(w, bf16_lo(e.w), acc[6]);
+      acc[7] = __fmaf_rn(w, bf16_hi(e.w), acc[7]);
+    }
+    if (shared_out) {
+      const uint4 s = __ldg(shared_out + (size_t)t * vpr + v);
+      acc[0] += bf16_lo(s.x);
+      acc[1] += bf16_hi(s.x);
+      acc[2] += bf16_lo(s.y);
+      acc[3] += bf16_hi(s.y);
+      acc[4] += bf16_lo(s.z);
+      acc[5] += bf16_hi(s.z);
+      acc[6] += bf16_lo(s.w);
+      acc[7] += bf16_hi(s.w);
+    }
+    uint4 out;
+    out.x = pack_bf16x2(acc[0], acc[1]);
+    out.y = pack_bf16x2(acc[2], acc[3]);
+    out.z = pack_bf16x2(acc[4], acc[5]);
+    out.w = pack_bf16x2(acc[6], acc[7]);
+    y[(size_t)t * vpr + v] = out;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_cfg& c, const void* ebuf, const int32_t* row_of,
+                           const float* topk_w, const void* shared_out, void* y,
+                           cudaStream_t st) {
+  const int vpr = c.d / 8;
+  int nslice = 1;
+  while (c.T * nslice < 2 * 152 && vpr / (nslice * 2) >= 128) nslice *= 2;
+  const int slice_vecs = (vpr + nslice - 1) / nslice;
+  nslice = (vpr + slice_vecs - 1) / slice_vecs;
+  dim3 grid(c.T, nslice);
+  combine_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(ebuf), row_of, topk_w,
+                                       static_cast<const uint4*>(shared_out),
+                                       static_cast<uint4*>(y), c.d, c.k, slice_vecs);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

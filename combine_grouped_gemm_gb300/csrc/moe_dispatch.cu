@@ -1,0 +1,249 @@
+// Dispatch kernels: per-source histogram, exclusive scan inside each destination rank, stable
+// scatter of token rows into the rank-major receive buffer (optionally quantised to e4m3).
+//
+// Method: "7.13 Serving Mixture-of-Experts" (llm-stack-book), Expert Parallelism Mechanics,
+// dispatch step (rows for the same destination made contiguous, one row per (token, expert));
+// "One-Sided Expert-Parallel All-to-All for Mixture-of-Experts Inference over NVLink",
+// abstract (each source pushes into rank-major buffers on the target with no metadata
+// exchange first); "Serving Mixture-of-Experts", DeepEP section (FP8 E4M3 dispatch; fixed-size
+// padded receive buffers, so no count has to be exchanged or read back by the host).
+//
+// Layout: destination rank r, source rank s, a segment of cap = (T/R)*min(k, E/R) rows. Inside
+// a segment, rows are grouped by local expert (ascending) and by token index inside an expert.
+// Each source computes its own offsets, so no rank needs another rank's counts.
+#include "moe_device.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kIndexWarps = 16;
+
+// One CTA per logical source rank. Shared memory: run[16][E] (per-warp histogram, then
+// running per-warp positions), mask[16][E] (lanes of the current 32-token chunk that chose e),
+// off[E] (first row of expert e inside its segment).
+__global__ void __launch_bounds__(kIndexWarps * 32) dispatch_index_kernel(
+    const int32_t* __restrict__ topk_idx, int32_t* __restrict__ counts,
+    int32_t* __restrict__ row_of, int32_t* __restrict__ src_tok, uint32_t* status, int T, int E,
+    int k, int R, int cap) {
+  extern __shared__ int32_t smi[];
+  int32_t* run = smi;                                              // [16][E]
+  uint32_t* mask = reinterpret_cast<uint32_t*>(run + kIndexWarps * E);  // [16][E]
+  int32_t* off = reinterpret_cast<int32_t*>(mask + kIndexWarps * E);    // [E]
+
+  const int s = blockIdx.x;
+  const int Ts = T / R, Er = E / R;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = (Ts + kIndexWarps - 1) / kIndexWarps;
+  const int my0 = s * Ts + min(Ts, warp * per);
+  const int my1 = s * Ts + min(Ts, (warp + 1) * per);
+
+  for (int i = threadIdx.x; i < 2 * kIndexWarps * E; i += blockDim.x) smi[i] = 0;
+  __syncthreads();
+
+  // 1. per-warp histograms of this source's choices
+  for (int t = my0 + lane; t < my1; t += 32)
+    for (int i = 0; i < k; ++i) {
+      const int e = topk_idx[(size_t)t * k + i];
+      if (e < 0 || e >= E) {
+        raise_status(status, MOE_DEV_BOUNDS);
+        continue;
+      }
+      atomicAdd(&run[warp * E + e], 1);
+    }
+  __syncthreads();
+
+  // 2. per expert: exclusive prefix over warps (each warp's first position), total count
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int acc = 0;
+    for (int w = 0; w < kIndexWarps; ++w) {
+      const int h = run[w * E + e];
+      run[w * E + e] = acc;
+      acc += h;
+    }
+    off[e] = acc;
+    counts[(size_t)s * E + e] = acc;
+  }
+  __syncthreads();
+
+  // 3. exclusive scan of counts over experts, restarted at every destination rank
+  if (warp == 0) {
+    const int chunk = (E + 31) / 32;
+    const int a = min(E, lane * chunk), b = min(E, (lane + 1) * chunk);
+    int local = 0;
+    for (int e = a; e < b; ++e) local += off[e];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int ex = incl - local;
+    for (int e = a; e < b; ++e) {
+      const int c = off[e];
+      off[e] = ex;  // global exclusive sum for now
+      ex += c;
+    }
+  }
+  __syncthreads();
+  // rebase to the destination rank's first expert (read all bases before overwriting)
+  int base_vals[4];
+  int nb = 0;
+  for (int e = threadIdx.x; e < E && nb < 4; e += blockDim.x) base_vals[nb++] = off[(e / Er) * Er];
+  __syncthreads();
+  nb = 0;
+  for (int e = threadIdx.x; e < E && nb < 4; e += blockDim.x) off[e] -= base_vals[nb++];
+  __syncthreads();
+
+  // 4. stable positions: walk the warp's tokens in chunks of 32, one token per lane
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int base = my0; base < my1; base += 32) {
+    const int t = base + lane;
+    const bool valid = t < my1;
+    if (valid)
+      for (int i = 0; i < k; ++i) {
+        const int e = topk_idx[(size_t)t * k + i];
+        if (e >= 0 && e < E) atomicOr(&mask[warp * E + e], 1u << lane);
+      }
+    __syncwarp();
+    if (valid)
+      for (int i = 0; i < k; ++i) {
+        const int e = topk_idx[(size_t)t * k + i];
+        if (e < 0 || e >= E) {
+          row_of[(size_t)t * k + i] = -1;
+          continue;
+        }
+        const uint32_t m = mask[warp * E + e];
+        const int pos = run[warp * E + e] + __popc(m & lt);
+        const int r = e / Er;
+        const int row = (r * R + s) * cap + off[e] + pos;
+        row_of[(size_t)t * k + i] = row;
+        if (src_tok) src_tok[row] = t;
+      }
+    __syncwarp();
+    if (valid)
+      for (int i = 0; i < k; ++i) {
+        const int e = topk_idx[(size_t)t * k + i];
+        if (e < 0 || e >= E) continue;
+        const uint32_t m = mask[warp * E + e];
+        if (m != 0u && (m & lt) == 0u) {  // lowest lane that chose e in this chunk
+          run[warp * E + e] += __popc(m);
+          mask[warp * E + e] = 0u;
+        }
+      }
+    __syncwarp();
+  }
+}
+
+// bf16 payload: block (token t, column slice); each 16-byte vector of x[t] is read once and
+// written to each of the token's k receive rows.
+__global__ void __launch_bounds__(128) dispatch_copy_bf16_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ row_of, uint4* __restrict__ recv,
+    int d, int k, int slice_vecs) {
+  __shared__ int32_t rows[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+  __syncthreads();
+  const int vpr = d / 8;  // 16-byte vectors per row
+  const int v0 = blockIdx.y * slice_vecs, v1 = min(vpr, v0 + slice_vecs);
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    const uint4 val = __ldg(x + (size_t)t * vpr + v);
+    for (int i = 0; i < k; ++i) {
+      const int row = rows[i];
+      if (row >= 0) recv[(size_t)row * vpr + v] = val;
+    }
+  }
+}
+
+// e4m3 payload: 16 threads per 128-column block, 8 columns per thread. amax over the block,
+// scale = amax/448 (1 if amax is 0), code = e4m3(x / scale) with IEEE division, nearest even,
+// saturating. The codes and the scale are written to each of the token's rows.
+__global__ void __launch_bounds__(128) dispatch_copy_e4m3_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ row_of, uint2* __restrict__ recv,
+    float* __restrict__ recv_scales, int d, int k, int slice_vecs) {
+  __shared__ int32_t rows[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+  __syncthreads();
+  const int vpr = d / 8;
+  const int v0 = blockIdx.y * slice_vecs, v1 = min(vpr, v0 + slice_vecs);
+  for (int vb = v0; vb < v1; vb += blockDim.x) {
+    const int v = vb + threadIdx.x;  // v0 and blockDim are multiples of 16: groups align
+    const bool in = v < v1;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (in) raw = __ldg(x + (size_t)t * vpr + v);
+    float f[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
+                  bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j += 2) {
+      const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(
+          make_float2(__fdiv_rn(f[j], scale), __fdiv_rn(f[j + 1], scale)), __NV_SATFINITE,
+          __NV_E4M3);
+      lo |= static_cast<uint32_t>(p) << (8 * j);
+    }
+#pragma unroll
+    for (int j = 4; j < 8; j += 2) {
+      const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(
+          make_float2(__fdiv_rn(f[j], scale), __fdiv_rn(f[j + 1], scale)), __NV_SATFINITE,
+          __NV_E4M3);
+      hi |= static_cast<uint32_t>(p) << (8 * (j - 4));
+    }
+    if (in) {
+      const bool leader = (threadIdx.x & 15) == 0;
+      for (int i = 0; i < k; ++i) {
+        const int row = rows[i];
+        if (row < 0) continue;
+        recv[(size_t)row * vpr + v] = make_uint2(lo, hi);
+        if (leader) recv_scales[(size_t)row * (d / 128) + v / 16] = scale;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk_idx, void* recv,
+                            float* recv_scales, int32_t* counts, int32_t* row_of,
+                            int32_t* src_tok, cudaStream_t st) {
+  const int cap = cap_of(c);
+  cudaError_t err;
+  if (src_tok) {
+    err = cudaMemsetAsync(src_tok, 0xff, sizeof(int32_t) * (size_t)c.R * c.R * cap, st);
+    if (err != cudaSuccess) return err;
+  }
+  const size_t smem = sizeof(int32_t) * (size_t)(2 * kIndexWarps + 1) * c.E;
+  err = cudaFuncSetAttribute(dispatch_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  if (err != cudaSuccess) return err;
+  dispatch_index_kernel<<<c.R, kIndexWarps * 32, smem, st>>>(topk_idx, counts, row_of, src_tok,
+                                                             nullptr, c.T, c.E, c.k, c.R, cap);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  // Column slices so that the grid covers every SM about twice even for few tokens.
+  const int vpr = c.d / 8;
+  int nslice = 1;
+  while (c.T * nslice < 2 * 152 && vpr / (nslice * 2) >= 128) nslice *= 2;
+  int slice_vecs = (vpr + nslice - 1) / nslice;
+  slice_vecs = (slice_vecs + 15) / 16 * 16;  // whole 128-column blocks for e4m3
+  nslice = (vpr + slice_vecs - 1) / slice_vecs;
+  dim3 grid(c.T, nslice);
+  if (c.act_dtype == MOE_FP8_E4M3) {
+    dispatch_copy_e4m3_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x), row_of,
+                                                    static_cast<uint2*>(recv), recv_scales, c.d,
+                                                    c.k, slice_vecs);
+  } else {
+    dispatch_copy_bf16_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x), row_of,
+                                                    static_cast<uint4*>(recv), c.d, c.k,
+                                                    slice_vecs);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,559 @@
+// Expert FFN: device-side tile schedule from the dispatch counts, then two grouped GEMMs on
+// the 5th-generation tensor cores (tcgen05, accumulators in tensor memory, operands staged in
+// shared memory by TMA):
+//   gate/up : for the rows of each expert, g = X Wg^T and u = X Wu^T into two tensor-memory
+//             accumulators; epilogue h = bf16(silu(g) * u)
+//   down    : o = h Wd^T; epilogue bf16 rows written back at the receive-row index.
+// The shared expert is one more group whose rows are the T tokens of x.
+//
+// Method: "7.13 Serving Mixture-of-Experts" (llm-stack-book), Expert Parallelism Mechanics,
+// expert compute (one grouped GEMM over the rows each expert received, ragged groups padded
+// or masked); "One-Sided Expert-Parallel All-to-All for Mixture-of-Experts Inference over
+// NVLink", abstract (the grouped GEMMs read the rank-major receive buffers in place rather
+// than a per-expert copy); "Mixture-of-experts serving" (learn-kernels), paragraph 1 (one
+// always-active shared expert).
+//
+// GEMM shape: the weights are the M operand (128 rows of W per tile: "swap AB"), the
+// expert's rows are the N operand (a token tile of up to BN rows, N padded to a multiple of
+// 16), K is the model width (gate/up) or d_ff (down). An expert's rows lie in up to R runs of
+// the receive buffer (one per source rank); the producer gathers them row by row with 1-row
+// TMA boxes, which land in the same 128-byte-swizzled layout an 8-row box would produce.
+// Columns of a tile past its real rows hold stale shared memory; they only feed accumulator
+// columns the epilogue never stores.
+//
+// Roles in a CTA (192 threads, one CTA per SM, persistent over the unit list):
+//   warp 0      TMA producer (lane 0: weight tiles; all lanes: gathered token rows)
+//   warp 1      tensor-memory allocation; lane 0 issues tcgen05.mma and commits
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, SwiGLU, bf16 stores
+// Shared-memory stages hand over through full/empty mbarriers; the two tensor-memory
+// accumulator buffers hand over through tmem_full/tmem_empty mbarriers, so the epilogue of a
+// unit overlaps the main loop of the next. Every wait is bounded (see moe_device.cuh).
+#include <mutex>
+
+#include "moe_device.cuh"
+
+namespace moe {
+namespace {
+
+// ---------------------------------------------------------------------------------------
+// Tile schedule (one CTA)
+// ---------------------------------------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == kPlanThreads).
+__device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  __syncthreads();
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    warp_sums[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) warp_sums[32] = wi;
+  }
+  __syncthreads();
+  const int ex = warp_sums[warp] + incl - v;
+  *total = warp_sums[32];
+  __syncthreads();
+  return ex;
+}
+
+// From counts[R][E]: rows per expert, their compact offsets, the receive row of every compact
+// row (expert-major, then source rank, then position), and the list of token tiles.
+__global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
+    const int32_t* __restrict__ counts, int32_t* __restrict__ grp_n, int32_t* __restrict__ grp_off,
+    int32_t* __restrict__ n_tiles, Tile* __restrict__ tiles, int32_t* __restrict__ row_list,
+    uint32_t* status, int E, int R, int cap, int bn, int max_tiles, int tk) {
+  __shared__ int warp_sums[33];
+  __shared__ int rank_base[64];
+  const int e = threadIdx.x;
+  const bool act = e < E;
+  const int Er = E / R;
+
+  int n = 0;
+  if (act)
+    for (int s = 0; s < R; ++s) {
+      const int c = counts[(size_t)s * E + e];
+      n += c > 0 ? c : 0;
+    }
+  int total;
+  const int off = block_exclusive_scan(act ? n : 0, &total, warp_sums);
+  if (threadIdx.x == 0 && total != tk) raise_status(status, MOE_DEV_BOUNDS);
+  const int nt = act ? (n + bn - 1) / bn : 0;
+  int tiles_total;
+  const int toff = block_exclusive_scan(nt, &tiles_total, warp_sums);
+  if (act) {
+    grp_n[e] = n;
+    grp_off[e] = off;
+    for (int j = 0; j < nt; ++j) {
+      const int ti = toff + j;
+      if (ti < max_tiles) tiles[ti] = Tile{e, j * bn, min(bn, n - j * bn), 0};
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (tiles_total > max_tiles) raise_status(status, MOE_DEV_BOUNDS);
+    *n_tiles = min(tiles_total, max_tiles);
+  }
+
+  // receive rows of every compact row
+  int pre = 0;
+  for (int s = 0; s < R; ++s) {
+    const int c = act ? max(0, counts[(size_t)s * E + e]) : 0;
+    int dummy;
+    const int ex = block_exclusive_scan(c, &dummy, warp_sums);
+    if (act && e % Er == 0) rank_base[e / Er] = ex;
+    __syncthreads();
+    if (act) {
+      const int r = e / Er;
+      const int in_seg = ex - rank_base[r];
+      const int seg0 = (r * R + s) * cap;
+      for (int q = 0; q < c; ++q) {
+        const int dst = off + pre + q;
+        if (dst < tk && in_seg + q < cap) row_list[dst] = seg0 + in_seg + q;
+        else raise_status(status, MOE_DEV_BOUNDS);
+      }
+      pre += c;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Grouped GEMM
+// ---------------------------------------------------------------------------------------
+struct GemmArgs {
+  const Tile* tiles;
+  const int32_t* n_tiles;
+  const int32_t* grp_off;
+  const int32_t* row_list;
+  int tk;                 // compact rows (T*k)
+  long long recv_rows;    // receive rows (bound of gathered / scattered row indices)
+  int T;                  // shared-expert rows
+  int mt_routed;          // 128-row weight tiles per routed expert
+  int mt_shared;          // 128-row weight tiles of the shared expert (0: none)
+  int n_shared_tiles;     // token tiles of the shared expert
+  int k_steps;            // K / 64
+  int a_rows_routed;      // weight rows per routed expert
+  int a_up_routed;        // offset of the up rows (gate/up stage)
+  int a_up_shared;
+  void* out_routed;       // gate/up: h [tk][F] (compact rows); down: ebuf [recv_rows][d]
+  void* out_shared;       // gate/up: hs [T][Fs]; down: shared_out [T][d]
+  int ld_routed;          // output row length (elements)
+  int ld_shared;
+  uint32_t* status;
+};
+
+struct Unit {
+  int g;       // routed expert, or -1 for the shared expert
+  int n0, nlen, m;
+};
+
+template <int BN>
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
+  Unit r;
+  const int us = a.n_shared_tiles * a.mt_shared;
+  if (u < us) {
+    const int tt = u / a.mt_shared;
+    r.g = -1;
+    r.m = u - tt * a.mt_shared;
+    r.n0 = tt * BN;
+    r.nlen = min(BN, a.T - r.n0);
+  } else {
+    const int v = u - us;
+    const int tt = v / a.mt_routed;
+    r.m = v - tt * a.mt_routed;
+    const Tile t = a.tiles[tt];
+    r.g = t.group;
+    r.n0 = t.n0;
+    r.nlen = t.nlen;
+  }
+  return r;
+}
+
+constexpr int kThreads = 192;
+
+template <int STAGE, int BN, int STAGES>
+struct GemmShape {
+  static constexpr int NA = STAGE == 0 ? 2 : 1;    // weight tiles per stage (gate, up)
+  static constexpr int A_BYTES = 128 * 128;        // 128 rows x 64 bf16
+  static constexpr int B_BYTES = BN * 128;         // BN rows x 64 bf16
+  static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = NA * BN;         // fp32 accumulator columns per buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : 2 * ACC_COLS;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+  static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "tensor memory");
+};
+
+template <int STAGE, int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    ffn_gemm_bf16_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap mapA,
+                         const __grid_constant__ CUtensorMap mapAs,
+                         const __grid_constant__ CUtensorMap mapB,
+                         const __grid_constant__ CUtensorMap mapBs) {
+  using S = GemmShape<STAGE, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&mapA);
+    tma_prefetch_map(&mapB);
+    if (a.mt_shared) {
+      tma_prefetch_map(&mapAs);
+      tma_prefetch_map(&mapBs);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int units = a.n_shared_tiles * a.mt_shared + (*a.n_tiles) * a.mt_routed;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_x = l2_policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit t = decode_unit<BN>(a, u);
+      const bool sh = t.g < 0;
+      const CUtensorMap* amap = sh ? &mapAs : &mapA;
+      const CUtensorMap* bmap = sh ? &mapBs : &mapB;
+      const int arow0 = (sh ? 0 : t.g * a.a_rows_routed) + t.m * 128;
+      const int arow1 = arow0 + (sh ? a.a_up_shared : a.a_up_routed);
+      int brow[BN / 32];
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) {
+        const int p = lane + 32 * q;
+        int row = -1;
+        if (p < t.nlen) {
+          if (sh) {
+            row = t.n0 + p;
+          } else if (STAGE == 0) {
+            const int ci = a.grp_off[t.g] + t.n0 + p;
+            row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+            if (row >= a.recv_rows) row = -1;
+          } else {
+            row = a.grp_off[t.g] + t.n0 + p;
+            if (row < 0 || row >= a.tk) row = -1;
+          }
+        }
+        brow[q] = row;
+      }
+      // bytes the stage barrier waits for: the weight tiles plus one 128-byte row per valid
+      // token row (an out-of-range row index is skipped and reported)
+      int nvalid = 0, nbad = 0;
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) {
+        nvalid += __popc(__ballot_sync(0xffffffffu, brow[q] >= 0));
+        nbad += __popc(__ballot_sync(0xffffffffu, brow[q] < 0 && lane + 32 * q < t.nlen));
+      }
+      if (nbad && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
+      const uint32_t tx = S::NA * S::A_BYTES + 128u * static_cast<uint32_t>(nvalid);
+      for (int ks = 0; ks < a.k_steps; ++ks) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + stage * S::STAGE_BYTES;
+        uint8_t* sb = sa + S::NA * S::A_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], tx);
+          tma_load_2d(sa, amap, &full[stage], ks * 64, arow0, pol_w);
+          if (S::NA == 2) tma_load_2d(sa + S::A_BYTES, amap, &full[stage], ks * 64, arow1, pol_w);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < BN / 32; ++q)
+          if (brow[q] >= 0)
+            tma_load_2d(sb + (lane + 32 * q) * 128, bmap, &full[stage], ks * 64, brow[q], pol_x);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+        const Unit t = decode_unit<BN>(a, u);
+        const uint32_t n_pad = static_cast<uint32_t>(max(16, (t.nlen + 15) & ~15));
+        const uint32_t idesc = idesc_bf16(128, n_pad);
+        const int b = it & 1;
+        if (!mbar_wait(&tempty[b], ((it >> 1) & 1) ^ 1u, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem + b * S::ACC_COLS;
+        const uint32_t d1 = d0 + BN;
+        for (int ks = 0; ks < a.k_steps; ++ks) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_addr(smem + stage * S::STAGE_BYTES);
+          const uint32_t sb = sa + S::NA * S::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t db = smem_desc_sw128(sb + kk * 32);
+            const uint32_t acc = (ks | kk) != 0;
+            mma_f16(d0, smem_desc_sw128(sa + kk * 32), db, idesc, acc);
+            if (S::NA == 2) mma_f16(d1, smem_desc_sw128(sa + S::A_BYTES + kk * 32), db, idesc, acc);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) mma_commit(&tfull[b]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
+    const int rrow = quarter * 32 + lane;
+    int it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+      const Unit t = decode_unit<BN>(a, u);
+      const bool sh = t.g < 0;
+      const int b = it & 1;
+      if (!mbar_wait(&tfull[b], (it >> 1) & 1, abort_flag, a.status)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * S::ACC_COLS;
+      const int f = t.m * 128 + rrow;  // output column
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sh ? a.out_shared : a.out_routed);
+      const int ld = sh ? a.ld_shared : a.ld_routed;
+      for (int c0 = 0; c0 < t.nlen; c0 += 16) {
+        uint32_t ra[16], rb[16];
+        tmem_ld16(tb + c0, ra);
+        if (S::NA == 2) tmem_ld16(tb + BN + c0, rb);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int p = c0 + j;
+          if (p >= t.nlen) break;
+          long long orow;
+          if (sh) {
+            orow = t.n0 + p;
+          } else if (STAGE == 0) {
+            orow = a.grp_off[t.g] + t.n0 + p;
+            if (orow < 0 || orow >= a.tk) continue;
+          } else {
+            const int ci = a.grp_off[t.g] + t.n0 + p;
+            if (ci < 0 || ci >= a.tk) continue;
+            orow = a.row_list[ci];
+            if (orow < 0 || orow >= a.recv_rows) continue;
+          }
+          float val;
+          if (S::NA == 2) val = silu(__uint_as_float(ra[j])) * __uint_as_float(rb[j]);
+          else val = __uint_as_float(ra[j]);
+          out[orow * ld + f] = __float2bfloat16_rn(val);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[b]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Host side: tensor maps and launches
+// ---------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [rows][cols] of 16-bit (elem_bytes 2) or 8-bit elements, box of
+// box_rows rows x 128 bytes, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int elem_bytes, uint64_t cols, uint64_t rows,
+              uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * elem_bytes};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      fn(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <int STAGE, int BN, int STAGES>
+cudaError_t run_gemm(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mAs,
+                     const CUtensorMap& mB, const CUtensorMap& mBs, cudaStream_t st) {
+  using S = GemmShape<STAGE, BN, STAGES>;
+  auto kern = ffn_gemm_bf16_kernel<STAGE, BN, STAGES>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+  if (err != cudaSuccess) return err;
+  kern<<<num_sms(), kThreads, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
+                             const void* x, char* ws, cudaStream_t st) {
+  (void)x;
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
+  ffn_plan_kernel<<<1, kPlanThreads, 0, st>>>(
+      counts, reinterpret_cast<int32_t*>(ws + L.grp_n), reinterpret_cast<int32_t*>(ws + L.grp_off),
+      reinterpret_cast<int32_t*>(ws + L.n_tiles), reinterpret_cast<Tile*>(ws + L.tiles),
+      reinterpret_cast<int32_t*>(ws + L.row_list), status, c.E, c.R, cap_of(c), L.bn,
+      L.max_tiles, c.T * c.k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
+                            const float* recv_scales, const void* x, const moe_weights& w,
+                            void* ebuf, void* shared_out, char* ws, cudaStream_t st) {
+  (void)recv_scales;
+  if (c.act_dtype != MOE_BF16) return cudaErrorNotSupported;
+  const int cap = cap_of(c);
+  const long long recv_rows = (long long)c.R * c.R * cap;
+  const int F = c.d_ff, Fs = c.d_ff_shared, d = c.d, tk = c.T * c.k;
+  const bool has_shared = Fs > 0;
+
+  GemmArgs a{};
+  a.tiles = reinterpret_cast<const Tile*>(ws + L.tiles);
+  a.n_tiles = reinterpret_cast<const int32_t*>(ws + L.n_tiles);
+  a.grp_off = reinterpret_cast<const int32_t*>(ws + L.grp_off);
+  a.row_list = reinterpret_cast<const int32_t*>(ws + L.row_list);
+  a.tk = tk;
+  a.recv_rows = recv_rows;
+  a.T = c.T;
+  a.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  a.n_shared_tiles = has_shared ? (c.T + L.bn - 1) / L.bn : 0;
+
+  CUtensorMap mA, mAs, mB, mBs;
+  bool ok = true;
+  if (stage == 0) {
+    a.mt_routed = F / 128;
+    a.mt_shared = has_shared ? Fs / 128 : 0;
+    a.k_steps = d / 64;
+    a.a_rows_routed = 2 * F;
+    a.a_up_routed = F;
+    a.a_up_shared = Fs;
+    a.out_routed = ws + L.h;
+    a.out_shared = has_shared ? static_cast<void*>(ws + L.hs) : nullptr;
+    a.ld_routed = F;
+    a.ld_shared = Fs;
+    ok &= make_map(&mA, w.w13, 2, d, (uint64_t)c.E * 2 * F, 128);
+    ok &= make_map(&mB, recv, 2, d, recv_rows, 1);
+    if (has_shared) {
+      ok &= make_map(&mAs, w.ws13, 2, d, 2ull * Fs, 128);
+      ok &= make_map(&mBs, x, 2, d, c.T, 1);
+    }
+  } else {
+    a.mt_routed = d / 128;
+    a.mt_shared = has_shared ? d / 128 : 0;
+    a.k_steps = F / 64;
+    a.a_rows_routed = d;
+    a.a_up_routed = 0;
+    a.a_up_shared = 0;
+    a.out_routed = ebuf;
+    a.out_shared = shared_out;
+    a.ld_routed = d;
+    a.ld_shared = d;
+    ok &= make_map(&mA, w.w2, 2, F, (uint64_t)c.E * d, 128);
+    ok &= make_map(&mB, ws + L.h, 2, F, tk, 1);
+    if (has_shared) {
+      if (Fs != F) return cudaErrorNotSupported;  // one K loop length per launch
+      ok &= make_map(&mAs, w.ws2, 2, Fs, d, 128);
+      ok &= make_map(&mBs, ws + L.hs, 2, Fs, c.T, 1);
+    }
+  }
+  if (stage == 0 && has_shared && Fs % 128) return cudaErrorInvalidValue;
+  if (!has_shared) {
+    mAs = mA;
+    mBs = mB;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+
+  if (L.bn == 64) {
+    if (stage == 0) return run_gemm<0, 64, 5>(a, mA, mAs, mB, mBs, st);
+    return run_gemm<1, 64, 8>(a, mA, mAs, mB, mBs, st);
+  }
+  if (stage == 0) return run_gemm<0, 128, 4>(a, mA, mAs, mB, mBs, st);
+  return run_gemm<1, 128, 6>(a, mA, mAs, mB, mBs, st);
+}
+
+}  // namespace moe

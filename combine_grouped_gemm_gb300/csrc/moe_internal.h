@@ -1,0 +1,73 @@
+// Internal declarations shared by the host API (moe_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Router: d is cut into this many equal chunks, each summed as one sequential FMA chain.
+constexpr int kRouteChunks = 16;
+
+// One entry of the expert-GEMM tile schedule: rows [n0, n0+nlen) of group g.
+struct Tile {
+  int32_t group;
+  int32_t n0;
+  int32_t nlen;
+  int32_t pad;
+};
+
+// Byte offsets of the pieces of the workspace (all 256-byte aligned).
+struct WsLayout {
+  size_t status;      // uint32 status word
+  size_t partials;    // router partial dot products: fp32 [16][T][E]
+  size_t grp_n;       // int32 [E]: rows received by each routed expert
+  size_t grp_off;     // int32 [E]: first compact row of each routed expert
+  size_t n_tiles;     // int32 [1]: routed tiles in the schedule
+  size_t tiles;       // Tile [max_tiles]
+  size_t row_list;    // int32 [T*k]: receive row of each compact row
+  size_t h;           // SwiGLU intermediate of routed rows: [T*k][d_ff] (bf16 or e4m3)
+  size_t h_scales;    // e4m3: fp32 [T*k][d_ff/128]
+  size_t hs;          // shared expert intermediate: [T][d_ff_shared]
+  size_t hs_scales;   // e4m3: fp32 [T][d_ff_shared/128]
+  size_t xq;          // e4m3: quantised shared-expert input [T][d]
+  size_t xq_scales;   // e4m3: fp32 [T][d/128]
+  size_t total;
+  int bn;             // token-tile width of the expert GEMMs
+  int max_tiles;      // bound on routed tiles: E + T*k/bn
+};
+
+int validate(const moe_cfg& c);
+WsLayout ws_layout(const moe_cfg& c);
+inline int cap_of(const moe_cfg& c) {
+  int Er = c.E / c.R, Ts = c.T / c.R;
+  return Ts * (c.k < Er ? c.k : Er);
+}
+inline size_t act_bytes(const moe_cfg& c) { return c.act_dtype == MOE_FP8_E4M3 ? 1 : 2; }
+
+// Kernel launchers. Each returns the launch error (cudaSuccess when enqueued).
+cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, const float* bias,
+                         int32_t* topk_idx, float* topk_w, float* partials, uint32_t* status,
+                         cudaStream_t st);
+
+cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk_idx, void* recv,
+                            float* recv_scales, int32_t* counts, int32_t* row_of,
+                            int32_t* src_tok, cudaStream_t st);
+
+cudaError_t launch_combine(const moe_cfg& c, const void* ebuf, const int32_t* row_of,
+                           const float* topk_w, const void* shared_out, void* y,
+                           cudaStream_t st);
+
+// Expert FFN set-up: tile schedule from counts (+ e4m3 quantisation of the shared input).
+cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
+                             const void* x, char* ws, cudaStream_t st);
+
+// The two grouped GEMMs. stage: 0 = gate/up with the SwiGLU epilogue, 1 = down projection.
+cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
+                            const float* recv_scales, const void* x, const moe_weights& w,
+                            void* ebuf, void* shared_out, char* ws, cudaStream_t st);
+
+}  // namespace moe

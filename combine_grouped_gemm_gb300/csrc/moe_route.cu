@@ -1,0 +1,261 @@
+// Router kernels: fp32 gate GEMM in a fixed summation order, sigmoid affinity, per-expert bias,
+// group-limited top-k and renormalised weights.
+//
+// Method: "Mixture-of-experts serving" (learn-kernels), paragraph 1 (sigmoid affinity per expert
+// plus a per-expert bias that steers selection), paragraph 3 (group-limited routing);
+// "7.13 Serving Mixture-of-Experts" (llm-stack-book), Expert Parallelism Mechanics, router
+// step (top-k, then the chosen weights renormalised).
+//
+// Bit-exact agreement with a CPU implementation needs one fixed sequence of fp32 operations:
+//  * z = x . w: d is cut into 16 equal chunks; each chunk is a sequential fused multiply-add
+//    chain starting from 0 at the chunk's first index; the 16 partials are added by a balanced
+//    pairwise tree ((p0+p1)+(p2+p3))+... No tensor cores (their accumulation order is not
+//    specified), no split of a chunk.
+//  * e^-z: Cody-Waite range reduction n = rint(z log2 e), r = z - n ln2 (ln2 in a 9-bit head
+//    and a tail, both subtracted with fused multiply-adds), e^r by the Taylor series to degree
+//    7 in Horner form, times 2^n from exponent bits; z clamped to [-87, 87].
+//  * s = 1/(1+e^-z) with IEEE division; v = s + b; group score = top1 + top2 of v.
+//  * ties in every ranking go to the lower index; weights = (s_i / sum_j s_j) * scale with the
+//    sum taken in selection order.
+// Every operation is an explicitly rounded intrinsic (__fmaf_rn, __fadd_rn, __fmul_rn,
+// __fdiv_rn) so the compiler cannot contract or reorder it.
+#include "moe_device.cuh"
+
+namespace moe {
+namespace {
+
+// ---------------------------------------------------------------------------------------
+// Partial logits: partials[c][t][e] = sum over the c-th chunk of d of x[t][i] * w[e][i],
+// one sequential FMA chain per (c, t, e).
+// ---------------------------------------------------------------------------------------
+template <int BT, int BE, int TM, int TN>
+__global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16* __restrict__ x,
+                                                             const float* __restrict__ wg,
+                                                             float* __restrict__ partials, int T,
+                                                             int d, int E) {
+  constexpr int BK = 8;
+  static_assert((BT / TM) * (BE / TN) == 256, "256 threads");
+  __shared__ __align__(16) float xs[2][BK][BT];
+  __shared__ __align__(16) float ws[2][BK][BE];
+
+  const int tid = threadIdx.x;
+  const int tx = tid % (BE / TN), ty = tid / (BE / TN);
+  const int e0 = blockIdx.x * BE, t0 = blockIdx.y * BT, c = blockIdx.z;
+  const int L = d / kRouteChunks;
+  const int kbeg = c * L;
+  const int nsteps = L / BK;
+
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+
+  // Loaders: x rows are 8 bf16 (one uint4) per step; w rows are 8 floats (two float4).
+  auto load = [&](int buf, int step) {
+    const int k0 = kbeg + step * BK;
+    for (int r = tid; r < BT; r += 256) {
+      const int t = t0 + r;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < T) v = *reinterpret_cast<const uint4*>(x + (size_t)t * d + k0);
+      xs[buf][0][r] = bf16_lo(v.x);
+      xs[buf][1][r] = bf16_hi(v.x);
+      xs[buf][2][r] = bf16_lo(v.y);
+      xs[buf][3][r] = bf16_hi(v.y);
+      xs[buf][4][r] = bf16_lo(v.z);
+      xs[buf][5][r] = bf16_hi(v.z);
+      xs[buf][6][r] = bf16_lo(v.w);
+      xs[buf][7][r] = bf16_hi(v.w);
+    }
+    for (int q = tid; q < BE * 2; q += 256) {
+      const int r = q >> 1, half = q & 1;
+      const int e = e0 + r;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < E) v = *reinterpret_cast<const float4*>(wg + (size_t)e * d + k0 + half * 4);
+      ws[buf][half * 4 + 0][r] = v.x;
+      ws[buf][half * 4 + 1][r] = v.y;
+      ws[buf][half * 4 + 2][r] = v.z;
+      ws[buf][half * 4 + 3][r] = v.w;
+    }
+  };
+
+  load(0, 0);
+  __syncthreads();
+  for (int step = 0; step < nsteps; ++step) {
+    const int buf = step & 1;
+    if (step + 1 < nsteps) load(buf ^ 1, step + 1);
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[TM], b[TN];
+#pragma unroll
+      for (int i = 0; i < TM; ++i) a[i] = xs[buf][kk][ty * TM + i];
+#pragma unroll
+      for (int j = 0; j < TN; ++j) b[j] = ws[buf][kk][tx + j * (BE / TN)];
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int t = t0 + ty * TM + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      const int e = e0 + tx + j * (BE / TN);
+      if (e < E) partials[((size_t)c * T + t) * E + e] = acc[i][j];
+    }
+  }
+}
+
+// e^z by Cody-Waite reduction and a degree-7 Taylor polynomial (see the file comment).
+__device__ __forceinline__ float route_exp(float z) {
+  const float kLog2e = 1.44269504088896341f;
+  const float kLn2Hi = 0.693359375f;      // 355/512: 9 significant bits
+  const float kLn2Lo = -2.12194440e-4f;   // ln 2 - kLn2Hi
+  z = fminf(fmaxf(z, -87.0f), 87.0f);
+  const float n = rintf(__fmul_rn(z, kLog2e));
+  float r = __fmaf_rn(-n, kLn2Hi, z);
+  r = __fmaf_rn(-n, kLn2Lo, r);
+  float p = 1.98412698e-4f;                // 1/7!
+  p = __fmaf_rn(p, r, 1.38888889e-3f);     // 1/6!
+  p = __fmaf_rn(p, r, 8.33333333e-3f);     // 1/5!
+  p = __fmaf_rn(p, r, 4.16666667e-2f);     // 1/4!
+  p = __fmaf_rn(p, r, 1.66666667e-1f);     // 1/3!
+  p = __fmaf_rn(p, r, 0.5f);               // 1/2!
+  p = __fmaf_rn(p, r, 1.0f);               // 1/1!
+  p = __fmaf_rn(p, r, 1.0f);               // 1/0!
+  const float two_n = __int_as_float((static_cast<int>(n) + 127) << 23);
+  return __fmul_rn(p, two_n);
+}
+
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// ---------------------------------------------------------------------------------------
+// Selection: one warp per token.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) route_select_kernel(
+    const float* __restrict__ partials, const float* __restrict__ bias,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int E, int k,
+    int n_group, int topk_group, float route_scale) {
+  extern __shared__ float sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  // per warp: s[E], v[E], gscore[64], keep[64] (as floats), sel_s[32]
+  float* s = sm + (size_t)warp * (2 * E + 160);
+  float* v = s + E;
+  float* gscore = v + E;
+  float* keep = gscore + 64;
+  float* sel_s = keep + 64;
+  if (t >= T) return;
+
+  for (int e = lane; e < E; e += 32) {
+    float p[kRouteChunks];
+#pragma unroll
+    for (int c = 0; c < kRouteChunks; ++c) p[c] = partials[((size_t)c * T + t) * E + e];
+#pragma unroll
+    for (int w = kRouteChunks; w > 1; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w / 2; ++j) p[j] = __fadd_rn(p[2 * j], p[2 * j + 1]);
+    const float si = __fdiv_rn(1.0f, __fadd_rn(1.0f, route_exp(-p[0])));
+    s[e] = si;
+    v[e] = __fadd_rn(si, bias[e]);
+  }
+  __syncwarp();
+
+  const int gs = E / n_group;
+  for (int g = lane; g < n_group; g += 32) {
+    int b1 = -1, b2 = -1;
+    for (int e = g * gs; e < (g + 1) * gs; ++e) {
+      if (b1 < 0 || ranks_before(v[e], e, v[b1], b1)) {
+        b2 = b1;
+        b1 = e;
+      } else if (b2 < 0 || ranks_before(v[e], e, v[b2], b2)) {
+        b2 = e;
+      }
+    }
+    gscore[g] = (b2 >= 0) ? __fadd_rn(v[b1], v[b2]) : v[b1];
+  }
+  __syncwarp();
+  for (int g = lane; g < n_group; g += 32) {
+    int rank = 0;
+    for (int h = 0; h < n_group; ++h) rank += ranks_before(gscore[h], h, gscore[g], g) ? 1 : 0;
+    keep[g] = rank < topk_group ? 1.0f : 0.0f;
+  }
+  __syncwarp();
+
+  // k rounds of a warp-wide argmax over eligible, untaken experts.
+  uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen (E <= 1024)
+  int sel_e = -1;      // lane i (< k) keeps the i-th choice
+  for (int i = 0; i < k; ++i) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int q = 0, e = lane; e < E; ++q, e += 32) {
+      if ((taken >> q) & 1u) continue;
+      if (keep[e / gs] == 0.0f) continue;
+      if (be == 0x7fffffff || ranks_before(v[e], e, bv, be)) {
+        bv = v[e];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (oe != 0x7fffffff && (be == 0x7fffffff || ranks_before(ov, oe, bv, be))) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == i) sel_e = be;
+  }
+  // gather the chosen scores in selection order through shared memory
+  if (lane < k) sel_s[lane] = s[sel_e];
+  __syncwarp();
+  if (lane == 0) {
+    float sum = 0.0f;
+    for (int i = 0; i < k; ++i) sum = __fadd_rn(sum, sel_s[i]);
+    for (int i = 0; i < k; ++i) sel_s[i] = __fmul_rn(__fdiv_rn(sel_s[i], sum), route_scale);
+  }
+  __syncwarp();
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = sel_e;
+    topk_w[(size_t)t * k + lane] = sel_s[lane];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, const float* bias,
+                         int32_t* topk_idx, float* topk_w, float* partials, uint32_t* status,
+                         cudaStream_t st) {
+  (void)status;
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (c.T >= 2048) {
+    dim3 grid((c.E + 127) / 128, (c.T + 127) / 128, kRouteChunks);
+    route_partials_kernel<128, 128, 8, 8><<<grid, 256, 0, st>>>(xb, w_gate, partials, c.T, c.d, c.E);
+  } else {
+    dim3 grid((c.E + 63) / 64, (c.T + 63) / 64, kRouteChunks);
+    route_partials_kernel<64, 64, 4, 4><<<grid, 256, 0, st>>>(xb, w_gate, partials, c.T, c.d, c.E);
+  }
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t smem = 8 * (size_t)(2 * c.E + 160) * sizeof(float);
+  if (smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  route_select_kernel<<<(c.T + 7) / 8, 256, smem, st>>>(partials, bias, topk_idx, topk_w, c.T, c.E,
+                                                         c.k, c.n_group, c.topk_group,
+                                                         c.route_scale);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,204 @@
+/*
+ * moe.h - C ABI of libmoe: the hot path of one expert-parallel MoE layer on one GB300 GPU.
+ *
+ * The layer (router -> dispatch -> grouped SwiGLU expert GEMMs + shared expert -> combine) is
+ * the one described in "7.13 Serving Mixture-of-Experts: Expert Parallelism & All-to-All
+ * Inference" (llm-stack-book), section "Expert Parallelism Mechanics: Dispatch, Compute,
+ * Combine", with the DeepSeek-V3 router of "Mixture-of-experts serving" (learn-kernels),
+ * paragraphs 1 and 3, and the receive-buffer design of "One-Sided Expert-Parallel All-to-All
+ * for Mixture-of-Experts Inference over NVLink" (abstract): every source pushes its rows into
+ * rank-major buffers with no metadata exchange first, and the grouped GEMMs read those buffers
+ * in place. The expert-parallel ranks are logical: R partitions of this GPU's memory.
+ *
+ * Conventions for every entry point
+ *  - All array pointers are DEVICE pointers, allocated and owned by the caller. The library
+ *    allocates nothing and keeps no state between calls except cached kernel attributes and
+ *    the driver entry point it uses to encode TMA tensor maps.
+ *  - Work is enqueued on `stream` and the call returns at once (asynchronous). No call
+ *    synchronises with the host or copies device memory to the host, except
+ *    moe_read_status, which says so.
+ *  - Arrays are dense and row-major with the shapes given. bf16 is IEEE bfloat16, e4m3 is the
+ *    8-bit float with 4 exponent bits (bias 7) and 3 mantissa bits (largest finite 448).
+ *    Device pointers must be 16-byte aligned.
+ *  - Return value: MOE_OK, or an MOE_ERR_* code describing the first failed check; nothing
+ *    is enqueued when a check fails. moe_strerror() names the code.
+ *  - Errors found on the device (a wait that ran out, a bounds check) are OR-ed into a status
+ *    word at the start of the workspace `ws`; read it with moe_read_status().
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+/* Return codes */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1  /* a shape constraint failed or a required pointer is NULL */
+#define MOE_ERR_UNSUPPORTED 2  /* valid MoE shape outside what these kernels implement */
+#define MOE_ERR_MISALIGNED 3   /* a device pointer is not 16-byte aligned */
+#define MOE_ERR_CUDA 4         /* a CUDA runtime/driver call or a kernel launch failed */
+
+/* Device status bits (moe_read_status) */
+#define MOE_DEV_TIMEOUT 1u     /* a bounded wait inside a kernel gave up; outputs invalid */
+#define MOE_DEV_BOUNDS 2u      /* an index read from device memory was out of range */
+
+/* Element formats */
+#define MOE_BF16 0
+#define MOE_FP8_E4M3 1
+
+/* Number of events moe_layer records when given an event array (see moe_layer). */
+#define MOE_LAYER_EVENTS 7
+
+/* Shape of one MoE layer. Notation of the pages: T tokens of width d, E routed experts, top-k
+ * routing with n_group groups of which topk_group are kept, SwiGLU experts of width d_ff,
+ * one shared expert of width d_ff_shared, R logical expert-parallel ranks. */
+typedef struct moe_cfg {
+  int32_t T;            /* tokens in the batch, all logical ranks together; T % R == 0 */
+  int32_t d;            /* model width; d % 128 == 0 */
+  int32_t E;            /* routed experts; E % R == 0, E % n_group == 0, E <= 1024 */
+  int32_t k;            /* experts per token; 1 <= k <= min(32, topk_group * E / n_group) */
+  int32_t n_group;      /* expert groups (contiguous blocks of E/n_group experts), <= 64 */
+  int32_t topk_group;   /* groups kept per token; 1 <= topk_group <= n_group */
+  int32_t d_ff;         /* routed expert SwiGLU width; d_ff % 128 == 0 */
+  int32_t d_ff_shared;  /* shared expert width; 0 = no shared expert, else % 128 == 0 */
+  int32_t R;            /* logical ranks; expert e lives on rank e / (E/R), token t is sent by
+                           rank t / (T/R); R <= 64 */
+  float route_scale;    /* factor applied to the renormalised gate weights */
+  int32_t act_dtype;    /* dispatched activations: MOE_BF16 or MOE_FP8_E4M3 */
+  int32_t w_dtype;      /* expert weights: must equal act_dtype */
+} moe_cfg;
+
+/* Buffer sizes the caller allocates for a configuration. */
+typedef struct moe_sizes {
+  int64_t recv_rows;        /* R * R * cap rows in the receive buffer */
+  int32_t cap;              /* rows per (destination rank, source rank) segment:
+                               (T/R) * min(k, E/R), the most one source can send one rank */
+  size_t recv_bytes;        /* recv: [R][R][cap][d], bf16 (2 B) or e4m3 (1 B) elements */
+  size_t recv_scale_bytes;  /* e4m3 only: recv_scales [R][R][cap][d/128] fp32; else 0 */
+  size_t ebuf_bytes;        /* ebuf: expert outputs, bf16 [R][R][cap][d] (same rows as recv) */
+  size_t ws_bytes;          /* ws: scratch workspace (status word, router partials, tile
+                               schedule, SwiGLU intermediates) */
+} moe_sizes;
+
+/* Expert weights, K-major (the reduction dimension is contiguous).
+ *  w13  [E][2*d_ff][d]: rows 0..d_ff-1 are the gate projection, d_ff..2*d_ff-1 the up one.
+ *  w2   [E][d][d_ff]:   down projection.
+ *  ws13 [2*d_ff_shared][d], ws2 [d][d_ff_shared]: the shared expert (NULL if none).
+ *  e4m3 weights carry one fp32 scale per 128x128 block: w13_scales [E][2*d_ff/128][d/128],
+ *  w2_scales [E][d/128][d_ff/128], ws13_scales [2*d_ff_shared/128][d/128],
+ *  ws2_scales [d/128][d_ff_shared/128]; all scale pointers are NULL for bf16. */
+typedef struct moe_weights {
+  const void* w13;
+  const float* w13_scales;
+  const void* w2;
+  const float* w2_scales;
+  const void* ws13;
+  const float* ws13_scales;
+  const void* ws2;
+  const float* ws2_scales;
+} moe_weights;
+
+/* Checks a configuration. Returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED. */
+int moe_validate(const moe_cfg* cfg);
+
+/* Fills *out with the buffer sizes for cfg. Same return codes as moe_validate. */
+int moe_query_sizes(const moe_cfg* cfg, moe_sizes* out);
+
+/* Router ("Mixture-of-experts serving", paragraphs 1 and 3; "Serving Mixture-of-Experts",
+ * Expert Parallelism Mechanics, router step). For every token t:
+ *   z[e] = x[t] . w_gate[e] in fp32, summed in a fixed order: d in 16 equal chunks, each a
+ *          sequential fused multiply-add chain, the 16 partials added by a pairwise tree;
+ *   s[e] = 1 / (1 + exp(-z[e])) (exp by Cody-Waite reduction and a degree-7 Taylor series);
+ *   v[e] = s[e] + bias[e]   (the bias steers selection only);
+ *   group score = sum of the two largest v in the group; the topk_group best groups are kept;
+ *   the k best experts of the kept groups by v are chosen (ties: lower index first);
+ *   topk_w[t][i] = s[e_i] / (s[e_0] + ... + s[e_{k-1}]) * route_scale.
+ * x bf16 [T][d]; w_gate fp32 [E][d]; bias fp32 [E]; outputs topk_idx int32 [T][k] in
+ * selection order and topk_w fp32 [T][k]. ws: workspace of moe_sizes.ws_bytes. */
+int moe_route(const moe_cfg* cfg, const void* x, const float* w_gate, const float* bias,
+              int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t stream);
+
+/* Dispatch ("Serving Mixture-of-Experts", Expert Parallelism Mechanics, dispatch step;
+ * "One-Sided Expert-Parallel All-to-All...", abstract; "Serving Mixture-of-Experts", DeepEP,
+ * FP8 dispatch and fixed-size buffers). Each logical source rank s (tokens s*T/R ..) counts
+ * its rows per expert, takes exclusive sums of those counts inside each destination rank, and
+ * writes one row per (token, chosen expert) into segment (r = rank(e), s) of the receive
+ * buffer: row (r*R + s)*cap + [sum of counts[s][e'] for e' on rank r, e' < e] + [number of
+ * earlier tokens of s that chose e]. No count is exchanged before the rows are written.
+ * bf16: recv[row] = x[t]. e4m3: x[t] is quantised once per 128-column block (scale =
+ * amax/448, or 1 if amax is 0; code = e4m3(x/scale), nearest even, saturating) and written to
+ * each of its rows with recv_scales[row][d/128].
+ * Inputs x bf16 [T][d], topk_idx int32 [T][k] (entries in [0, E), distinct per token).
+ * Outputs recv (see moe_sizes), recv_scales (e4m3 only, else NULL), counts int32 [R][E],
+ * row_of int32 [T][k] (receive row of each choice), src_tok int32 [recv_rows] (token of each
+ * row, -1 for empty rows; NULL to skip). Receive rows that get no token are not written. */
+int moe_dispatch(const moe_cfg* cfg, const void* x, const int32_t* topk_idx, void* recv,
+                 float* recv_scales, int32_t* counts, int32_t* row_of, int32_t* src_tok,
+                 cudaStream_t stream);
+
+/* Expert FFNs ("Serving Mixture-of-Experts", Expert Parallelism Mechanics, expert compute: a
+ * grouped GEMM over the rows each expert received; Hot-Expert Skew section and
+ * "Mixture-of-experts serving" paragraph 1: the always-on shared expert). For every filled
+ * receive row of expert e, read in place from recv:
+ *   h = silu(row . Wgate_e^T) * (row . Wup_e^T), rounded to the activation format
+ *       (e4m3: re-quantised per 128 columns like the dispatch);
+ *   ebuf[row] = bf16(h . Wdown_e^T).
+ * The shared expert does the same for every token of x: shared_out[t] (bf16 [T][d]).
+ * counts: the dispatch's counts [R][E] (the only metadata; rows are located from it).
+ * x: bf16 [T][d], the shared expert's input (NULL when d_ff_shared == 0). For e4m3 the shared
+ * input is quantised here with the dispatch's rule. Rows of ebuf that hold no token are not
+ * written. ws: workspace (holds the tile schedule and the SwiGLU intermediates). */
+int moe_expert_ffn(const moe_cfg* cfg, const void* recv, const float* recv_scales,
+                   const int32_t* counts, const void* x, const moe_weights* w, void* ebuf,
+                   void* shared_out, void* ws, cudaStream_t stream);
+
+/* Combine ("Serving Mixture-of-Experts", Expert Parallelism Mechanics, combine step: the k
+ * partial results of a token weighted-summed by its gate weights; DeepEP section: BF16
+ * combine). y[t] = bf16( sum_i topk_w[t][i] * ebuf[row_of[t][i]] + shared_out[t] ), summed in
+ * fp32 in selection order. ebuf bf16 [recv_rows][d]; row_of int32 [T][k]; topk_w fp32
+ * [T][k]; shared_out bf16 [T][d] or NULL; y bf16 [T][d]. Passing the receive buffer as ebuf
+ * (bf16) gives route_scale * x: the identity-expert check of the dispatch/combine pair. */
+int moe_combine(const moe_cfg* cfg, const void* ebuf, const int32_t* row_of,
+                const float* topk_w, const void* shared_out, void* y, cudaStream_t stream);
+
+/* The whole layer on one stream: moe_route, moe_dispatch, moe_expert_ffn, moe_combine.
+ * Buffers as in those calls (src_tok is not produced). events: NULL, or MOE_LAYER_EVENTS
+ * created events that are recorded on `stream` before the router, after the router, after
+ * the dispatch, after the FFN set-up (schedule and shared-input quantisation), after the
+ * gate/up GEMM, after the down GEMM, and after the combine. */
+int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const float* bias,
+              const moe_weights* w, int32_t* topk_idx, float* topk_w, void* recv,
+              float* recv_scales, int32_t* counts, int32_t* row_of, void* ebuf,
+              void* shared_out, void* y, void* ws, cudaStream_t stream,
+              const cudaEvent_t* events);
+
+/* Sets the device status word in ws to 0 (enqueued on stream). */
+int moe_clear_status(void* ws, cudaStream_t stream);
+
+/* Synchronises `stream`, then copies the device status word of ws into *status (MOE_DEV_*
+ * bits). This is the one call that blocks the host. */
+int moe_read_status(const void* ws, uint32_t* status, cudaStream_t stream);
+
+/* Static name of a return code. */
+const char* moe_strerror(int code);
+
+/* MOE_ABI_VERSION of the library. */
+int moe_abi_version(void);
+
+/* The cudaError_t value behind the last MOE_ERR_CUDA returned on this host thread (0 if
+ * none). */
+int moe_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

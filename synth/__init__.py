@@ -101,6 +101,11 @@ CONFIGS = {
     # (128x128 scales).
     "dsv3_fp8_prefill": MoEConfig("dsv3_fp8_prefill", T=16384, act="fp8", w="fp8", seed=4000,
                                   **_DSV3),
+    # Profiling stand-in for the decode layer: the same per-expert shapes, 32 experts (E/R = 4
+    # per logical rank, groups of 4), so one capture holds about 3 GB on the device.
+    "dsv3_decode_e32": MoEConfig("dsv3_decode_e32", T=64, d=7168, E=32, k=8, n_group=8,
+                                 topk_group=4, d_ff=2048, d_ff_shared=2048, R=8,
+                                 route_scale=2.5, seed=1000),
 }
 SWEEP_T = [8 * m for m in (1, 2, 4, 8, 16, 32, 64, 128)]
 

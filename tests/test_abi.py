@@ -1,0 +1,97 @@
+"""The C-ABI library loads, exports every symbol include/moe.h declares, and its host-side
+checks behave; nothing here launches GPU work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from combine_grouped_gemm_gb300 import build
+    build.build()
+    import combine_grouped_gemm_gb300 as m
+    return m
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(moe):
+    names = declared_functions()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moe.EXPORTED)
+
+
+def test_abi_version_and_strerror(moe):
+    assert moe.abi_version() == 1
+    for code in range(5):
+        assert moe._lib.moe_strerror(code)
+    assert b"unknown" in moe._lib.moe_strerror(99)
+
+
+def test_workload_configs_validate(moe):
+    for c in synth.CONFIGS.values():
+        assert moe.validate(c) == 0, c.name
+
+
+@pytest.mark.parametrize("change,code", [
+    (dict(T=17), 1),                      # T % R
+    (dict(E=15), 1),                      # E % R
+    (dict(k=9), 1),                       # k > topk_group * E / n_group (16 / 1 ... with n_group 2)
+    (dict(topk_group=3), 1),              # topk_group > n_group
+    (dict(d=200), 2),                     # d % 128
+    (dict(d_ff=100), 2),                  # d_ff % 128
+    (dict(E=2048, R=2), 2),               # E > 1024
+    (dict(k=33, E=64, n_group=1), 2),     # k > 32
+    (dict(d_ff_shared=256), 2),           # shared width != routed width
+    (dict(act="fp8"), 2),                 # mixed activation / weight formats
+])
+def test_invalid_configs_are_rejected(moe, change, code):
+    import dataclasses
+    base = dataclasses.replace(synth.CONFIGS["tiny"], n_group=2, topk_group=1)
+    c = dataclasses.replace(base, **change)
+    assert moe.validate(c) == code
+
+
+def test_sizes_follow_the_layout(moe):
+    c = synth.CONFIGS["dsv3_decode"]
+    s = moe.query_sizes(c)
+    assert s["cap"] == c.cap == 64
+    assert s["recv_rows"] == c.R * c.R * c.cap
+    assert s["recv_bytes"] == s["recv_rows"] * c.d * 2 == s["ebuf_bytes"]
+    assert s["recv_scale_bytes"] == 0
+    f = synth.CONFIGS["dsv3_fp8_prefill"]
+    s8 = moe.query_sizes(f)
+    assert s8["recv_bytes"] == s8["recv_rows"] * f.d
+    assert s8["recv_scale_bytes"] == s8["recv_rows"] * (f.d // 128) * 4
+    assert s8["ebuf_bytes"] == 2 * s8["recv_bytes"]
+
+
+def test_null_and_misaligned_pointers_are_rejected_before_any_launch(moe):
+    c = moe.make_cfg(synth.CONFIGS["tiny"])
+    L = moe._lib
+    ok = 1 << 20  # an aligned fake address: never dereferenced, checks fail first
+    assert L.moe_route(ctypes.byref(c), None, ok, ok, ok, ok, ok, None) == 1
+    assert L.moe_route(ctypes.byref(c), ok + 2, ok, ok, ok, ok, ok, None) == 3
+    assert L.moe_combine(ctypes.byref(c), ok, ok, ok, ok + 8, ok, None) == 3
+    assert L.moe_dispatch(ctypes.byref(c), ok, ok, ok, None, ok, None, None, None) == 1
+    w = moe.Weights()
+    assert L.moe_expert_ffn(ctypes.byref(c), ok, None, ok, None, ctypes.byref(w), ok, None, ok,
+                            None) == 1
+    bad = moe.make_cfg(synth.CONFIGS["tiny"])
+    bad.T = 15
+    assert L.moe_layer(ctypes.byref(bad), *([ok] * 14), None, None) == 1
+    assert L.moe_read_status(None, None, None) == 1

@@ -1,0 +1,414 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle.
+
+Indices, counts, permutations and e4m3 codes must match bit for bit; gate weights within 1e-5;
+expert outputs and layer outputs within 2e-2 of max-abs error relative to the output RMS (bf16).
+Small workloads are compared element by element in full; the DeepSeek-V3-sized workloads on
+sampled tokens / rows the oracle computes one by one, plus invariants that hold at any size.
+"""
+import dataclasses
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import (bf16_to_f64, device_inputs, expert_getter, host_bits, rel_max_err,
+                      shared_host, weight_dict)
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+
+
+@functools.lru_cache(maxsize=1)
+def moe():
+    import combine_grouped_gemm_gb300 as m
+    return m
+
+
+# A small layer whose shapes span several tiles and ragged tails: 5 gate/up weight tiles,
+# 3 down tiles, a shared expert with more rows than one token tile, 3 logical ranks.
+SMALL = synth.MoEConfig("small", T=96, d=384, E=12, k=3, n_group=4, topk_group=2, d_ff=640,
+                        d_ff_shared=640, R=3, route_scale=2.5, seed=77)
+# One expert receives every token (bias +10): several token tiles of one expert.
+HOT = synth.MoEConfig("hot", T=256, d=256, E=16, k=2, n_group=1, topk_group=1, d_ff=256,
+                      d_ff_shared=256, R=2, route_scale=1.0, seed=5)
+
+_cache = {}
+
+
+def inputs(cfg):
+    """Device inputs for cfg; keeps only the most recent large weight set alive."""
+    key = (cfg.name, cfg.seed, cfg.T, cfg.bias)
+    if key not in _cache:
+        big = cfg.d * cfg.d_ff * cfg.E > 10 ** 8
+        if big:
+            for k in [k for k in _cache if _cache[k][2]]:
+                del _cache[k]
+            torch.cuda.empty_cache()
+        inp, W = device_inputs(cfg)
+        if cfg.name == "hot":
+            inp["bias"][3] = 10.0
+        _cache[key] = (inp, W, big)
+    return _cache[key][0], _cache[key][1]
+
+
+def run_stages(cfg, inp, W, src_tok=True):
+    m = moe()
+    b = m.Buffers(cfg)
+    m.clear_status(b["ws"])
+    m.route(cfg, inp["x"], inp["w_gate"], inp["bias"], b["topk_idx"], b["topk_w"], b["ws"])
+    st = None
+    if src_tok:
+        st = torch.empty(b.sizes["recv_rows"], dtype=torch.int32, device="cuda")
+    m.dispatch(cfg, inp["x"], b["topk_idx"], b["recv"], b["recv_scales"], b["counts"],
+               b["row_of"], st)
+    out = dict(b)
+    out["src_tok"] = st
+    return out
+
+
+def oracle_route(cfg, inp, tokens=None):
+    x = host_bits(inp["x"])
+    if tokens is not None:
+        x = x[tokens]
+    return oracle.route(x, inp["w_gate"].cpu().numpy(), inp["bias"].cpu().numpy(), cfg.k,
+                        cfg.n_group, cfg.topk_group, cfg.route_scale)
+
+
+# ------------------------------------------------------------------------------------------
+# Router
+# ------------------------------------------------------------------------------------------
+ROUTE_FULL = [synth.CONFIGS["tiny"], SMALL, HOT, synth.CONFIGS["dsv3_decode"],
+              synth.CONFIGS["dsv3_sweep"].with_T(8), synth.CONFIGS["dsv3_sweep"].with_T(1024)]
+
+
+@pytest.mark.parametrize("cfg", ROUTE_FULL, ids=lambda c: c.name)
+def test_route_bit_exact(cfg):
+    inp, W = inputs(cfg)
+    r = run_stages(cfg, inp, W)
+    idx, w = oracle_route(cfg, inp)
+    assert np.array_equal(r["topk_idx"].cpu().numpy(), idx)
+    assert np.abs(r["topk_w"].cpu().numpy() - w).max() <= 1e-5
+    assert np.array_equal(r["topk_w"].cpu().numpy(), w)   # same op sequence: exact
+
+
+@pytest.mark.parametrize("name", ["dsv3_skew_prefill", "dsv3_fp8_prefill"])
+def test_route_bit_exact_sampled_large(name):
+    cfg = synth.CONFIGS[name]
+    inp = synth.make_router_inputs(cfg, "cuda")
+    m = moe()
+    ws = torch.zeros(m.query_sizes(cfg)["ws_bytes"], dtype=torch.uint8, device="cuda")
+    idx_d = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device="cuda")
+    w_d = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device="cuda")
+    m.route(cfg, inp["x"], inp["w_gate"], inp["bias"], idx_d, w_d, ws)
+    rng = np.random.default_rng(cfg.seed)
+    tokens = np.unique(np.concatenate([[0, cfg.T - 1], rng.choice(cfg.T, 254, replace=False)]))
+    idx, w = oracle_route(cfg, inp, tokens)
+    assert np.array_equal(idx_d.cpu().numpy()[tokens], idx)
+    assert np.abs(w_d.cpu().numpy()[tokens] - w).max() <= 1e-5
+    if cfg.bias == "zipf":   # the skew recipe: hottest expert about 10x the mean load
+        c = np.bincount(idx_d.cpu().numpy().reshape(-1), minlength=cfg.E)
+        assert 8.0 <= c.max() / c.mean() <= 12.0
+
+
+# ------------------------------------------------------------------------------------------
+# Dispatch
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg", ROUTE_FULL, ids=lambda c: c.name)
+def test_dispatch_bit_exact(cfg):
+    inp, W = inputs(cfg)
+    r = run_stages(cfg, inp, W)
+    idx = r["topk_idx"].cpu().numpy()
+    counts, _, row_of, src_tok = oracle.dispatch_index(oracle_route(cfg, inp)[0], cfg.E, cfg.R)
+    assert np.array_equal(r["counts"].cpu().numpy(), counts)
+    assert np.array_equal(r["row_of"].cpu().numpy(), row_of)
+    assert np.array_equal(r["src_tok"].cpu().numpy(), src_tok)
+    recv = host_bits(r["recv"])
+    ref, _ = oracle.dispatch_payload(host_bits(inp["x"]), row_of, src_tok.size)
+    filled = src_tok >= 0
+    assert np.array_equal(recv[filled], ref[filled])
+    assert counts.sum() == cfg.T * cfg.k and idx.shape == (cfg.T, cfg.k)
+
+
+def test_dispatch_given_topk_matches_oracle():
+    """Dispatch alone on seeded random choices (not produced by the router)."""
+    cfg = SMALL
+    rng = np.random.default_rng(3)
+    ti = np.stack([rng.permutation(cfg.E)[:cfg.k] for _ in range(cfg.T)]).astype(np.int32)
+    inp, _ = inputs(cfg)
+    m = moe()
+    b = m.Buffers(cfg)
+    st = torch.empty(b.sizes["recv_rows"], dtype=torch.int32, device="cuda")
+    m.dispatch(cfg, inp["x"], torch.from_numpy(ti).cuda(), b["recv"], None, b["counts"],
+               b["row_of"], st)
+    counts, _, row_of, src_tok = oracle.dispatch_index(ti, cfg.E, cfg.R)
+    assert np.array_equal(b["counts"].cpu().numpy(), counts)
+    assert np.array_equal(b["row_of"].cpu().numpy(), row_of)
+    assert np.array_equal(st.cpu().numpy(), src_tok)
+
+
+FP8_SMALL = dataclasses.replace(SMALL, name="small_fp8", act="fp8", w="fp8", d=512, d_ff=256,
+                                d_ff_shared=256)
+
+
+def test_dispatch_e4m3_codes_and_scales_bit_exact():
+    cfg = FP8_SMALL
+    inp = synth.make_router_inputs(cfg, "cuda")
+    m = moe()
+    b = m.Buffers(cfg)
+    m.route(cfg, inp["x"], inp["w_gate"], inp["bias"], b["topk_idx"], b["topk_w"], b["ws"])
+    m.dispatch(cfg, inp["x"], b["topk_idx"], b["recv"], b["recv_scales"], b["counts"],
+               b["row_of"], None)
+    idx, _ = oracle_route(cfg, inp)
+    assert np.array_equal(b["topk_idx"].cpu().numpy(), idx)
+    _, _, row_of, src_tok = oracle.dispatch_index(idx, cfg.E, cfg.R)
+    q, sc = oracle.dispatch_payload(host_bits(inp["x"]), row_of, src_tok.size, fp8=True)
+    filled = src_tok >= 0
+    assert np.array_equal(b["recv"].cpu().numpy()[filled], q[filled])
+    assert np.array_equal(b["recv_scales"].cpu().numpy()[filled], sc[filled])
+
+
+@pytest.mark.parametrize("name", ["dsv3_skew_prefill", "dsv3_fp8_prefill"])
+def test_dispatch_invariants_large(name):
+    """At full size: the permutation is the unique stable rank-major layout of the routing,
+    and sampled receive rows hold their token's row (bf16) or its e4m3 codes."""
+    cfg = synth.CONFIGS[name]
+    inp = synth.make_router_inputs(cfg, "cuda")
+    m = moe()
+    b = m.Buffers(cfg)
+    st = torch.empty(b.sizes["recv_rows"], dtype=torch.int32, device="cuda")
+    m.route(cfg, inp["x"], inp["w_gate"], inp["bias"], b["topk_idx"], b["topk_w"], b["ws"])
+    m.dispatch(cfg, inp["x"], b["topk_idx"], b["recv"], b["recv_scales"], b["counts"],
+               b["row_of"], st)
+    ti = b["topk_idx"].cpu().numpy().astype(np.int64)
+    ro = b["row_of"].cpu().numpy().astype(np.int64)
+    counts = b["counts"].cpu().numpy()
+    src = st.cpu().numpy()
+    T, k, E, R = cfg.T, cfg.k, cfg.E, cfg.R
+    Ts, Er, cap = cfg.T_s, cfg.E_r, cfg.cap
+    assert counts.sum() == T * k
+    assert len(np.unique(ro)) == T * k                      # injective
+    tok = np.repeat(np.arange(T), k)
+    assert np.array_equal(src[ro.reshape(-1)], tok)          # src_tok inverts row_of
+    assert (src >= 0).sum() == T * k
+    s_of = tok // Ts
+    e_of = ti.reshape(-1)
+    r_of = e_of // Er
+    seg = ro.reshape(-1) // cap
+    assert np.array_equal(seg, r_of * R + s_of)              # right (destination, source) segment
+    # inside a segment: expert-major (ascending), token ascending, packed from 0
+    exp_cnt = np.zeros((R, E), np.int64)
+    np.add.at(exp_cnt, (s_of, e_of), 1)
+    assert np.array_equal(exp_cnt, counts)
+    ex = np.cumsum(counts.reshape(R, R, Er), axis=2) - counts.reshape(R, R, Er)
+    first = ex.reshape(R, E)[s_of, e_of]
+    order = np.lexsort((tok, e_of, seg))
+    pos = np.empty(T * k, np.int64)
+    run = np.zeros((R, E), np.int64)
+    for j in order:                                          # ranks by token inside (s, e)
+        pos[j] = run[s_of[j], e_of[j]]
+        run[s_of[j], e_of[j]] += 1
+    assert np.array_equal(ro.reshape(-1) % cap, first + pos)
+    rng = np.random.default_rng(1)
+    rows = rng.choice(T * k, 64, replace=False)
+    x = host_bits(inp["x"])
+    if cfg.act == "fp8":
+        toks = tok[rows]
+        q, sc = oracle.quant_rows_e4m3(oracle.bf16_to_f32(x[toks]))
+        assert np.array_equal(b["recv"][ro.reshape(-1)[rows]].cpu().numpy(), q)
+        assert np.array_equal(b["recv_scales"][ro.reshape(-1)[rows]].cpu().numpy(), sc)
+    else:
+        assert np.array_equal(host_bits(b["recv"][ro.reshape(-1)[rows]]), x[tok[rows]])
+
+
+# ------------------------------------------------------------------------------------------
+# Combine
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, synth.CONFIGS["dsv3_decode"]],
+                         ids=lambda c: c.name)
+def test_combine_identity_experts_give_scaled_x(cfg):
+    inp, W = inputs(cfg)
+    r = run_stages(cfg, inp, W)
+    m = moe()
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    m.combine(cfg, r["recv"], r["row_of"], r["topk_w"], None, y)
+    x = bf16_to_f64(host_bits(inp["x"]))
+    yf = bf16_to_f64(host_bits(y))
+    assert np.all(np.abs(yf - cfg.route_scale * x) <= 2 ** -7 * np.abs(cfg.route_scale * x) + 1e-30)
+    ref = oracle.combine(host_bits(r["recv"]), r["row_of"].cpu().numpy(), r["topk_w"].cpu().numpy())
+    assert np.abs(host_bits(y).astype(np.int32) - ref.astype(np.int32)).max() <= 1
+
+
+def test_combine_with_shared_matches_oracle():
+    cfg = SMALL
+    inp, W = inputs(cfg)
+    r = run_stages(cfg, inp, W)
+    g = torch.Generator().manual_seed(4)
+    ebuf = (torch.randn(r["ebuf"].shape, generator=g) * 0.5).to(torch.bfloat16).cuda()
+    sh = torch.randn((cfg.T, cfg.d), generator=g).to(torch.bfloat16).cuda()
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    moe().combine(cfg, ebuf, r["row_of"], r["topk_w"], sh, y)
+    ref = oracle.combine(host_bits(ebuf), r["row_of"].cpu().numpy(), r["topk_w"].cpu().numpy(),
+                         host_bits(sh))
+    assert np.abs(host_bits(y).astype(np.int32) - ref.astype(np.int32)).max() <= 1
+
+
+# ------------------------------------------------------------------------------------------
+# Expert FFN and the whole layer
+# ------------------------------------------------------------------------------------------
+def _ffn(cfg, inp, W, r):
+    m = moe()
+    m.expert_ffn(cfg, r["recv"], r["recv_scales"], r["counts"], inp["x"], weight_dict(W),
+                 r["ebuf"], r["shared_out"], r["ws"])
+    return r
+
+
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, HOT], ids=lambda c: c.name)
+def test_expert_ffn_every_row(cfg):
+    inp, W = inputs(cfg)
+    r = _ffn(cfg, inp, W, run_stages(cfg, inp, W))
+    assert moe().read_status(r["ws"]) == 0
+    src = r["src_tok"].cpu().numpy()
+    ti = r["topk_idx"].cpu().numpy()
+    ro = r["row_of"].cpu().numpy()
+    x = host_bits(inp["x"])
+    eb = host_bits(r["ebuf"])
+    get = expert_getter(W, False)
+    worst = 0.0
+    for e in range(cfg.E):
+        Wt = get(e)
+        for t, i in zip(*np.nonzero(ti == e)):
+            ref, _ = oracle.swiglu_row_bf16(x[t], Wt["w13"], Wt["w2"])
+            worst = max(worst, rel_max_err(bf16_to_f64(eb[ro[t, i]]), bf16_to_f64(ref)))
+            assert src[ro[t, i]] == t
+    assert worst <= TOL_BF16, worst
+    if cfg.d_ff_shared:
+        S = shared_host(W, False)
+        sh = host_bits(r["shared_out"])
+        for t in range(cfg.T):
+            ref, _ = oracle.swiglu_row_bf16(x[t], S["ws13"], S["ws2"])
+            assert rel_max_err(bf16_to_f64(sh[t]), bf16_to_f64(ref)) <= TOL_BF16
+
+
+def _layer_tokens_check(cfg, tokens, inp, W, y):
+    ref = oracle.layer_tokens(cfg, host_bits(inp["x"]), inp["w_gate"].cpu().numpy(),
+                              inp["bias"].cpu().numpy(), expert_getter(W, cfg.w == "fp8"),
+                              shared_host(W, cfg.w == "fp8"), tokens)
+    got = bf16_to_f64(host_bits(y)[tokens])
+    err = rel_max_err(got, bf16_to_f64(ref["y"]))
+    return err
+
+
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, HOT], ids=lambda c: c.name)
+def test_layer_all_tokens(cfg):
+    inp, W = inputs(cfg)
+    lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y = lay(inp["x"])
+    assert moe().read_status(lay.bufs["ws"]) == 0
+    assert _layer_tokens_check(cfg, np.arange(cfg.T), inp, W, y) <= TOL_BF16
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg,n", [(synth.CONFIGS["dsv3_decode"], 4),
+                                   (synth.CONFIGS["dsv3_sweep"].with_T(8), 8),
+                                   (synth.CONFIGS["dsv3_sweep"].with_T(1024), 3)],
+                         ids=lambda v: getattr(v, "name", str(v)))
+def test_layer_dsv3_sampled_tokens(cfg, n):
+    inp, W = inputs(cfg)
+    lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y = lay(inp["x"])
+    assert moe().read_status(lay.bufs["ws"]) == 0
+    rng = np.random.default_rng(cfg.T)
+    tokens = np.sort(rng.choice(cfg.T, n, replace=False))
+    assert _layer_tokens_check(cfg, tokens, inp, W, y) <= TOL_BF16
+
+
+@pytest.mark.slow
+def test_layer_skew_prefill_hot_expert_rows():
+    """The skewed prefill: tokens of the hottest expert (many token tiles) and a few others."""
+    cfg = synth.CONFIGS["dsv3_skew_prefill"]
+    inp, W = inputs(cfg)
+    lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y = lay(inp["x"])
+    assert moe().read_status(lay.bufs["ws"]) == 0
+    ti = lay.bufs["topk_idx"].cpu().numpy()
+    hot = int(np.bincount(ti.reshape(-1), minlength=cfg.E).argmax())
+    hot_tokens = np.nonzero((ti == hot).any(1))[0]
+    tokens = np.unique(np.concatenate([hot_tokens[[0, len(hot_tokens) // 2, -1]], [5]]))
+    assert _layer_tokens_check(cfg, tokens, inp, W, y) <= TOL_BF16
+
+
+def test_layer_equals_stage_calls_and_is_deterministic():
+    cfg = SMALL
+    inp, W = inputs(cfg)
+    lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y1 = lay(inp["x"]).clone()
+    y2 = lay(inp["x"]).clone()
+    assert torch.equal(y1, y2)
+    r = _ffn(cfg, inp, W, run_stages(cfg, inp, W))
+    y3 = torch.empty_like(y1)
+    moe().combine(cfg, r["ebuf"], r["row_of"], r["topk_w"], r["shared_out"], y3)
+    assert torch.equal(y1, y3)
+
+
+def test_layer_events_are_recorded_in_order():
+    cfg = SMALL
+    inp, W = inputs(cfg)
+    lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(moe().MOE_LAYER_EVENTS)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    lay(inp["x"], events=evs)
+    torch.cuda.synchronize()
+    times = [evs[0].elapsed_time(e) for e in evs]
+    assert all(b >= a for a, b in zip(times, times[1:]))
+
+
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL], ids=lambda c: c.name)
+def test_gate_up_intermediate_and_schedule(cfg):
+    """The expert schedule (compact rows expert-major, then source rank, then position) and the
+    SwiGLU intermediate h of every compact row, before the down projection."""
+    from gpu_util import ws_offsets
+    inp, W = inputs(cfg)
+    r = _ffn(cfg, inp, W, run_stages(cfg, inp, W))
+    o = ws_offsets(cfg)
+    ws = r["ws"]
+    tk = cfg.T * cfg.k
+    grp_n = ws[o["grp_n"]:o["grp_n"] + 4 * cfg.E].view(torch.int32).cpu().numpy()
+    grp_off = ws[o["grp_off"]:o["grp_off"] + 4 * cfg.E].view(torch.int32).cpu().numpy()
+    row_list = ws[o["row_list"]:o["row_list"] + 4 * tk].view(torch.int32).cpu().numpy()
+    counts = r["counts"].cpu().numpy()
+    assert np.array_equal(grp_n, counts.sum(0))
+    assert np.array_equal(grp_off, np.cumsum(grp_n) - grp_n)
+    src = r["src_tok"].cpu().numpy()
+    ti = r["topk_idx"].cpu().numpy()
+    # expected compact order: expert, then source rank, then token
+    exp_rows = []
+    for e in range(cfg.E):
+        toks = [t for t in range(cfg.T) if e in ti[t]]
+        ro = r["row_of"].cpu().numpy()
+        exp_rows += [int(ro[t, list(ti[t]).index(e)]) for t in toks]
+    assert np.array_equal(row_list, np.array(exp_rows, dtype=np.int32))
+    h = ws[o["h"]:o["h"] + 2 * tk * cfg.d_ff].view(torch.bfloat16).view(tk, cfg.d_ff)
+    h = bf16_to_f64(host_bits(h))
+    x = host_bits(inp["x"])
+    get = expert_getter(W, False)
+    worst = 0.0
+    for e in range(cfg.E):
+        Wt = get(e)
+        for p in range(grp_n[e]):
+            c = grp_off[e] + p
+            t = src[row_list[c]]
+            _, href = oracle.swiglu_row_bf16(x[t], Wt["w13"], Wt["w2"])
+            err = rel_max_err(h[c], href)
+            if err > TOL_BF16:   # diagnostics: which reference row does it look like?
+                best = min(range(cfg.T), key=lambda tt: rel_max_err(
+                    h[c], oracle.swiglu_row_bf16(x[tt], Wt["w13"], Wt["w2"])[1]))
+                print(f"h mismatch e={e} p={p} t={t} err={err:.3e} closest token={best} "
+                      f"got[:6]={h[c][:6]} ref[:6]={href[:6]}")
+            worst = max(worst, err)
+    assert worst <= TOL_BF16, worst
