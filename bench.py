@@ -165,6 +165,20 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest value over all ranks (the job is as slow as its slowest replica)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(T: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own T tokens per step."""
+    return T * world / (ms_per_step * 1e-3)
+
+
 # ------------------------------------------------------------------------------------------
 # Our arm
 # ------------------------------------------------------------------------------------------
@@ -221,11 +235,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     for row in evs:
         for j, n in enumerate(moe.STAGE_NAMES):
             stage_ms[n] += row[j].elapsed_time(row[j + 1]) / args.steps
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dev)
 
     # end to end through the public API: pinned host buffers, copies inside the timed region
     x_host = inp["x"].cpu().pin_memory()
@@ -242,11 +252,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
 
     counts = lay.bufs["counts"].cpu().numpy()
     return dict(ms=ms_max, ms_local=ms, stage_ms=stage_ms, clocks=clk, ms_e2e=ms_e2e,
@@ -317,7 +323,7 @@ def main():
                 "traffic": measured_traffic(dom, cfg.name),
                 "algorithmic_bytes_per_launch": b[dom], "launch_ms": round(dom_ms, 4)}
         layer_bytes = sum(b.values())
-        tokens_per_s = cfg.T * world / (r["ms"] * 1e-3)
+        tokens_per_s = job_tokens_per_s(cfg.T, world, r["ms"])
         out = {
             "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -337,7 +343,7 @@ def main():
             "roofline": roof,
             "gpu_launches": KERNELS_PER_STEP * args.steps,
             "clocks": r["clocks"],
-            "e2e": {"value": round(cfg.T * world / (r["ms_e2e"] * 1e-3), 1), "unit": "tokens/s",
+            "e2e": {"value": round(job_tokens_per_s(cfg.T, world, r["ms_e2e"]), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
                     "ms_per_step": round(r["ms_e2e"], 5)},
         }

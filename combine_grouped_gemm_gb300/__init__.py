@@ -4,7 +4,7 @@ Argument marshalling only: every function below passes device pointers of torch 
 and the current CUDA stream to the C ABI declared in include/moe.h, and raises MoEError on a
 non-zero return code. All the work runs in the library's CUDA kernels; there is no fallback.
 If the shared library is missing, importing this package raises at once: build it with
-``python -m combine_grouped_gemm_gb300.build``.
+``python combine_grouped_gemm_gb300/build.py``.
 """
 from __future__ import annotations
 
@@ -53,7 +53,7 @@ class Weights(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libmoe.so not found at {LIB_PATH}; build it with "
-                          "`python -m combine_grouped_gemm_gb300.build`")
+                          "`python combine_grouped_gemm_gb300/build.py`")
     L = ctypes.CDLL(LIB_PATH)
     P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
     sigs = {

@@ -1,7 +1,7 @@
 """Builds libmoe.so in-tree (combine_grouped_gemm_gb300/_lib/) with nvcc for sm_103a.
 
 Each .cu file under csrc/ is compiled in parallel, then linked into one shared library with
-the shared CUDA runtime. Run: python -m combine_grouped_gemm_gb300.build
+the shared CUDA runtime. Run: python combine_grouped_gemm_gb300/build.py [--force] [-v]
 """
 from __future__ import annotations
 

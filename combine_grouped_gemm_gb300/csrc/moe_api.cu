@@ -47,7 +47,9 @@ WsLayout ws_layout(const moe_cfg& c) {
   const size_t tk = (size_t)c.T * c.k;
   const size_t ab = act_bytes(c);
   const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
-  L.bn = (tk >= (size_t)64 * c.E) ? 128 : 64;
+  // token tile: 128 rows for e4m3 (the token rows are the M operand there) and for bf16 when
+  // experts average 64 rows or more; 64 otherwise
+  L.bn = (fp8 || tk >= (size_t)64 * c.E) ? 128 : 64;
   L.max_tiles = c.E + (int)((tk + L.bn - 1) / L.bn);
   size_t o = 0;
   L.status = o;     o = up256(o + 16);
@@ -187,7 +189,6 @@ int moe_expert_ffn(const moe_cfg* cfg, const void* recv, const float* recv_scale
       MOE_NEED(w->ws2_scales);
     }
   }
-  if (fp8) return MOE_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(c);
   char* wsp = static_cast<char*>(ws);
   cudaError_t e = launch_ffn_setup(c, L, counts, x, wsp, stream);
@@ -246,7 +247,6 @@ int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const floa
       MOE_NEED(w->ws2_scales);
     }
   }
-  if (fp8) return MOE_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(c);
   char* wsp = static_cast<char*>(ws);
   auto rec = [&](int i) -> cudaError_t {

@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(128) dispatch_copy_e4m3_kernel(
     float* __restrict__ recv_scales, int d, int k, int slice_vecs) {
   __shared__ int32_t rows[32];
   const int t = blockIdx.x;
-  if (threadIdx.x < k) rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+  // row_of == nullptr: quantise token t into row t (the shared expert's input)
+  if (threadIdx.x < k) rows[threadIdx.x] = row_of ? row_of[(size_t)t * k + threadIdx.x] : t;
   __syncthreads();
   const int vpr = d / 8;
   const int v0 = blockIdx.y * slice_vecs, v1 = min(vpr, v0 + slice_vecs);
@@ -206,7 +207,28 @@ __global__ void __launch_bounds__(128) dispatch_copy_e4m3_kernel(
   }
 }
 
+// Column slices so that the grid covers every SM about twice even for few tokens; slices are
+// whole 128-column blocks.
+void copy_grid(int T, int d, int* nslice_out, int* slice_vecs_out) {
+  const int vpr = d / 8;
+  int nslice = 1;
+  while (T * nslice < 2 * 152 && vpr / (nslice * 2) >= 128) nslice *= 2;
+  int slice_vecs = (vpr + nslice - 1) / nslice;
+  slice_vecs = (slice_vecs + 15) / 16 * 16;
+  *slice_vecs_out = slice_vecs;
+  *nslice_out = (vpr + slice_vecs - 1) / slice_vecs;
+}
+
 }  // namespace
+
+cudaError_t launch_quant_rows_e4m3(const void* x, int T, int d, void* out, float* scales,
+                                   cudaStream_t st) {
+  int nslice, slice_vecs;
+  copy_grid(T, d, &nslice, &slice_vecs);
+  dispatch_copy_e4m3_kernel<<<dim3(T, nslice), 128, 0, st>>>(
+      static_cast<const uint4*>(x), nullptr, static_cast<uint2*>(out), scales, d, 1, slice_vecs);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk_idx, void* recv,
                             float* recv_scales, int32_t* counts, int32_t* row_of,
@@ -226,13 +248,8 @@ cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
-  // Column slices so that the grid covers every SM about twice even for few tokens.
-  const int vpr = c.d / 8;
-  int nslice = 1;
-  while (c.T * nslice < 2 * 152 && vpr / (nslice * 2) >= 128) nslice *= 2;
-  int slice_vecs = (vpr + nslice - 1) / nslice;
-  slice_vecs = (slice_vecs + 15) / 16 * 16;  // whole 128-column blocks for e4m3
-  nslice = (vpr + slice_vecs - 1) / slice_vecs;
+  int nslice, slice_vecs;
+  copy_grid(c.T, c.d, &nslice, &slice_vecs);
   dim3 grid(c.T, nslice);
   if (c.act_dtype == MOE_FP8_E4M3) {
     dispatch_copy_e4m3_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x), row_of,

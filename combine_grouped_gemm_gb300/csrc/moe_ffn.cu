@@ -409,8 +409,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int STAGE, int BN, int STAGES>
+cudaError_t run_gemm(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mAs,
+                     const CUtensorMap& mB, const CUtensorMap& mBs, cudaStream_t st) {
+  using S = GemmShape<STAGE, BN, STAGES>;
+  auto kern = ffn_gemm_bf16_kernel<STAGE, BN, STAGES>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+  if (err != cudaSuccess) return err;
+  kern<<<sm_count(), kThreads, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 // ---------------------------------------------------------------------------------------
-// Host side: tensor maps and launches
+// Host side: tensor maps
 // ---------------------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -433,7 +447,7 @@ EncodeTiledFn encode_fn() {
 
 // 2-D row-major tensor [rows][cols] of 16-bit (elem_bytes 2) or 8-bit elements, box of
 // box_rows rows x 128 bytes, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int elem_bytes, uint64_t cols, uint64_t rows,
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t cols, uint64_t rows,
               uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -449,30 +463,21 @@ bool make_map(CUtensorMap* m, const void* base, int elem_bytes, uint64_t cols, u
   return r == CUDA_SUCCESS;
 }
 
-int num_sms() {
+int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   return n > 0 ? n : 1;
 }
 
-template <int STAGE, int BN, int STAGES>
-cudaError_t run_gemm(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mAs,
-                     const CUtensorMap& mB, const CUtensorMap& mBs, cudaStream_t st) {
-  using S = GemmShape<STAGE, BN, STAGES>;
-  auto kern = ffn_gemm_bf16_kernel<STAGE, BN, STAGES>;
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-  if (err != cudaSuccess) return err;
-  kern<<<num_sms(), kThreads, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
-  return cudaGetLastError();
-}
-
-}  // namespace
 
 cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
                              const void* x, char* ws, cudaStream_t st) {
-  (void)x;
+  if (c.act_dtype == MOE_FP8_E4M3 && c.d_ff_shared) {
+    const cudaError_t err = launch_quant_rows_e4m3(x, c.T, c.d, ws + L.xq,
+                                                   reinterpret_cast<float*>(ws + L.xq_scales), st);
+    if (err != cudaSuccess) return err;
+  }
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
   ffn_plan_kernel<<<1, kPlanThreads, 0, st>>>(
       counts, reinterpret_cast<int32_t*>(ws + L.grp_n), reinterpret_cast<int32_t*>(ws + L.grp_off),
@@ -485,8 +490,8 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
 cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                             const float* recv_scales, const void* x, const moe_weights& w,
                             void* ebuf, void* shared_out, char* ws, cudaStream_t st) {
-  (void)recv_scales;
-  if (c.act_dtype != MOE_BF16) return cudaErrorNotSupported;
+  if (c.act_dtype == MOE_FP8_E4M3)
+    return launch_ffn_gemm_e4m3(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st);
   const int cap = cap_of(c);
   const long long recv_rows = (long long)c.R * c.R * cap;
   const int F = c.d_ff, Fs = c.d_ff_shared, d = c.d, tk = c.T * c.k;
@@ -516,11 +521,11 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
     a.out_shared = has_shared ? static_cast<void*>(ws + L.hs) : nullptr;
     a.ld_routed = F;
     a.ld_shared = Fs;
-    ok &= make_map(&mA, w.w13, 2, d, (uint64_t)c.E * 2 * F, 128);
-    ok &= make_map(&mB, recv, 2, d, recv_rows, 1);
+    ok &= make_tensor_map_2d(&mA, w.w13, 2, d, (uint64_t)c.E * 2 * F, 128);
+    ok &= make_tensor_map_2d(&mB, recv, 2, d, recv_rows, 1);
     if (has_shared) {
-      ok &= make_map(&mAs, w.ws13, 2, d, 2ull * Fs, 128);
-      ok &= make_map(&mBs, x, 2, d, c.T, 1);
+      ok &= make_tensor_map_2d(&mAs, w.ws13, 2, d, 2ull * Fs, 128);
+      ok &= make_tensor_map_2d(&mBs, x, 2, d, c.T, 1);
     }
   } else {
     a.mt_routed = d / 128;
@@ -533,12 +538,12 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
     a.out_shared = shared_out;
     a.ld_routed = d;
     a.ld_shared = d;
-    ok &= make_map(&mA, w.w2, 2, F, (uint64_t)c.E * d, 128);
-    ok &= make_map(&mB, ws + L.h, 2, F, tk, 1);
+    ok &= make_tensor_map_2d(&mA, w.w2, 2, F, (uint64_t)c.E * d, 128);
+    ok &= make_tensor_map_2d(&mB, ws + L.h, 2, F, tk, 1);
     if (has_shared) {
       if (Fs != F) return cudaErrorNotSupported;  // one K loop length per launch
-      ok &= make_map(&mAs, w.ws2, 2, Fs, d, 128);
-      ok &= make_map(&mBs, ws + L.hs, 2, Fs, c.T, 1);
+      ok &= make_tensor_map_2d(&mAs, w.ws2, 2, Fs, d, 128);
+      ok &= make_tensor_map_2d(&mBs, ws + L.hs, 2, Fs, c.T, 1);
     }
   }
   if (stage == 0 && has_shared && Fs % 128) return cudaErrorInvalidValue;

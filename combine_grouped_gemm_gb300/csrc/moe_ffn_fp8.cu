@@ -1,0 +1,498 @@
+// e4m3 expert GEMMs with fp32 block scales (the FP8 prefill path).
+//
+// Method: as in moe_ffn.cu ("7.13 Serving Mixture-of-Experts", Expert Parallelism Mechanics,
+// expert compute; "One-Sided Expert-Parallel All-to-All ...", abstract, grouped GEMMs reading
+// the receive buffers in place), with DeepEP-style FP8 activations ("Serving
+// Mixture-of-Experts", DeepEP section): activations carry one fp32 scale per token per 128
+// columns, weights one fp32 scale per 128x128 block, and the SwiGLU intermediate is
+// re-quantised the same way before the down projection.
+//
+// Because every 128-wide block of K carries its own pair of scales, the product of one block
+// is accumulated alone in tensor memory (tcgen05.mma kind::f8f6f4, fp32 accumulate) and then
+// "promoted": added into fp32 registers times (token scale x weight scale). To make that a
+// single scalar per thread, this kernel is NOT swapped: the token rows are the M operand (128
+// rows per tile, one tensor-memory lane each) and the weight rows the N operand (128 per
+// tile), so the thread that owns lane j multiplies a whole partial row by one number.
+// Two partial buffers in tensor memory alternate so the tensor core computes block kb+1 while
+// the promoter warps read block kb.
+//
+// Roles (320 threads, one CTA per SM, persistent over the unit list):
+//   warp 0      TMA producer (token rows gathered with 1-row boxes; weight tiles 128 rows)
+//   warp 1      tensor-memory allocation; lane 0 issues the MMAs
+//   warps 2..9  promoters / epilogue: warp w owns lanes 32*(w%4).. and the column half
+//               (w-2)/4 of each accumulator (64 columns)
+#include "moe_device.cuh"
+
+namespace moe {
+namespace {
+
+struct Fp8Args {
+  const Tile* tiles;
+  const int32_t* n_tiles;
+  const int32_t* grp_off;
+  const int32_t* row_list;
+  int tk;
+  long long a_rows_routed;      // bound of routed A row indices
+  int T;
+  int mt_routed, mt_shared;     // 128-row weight tiles per group
+  int n_shared_tiles;
+  int k_steps;                  // K / 128
+  int b_rows_routed;            // weight rows per routed expert (2F or d)
+  int b_up_routed, b_up_shared; // offset of the up rows (gate/up) or 0
+  const float* a_sc_routed;     // token scales of routed A rows [rows][K/128]
+  const float* a_sc_shared;     // token scales of shared A rows [T][K/128]
+  const float* w_sc_routed;     // [E][b_rows_routed/128][K/128]
+  const float* w_sc_shared;     // [b_rows_shared/128][K/128]
+  void* out_routed;             // gate/up: e4m3 h [tk][F]; down: bf16 ebuf [recv rows][d]
+  float* out_sc_routed;         // gate/up: h scales [tk][F/128]
+  void* out_shared;             // gate/up: e4m3 hs [T][Fs]; down: bf16 shared_out [T][d]
+  float* out_sc_shared;
+  int ld_routed, ld_shared;     // output row length (elements)
+  long long out_rows_routed;    // bound of routed output row indices
+  uint32_t* status;
+};
+
+struct Unit8 {
+  int g, n0, nlen, m;
+};
+
+__device__ __forceinline__ Unit8 decode_unit8(const Fp8Args& a, int u) {
+  Unit8 r;
+  const int us = a.n_shared_tiles * a.mt_shared;
+  if (u < us) {
+    const int tt = u / a.mt_shared;
+    r.g = -1;
+    r.m = u - tt * a.mt_shared;
+    r.n0 = tt * 128;
+    r.nlen = min(128, a.T - r.n0);
+  } else {
+    const int v = u - us;
+    const int tt = v / a.mt_routed;
+    r.m = v - tt * a.mt_routed;
+    const Tile t = a.tiles[tt];
+    r.g = t.group;
+    r.n0 = t.n0;
+    r.nlen = t.nlen;
+  }
+  return r;
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+constexpr int kThreads8 = 320;
+
+template <int STAGE, int STAGES>
+struct Fp8Shape {
+  static constexpr int NB = STAGE == 0 ? 2 : 1;      // weight tiles per stage (gate, up)
+  static constexpr int A_BYTES = 128 * 128;          // 128 token rows x 128 e4m3
+  static constexpr int B_BYTES = 128 * 128;          // 128 weight rows x 128 e4m3
+  static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+  static constexpr int ACC_COLS = NB * 128;          // partial accumulator columns per buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;     // two partial buffers
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 512 + 1024;
+  static_assert(TMEM_COLS <= 512, "tensor memory");
+};
+
+template <int STAGE, int STAGES>
+__global__ void __launch_bounds__(kThreads8, 1)
+    ffn_gemm_e4m3_kernel(const Fp8Args a, const __grid_constant__ CUtensorMap mapA,
+                         const __grid_constant__ CUtensorMap mapAs,
+                         const __grid_constant__ CUtensorMap mapB,
+                         const __grid_constant__ CUtensorMap mapBs) {
+  using S = Fp8Shape<STAGE, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* pfull = empty + STAGES;    // [2] partial buffer written
+  uint64_t* pempty = pfull + 2;        // [2] partial buffer read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* amax_x = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES + 512);  // [4][32][2]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&pfull[i], 1);
+      mbar_init(&pempty[i], 256);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&mapA);
+    tma_prefetch_map(&mapB);
+    if (a.mt_shared) {
+      tma_prefetch_map(&mapAs);
+      tma_prefetch_map(&mapBs);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int units = a.n_shared_tiles * a.mt_shared + (*a.n_tiles) * a.mt_routed;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    const uint64_t pol_w = l2_policy_evict_last();   // weight tiles are reused by token tiles
+    const uint64_t pol_x = l2_policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit8 t = decode_unit8(a, u);
+      const bool sh = t.g < 0;
+      const CUtensorMap* amap = sh ? &mapAs : &mapA;
+      const CUtensorMap* bmap = sh ? &mapBs : &mapB;
+      const int brow0 = (sh ? 0 : t.g * a.b_rows_routed) + t.m * 128;
+      const int brow1 = brow0 + (sh ? a.b_up_shared : a.b_up_routed);
+      int arow[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int p = lane + 32 * q;
+        int row = -1;
+        if (p < t.nlen) {
+          if (sh) {
+            row = t.n0 + p;
+          } else if (STAGE == 0) {
+            const int ci = a.grp_off[t.g] + t.n0 + p;
+            row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+          } else {
+            row = a.grp_off[t.g] + t.n0 + p;
+          }
+          if (!sh && (row < 0 || row >= a.a_rows_routed)) row = -1;
+        }
+        arow[q] = row;
+      }
+      int nvalid = 0, nbad = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        nvalid += __popc(__ballot_sync(0xffffffffu, arow[q] >= 0));
+        nbad += __popc(__ballot_sync(0xffffffffu, arow[q] < 0 && lane + 32 * q < t.nlen));
+      }
+      if (nbad && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
+      const uint32_t tx = S::NB * S::B_BYTES + 128u * static_cast<uint32_t>(nvalid);
+      for (int ks = 0; ks < a.k_steps; ++ks) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + stage * S::STAGE_BYTES;
+        uint8_t* sb = sa + S::A_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], tx);
+          tma_load_2d(sb, bmap, &full[stage], ks * 128, brow0, pol_w);
+          if (S::NB == 2) tma_load_2d(sb + S::B_BYTES, bmap, &full[stage], ks * 128, brow1, pol_w);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (arow[q] >= 0)
+            tma_load_2d(sa + (lane + 32 * q) * 128, amap, &full[stage], ks * 128, arow[q], pol_x);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_e4m3(128, 128);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pk = 0;  // partial-buffer use counter
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        for (int ks = 0; ks < a.k_steps; ++ks, ++pk) {
+          const uint32_t pb = pk & 1u;
+          if (!mbar_wait(&pempty[pb], ((pk >> 1) & 1u) ^ 1u, abort_flag, a.status) ||
+              !mbar_wait(&full[stage], phase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_addr(smem + stage * S::STAGE_BYTES);
+          const uint32_t sb = sa + S::A_BYTES;
+          const uint32_t d0 = tmem + pb * S::ACC_COLS;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = smem_desc_sw128(sa + kk * 32);
+            mma_f8(d0, da, smem_desc_sw128(sb + kk * 32), idesc, kk != 0);
+            if (S::NB == 2) mma_f8(d0 + 128, da, smem_desc_sw128(sb + S::B_BYTES + kk * 32), idesc, kk != 0);
+          }
+          mma_commit(&empty[stage]);
+          mma_commit(&pfull[pb]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ promoters / epilogue ------------------------------
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;      // 0: columns 0..63, 1: columns 64..127
+    const int r = quarter * 32 + lane;     // token row of the tile (tensor-memory lane)
+    const int kb_n = a.k_steps;
+    uint32_t pk = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit8 t = decode_unit8(a, u);
+      const bool sh = t.g < 0;
+      const bool live = r < t.nlen;
+      // the A row of this lane and its token-scale row
+      long long arow = -1;
+      if (live) {
+        if (sh) arow = t.n0 + r;
+        else if (STAGE == 0) {
+          const int ci = a.grp_off[t.g] + t.n0 + r;
+          arow = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+        } else {
+          arow = a.grp_off[t.g] + t.n0 + r;
+        }
+        if (!sh && (arow < 0 || arow >= a.a_rows_routed)) arow = -1;
+      }
+      const float* xs = arow >= 0 ? (sh ? a.a_sc_shared : a.a_sc_routed) + arow * kb_n : nullptr;
+      const float* wsc = sh ? a.w_sc_shared
+                            : a.w_sc_routed + (size_t)t.g * (a.b_rows_routed / 128) * kb_n;
+      const int blk0 = t.m;
+      const int blk1 = t.m + (sh ? a.b_up_shared : a.b_up_routed) / 128;
+      float acc0[64], acc1[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc0[j] = acc1[j] = 0.0f;
+      float xs_next = xs ? __ldg(xs) : 0.0f;
+      bool ok = true;
+      for (int ks = 0; ks < kb_n; ++ks, ++pk) {
+        const float xsv = xs_next;
+        if (xs && ks + 1 < kb_n) xs_next = __ldg(xs + ks + 1);
+        const float s0 = xsv * __ldg(wsc + blk0 * kb_n + ks);
+        const float s1 = S::NB == 2 ? xsv * __ldg(wsc + blk1 * kb_n + ks) : 0.0f;
+        const uint32_t pb = pk & 1u;
+        if (!mbar_wait(&pfull[pb], (pk >> 1) & 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + pb * S::ACC_COLS +
+                            half * 64;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tb + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc0[c * 32 + j] = fmaf(__uint_as_float(v[j]), s0, acc0[c * 32 + j]);
+        }
+        if (S::NB == 2) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tb + 128 + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              acc1[c * 32 + j] = fmaf(__uint_as_float(v[j]), s1, acc1[c * 32 + j]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&pempty[pb]);
+      }
+      if (!ok) break;
+
+      // ---- epilogue of the unit ----
+      if (STAGE == 0) {
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          acc0[j] = silu(acc0[j]) * acc1[j];
+          amax = fmaxf(amax, fabsf(acc0[j]));
+        }
+        amax_x[(quarter * 32 + lane) * 2 + half] = amax;
+        named_barrier(1 + quarter, 64);    // the two warps sharing these lanes
+        amax = fmaxf(amax_x[(quarter * 32 + lane) * 2], amax_x[(quarter * 32 + lane) * 2 + 1]);
+        named_barrier(1 + quarter, 64);
+        const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        if (live) {
+          long long orow = sh ? (long long)t.n0 + r : (long long)a.grp_off[t.g] + t.n0 + r;
+          const bool in = sh || (orow >= 0 && orow < a.tk);
+          if (in) {
+            uint8_t* out = static_cast<uint8_t*>(sh ? a.out_shared : a.out_routed) +
+                           orow * (sh ? a.ld_shared : a.ld_routed) + t.m * 128 + half * 64;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w[4];
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                const int j = q * 16 + b * 4;
+                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(acc0[j], scale), __fdiv_rn(acc0[j + 1], scale)),
+                    __NV_SATFINITE, __NV_E4M3);
+                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(acc0[j + 2], scale), __fdiv_rn(acc0[j + 3], scale)),
+                    __NV_SATFINITE, __NV_E4M3);
+                w[b] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+              }
+              reinterpret_cast<uint4*>(out)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            if (half == 0) {
+              float* osc = sh ? a.out_sc_shared : a.out_sc_routed;
+              const int nblk = (sh ? a.ld_shared : a.ld_routed) / 128;
+              osc[orow * nblk + t.m] = scale;
+            }
+          }
+        }
+      } else if (live) {
+        long long orow;
+        bool in = true;
+        if (sh) {
+          orow = t.n0 + r;
+        } else {
+          const int ci = a.grp_off[t.g] + t.n0 + r;
+          in = ci >= 0 && ci < a.tk;
+          orow = in ? a.row_list[ci] : -1;
+          in = in && orow >= 0 && orow < a.out_rows_routed;
+        }
+        if (in) {
+          uint4* out = reinterpret_cast<uint4*>(
+              static_cast<__nv_bfloat16*>(sh ? a.out_shared : a.out_routed) +
+              orow * (sh ? a.ld_shared : a.ld_routed) + t.m * 128 + half * 64);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int j = q * 8;
+            out[q] = make_uint4(pack_bf16x2(acc0[j], acc0[j + 1]), pack_bf16x2(acc0[j + 2], acc0[j + 3]),
+                                pack_bf16x2(acc0[j + 4], acc0[j + 5]), pack_bf16x2(acc0[j + 6], acc0[j + 7]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
+                                 const float* recv_scales, const moe_weights& w, void* ebuf,
+                                 void* shared_out, char* ws, cudaStream_t st) {
+  const int cap = cap_of(c);
+  const long long recv_rows = (long long)c.R * c.R * cap;
+  const int F = c.d_ff, Fs = c.d_ff_shared, d = c.d, tk = c.T * c.k;
+  const bool has_shared = Fs > 0;
+  Fp8Args a{};
+  a.tiles = reinterpret_cast<const Tile*>(ws + L.tiles);
+  a.n_tiles = reinterpret_cast<const int32_t*>(ws + L.n_tiles);
+  a.grp_off = reinterpret_cast<const int32_t*>(ws + L.grp_off);
+  a.row_list = reinterpret_cast<const int32_t*>(ws + L.row_list);
+  a.tk = tk;
+  a.T = c.T;
+  a.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  a.n_shared_tiles = has_shared ? (c.T + 127) / 128 : 0;
+  a.out_rows_routed = recv_rows;
+  CUtensorMap mA, mAs, mB, mBs;
+  bool ok = true;
+  if (stage == 0) {
+    a.a_rows_routed = recv_rows;
+    a.mt_routed = F / 128;
+    a.mt_shared = has_shared ? Fs / 128 : 0;
+    a.k_steps = d / 128;
+    a.b_rows_routed = 2 * F;
+    a.b_up_routed = F;
+    a.b_up_shared = Fs;
+    a.a_sc_routed = recv_scales;
+    a.a_sc_shared = reinterpret_cast<const float*>(ws + L.xq_scales);
+    a.w_sc_routed = w.w13_scales;
+    a.w_sc_shared = w.ws13_scales;
+    a.out_routed = ws + L.h;
+    a.out_sc_routed = reinterpret_cast<float*>(ws + L.h_scales);
+    a.out_shared = ws + L.hs;
+    a.out_sc_shared = reinterpret_cast<float*>(ws + L.hs_scales);
+    a.ld_routed = F;
+    a.ld_shared = Fs;
+    ok &= make_tensor_map_2d(&mA, recv, 1, d, recv_rows, 1);
+    ok &= make_tensor_map_2d(&mB, w.w13, 1, d, (uint64_t)c.E * 2 * F, 128);
+    if (has_shared) {
+      ok &= make_tensor_map_2d(&mAs, ws + L.xq, 1, d, c.T, 1);
+      ok &= make_tensor_map_2d(&mBs, w.ws13, 1, d, 2ull * Fs, 128);
+    }
+  } else {
+    if (has_shared && Fs != F) return cudaErrorNotSupported;
+    a.a_rows_routed = tk;
+    a.mt_routed = d / 128;
+    a.mt_shared = has_shared ? d / 128 : 0;
+    a.k_steps = F / 128;
+    a.b_rows_routed = d;
+    a.b_up_routed = 0;
+    a.b_up_shared = 0;
+    a.a_sc_routed = reinterpret_cast<const float*>(ws + L.h_scales);
+    a.a_sc_shared = reinterpret_cast<const float*>(ws + L.hs_scales);
+    a.w_sc_routed = w.w2_scales;
+    a.w_sc_shared = w.ws2_scales;
+    a.out_routed = ebuf;
+    a.out_shared = shared_out;
+    a.ld_routed = d;
+    a.ld_shared = d;
+    ok &= make_tensor_map_2d(&mA, ws + L.h, 1, F, tk, 1);
+    ok &= make_tensor_map_2d(&mB, w.w2, 1, F, (uint64_t)c.E * d, 128);
+    if (has_shared) {
+      ok &= make_tensor_map_2d(&mAs, ws + L.hs, 1, Fs, c.T, 1);
+      ok &= make_tensor_map_2d(&mBs, w.ws2, 1, Fs, d, 128);
+    }
+  }
+  if (!has_shared) {
+    mAs = mA;
+    mBs = mB;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  cudaError_t err;
+  if (stage == 0) {
+    using S = Fp8Shape<0, 4>;
+    auto kern = ffn_gemm_e4m3_kernel<0, 4>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (err != cudaSuccess) return err;
+    kern<<<sm_count(), kThreads8, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+  } else {
+    using S = Fp8Shape<1, 6>;
+    auto kern = ffn_gemm_e4m3_kernel<1, 6>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (err != cudaSuccess) return err;
+    kern<<<sm_count(), kThreads8, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

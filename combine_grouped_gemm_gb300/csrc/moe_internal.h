@@ -1,6 +1,7 @@
 // Internal declarations shared by the host API (moe_api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -69,5 +70,21 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
 cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                             const float* recv_scales, const void* x, const moe_weights& w,
                             void* ebuf, void* shared_out, char* ws, cudaStream_t st);
+
+// e4m3 grouped GEMMs (non-swapped, per-128-K-block scale promotion), same stages.
+cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
+                                 const float* recv_scales, const moe_weights& w, void* ebuf,
+                                 void* shared_out, char* ws, cudaStream_t st);
+
+// 1x128 e4m3 quantisation of T rows of width d (the dispatch's rule), row t -> row t.
+cudaError_t launch_quant_rows_e4m3(const void* x, int T, int d, void* out, float* scales,
+                                   cudaStream_t st);
+
+// 2-D row-major tensor map [rows][cols] with a box of box_rows x 128 bytes, 128-byte swizzle.
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t cols,
+                        uint64_t rows, uint32_t box_rows);
+
+// Streaming multiprocessors of the current device.
+int sm_count();
 
 }  // namespace moe

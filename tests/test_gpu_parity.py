@@ -397,18 +397,68 @@ def test_gate_up_intermediate_and_schedule(cfg):
     h = bf16_to_f64(host_bits(h))
     x = host_bits(inp["x"])
     get = expert_getter(W, False)
-    worst = 0.0
+    n_off = n_all = 0
     for e in range(cfg.E):
         Wt = get(e)
         for p in range(grp_n[e]):
             c = grp_off[e] + p
             t = src[row_list[c]]
             _, href = oracle.swiglu_row_bf16(x[t], Wt["w13"], Wt["w2"])
-            err = rel_max_err(h[c], href)
-            if err > TOL_BF16:   # diagnostics: which reference row does it look like?
-                best = min(range(cfg.T), key=lambda tt: rel_max_err(
-                    h[c], oracle.swiglu_row_bf16(x[tt], Wt["w13"], Wt["w2"])[1]))
-                print(f"h mismatch e={e} p={p} t={t} err={err:.3e} closest token={best} "
-                      f"got[:6]={h[c][:6]} ref[:6]={href[:6]}")
-            worst = max(worst, err)
-    assert worst <= TOL_BF16, worst
+            # h is rounded to bf16 on both sides from sums taken in different orders (fp32
+            # here, fp64 in the oracle): elements agree or sit one bf16 ulp apart.
+            diff = np.abs(h[c] - href)
+            bound = 2.0 ** -7 * np.abs(href) + 1e-6 * np.sqrt(np.mean(href * href))
+            assert np.all(diff <= bound), (e, p, t, float((diff / np.maximum(bound, 1e-30)).max()))
+            n_off += int((diff > 0).sum())
+            n_all += diff.size
+    assert n_off <= 0.01 * n_all, (n_off, n_all)
+
+
+# ------------------------------------------------------------------------------------------
+# e4m3 path
+# ------------------------------------------------------------------------------------------
+TOL_FP8 = 6e-2
+FP8_HOT = dataclasses.replace(HOT, name="hot_fp8", act="fp8", w="fp8", d=256, d_ff=256,
+                              d_ff_shared=256)
+
+
+@pytest.mark.parametrize("cfg", [FP8_SMALL, FP8_HOT], ids=lambda c: c.name)
+def test_fp8_expert_rows_and_layer(cfg):
+    inp, W = inputs(cfg)
+    m = moe()
+    lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y = lay(inp["x"])
+    assert m.read_status(lay.bufs["ws"]) == 0
+    b = lay.bufs
+    ti = b["topk_idx"].cpu().numpy()
+    ro = b["row_of"].cpu().numpy()
+    idx, _ = oracle_route(cfg, inp)
+    assert np.array_equal(ti, idx)
+    x = host_bits(inp["x"])
+    xq, xs = oracle.quant_rows_e4m3(oracle.bf16_to_f32(x))
+    get = expert_getter(W, True)
+    eb = host_bits(b["ebuf"])
+    worst = 0.0
+    for e in np.unique(ti):
+        Wt = get(int(e))
+        for t, i in zip(*np.nonzero(ti == e)):
+            ref, _ = oracle.swiglu_row_fp8(xq[t], xs[t], Wt["w13"], Wt["w13_s"], Wt["w2"], Wt["w2_s"])
+            worst = max(worst, rel_max_err(bf16_to_f64(eb[ro[t, i]]), bf16_to_f64(ref)))
+    assert worst <= TOL_FP8, worst
+    S = shared_host(W, True)
+    sh = host_bits(b["shared_out"])
+    for t in range(0, cfg.T, 7):
+        ref, _ = oracle.swiglu_row_fp8(xq[t], xs[t], S["ws13"], S["ws13_s"], S["ws2"], S["ws2_s"])
+        assert rel_max_err(bf16_to_f64(sh[t]), bf16_to_f64(ref)) <= TOL_FP8
+    assert _layer_tokens_check(cfg, np.arange(cfg.T), inp, W, y) <= TOL_FP8
+
+
+@pytest.mark.slow
+def test_fp8_prefill_sampled_tokens():
+    cfg = synth.CONFIGS["dsv3_fp8_prefill"]
+    inp, W = inputs(cfg)
+    lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y = lay(inp["x"])
+    assert moe().read_status(lay.bufs["ws"]) == 0
+    tokens = np.array([0, 4097, 9999, cfg.T - 1])
+    assert _layer_tokens_check(cfg, tokens, inp, W, y) <= TOL_FP8
