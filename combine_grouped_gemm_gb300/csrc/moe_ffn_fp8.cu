@@ -92,10 +92,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void named_barrier(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 constexpr int kThreads8 = 320;
 
 template <int STAGE, int STAGES>
@@ -106,7 +102,8 @@ struct Fp8Shape {
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   static constexpr int ACC_COLS = NB * 128;          // partial accumulator columns per buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS;     // two partial buffers
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 512 + 1024;
+  // stages + alignment slack + barriers (512 B) + amax exchange [2][4][32][2] floats (2 KB)
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 512 + 2048;
   static_assert(TMEM_COLS <= 512, "tensor memory");
 };
 
@@ -124,9 +121,10 @@ __global__ void __launch_bounds__(kThreads8, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* pfull = empty + STAGES;    // [2] partial buffer written
   uint64_t* pempty = pfull + 2;        // [2] partial buffer read
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + 2);
+  uint64_t* xbar = pempty + 2;         // [4] amax exchange of the two warps on one lane quarter
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* amax_x = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES + 512);  // [4][32][2]
+  float* amax_x = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES + 512);  // [2][4][32][2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -138,6 +136,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
       mbar_init(&pfull[i], 1);
       mbar_init(&pempty[i], 256);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 64);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -265,7 +264,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
     const int r = quarter * 32 + lane;     // token row of the tile (tensor-memory lane)
     const int kb_n = a.k_steps;
     uint32_t pk = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
       const Unit8 t = decode_unit8(a, u);
       const bool sh = t.g < 0;
       const bool live = r < t.nlen;
@@ -336,10 +336,14 @@ __global__ void __launch_bounds__(kThreads8, 1)
           acc0[j] = silu(acc0[j]) * acc1[j];
           amax = fmaxf(amax, fabsf(acc0[j]));
         }
-        amax_x[(quarter * 32 + lane) * 2 + half] = amax;
-        named_barrier(1 + quarter, 64);    // the two warps sharing these lanes
-        amax = fmaxf(amax_x[(quarter * 32 + lane) * 2], amax_x[(quarter * 32 + lane) * 2 + 1]);
-        named_barrier(1 + quarter, 64);
+        // the 128-column block of h is split between this warp and the one on the same lane
+        // quarter: exchange the two halves' amax (slots alternate by unit parity so a fast
+        // warp's next write never meets its partner's pending read)
+        float* slot = amax_x + (((it & 1u) * 4 + quarter) * 32 + lane) * 2;
+        slot[half] = amax;
+        mbar_arrive(&xbar[quarter]);
+        if (!mbar_wait(&xbar[quarter], it & 1u, abort_flag, a.status)) break;
+        amax = fmaxf(slot[0], slot[1]);
         const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
         if (live) {
           long long orow = sh ? (long long)t.n0 + r : (long long)a.grp_off[t.g] + t.n0 + r;

@@ -27,14 +27,19 @@ namespace {
 // ---------------------------------------------------------------------------------------
 // Partial logits: partials[c][t][e] = sum over the c-th chunk of d of x[t][i] * w[e][i],
 // one sequential FMA chain per (c, t, e).
+// CTA tile BT tokens x BE experts of one chunk; thread tile TM x TN; k-steps of BK columns,
+// staged through shared memory (k-major, so the compute loop reads conflict-free) with the next
+// step's global loads held in registers while the current step computes.
 // ---------------------------------------------------------------------------------------
-template <int BT, int BE, int TM, int TN>
+template <int BT, int BE, int TM, int TN, int BK>
 __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16* __restrict__ x,
                                                              const float* __restrict__ wg,
                                                              float* __restrict__ partials, int T,
                                                              int d, int E) {
-  constexpr int BK = 8;
   static_assert((BT / TM) * (BE / TN) == 256, "256 threads");
+  constexpr int XV = BT * BK / 8;            // 16-byte vectors of x per step (8 bf16)
+  constexpr int WV = BE * BK / 4;            // 16-byte vectors of w per step (4 floats)
+  constexpr int NX = (XV + 255) / 256, NW = (WV + 255) / 256;
   __shared__ __align__(16) float xs[2][BK][BT];
   __shared__ __align__(16) float ws[2][BK][BE];
 
@@ -51,39 +56,66 @@ __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
-  // Loaders: x rows are 8 bf16 (one uint4) per step; w rows are 8 floats (two float4).
-  auto load = [&](int buf, int step) {
+  uint4 rx[NX];
+  float4 rw[NW];
+  auto fetch = [&](int step) {
     const int k0 = kbeg + step * BK;
-    for (int r = tid; r < BT; r += 256) {
-      const int t = t0 + r;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < T) v = *reinterpret_cast<const uint4*>(x + (size_t)t * d + k0);
-      xs[buf][0][r] = bf16_lo(v.x);
-      xs[buf][1][r] = bf16_hi(v.x);
-      xs[buf][2][r] = bf16_lo(v.y);
-      xs[buf][3][r] = bf16_hi(v.y);
-      xs[buf][4][r] = bf16_lo(v.z);
-      xs[buf][5][r] = bf16_hi(v.z);
-      xs[buf][6][r] = bf16_lo(v.w);
-      xs[buf][7][r] = bf16_hi(v.w);
+#pragma unroll
+    for (int n = 0; n < NX; ++n) {
+      const int q = tid + n * 256;
+      rx[n] = make_uint4(0, 0, 0, 0);
+      if (q < XV) {
+        const int r = q % BT, kv = q / BT;   // consecutive threads: consecutive tokens
+        const int t = t0 + r;
+        if (t < T) rx[n] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d + k0 + kv * 8));
+      }
     }
-    for (int q = tid; q < BE * 2; q += 256) {
-      const int r = q >> 1, half = q & 1;
-      const int e = e0 + r;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < E) v = *reinterpret_cast<const float4*>(wg + (size_t)e * d + k0 + half * 4);
-      ws[buf][half * 4 + 0][r] = v.x;
-      ws[buf][half * 4 + 1][r] = v.y;
-      ws[buf][half * 4 + 2][r] = v.z;
-      ws[buf][half * 4 + 3][r] = v.w;
+#pragma unroll
+    for (int n = 0; n < NW; ++n) {
+      const int q = tid + n * 256;
+      rw[n] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q < WV) {
+        const int r = q % BE, kv = q / BE;
+        const int e = e0 + r;
+        if (e < E) rw[n] = __ldg(reinterpret_cast<const float4*>(wg + (size_t)e * d + k0 + kv * 4));
+      }
+    }
+  };
+  auto stash = [&](int buf) {
+#pragma unroll
+    for (int n = 0; n < NX; ++n) {
+      const int q = tid + n * 256;
+      if (q < XV) {
+        const int r = q % BT, kv = q / BT;
+        xs[buf][kv * 8 + 0][r] = bf16_lo(rx[n].x);
+        xs[buf][kv * 8 + 1][r] = bf16_hi(rx[n].x);
+        xs[buf][kv * 8 + 2][r] = bf16_lo(rx[n].y);
+        xs[buf][kv * 8 + 3][r] = bf16_hi(rx[n].y);
+        xs[buf][kv * 8 + 4][r] = bf16_lo(rx[n].z);
+        xs[buf][kv * 8 + 5][r] = bf16_hi(rx[n].z);
+        xs[buf][kv * 8 + 6][r] = bf16_lo(rx[n].w);
+        xs[buf][kv * 8 + 7][r] = bf16_hi(rx[n].w);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < NW; ++n) {
+      const int q = tid + n * 256;
+      if (q < WV) {
+        const int r = q % BE, kv = q / BE;
+        ws[buf][kv * 4 + 0][r] = rw[n].x;
+        ws[buf][kv * 4 + 1][r] = rw[n].y;
+        ws[buf][kv * 4 + 2][r] = rw[n].z;
+        ws[buf][kv * 4 + 3][r] = rw[n].w;
+      }
     }
   };
 
-  load(0, 0);
+  fetch(0);
+  stash(0);
   __syncthreads();
   for (int step = 0; step < nsteps; ++step) {
     const int buf = step & 1;
-    if (step + 1 < nsteps) load(buf ^ 1, step + 1);
+    if (step + 1 < nsteps) fetch(step + 1);   // in flight while this step computes
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float a[TM], b[TN];
@@ -96,6 +128,7 @@ __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
     }
+    if (step + 1 < nsteps) stash(buf ^ 1);
     __syncthreads();
   }
 
@@ -109,6 +142,23 @@ __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16
       if (e < E) partials[((size_t)c * T + t) * E + e] = acc[i][j];
     }
   }
+}
+
+// MAXBK caps the k-step so the static shared memory (2 x BK x (BT + BE) floats) stays within
+// 48 KB.
+template <int BT, int BE, int TM, int TN, int MAXBK>
+cudaError_t launch_partials(const __nv_bfloat16* x, const float* wg, float* partials, int T, int d,
+                            int E, cudaStream_t st) {
+  static_assert(2 * MAXBK * (BT + BE) * 4 <= 48 * 1024, "static shared memory");
+  const int L = d / kRouteChunks;
+  dim3 grid((E + BE - 1) / BE, (T + BT - 1) / BT, kRouteChunks);
+  if (MAXBK >= 32 && L % 32 == 0)
+    route_partials_kernel<BT, BE, TM, TN, (MAXBK >= 32 ? 32 : 16)><<<grid, 256, 0, st>>>(x, wg, partials, T, d, E);
+  else if (L % 16 == 0)
+    route_partials_kernel<BT, BE, TM, TN, 16><<<grid, 256, 0, st>>>(x, wg, partials, T, d, E);
+  else
+    route_partials_kernel<BT, BE, TM, TN, 8><<<grid, 256, 0, st>>>(x, wg, partials, T, d, E);
+  return cudaGetLastError();
 }
 
 // e^z by Cody-Waite reduction and a degree-7 Taylor polynomial (see the file comment).
@@ -237,14 +287,11 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
                          cudaStream_t st) {
   (void)status;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  if (c.T >= 2048) {
-    dim3 grid((c.E + 127) / 128, (c.T + 127) / 128, kRouteChunks);
-    route_partials_kernel<128, 128, 8, 8><<<grid, 256, 0, st>>>(xb, w_gate, partials, c.T, c.d, c.E);
-  } else {
-    dim3 grid((c.E + 63) / 64, (c.T + 63) / 64, kRouteChunks);
-    route_partials_kernel<64, 64, 4, 4><<<grid, 256, 0, st>>>(xb, w_gate, partials, c.T, c.d, c.E);
-  }
-  cudaError_t err = cudaGetLastError();
+  // Large batches: 128x128 tiles, 8x8 per thread. Small batches: 32x32 tiles, 2x2 per thread,
+  // so the 16 chunks x E/32 x T/32 grid still fills the GPU several CTAs per SM deep.
+  cudaError_t err = c.T >= 2048
+                        ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st)
+                        : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st);
   if (err != cudaSuccess) return err;
   const size_t smem = 8 * (size_t)(2 * c.E + 160) * sizeof(float);
   if (smem > 48 * 1024) {
