@@ -60,6 +60,7 @@ def _load():
         "moe_validate": [P],
         "moe_query_sizes": [P, P],
         "moe_route": [P, P, P, P, P, P, P, S],
+        "moe_route_noalloc": [P, P, P, P, P, P, S],
         "moe_dispatch": [P, P, P, P, P, P, P, P, S],
         "moe_expert_ffn": [P, P, P, P, P, P, P, P, P, S],
         "moe_combine": [P, P, P, P, P, P, S],
@@ -79,7 +80,8 @@ def _load():
 
 _lib = _load()
 
-EXPORTED = ["moe_validate", "moe_query_sizes", "moe_route", "moe_dispatch", "moe_expert_ffn",
+EXPORTED = ["moe_validate", "moe_query_sizes", "moe_route", "moe_route_noalloc", "moe_dispatch",
+            "moe_expert_ffn",
             "moe_combine", "moe_layer", "moe_clear_status", "moe_read_status", "moe_strerror",
             "moe_abi_version", "moe_last_cuda_error"]
 
@@ -143,6 +145,14 @@ def query_sizes(cfg) -> dict:
 def route(cfg, x, w_gate, bias, topk_idx, topk_w, ws, stream=None):
     _check("moe_route", _lib.moe_route(ctypes.byref(make_cfg(cfg)), _p(x), _p(w_gate), _p(bias),
                                        _p(topk_idx), _p(topk_w), _p(ws), _s(stream)))
+
+
+def route_noalloc(cfg, x, w_gate, bias, topk_idx, topk_w, stream=None):
+    """moe_route for callers that cannot supply a workspace: the library's own fixed device
+    array holds the router's scratch (see moe_route_noalloc in include/moe.h)."""
+    _check("moe_route_noalloc", _lib.moe_route_noalloc(ctypes.byref(make_cfg(cfg)), _p(x),
+                                                       _p(w_gate), _p(bias), _p(topk_idx),
+                                                       _p(topk_w), _s(stream)))
 
 
 def dispatch(cfg, x, topk_idx, recv, recv_scales, counts, row_of, src_tok=None, stream=None):

@@ -126,6 +126,25 @@ int moe_query_sizes(const moe_cfg* cfg, moe_sizes* out);
 int moe_route(const moe_cfg* cfg, const void* x, const float* w_gate, const float* bias,
               int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t stream);
 
+/* The router of moe_route for callers that cannot give the library any device memory beyond
+ * their inputs and outputs: a plugin inside another framework with no access to its
+ * allocator, a deployment whose device memory is fully planned at start-up, or a hot path that
+ * must not enter the driver allocator (cudaMalloc/cudaFree can synchronise the device). It
+ * needs no ws: its scratch (16 partial dot products per token and expert) is a fixed 8 MiB
+ * device array inside the library, which every device that loads the library holds until the
+ * process exits. The pages have no counterpart to this entry point; it exists for such
+ * callers only. Arguments and results are those of moe_route. Limits and behaviour:
+ *  - returns MOE_ERR_UNSUPPORTED when 16 * T * E exceeds 2^21 floats (T*E > 131072, e.g. more
+ *    than 512 tokens at 256 experts); nothing is enqueued then;
+ *  - the first call on a device looks up the array's device address with that device current
+ *    (cudaGetSymbolAddress); make that first call before any stream capture;
+ *  - it allocates nothing (no cudaMalloc, no cudaFree, no allocating library call);
+ *  - every call shares the array and leaves its contents behind; each call writes every entry
+ *    it reads, so nothing needs clearing, but calls whose kernels overlap on the GPU (other
+ *    streams, other host threads on the same device) race on it: serialise them. */
+int moe_route_noalloc(const moe_cfg* cfg, const void* x, const float* w_gate, const float* bias,
+                      int32_t* topk_idx, float* topk_w, cudaStream_t stream);
+
 /* Dispatch ("Serving Mixture-of-Experts", Expert Parallelism Mechanics, dispatch step;
  * "One-Sided Expert-Parallel All-to-All...", abstract; "Serving Mixture-of-Experts", DeepEP,
  * FP8 dispatch and fixed-size buffers). Each logical source rank s (tokens s*T/R ..) counts
