@@ -31,19 +31,27 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int i = 0; i < k; ++i) {
-      const int row = rows[i];
-      if (row < 0) continue;
-      const uint4 e = __ldg(ebuf + (size_t)row * vpr + v);
-      const float w = wts[i];
-      acc[0] = __fmaf_rn(w, bf16_lo(e.x), acc[0]);
-      acc[1] = __fmaf_rn(w, bf16_hi(e.x), acc[1]);
-      acc[2] = __fmaf_rn(w, bf16_lo(e.y), acc[2]);
-      acc[3] = __fmaf_rn(w, bf16_hi(e.y), acc[3]);
-      acc[4] = __fmaf_rn(w, bf16_lo(e.z), acc[4]);
-      acc[5] = __fmaf_rn(w, bf16_hi(e.z), acc[5]);
-      acc[6] = __fmaf_rn(w, bf16_lo(e.w), acc[6]);
-      acc[7] = __fmaf_rn(w, bf16_hi(e.w), acc[7]);
+    // rows in groups of 8 whose loads are all issued before the first is used
+    for (int i0 = 0; i0 < k; i0 += 8) {
+      uint4 e[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int row = (i0 + u < k) ? rows[i0 + u] : -1;
+        e[u] = row >= 0 ? __ldg(ebuf + (size_t)row * vpr + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (i0 + u >= k || rows[i0 + u] < 0) continue;
+        const float w = wts[i0 + u];
+        acc[0] = __fmaf_rn(w, bf16_lo(e[u].x), acc[0]);
+        acc[1] = __fmaf_rn(w, bf16_hi(e[u].x), acc[1]);
+        acc[2] = __fmaf_rn(w, bf16_lo(e[u].y), acc[2]);
+        acc[3] = __fmaf_rn(w, bf16_hi(e[u].y), acc[3]);
+        acc[4] = __fmaf_rn(w, bf16_lo(e[u].z), acc[4]);
+        acc[5] = __fmaf_rn(w, bf16_hi(e[u].z), acc[5]);
+        acc[6] = __fmaf_rn(w, bf16_lo(e[u].w), acc[6]);
+        acc[7] = __fmaf_rn(w, bf16_hi(e[u].w), acc[7]);
+      }
     }
     if (shared_out) {
       const uint4 s = __ldg(shared_out + (size_t)t * vpr + v);

@@ -39,6 +39,7 @@ namespace {
 // Tile schedule (one CTA)
 // ---------------------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
+constexpr size_t kPlanStageBytes = 48 * 1024;   // counts table staged in shared memory up to this
 
 // Block-wide exclusive scan of one int per thread (blockDim.x == kPlanThreads).
 __device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
@@ -78,16 +79,21 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     uint32_t* status, int E, int R, int cap, int bn, int max_tiles, int tk) {
   __shared__ int warp_sums[33];
   __shared__ int rank_base[64];
+  extern __shared__ int32_t cnt_s[];   // counts staged once: [R][E] when it fits, else unused
   const int e = threadIdx.x;
   const bool act = e < E;
   const int Er = E / R;
+  const bool staged = (size_t)R * E * sizeof(int32_t) <= kPlanStageBytes;
+  if (staged)
+    for (int i = threadIdx.x; i < R * E; i += blockDim.x) cnt_s[i] = max(0, counts[i]);
+  __syncthreads();
+  auto cnt = [&](int s_) -> int {
+    return staged ? cnt_s[s_ * E + e] : max(0, counts[(size_t)s_ * E + e]);
+  };
 
   int n = 0;
   if (act)
-    for (int s = 0; s < R; ++s) {
-      const int c = counts[(size_t)s * E + e];
-      n += c > 0 ? c : 0;
-    }
+    for (int s = 0; s < R; ++s) n += cnt(s);
   int total;
   const int off = block_exclusive_scan(act ? n : 0, &total, warp_sums);
   if (threadIdx.x == 0 && total != tk) raise_status(status, MOE_DEV_BOUNDS);
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
   // receive rows of every compact row
   int pre = 0;
   for (int s = 0; s < R; ++s) {
-    const int c = act ? max(0, counts[(size_t)s * E + e]) : 0;
+    const int c = act ? cnt(s) : 0;
     int dummy;
     const int ex = block_exclusive_scan(c, &dummy, warp_sums);
     if (act && e % Er == 0) rank_base[e / Er] = ex;
@@ -152,6 +158,8 @@ struct GemmArgs {
   void* out_shared;       // gate/up: hs [T][Fs]; down: shared_out [T][d]
   int ld_routed;          // output row length (elements)
   int ld_shared;
+  int box_routed;         // down stage: rows per box of the routed / shared input maps
+  int box_shared;
   uint32_t* status;
 };
 
@@ -261,35 +269,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
       const int arow0 = (sh ? 0 : t.g * a.a_rows_routed) + t.m * 128;
       const int arow1 = arow0 + (sh ? a.a_up_shared : a.a_up_routed);
-      int brow[BN / 32];
+      // Token rows of the unit. Gate/up: gathered four at a time (tile::gather4, lane j loads
+      // rows 4j..4j+3 of the tile; a missing row repeats a valid one of its group, which only
+      // fills a column the epilogue never stores). Down: the rows are contiguous compact rows,
+      // loaded as one box of box rows per k-step.
+      int g4[4] = {-1, -1, -1, -1};
+      bool g4_on = false;
+      int box_row = -1;
+      uint32_t b_bytes = 0;
+      if (STAGE == 0) {
+        int nbad = 0;
+        if (lane < BN / 4) {
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        const int p = lane + 32 * q;
-        int row = -1;
-        if (p < t.nlen) {
-          if (sh) {
-            row = t.n0 + p;
-          } else if (STAGE == 0) {
-            const int ci = a.grp_off[t.g] + t.n0 + p;
-            row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
-            if (row >= a.recv_rows) row = -1;
-          } else {
-            row = a.grp_off[t.g] + t.n0 + p;
-            if (row < 0 || row >= a.tk) row = -1;
+          for (int i = 0; i < 4; ++i) {
+            const int p = 4 * lane + i;
+            int row = -1;
+            if (p < t.nlen) {
+              if (sh) {
+                row = t.n0 + p;
+              } else {
+                const int ci = a.grp_off[t.g] + t.n0 + p;
+                row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+                if (row >= a.recv_rows) row = -1;
+              }
+              if (row < 0) ++nbad;
+            }
+            g4[i] = row;
           }
-        }
-        brow[q] = row;
-      }
-      // bytes the stage barrier waits for: the weight tiles plus one 128-byte row per valid
-      // token row (an out-of-range row index is skipped and reported)
-      int nvalid = 0, nbad = 0;
+          int first = -1;
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        nvalid += __popc(__ballot_sync(0xffffffffu, brow[q] >= 0));
-        nbad += __popc(__ballot_sync(0xffffffffu, brow[q] < 0 && lane + 32 * q < t.nlen));
+          for (int i = 3; i >= 0; --i) first = g4[i] >= 0 ? g4[i] : first;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) g4[i] = g4[i] >= 0 ? g4[i] : first;
+          g4_on = first >= 0;
+        }
+        const uint32_t on = __ballot_sync(0xffffffffu, g4_on);
+        if (__any_sync(0xffffffffu, nbad > 0) && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
+        b_bytes = 512u * __popc(on);
+      } else {
+        const int row0 = sh ? t.n0 : a.grp_off[t.g] + t.n0;
+        const bool in = row0 >= 0 && row0 < (sh ? a.T : a.tk);
+        if (!in && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
+        box_row = in ? row0 : -1;
+        b_bytes = in ? 128u * static_cast<uint32_t>(sh ? a.box_shared : a.box_routed) : 0u;
       }
-      if (nbad && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
-      const uint32_t tx = S::NA * S::A_BYTES + 128u * static_cast<uint32_t>(nvalid);
+      const uint32_t tx = S::NA * S::A_BYTES + b_bytes;
       for (int ks = 0; ks < a.k_steps; ++ks) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
           ok = false;
@@ -301,12 +325,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[stage], tx);
           tma_load_2d(sa, amap, &full[stage], ks * 64, arow0, pol_w);
           if (S::NA == 2) tma_load_2d(sa + S::A_BYTES, amap, &full[stage], ks * 64, arow1, pol_w);
+          if (STAGE == 1 && box_row >= 0)
+            tma_load_2d(sb, bmap, &full[stage], ks * 64, box_row, pol_x);
         }
         __syncwarp();
-#pragma unroll
-        for (int q = 0; q < BN / 32; ++q)
-          if (brow[q] >= 0)
-            tma_load_2d(sb + (lane + 32 * q) * 128, bmap, &full[stage], ks * 64, brow[q], pol_x);
+        if (STAGE == 0 && g4_on)
+          tma_gather4(sb + lane * 512, bmap, &full[stage], ks * 64, g4[0], g4[1], g4[2], g4[3],
+                      pol_x);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -479,7 +504,8 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
     if (err != cudaSuccess) return err;
   }
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
-  ffn_plan_kernel<<<1, kPlanThreads, 0, st>>>(
+  const size_t stage = (size_t)c.R * c.E * sizeof(int32_t);
+  ffn_plan_kernel<<<1, kPlanThreads, stage <= kPlanStageBytes ? stage : 0, st>>>(
       counts, reinterpret_cast<int32_t*>(ws + L.grp_n), reinterpret_cast<int32_t*>(ws + L.grp_off),
       reinterpret_cast<int32_t*>(ws + L.n_tiles), reinterpret_cast<Tile*>(ws + L.tiles),
       reinterpret_cast<int32_t*>(ws + L.row_list), status, c.E, c.R, cap_of(c), L.bn,
@@ -538,12 +564,15 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
     a.out_shared = shared_out;
     a.ld_routed = d;
     a.ld_shared = d;
+    // the down projection's input rows are contiguous: one box of up to bn rows per k-step
+    a.box_routed = tk < L.bn ? tk : L.bn;
+    a.box_shared = c.T < L.bn ? c.T : L.bn;
     ok &= make_tensor_map_2d(&mA, w.w2, 2, F, (uint64_t)c.E * d, 128);
-    ok &= make_tensor_map_2d(&mB, ws + L.h, 2, F, tk, 1);
+    ok &= make_tensor_map_2d(&mB, ws + L.h, 2, F, tk, a.box_routed);
     if (has_shared) {
       if (Fs != F) return cudaErrorNotSupported;  // one K loop length per launch
       ok &= make_tensor_map_2d(&mAs, w.ws2, 2, Fs, d, 128);
-      ok &= make_tensor_map_2d(&mBs, ws + L.hs, 2, Fs, c.T, 1);
+      ok &= make_tensor_map_2d(&mBs, ws + L.hs, 2, Fs, c.T, a.box_shared);
     }
   }
   if (stage == 0 && has_shared && Fs % 128) return cudaErrorInvalidValue;

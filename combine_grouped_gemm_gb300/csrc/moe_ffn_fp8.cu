@@ -49,6 +49,7 @@ struct Fp8Args {
   float* out_sc_shared;
   int ld_routed, ld_shared;     // output row length (elements)
   long long out_rows_routed;    // bound of routed output row indices
+  int box_routed, box_shared;   // down stage: rows per box of the routed / shared input maps
   uint32_t* status;
 };
 
@@ -172,32 +173,48 @@ __global__ void __launch_bounds__(kThreads8, 1)
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
       const int brow0 = (sh ? 0 : t.g * a.b_rows_routed) + t.m * 128;
       const int brow1 = brow0 + (sh ? a.b_up_shared : a.b_up_routed);
-      int arow[4];
+      // Token rows: gate/up gathers them four at a time (tile::gather4; lane j loads rows
+      // 4j..4j+3; a missing row repeats a valid one of its group, filling a lane whose result
+      // is never stored); down reads contiguous compact rows as one box per k-step.
+      int g4[4] = {-1, -1, -1, -1};
+      bool g4_on = false;
+      int box_row = -1;
+      uint32_t a_bytes = 0;
+      if (STAGE == 0) {
+        int nbad = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int p = lane + 32 * q;
-        int row = -1;
-        if (p < t.nlen) {
-          if (sh) {
-            row = t.n0 + p;
-          } else if (STAGE == 0) {
-            const int ci = a.grp_off[t.g] + t.n0 + p;
-            row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
-          } else {
-            row = a.grp_off[t.g] + t.n0 + p;
+        for (int i = 0; i < 4; ++i) {
+          const int p = 4 * lane + i;
+          int row = -1;
+          if (p < t.nlen) {
+            if (sh) {
+              row = t.n0 + p;
+            } else {
+              const int ci = a.grp_off[t.g] + t.n0 + p;
+              row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+              if (row >= a.a_rows_routed) row = -1;
+            }
+            if (row < 0) ++nbad;
           }
-          if (!sh && (row < 0 || row >= a.a_rows_routed)) row = -1;
+          g4[i] = row;
         }
-        arow[q] = row;
-      }
-      int nvalid = 0, nbad = 0;
+        int first = -1;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        nvalid += __popc(__ballot_sync(0xffffffffu, arow[q] >= 0));
-        nbad += __popc(__ballot_sync(0xffffffffu, arow[q] < 0 && lane + 32 * q < t.nlen));
+        for (int i = 3; i >= 0; --i) first = g4[i] >= 0 ? g4[i] : first;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) g4[i] = g4[i] >= 0 ? g4[i] : first;
+        g4_on = first >= 0;
+        const uint32_t on = __ballot_sync(0xffffffffu, g4_on);
+        if (__any_sync(0xffffffffu, nbad > 0) && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
+        a_bytes = 512u * __popc(on);
+      } else {
+        const int row0 = sh ? t.n0 : a.grp_off[t.g] + t.n0;
+        const bool in = row0 >= 0 && row0 < (sh ? a.T : a.tk);
+        if (!in && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
+        box_row = in ? row0 : -1;
+        a_bytes = in ? 128u * static_cast<uint32_t>(sh ? a.box_shared : a.box_routed) : 0u;
       }
-      if (nbad && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
-      const uint32_t tx = S::NB * S::B_BYTES + 128u * static_cast<uint32_t>(nvalid);
+      const uint32_t tx = S::NB * S::B_BYTES + a_bytes;
       for (int ks = 0; ks < a.k_steps; ++ks) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
           ok = false;
@@ -209,12 +226,13 @@ __global__ void __launch_bounds__(kThreads8, 1)
           mbar_arrive_expect_tx(&full[stage], tx);
           tma_load_2d(sb, bmap, &full[stage], ks * 128, brow0, pol_w);
           if (S::NB == 2) tma_load_2d(sb + S::B_BYTES, bmap, &full[stage], ks * 128, brow1, pol_w);
+          if (STAGE == 1 && box_row >= 0)
+            tma_load_2d(sa, amap, &full[stage], ks * 128, box_row, pol_x);
         }
         __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (arow[q] >= 0)
-            tma_load_2d(sa + (lane + 32 * q) * 128, amap, &full[stage], ks * 128, arow[q], pol_x);
+        if (STAGE == 0 && g4_on)
+          tma_gather4(sa + lane * 512, amap, &full[stage], ks * 128, g4[0], g4[1], g4[2], g4[3],
+                      pol_x);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -470,10 +488,12 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     a.out_shared = shared_out;
     a.ld_routed = d;
     a.ld_shared = d;
-    ok &= make_tensor_map_2d(&mA, ws + L.h, 1, F, tk, 1);
+    a.box_routed = tk < 128 ? tk : 128;
+    a.box_shared = c.T < 128 ? c.T : 128;
+    ok &= make_tensor_map_2d(&mA, ws + L.h, 1, F, tk, a.box_routed);
     ok &= make_tensor_map_2d(&mB, w.w2, 1, F, (uint64_t)c.E * d, 128);
     if (has_shared) {
-      ok &= make_tensor_map_2d(&mAs, ws + L.hs, 1, Fs, c.T, 1);
+      ok &= make_tensor_map_2d(&mAs, ws + L.hs, 1, Fs, c.T, a.box_shared);
       ok &= make_tensor_map_2d(&mBs, w.ws2, 1, Fs, d, 128);
     }
   }

@@ -187,24 +187,31 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
 }
 
 // ---------------------------------------------------------------------------------------
-// Selection: one warp per token.
+// Selection: one CTA (256 threads) per token.
+//  1. thread e: the 16 chunk partials of expert e (coalesced across threads), pairwise tree,
+//     sigmoid, selection key v = s + bias;
+//  2. warp w: scores of groups w, w+8, ...: the two largest keys of the group by a warp-wide
+//     top-2 merge (values only: equal keys give equal scores whichever expert carries them);
+//  3. thread g: rank of group g among all groups -> kept or not;
+//  4. warp 0: k rounds of a warp-wide argmax over the eligible experts (key desc, index asc),
+//     then the weights from the raw sigmoid scores in selection order.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) route_select_kernel(
+constexpr int kSelThreads = 256;
+
+__global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     const float* __restrict__ partials, const float* __restrict__ bias,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int E, int k,
     int n_group, int topk_group, float route_scale) {
   extern __shared__ float sm[];
+  float* s = sm;                 // [E] sigmoid scores
+  float* v = s + E;              // [E] selection keys
+  float* gscore = v + E;         // [64]
+  int* keep = reinterpret_cast<int*>(gscore + 64);   // [64]
+  float* sel_s = reinterpret_cast<float*>(keep + 64); // [32]
+  const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  // per warp: s[E], v[E], gscore[64], keep[64] (as floats), sel_s[32]
-  float* s = sm + (size_t)warp * (2 * E + 160);
-  float* v = s + E;
-  float* gscore = v + E;
-  float* keep = gscore + 64;
-  float* sel_s = keep + 64;
-  if (t >= T) return;
 
-  for (int e = lane; e < E; e += 32) {
+  for (int e = threadIdx.x; e < E; e += kSelThreads) {
     float p[kRouteChunks];
 #pragma unroll
     for (int c = 0; c < kRouteChunks; ++c) p[c] = partials[((size_t)c * T + t) * E + e];
@@ -216,38 +223,47 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     s[e] = si;
     v[e] = __fadd_rn(si, bias[e]);
   }
-  __syncwarp();
+  __syncthreads();
 
   const int gs = E / n_group;
-  for (int g = lane; g < n_group; g += 32) {
-    int b1 = -1, b2 = -1;
-    for (int e = g * gs; e < (g + 1) * gs; ++e) {
-      if (b1 < 0 || ranks_before(v[e], e, v[b1], b1)) {
-        b2 = b1;
-        b1 = e;
-      } else if (b2 < 0 || ranks_before(v[e], e, v[b2], b2)) {
-        b2 = e;
+  for (int g = warp; g < n_group; g += kSelThreads / 32) {
+    float a = -INFINITY, b = -INFINITY;  // this lane's two largest keys of group g
+    for (int e = g * gs + lane; e < (g + 1) * gs; e += 32) {
+      const float x = v[e];
+      if (x > a) {
+        b = a;
+        a = x;
+      } else if (x > b) {
+        b = x;
       }
     }
-    gscore[g] = (b2 >= 0) ? __fadd_rn(v[b1], v[b2]) : v[b1];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float c = __shfl_xor_sync(0xffffffffu, a, off);
+      const float d = __shfl_xor_sync(0xffffffffu, b, off);
+      const float hi = fmaxf(a, c);
+      b = fmaxf(fminf(a, c), fmaxf(b, d));
+      a = hi;
+    }
+    if (lane == 0) gscore[g] = gs >= 2 ? __fadd_rn(a, b) : a;
   }
-  __syncwarp();
-  for (int g = lane; g < n_group; g += 32) {
+  __syncthreads();
+  for (int g = threadIdx.x; g < n_group; g += kSelThreads) {
     int rank = 0;
     for (int h = 0; h < n_group; ++h) rank += ranks_before(gscore[h], h, gscore[g], g) ? 1 : 0;
-    keep[g] = rank < topk_group ? 1.0f : 0.0f;
+    keep[g] = rank < topk_group;
   }
-  __syncwarp();
+  __syncthreads();
+  if (warp != 0) return;
 
-  // k rounds of a warp-wide argmax over eligible, untaken experts.
-  uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen (E <= 1024)
+  uint32_t taken = 0;  // bit q: expert lane + 32*q already chosen (E <= 1024)
   int sel_e = -1;      // lane i (< k) keeps the i-th choice
   for (int i = 0; i < k; ++i) {
     float bv = -INFINITY;
     int be = 0x7fffffff;
     for (int q = 0, e = lane; e < E; ++q, e += 32) {
       if ((taken >> q) & 1u) continue;
-      if (keep[e / gs] == 0.0f) continue;
+      if (!keep[e / gs]) continue;
       if (be == 0x7fffffff || ranks_before(v[e], e, bv, be)) {
         bv = v[e];
         be = e;
@@ -265,7 +281,6 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == i) sel_e = be;
   }
-  // gather the chosen scores in selection order through shared memory
   if (lane < k) sel_s[lane] = s[sel_e];
   __syncwarp();
   if (lane == 0) {
@@ -293,15 +308,9 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
                         ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st)
                         : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st);
   if (err != cudaSuccess) return err;
-  const size_t smem = 8 * (size_t)(2 * c.E + 160) * sizeof(float);
-  if (smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-    if (err != cudaSuccess) return err;
-  }
-  route_select_kernel<<<(c.T + 7) / 8, 256, smem, st>>>(partials, bias, topk_idx, topk_w, c.T, c.E,
-                                                         c.k, c.n_group, c.topk_group,
-                                                         c.route_scale);
+  const size_t smem = (size_t)(2 * c.E + 64 + 64 + 32) * sizeof(float);
+  route_select_kernel<<<c.T, kSelThreads, smem, st>>>(partials, bias, topk_idx, topk_w, c.T, c.E,
+                                                      c.k, c.n_group, c.topk_group, c.route_scale);
   return cudaGetLastError();
 }
 
