@@ -35,7 +35,10 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "MoE layer µs & tokens/s vs tokens (1–16K); % of HBM / tensor roofline"
-KERNELS_PER_STEP = 8   # route x2, dispatch x2, ffn schedule, gate/up GEMM, down GEMM, combine
+# route x2, dispatch x2, ffn schedule, gate/up GEMM, down GEMM, combine (+ the shared
+# expert's input quantisation on the e4m3 path)
+def kernels_per_step(cfg):
+    return 8 + (1 if cfg.act == "fp8" and cfg.d_ff_shared else 0)
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -104,6 +107,36 @@ def peaks():
                 "source": "measured"}
     except Exception:
         return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+KERNEL_NAMES = {"ffn_gate_up": "ffn_gemm_{}_kernel<0> (gate/up + SwiGLU)",
+                "ffn_down": "ffn_gemm_{}_kernel<1> (down)",
+                "route": "route_partials_kernel + route_select_kernel",
+                "dispatch": "dispatch_index_kernel + dispatch_copy_kernel",
+                "combine": "combine_kernel", "ffn_setup": "ffn_plan_kernel"}
+
+
+def roofline(cfg, stage, ms, bytes_, flops, pk):
+    """Roofline entry of one stage: the binding roof is the one whose ideal time is longer —
+    HBM (algorithmic bytes / measured copy bandwidth) or the tensor cores (flops / the dtype's
+    peak: measured bf16 burst, e4m3 = 2x that by the nominal ratio)."""
+    tc_peak = pk["bf16"] * (2.0 if cfg.w == "fp8" else 1.0)
+    t_hbm = bytes_[stage] / (pk["hbm"] * 1e9)
+    t_tc = flops.get(stage, 0) / (tc_peak * 1e12) if stage in ("ffn_gate_up", "ffn_down") else 0.0
+    name = KERNEL_NAMES[stage].format("e4m3" if cfg.w == "fp8" else "bf16")
+    base = {"kernel": name, "launch_ms": round(ms, 4),
+            "traffic": measured_traffic(stage, cfg.name),
+            "algorithmic_bytes_per_launch": bytes_[stage],
+            "algorithmic_flops_per_launch": flops.get(stage, 0)}
+    if t_tc > t_hbm:
+        ach = flops[stage] / (ms * 1e-3) / 1e12
+        return {**base, "bound": "tensor", "achieved": round(ach, 1), "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": round(ach / tc_peak, 4),
+                "peak_source": f"{pk['source']} bf16_tflops" + (" x2 (e4m3 nominal ratio)"
+                                                                 if cfg.w == "fp8" else "")}
+    ach = bytes_[stage] / (ms * 1e-3) / 1e9
+    return {**base, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm"], "unit": "GB/s",
+            "frac": round(ach / pk["hbm"], 4), "peak_source": f"{pk['source']} hbm_gbs"}
 
 
 def measured_traffic(kernel, workload_name):
@@ -314,14 +347,7 @@ def main():
         pk = peaks()
         dom = max(r["stage_ms"], key=lambda n: r["stage_ms"][n])
         dom_ms = r["stage_ms"][dom]
-        achieved = b[dom] / (dom_ms * 1e-3) / 1e9
-        roof = {"kernel": {"ffn_gate_up": "ffn_gemm_bf16_kernel<0>",
-                           "ffn_down": "ffn_gemm_bf16_kernel<1>"}.get(dom, dom),
-                "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"],
-                "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
-                "peak_source": f"{pk['source']} hbm_gbs",
-                "traffic": measured_traffic(dom, cfg.name),
-                "algorithmic_bytes_per_launch": b[dom], "launch_ms": round(dom_ms, 4)}
+        roof = roofline(cfg, dom, dom_ms, b, f, pk)
         layer_bytes = sum(b.values())
         tokens_per_s = job_tokens_per_s(cfg.T, world, r["ms"])
         out = {
@@ -336,12 +362,15 @@ def main():
             "layer_us": round(r["ms"] * 1e3, 2),
             "stages_us": {n: round(v * 1e3, 2) for n, v in r["stage_ms"].items()},
             "layer_hbm_frac": round(layer_bytes / (r["ms"] * 1e-3) / 1e9 / pk["hbm"], 4),
+            "stages_roofline": {n: {k2: v2 for k2, v2 in roofline(cfg, n, r["stage_ms"][n], b, f, pk).items()
+                                    if k2 in ("bound", "achieved", "unit", "frac")}
+                                for n in ("ffn_gate_up", "ffn_down")},
             "experts_touched": touched,
             "imbalance_factor": round(float(np.bincount(
                 np.repeat(np.arange(cfg.E), r["counts"].sum(0)), minlength=cfg.E)
                 .reshape(cfg.R, -1).sum(1).max() / (cfg.T * cfg.k / cfg.R)), 4),
             "roofline": roof,
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": kernels_per_step(cfg) * args.steps,
             "clocks": r["clocks"],
             "e2e": {"value": round(job_tokens_per_s(cfg.T, world, r["ms_e2e"]), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,

@@ -16,11 +16,11 @@
 // Two partial buffers in tensor memory alternate so the tensor core computes block kb+1 while
 // the promoter warps read block kb.
 //
-// Roles (320 threads, one CTA per SM, persistent over the unit list):
-//   warp 0      TMA producer (token rows gathered with 1-row boxes; weight tiles 128 rows)
-//   warp 1      tensor-memory allocation; lane 0 issues the MMAs
-//   warps 2..9  promoters / epilogue: warp w owns lanes 32*(w%4).. and the column half
-//               (w-2)/4 of each accumulator (64 columns)
+// Roles (576 threads, one CTA per SM, persistent over the unit list):
+//   warp 0       TMA producer (token rows gathered four at a time or one box; weight tiles)
+//   warp 1       tensor-memory allocation; lane 0 issues the MMAs
+//   warps 2..17  promoters / epilogue: warp w owns lanes 32*(w%4).. and the column quarter
+//                (w-2)/4 of each accumulator (32 columns of gate and of up)
 #include "moe_device.cuh"
 
 namespace moe {
@@ -93,7 +93,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
-constexpr int kThreads8 = 320;
+constexpr int kPromoWarps = 16;                  // 4 per tensor-memory lane quarter
+constexpr int kPromoThreads = kPromoWarps * 32;
+constexpr int kThreads8 = 64 + kPromoThreads;
+// Scale prefetch ring: each promoter thread keeps the (token scale, gate/weight scale, up scale)
+// of the next kRing-1 k-steps in flight with cp.async.
+constexpr int kRing = 4;
+
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_ring() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 2) : "memory");
+}
 
 template <int STAGE, int STAGES>
 struct Fp8Shape {
@@ -103,8 +119,10 @@ struct Fp8Shape {
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   static constexpr int ACC_COLS = NB * 128;          // partial accumulator columns per buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS;     // two partial buffers
-  // stages + alignment slack + barriers (512 B) + amax exchange [2][4][32][2] floats (2 KB)
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 512 + 2048;
+  // stages + barriers (512 B) + amax exchange [2][4][32][4] floats (4 KB)
+  // + scale ring [kRing][3][kPromoThreads] floats (24 KB) + alignment slack
+  static constexpr int RING_OFF = STAGES * STAGE_BYTES + 512 + 4096;
+  static constexpr int SMEM = RING_OFF + kRing * 3 * kPromoThreads * 4 + 1024;
   static_assert(TMEM_COLS <= 512, "tensor memory");
 };
 
@@ -125,7 +143,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
   uint64_t* xbar = pempty + 2;         // [4] amax exchange of the two warps on one lane quarter
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* amax_x = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES + 512);  // [2][4][32][2]
+  float* amax_x = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES + 512);  // [2][4][32][4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -135,9 +153,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&pfull[i], 1);
-      mbar_init(&pempty[i], 256);
+      mbar_init(&pempty[i], kPromoThreads);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 64);
+    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 4 * 32);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -242,7 +260,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_e4m3(128, 128);
+      // gate/up: the gate and up weight tiles sit back to back in shared memory, so one MMA
+      // with N = 256 computes both (columns 0..127 gate, 128..255 up)
+      const uint32_t idesc = idesc_e4m3(128, S::NB * 128);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t pk = 0;  // partial-buffer use counter
@@ -261,9 +281,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
           const uint32_t d0 = tmem + pb * S::ACC_COLS;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t da = smem_desc_sw128(sa + kk * 32);
-            mma_f8(d0, da, smem_desc_sw128(sb + kk * 32), idesc, kk != 0);
-            if (S::NB == 2) mma_f8(d0 + 128, da, smem_desc_sw128(sb + S::B_BYTES + kk * 32), idesc, kk != 0);
+            mma_f8(d0, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc, kk != 0);
           }
           mma_commit(&empty[stage]);
           mma_commit(&pfull[pb]);
@@ -278,18 +296,25 @@ __global__ void __launch_bounds__(kThreads8, 1)
   } else {
     // ------------------------------ promoters / epilogue ------------------------------
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;      // 0: columns 0..63, 1: columns 64..127
+    const int part = (warp - 2) >> 2;      // columns 32*part .. 32*part+31 of each accumulator
     const int r = quarter * 32 + lane;     // token row of the tile (tensor-memory lane)
     const int kb_n = a.k_steps;
-    uint32_t pk = 0;
-    uint32_t it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+    const int pid = threadIdx.x - 64;      // 0 .. kPromoThreads-1
+    float* ring = reinterpret_cast<float*>(smem + S::RING_OFF);
+
+    // Scale sources of one unit for this thread: its token row's scale row and the two weight
+    // block scale rows (gate, up); a lane past the unit's rows reads the weight row instead
+    // (its results are never stored).
+    struct Src {
+      const float* xs;
+      const float* w0;   // the up block's row is w0 + w_up
+    };
+    const int w_up = (STAGE == 0 ? a.b_up_routed : 0) / 128 * kb_n;  // routed and shared alike
+    auto sources = [&](int u) -> Src {
       const Unit8 t = decode_unit8(a, u);
       const bool sh = t.g < 0;
-      const bool live = r < t.nlen;
-      // the A row of this lane and its token-scale row
       long long arow = -1;
-      if (live) {
+      if (r < t.nlen) {
         if (sh) arow = t.n0 + r;
         else if (STAGE == 0) {
           const int ci = a.grp_off[t.g] + t.n0 + r;
@@ -299,21 +324,54 @@ __global__ void __launch_bounds__(kThreads8, 1)
         }
         if (!sh && (arow < 0 || arow >= a.a_rows_routed)) arow = -1;
       }
-      const float* xs = arow >= 0 ? (sh ? a.a_sc_shared : a.a_sc_routed) + arow * kb_n : nullptr;
       const float* wsc = sh ? a.w_sc_shared
                             : a.w_sc_routed + (size_t)t.g * (a.b_rows_routed / 128) * kb_n;
-      const int blk0 = t.m;
-      const int blk1 = t.m + (sh ? a.b_up_shared : a.b_up_routed) / 128;
-      float acc0[64], acc1[64];
+      Src q;
+      q.w0 = wsc + (size_t)t.m * kb_n;
+      q.xs = arow >= 0 ? (sh ? a.a_sc_shared : a.a_sc_routed) + arow * kb_n : q.w0;
+      return q;
+    };
+    // prefetch cursor: unit pu, k-step pks (runs kRing-1 k-steps ahead of consumption)
+    int pu = blockIdx.x, pks = 0;
+    Src ps = pu < units ? sources(pu) : Src{nullptr, nullptr};
+    // the cursor's stream position is always pk + kRing - 1 (pk: consumed k-steps)
+    uint32_t pk = 0;
+    auto prefetch_one = [&]() {
+      if (pu < units) {
+        float* slot = ring + ((pk + kRing - 1) % kRing) * 3 * kPromoThreads + pid;
+        cp_async4(slot, ps.xs + pks);
+        cp_async4(slot + kPromoThreads, ps.w0 + pks);
+        if (S::NB == 2) cp_async4(slot + 2 * kPromoThreads, ps.w0 + w_up + pks);
+        if (++pks == kb_n) {
+          pks = 0;
+          pu += gridDim.x;
+          if (pu < units) ps = sources(pu);
+        }
+      }
+      cp_async_commit();   // an empty group past the end keeps the group count uniform
+    };
+    // prime the ring: stream positions 0 .. kRing-2
+    for (int i = 0; i < kRing - 1; ++i) {
+      pk = static_cast<uint32_t>(i) - (kRing - 1);   // so that pk + kRing - 1 == i
+      prefetch_one();
+    }
+    pk = 0;
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+      const Unit8 t = decode_unit8(a, u);
+      const bool sh = t.g < 0;
+      const bool live = r < t.nlen;
+      float acc0[32], acc1[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc0[j] = acc1[j] = 0.0f;
-      float xs_next = xs ? __ldg(xs) : 0.0f;
+      for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = 0.0f;
       bool ok = true;
       for (int ks = 0; ks < kb_n; ++ks, ++pk) {
-        const float xsv = xs_next;
-        if (xs && ks + 1 < kb_n) xs_next = __ldg(xs + ks + 1);
-        const float s0 = xsv * __ldg(wsc + blk0 * kb_n + ks);
-        const float s1 = S::NB == 2 ? xsv * __ldg(wsc + blk1 * kb_n + ks) : 0.0f;
+        cp_async_wait_ring();               // this k-step's scales have landed
+        const float* slot = ring + (pk % kRing) * 3 * kPromoThreads + pid;
+        const float xsv = slot[0];
+        const float s0 = xsv * slot[kPromoThreads];
+        const float s1 = S::NB == 2 ? xsv * slot[2 * kPromoThreads] : 0.0f;
+        prefetch_one();
         const uint32_t pb = pk & 1u;
         if (!mbar_wait(&pfull[pb], (pk >> 1) & 1u, abort_flag, a.status)) {
           ok = false;
@@ -321,24 +379,24 @@ __global__ void __launch_bounds__(kThreads8, 1)
         }
         tc_fence_after();
         const uint32_t tb = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + pb * S::ACC_COLS +
-                            half * 64;
+                            part * 32;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tb + c * 32, v);
+          uint32_t v[16];
+          tmem_ld16(tb + c * 16, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc0[c * 32 + j] = fmaf(__uint_as_float(v[j]), s0, acc0[c * 32 + j]);
+          for (int j = 0; j < 16; ++j) acc0[c * 16 + j] = fmaf(__uint_as_float(v[j]), s0, acc0[c * 16 + j]);
         }
         if (S::NB == 2) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tb + 128 + c * 32, v);
+            uint32_t v[16];
+            tmem_ld16(tb + 128 + c * 16, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              acc1[c * 32 + j] = fmaf(__uint_as_float(v[j]), s1, acc1[c * 32 + j]);
+            for (int j = 0; j < 16; ++j)
+              acc1[c * 16 + j] = fmaf(__uint_as_float(v[j]), s1, acc1[c * 16 + j]);
           }
         }
         tc_fence_before();
@@ -350,27 +408,27 @@ __global__ void __launch_bounds__(kThreads8, 1)
       if (STAGE == 0) {
         float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < 32; ++j) {
           acc0[j] = silu(acc0[j]) * acc1[j];
           amax = fmaxf(amax, fabsf(acc0[j]));
         }
-        // the 128-column block of h is split between this warp and the one on the same lane
-        // quarter: exchange the two halves' amax (slots alternate by unit parity so a fast
-        // warp's next write never meets its partner's pending read)
-        float* slot = amax_x + (((it & 1u) * 4 + quarter) * 32 + lane) * 2;
-        slot[half] = amax;
+        // the 128-column block of h is split over the four warps of this lane quarter:
+        // exchange their amax (slots alternate by unit parity so a fast warp's next write never
+        // meets a partner's pending read)
+        float* slot = amax_x + (((it & 1u) * 4 + quarter) * 32 + lane) * 4;
+        slot[part] = amax;
         mbar_arrive(&xbar[quarter]);
         if (!mbar_wait(&xbar[quarter], it & 1u, abort_flag, a.status)) break;
-        amax = fmaxf(slot[0], slot[1]);
+        amax = fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
         const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
         if (live) {
           long long orow = sh ? (long long)t.n0 + r : (long long)a.grp_off[t.g] + t.n0 + r;
           const bool in = sh || (orow >= 0 && orow < a.tk);
           if (in) {
             uint8_t* out = static_cast<uint8_t*>(sh ? a.out_shared : a.out_routed) +
-                           orow * (sh ? a.ld_shared : a.ld_routed) + t.m * 128 + half * 64;
+                           orow * (sh ? a.ld_shared : a.ld_routed) + t.m * 128 + part * 32;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
               uint32_t w[4];
 #pragma unroll
               for (int b = 0; b < 4; ++b) {
@@ -385,7 +443,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
               }
               reinterpret_cast<uint4*>(out)[q] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            if (half == 0) {
+            if (part == 0) {
               float* osc = sh ? a.out_sc_shared : a.out_sc_routed;
               const int nblk = (sh ? a.ld_shared : a.ld_routed) / 128;
               osc[orow * nblk + t.m] = scale;
@@ -406,9 +464,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
         if (in) {
           uint4* out = reinterpret_cast<uint4*>(
               static_cast<__nv_bfloat16*>(sh ? a.out_shared : a.out_routed) +
-              orow * (sh ? a.ld_shared : a.ld_routed) + t.m * 128 + half * 64);
+              orow * (sh ? a.ld_shared : a.ld_routed) + t.m * 128 + part * 32);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < 4; ++q) {
             const int j = q * 8;
             out[q] = make_uint4(pack_bf16x2(acc0[j], acc0[j + 1]), pack_bf16x2(acc0[j + 2], acc0[j + 3]),
                                 pack_bf16x2(acc0[j + 4], acc0[j + 5]), pack_bf16x2(acc0[j + 6], acc0[j + 7]));

@@ -106,6 +106,11 @@ CONFIGS = {
     "dsv3_decode_e32": MoEConfig("dsv3_decode_e32", T=64, d=7168, E=32, k=8, n_group=8,
                                  topk_group=4, d_ff=2048, d_ff_shared=2048, R=8,
                                  route_scale=2.5, seed=1000),
+    # Profiling stand-in for the bf16 prefill layer: the same per-expert shapes, 32 experts and
+    # 512 tokens (128 rows per expert, as at T=4096 with 256 experts), ~2.9 GB of weights.
+    "dsv3_prefill_e32": MoEConfig("dsv3_prefill_e32", T=512, d=7168, E=32, k=8, n_group=8,
+                                  topk_group=4, d_ff=2048, d_ff_shared=2048, R=8,
+                                  route_scale=2.5, seed=3000),
     # Profiling stand-in for the FP8 prefill layer: the same per-expert shapes, 32 experts and
     # 2048 tokens (512 rows per expert, as at T=16384 with 256 experts), ~1.5 GB of weights.
     "dsv3_fp8_e32": MoEConfig("dsv3_fp8_e32", T=2048, d=7168, E=32, k=8, n_group=8, topk_group=4,
