@@ -158,8 +158,10 @@ struct GemmArgs {
   void* out_shared;       // gate/up: hs [T][Fs]; down: shared_out [T][d]
   int ld_routed;          // output row length (elements)
   int ld_shared;
-  int box_routed;         // down stage: rows per box of the routed / shared input maps
+  int box_routed;         // rows per box of the contiguous token-row maps (routed / shared)
   int box_shared;
+  const uint8_t* gather_base;  // gate/up: receive buffer (routed token rows are gathered)
+  long long gather_ld;         // bytes per receive row
   uint32_t* status;
 };
 
@@ -190,7 +192,14 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
   return r;
 }
 
-constexpr int kThreads = 192;
+// Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies.
+constexpr int kGatherWarps = 2;
+constexpr int kGatherThreads = kGatherWarps * 32;
+template <int STAGE>
+struct GemmThreads {
+  static constexpr int kGather = STAGE == 0 ? kGatherThreads : 0;
+  static constexpr int kAll = 192 + kGather;
+};
 
 template <int STAGE, int BN, int STAGES>
 struct GemmShape {
@@ -206,7 +215,7 @@ struct GemmShape {
 };
 
 template <int STAGE, int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     ffn_gemm_bf16_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap mapA,
                          const __grid_constant__ CUtensorMap mapAs,
                          const __grid_constant__ CUtensorMap mapB,
@@ -226,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], 1);
+      // the TMA lane's expect_tx arrival, plus one per gather thread (gate/up)
+      mbar_init(&full[i], 1 + GemmThreads<STAGE>::kGather);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -269,44 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
       const int arow0 = (sh ? 0 : t.g * a.a_rows_routed) + t.m * 128;
       const int arow1 = arow0 + (sh ? a.a_up_shared : a.a_up_routed);
-      // Token rows of the unit. Gate/up: gathered four at a time (tile::gather4, lane j loads
-      // rows 4j..4j+3 of the tile; a missing row repeats a valid one of its group, which only
-      // fills a column the epilogue never stores). Down: the rows are contiguous compact rows,
-      // loaded as one box of box rows per k-step.
-      int g4[4] = {-1, -1, -1, -1};
-      bool g4_on = false;
+      // Token rows of the unit: routed gate/up rows are gathered by the gather warps
+      // (cp.async); the shared expert's rows (x) and the down projection's rows (h) are
+      // contiguous: one box per k-step.
       int box_row = -1;
       uint32_t b_bytes = 0;
-      if (STAGE == 0) {
-        int nbad = 0;
-        if (lane < BN / 4) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int p = 4 * lane + i;
-            int row = -1;
-            if (p < t.nlen) {
-              if (sh) {
-                row = t.n0 + p;
-              } else {
-                const int ci = a.grp_off[t.g] + t.n0 + p;
-                row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
-                if (row >= a.recv_rows) row = -1;
-              }
-              if (row < 0) ++nbad;
-            }
-            g4[i] = row;
-          }
-          int first = -1;
-#pragma unroll
-          for (int i = 3; i >= 0; --i) first = g4[i] >= 0 ? g4[i] : first;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) g4[i] = g4[i] >= 0 ? g4[i] : first;
-          g4_on = first >= 0;
-        }
-        const uint32_t on = __ballot_sync(0xffffffffu, g4_on);
-        if (__any_sync(0xffffffffu, nbad > 0) && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
-        b_bytes = 512u * __popc(on);
-      } else {
+      if (STAGE == 1 || sh) {
         const int row0 = sh ? t.n0 : a.grp_off[t.g] + t.n0;
         const bool in = row0 >= 0 && row0 < (sh ? a.T : a.tk);
         if (!in && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
@@ -325,13 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[stage], tx);
           tma_load_2d(sa, amap, &full[stage], ks * 64, arow0, pol_w);
           if (S::NA == 2) tma_load_2d(sa + S::A_BYTES, amap, &full[stage], ks * 64, arow1, pol_w);
-          if (STAGE == 1 && box_row >= 0)
-            tma_load_2d(sb, bmap, &full[stage], ks * 64, box_row, pol_x);
+          if (box_row >= 0) tma_load_2d(sb, bmap, &full[stage], ks * 64, box_row, pol_x);
         }
         __syncwarp();
-        if (STAGE == 0 && g4_on)
-          tma_gather4(sb + lane * 512, bmap, &full[stage], ks * 64, g4[0], g4[1], g4[2], g4[3],
-                      pol_x);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -379,6 +353,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------ token-row gather (gate/up) ------------------------------
+    // Thread gt copies 16-byte chunk j = gt % 8 of rows p = gt/8 + 8i of the token tile into
+    // the 128-byte-swizzled layout (chunk j of row p at chunk j ^ (p % 8) = j ^ gt/8).
+    // Completion is observed kLag stages late: wait for the copies, make them visible to the
+    // async proxy, then arrive on that stage's barrier.
+    constexpr int kLag = STAGES - 1;
+    constexpr int kRowsPer = BN / 8;
+    const int gt = threadIdx.x - 192;
+    const int j = gt & 7, rg = gt >> 3;
+    const uint32_t dst_off = static_cast<uint32_t>(rg * 128 + ((j ^ rg) << 4));
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t q = 0;  // k-steps issued
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit t = decode_unit<BN>(a, u);
+      const bool gather = STAGE == 0 && t.g >= 0;
+      const uint8_t* src[kRowsPer];
+#pragma unroll
+      for (int i = 0; i < kRowsPer; ++i) {
+        const int p = rg + 8 * i;
+        src[i] = nullptr;
+        if (gather && p < t.nlen) {
+          const int ci = a.grp_off[t.g] + t.n0 + p;
+          const long long row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+          if (row >= 0 && row < a.recv_rows) src[i] = a.gather_base + row * a.gather_ld + j * 16;
+          else raise_status(a.status, MOE_DEV_BOUNDS);
+        }
+      }
+      for (int ks = 0; ks < a.k_steps; ++ks) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sb =
+            smem_addr(smem + stage * S::STAGE_BYTES + S::NA * S::A_BYTES) + dst_off;
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i)
+          if (src[i])
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sb + i * 1024),
+                         "l"(src[i] + ks * 128)
+                         : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (++q > kLag) {
+          asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
+          fence_proxy_async_smem();
+          mbar_arrive(&full[(q - 1 - kLag) % STAGES]);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // the last kLag stages (or, after an abort, every copy still in flight)
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    fence_proxy_async_smem();
+    if (ok)
+      for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2) mbar_arrive(&full[r2 % STAGES]);
   } else {
     // ------------------------------ epilogue ------------------------------
     const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
@@ -442,7 +476,7 @@ cudaError_t run_gemm(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
   if (err != cudaSuccess) return err;
-  kern<<<sm_count(), kThreads, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+  kern<<<sm_count(), GemmThreads<STAGE>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
   return cudaGetLastError();
 }
 
@@ -547,11 +581,15 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
     a.out_shared = has_shared ? static_cast<void*>(ws + L.hs) : nullptr;
     a.ld_routed = F;
     a.ld_shared = Fs;
+    a.gather_base = static_cast<const uint8_t*>(recv);
+    a.gather_ld = 2ll * d;
+    a.box_routed = 1;
+    a.box_shared = c.T < L.bn ? c.T : L.bn;
     ok &= make_tensor_map_2d(&mA, w.w13, 2, d, (uint64_t)c.E * 2 * F, 128);
     ok &= make_tensor_map_2d(&mB, recv, 2, d, recv_rows, 1);
     if (has_shared) {
       ok &= make_tensor_map_2d(&mAs, w.ws13, 2, d, 2ull * Fs, 128);
-      ok &= make_tensor_map_2d(&mBs, x, 2, d, c.T, 1);
+      ok &= make_tensor_map_2d(&mBs, x, 2, d, c.T, a.box_shared);
     }
   } else {
     a.mt_routed = d / 128;

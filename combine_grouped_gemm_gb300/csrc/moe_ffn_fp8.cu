@@ -49,7 +49,9 @@ struct Fp8Args {
   float* out_sc_shared;
   int ld_routed, ld_shared;     // output row length (elements)
   long long out_rows_routed;    // bound of routed output row indices
-  int box_routed, box_shared;   // down stage: rows per box of the routed / shared input maps
+  int box_routed, box_shared;   // rows per box of the contiguous token-row maps
+  const uint8_t* gather_base;   // gate/up: receive buffer (routed token rows are gathered)
+  long long gather_ld;          // bytes per receive row
   uint32_t* status;
 };
 
@@ -95,7 +97,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 constexpr int kPromoWarps = 16;                  // 4 per tensor-memory lane quarter
 constexpr int kPromoThreads = kPromoWarps * 32;
-constexpr int kThreads8 = 64 + kPromoThreads;
+// Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies.
+constexpr int kGatherWarps = 2;
+constexpr int kGatherThreads = kGatherWarps * 32;
+template <int STAGE>
+struct Fp8Threads {
+  static constexpr int kGather = STAGE == 0 ? kGatherThreads : 0;
+  static constexpr int kAll = 64 + kPromoThreads + kGather;
+};
 // Scale prefetch ring: each promoter thread keeps the (token scale, gate/weight scale, up scale)
 // of the next kRing-1 k-steps in flight with cp.async.
 constexpr int kRing = 4;
@@ -127,7 +136,7 @@ struct Fp8Shape {
 };
 
 template <int STAGE, int STAGES>
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     ffn_gemm_e4m3_kernel(const Fp8Args a, const __grid_constant__ CUtensorMap mapA,
                          const __grid_constant__ CUtensorMap mapAs,
                          const __grid_constant__ CUtensorMap mapB,
@@ -148,7 +157,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], 1);
+      // the TMA lane's expect_tx arrival, plus one per gather thread (gate/up)
+      mbar_init(&full[i], 1 + Fp8Threads<STAGE>::kGather);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -191,41 +201,12 @@ __global__ void __launch_bounds__(kThreads8, 1)
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
       const int brow0 = (sh ? 0 : t.g * a.b_rows_routed) + t.m * 128;
       const int brow1 = brow0 + (sh ? a.b_up_shared : a.b_up_routed);
-      // Token rows: gate/up gathers them four at a time (tile::gather4; lane j loads rows
-      // 4j..4j+3; a missing row repeats a valid one of its group, filling a lane whose result
-      // is never stored); down reads contiguous compact rows as one box per k-step.
-      int g4[4] = {-1, -1, -1, -1};
-      bool g4_on = false;
+      // Token rows: routed gate/up rows are gathered by the gather warps (cp.async); the shared
+      // expert's rows (x, contiguous) and the down projection's rows (h, contiguous) are one
+      // box per k-step.
       int box_row = -1;
       uint32_t a_bytes = 0;
-      if (STAGE == 0) {
-        int nbad = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int p = 4 * lane + i;
-          int row = -1;
-          if (p < t.nlen) {
-            if (sh) {
-              row = t.n0 + p;
-            } else {
-              const int ci = a.grp_off[t.g] + t.n0 + p;
-              row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
-              if (row >= a.a_rows_routed) row = -1;
-            }
-            if (row < 0) ++nbad;
-          }
-          g4[i] = row;
-        }
-        int first = -1;
-#pragma unroll
-        for (int i = 3; i >= 0; --i) first = g4[i] >= 0 ? g4[i] : first;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) g4[i] = g4[i] >= 0 ? g4[i] : first;
-        g4_on = first >= 0;
-        const uint32_t on = __ballot_sync(0xffffffffu, g4_on);
-        if (__any_sync(0xffffffffu, nbad > 0) && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
-        a_bytes = 512u * __popc(on);
-      } else {
+      if (STAGE == 1 || sh) {
         const int row0 = sh ? t.n0 : a.grp_off[t.g] + t.n0;
         const bool in = row0 >= 0 && row0 < (sh ? a.T : a.tk);
         if (!in && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
@@ -244,13 +225,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
           mbar_arrive_expect_tx(&full[stage], tx);
           tma_load_2d(sb, bmap, &full[stage], ks * 128, brow0, pol_w);
           if (S::NB == 2) tma_load_2d(sb + S::B_BYTES, bmap, &full[stage], ks * 128, brow1, pol_w);
-          if (STAGE == 1 && box_row >= 0)
-            tma_load_2d(sa, amap, &full[stage], ks * 128, box_row, pol_x);
+          if (box_row >= 0) tma_load_2d(sa, amap, &full[stage], ks * 128, box_row, pol_x);
         }
         __syncwarp();
-        if (STAGE == 0 && g4_on)
-          tma_gather4(sa + lane * 512, amap, &full[stage], ks * 128, g4[0], g4[1], g4[2], g4[3],
-                      pol_x);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -293,6 +270,64 @@ __global__ void __launch_bounds__(kThreads8, 1)
       }
     }
     __syncwarp();
+  } else if (warp >= 2 + kPromoWarps) {
+    // ------------------------------ token-row gather (gate/up) ------------------------------
+    // Thread gt copies 16-byte chunk j = gt % 8 of rows p = gt/8 + 8i (i < 16) of the tile
+    // into the 128-byte-swizzled layout the MMA descriptor expects (chunk j of row p at
+    // chunk j ^ (p % 8) = j ^ gt/8). Completion is observed kLag stages late: wait for the
+    // copies, make them visible to the async proxy, then arrive on that stage's barrier.
+    constexpr int kLag = STAGES - 1;
+    const int gt = threadIdx.x - (64 + kPromoThreads);
+    const int j = gt & 7, rg = gt >> 3;
+    const uint32_t dst_off = static_cast<uint32_t>(rg * 128 + ((j ^ rg) << 4));
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t q = 0;  // k-steps issued
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit8 t = decode_unit8(a, u);
+      const bool gather = STAGE == 0 && t.g >= 0;
+      const uint8_t* src[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int p = rg + 8 * i;
+        src[i] = nullptr;
+        if (gather && p < t.nlen) {
+          const int ci = a.grp_off[t.g] + t.n0 + p;
+          const long long row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+          if (row >= 0 && row < a.a_rows_routed) src[i] = a.gather_base + row * a.gather_ld + j * 16;
+          else raise_status(a.status, MOE_DEV_BOUNDS);
+        }
+      }
+      for (int ks = 0; ks < a.k_steps; ++ks) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_addr(smem + stage * S::STAGE_BYTES) + dst_off;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (src[i])
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa + i * 1024),
+                         "l"(src[i] + ks * 128)
+                         : "memory");
+        cp_async_commit();
+        if (++q > kLag) {
+          asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
+          fence_proxy_async_smem();
+          mbar_arrive(&full[(q - 1 - kLag) % STAGES]);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // the last kLag stages (or, after an abort, every copy still in flight)
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    fence_proxy_async_smem();
+    if (ok)
+      for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2) mbar_arrive(&full[r2 % STAGES]);
   } else {
     // ------------------------------ promoters / epilogue ------------------------------
     const int quarter = warp & 3;
@@ -523,10 +558,14 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     a.out_sc_shared = reinterpret_cast<float*>(ws + L.hs_scales);
     a.ld_routed = F;
     a.ld_shared = Fs;
+    a.gather_base = static_cast<const uint8_t*>(recv);
+    a.gather_ld = d;
+    a.box_routed = 1;
+    a.box_shared = c.T < 128 ? c.T : 128;
     ok &= make_tensor_map_2d(&mA, recv, 1, d, recv_rows, 1);
     ok &= make_tensor_map_2d(&mB, w.w13, 1, d, (uint64_t)c.E * 2 * F, 128);
     if (has_shared) {
-      ok &= make_tensor_map_2d(&mAs, ws + L.xq, 1, d, c.T, 1);
+      ok &= make_tensor_map_2d(&mAs, ws + L.xq, 1, d, c.T, a.box_shared);
       ok &= make_tensor_map_2d(&mBs, w.ws13, 1, d, 2ull * Fs, 128);
     }
   } else {
@@ -566,13 +605,13 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     auto kern = ffn_gemm_e4m3_kernel<0, 4>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (err != cudaSuccess) return err;
-    kern<<<sm_count(), kThreads8, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+    kern<<<sm_count(), Fp8Threads<0>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
   } else {
     using S = Fp8Shape<1, 6>;
     auto kern = ffn_gemm_e4m3_kernel<1, 6>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (err != cudaSuccess) return err;
-    kern<<<sm_count(), kThreads8, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+    kern<<<sm_count(), Fp8Threads<1>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
   }
   return cudaGetLastError();
 }
