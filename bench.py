@@ -35,10 +35,10 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "MoE layer µs & tokens/s vs tokens (1–16K); % of HBM / tensor roofline"
-# route x2, dispatch x2, ffn schedule, gate/up GEMM, down GEMM, combine (+ the shared
-# expert's input quantisation on the e4m3 path)
+# route x2, dispatch x2, ffn schedule x2 (plan, row list), gate/up GEMM, down GEMM, combine
+# (+ the shared expert's input quantisation on the e4m3 path)
 def kernels_per_step(cfg):
-    return 8 + (1 if cfg.act == "fp8" and cfg.d_ff_shared else 0)
+    return 9 + (1 if cfg.act == "fp8" and cfg.d_ff_shared else 0)
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -113,7 +113,7 @@ KERNEL_NAMES = {"ffn_gate_up": "ffn_gemm_{}_kernel<0> (gate/up + SwiGLU)",
                 "ffn_down": "ffn_gemm_{}_kernel<1> (down)",
                 "route": "route_partials_kernel + route_select_kernel",
                 "dispatch": "dispatch_index_kernel + dispatch_copy_kernel",
-                "combine": "combine_kernel", "ffn_setup": "ffn_plan_kernel"}
+                "combine": "combine_kernel", "ffn_setup": "ffn_plan_kernel + ffn_rows_kernel"}
 
 
 def roofline(cfg, stage, ms, bytes_, flops, pk):

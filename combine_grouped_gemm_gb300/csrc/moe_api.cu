@@ -65,6 +65,8 @@ WsLayout ws_layout(const moe_cfg& c) {
   L.hs_scales = o;  o = up256(o + (fp8 ? sizeof(float) * (size_t)c.T * (c.d_ff_shared / 128) : 0));
   L.xq = o;         o = up256(o + (fp8 && c.d_ff_shared ? (size_t)c.T * c.d : 0));
   L.xq_scales = o;  o = up256(o + (fp8 && c.d_ff_shared ? sizeof(float) * (size_t)c.T * (c.d / 128) : 0));
+  L.run_start = o;  o = up256(o + sizeof(int32_t) * (size_t)c.R * c.E);
+  L.run_pre = o;    o = up256(o + sizeof(int32_t) * (size_t)c.R * c.E);
   L.total = o;
   return L;
 }

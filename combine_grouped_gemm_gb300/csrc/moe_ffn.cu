@@ -71,12 +71,15 @@ __device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
   return ex;
 }
 
-// From counts[R][E]: rows per expert, their compact offsets, the receive row of every compact
-// row (expert-major, then source rank, then position), and the list of token tiles.
+// From counts[R][E]: rows per expert and their compact offsets, the list of token tiles, and
+// for every (source, expert) run the receive row of its first row and the number of the
+// expert's rows from earlier sources (compact rows are expert-major, then source, then
+// position). The row list itself is filled by ffn_rows_kernel.
 __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     const int32_t* __restrict__ counts, int32_t* __restrict__ grp_n, int32_t* __restrict__ grp_off,
-    int32_t* __restrict__ n_tiles, Tile* __restrict__ tiles, int32_t* __restrict__ row_list,
-    uint32_t* status, int E, int R, int cap, int bn, int max_tiles, int tk) {
+    int32_t* __restrict__ n_tiles, Tile* __restrict__ tiles, int32_t* __restrict__ run_start,
+    int32_t* __restrict__ run_pre, uint32_t* status, int E, int R, int cap, int bn, int max_tiles,
+    int tk) {
   __shared__ int warp_sums[33];
   __shared__ int rank_base[64];
   extern __shared__ int32_t cnt_s[];   // counts staged once: [R][E] when it fits, else unused
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     *n_tiles = min(tiles_total, max_tiles);
   }
 
-  // receive rows of every compact row
+  // per (source, expert) run: first receive row, rows from earlier sources
   int pre = 0;
   for (int s = 0; s < R; ++s) {
     const int c = act ? cnt(s) : 0;
@@ -124,15 +127,42 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     if (act) {
       const int r = e / Er;
       const int in_seg = ex - rank_base[r];
-      const int seg0 = (r * R + s) * cap;
-      for (int q = 0; q < c; ++q) {
-        const int dst = off + pre + q;
-        if (dst < tk && in_seg + q < cap) row_list[dst] = seg0 + in_seg + q;
-        else raise_status(status, MOE_DEV_BOUNDS);
-      }
+      if (in_seg + c > cap) raise_status(status, MOE_DEV_BOUNDS);
+      run_start[s * E + e] = (r * R + s) * cap + in_seg;
+      run_pre[s * E + e] = pre;
       pre += c;
     }
     __syncthreads();
+  }
+}
+
+// row_list[c] for every compact row c: its expert by binary search on the compact offsets,
+// its source run by a scan of the run prefixes, then the run's receive row plus the position.
+__global__ void __launch_bounds__(256) ffn_rows_kernel(const int32_t* __restrict__ grp_n,
+                                                       const int32_t* __restrict__ grp_off,
+                                                       const int32_t* __restrict__ run_start,
+                                                       const int32_t* __restrict__ run_pre,
+                                                       int32_t* __restrict__ row_list,
+                                                       uint32_t* status, int E, int R, int tk) {
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < tk; c += gridDim.x * blockDim.x) {
+    int lo = 0, hi = E - 1;  // last expert whose compact offset is <= c
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (grp_off[mid] <= c) lo = mid;
+      else hi = mid - 1;
+    }
+    int e = lo;
+    while (e > 0 && grp_n[e] == 0) --e;  // an empty expert shares its offset with the next
+    while (e < E - 1 && c >= grp_off[e] + grp_n[e]) ++e;
+    const int p = c - grp_off[e];
+    if (p < 0 || p >= grp_n[e]) {
+      raise_status(status, MOE_DEV_BOUNDS);
+      row_list[c] = -1;
+      continue;
+    }
+    int s = 0;
+    while (s + 1 < R && run_pre[(s + 1) * E + e] <= p) ++s;
+    row_list[c] = run_start[s * E + e] + (p - run_pre[s * E + e]);
   }
 }
 
@@ -192,8 +222,10 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
   return r;
 }
 
-// Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies.
+// Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies (tiles of
+// more than kSmallTile rows; smaller ones are four-row TMA gathers).
 constexpr int kGatherWarps = 2;
+constexpr int kSmallTile = 32;
 constexpr int kGatherThreads = kGatherWarps * 32;
 template <int STAGE>
 struct GemmThreads {
@@ -235,8 +267,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      // the TMA lane's expect_tx arrival, plus one per gather thread (gate/up)
-      mbar_init(&full[i], 1 + GemmThreads<STAGE>::kGather);
+      // the TMA lane's expect_tx arrival, plus one per gather warp (gate/up)
+      mbar_init(&full[i], 1 + GemmThreads<STAGE>::kGather / 32);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -279,11 +311,41 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
       const int arow0 = (sh ? 0 : t.g * a.a_rows_routed) + t.m * 128;
       const int arow1 = arow0 + (sh ? a.a_up_shared : a.a_up_routed);
-      // Token rows of the unit: routed gate/up rows are gathered by the gather warps
-      // (cp.async); the shared expert's rows (x) and the down projection's rows (h) are
-      // contiguous: one box per k-step.
+      // Token rows of the unit. Routed gate/up rows are gathered: a small tile (decode) by
+      // this warp with tile::gather4 (lane j loads rows 4j..4j+3; a missing row repeats a valid
+      // one of its group, filling a column the epilogue never stores), a larger one by the
+      // gather warps with cp.async. The shared expert's rows (x) and the down projection's
+      // rows (h) are contiguous: one box per k-step.
       int box_row = -1;
       uint32_t b_bytes = 0;
+      int g4[4] = {-1, -1, -1, -1};
+      bool g4_on = false;
+      if (STAGE == 0 && !sh && t.nlen <= kSmallTile) {
+        int nbad = 0;
+        if (lane < kSmallTile / 4) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int p = 4 * lane + i;
+            int row = -1;
+            if (p < t.nlen) {
+              const int ci = a.grp_off[t.g] + t.n0 + p;
+              row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+              if (row >= a.recv_rows) row = -1;
+              if (row < 0) ++nbad;
+            }
+            g4[i] = row;
+          }
+          int first = -1;
+#pragma unroll
+          for (int i = 3; i >= 0; --i) first = g4[i] >= 0 ? g4[i] : first;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) g4[i] = g4[i] >= 0 ? g4[i] : first;
+          g4_on = first >= 0;
+        }
+        const uint32_t on = __ballot_sync(0xffffffffu, g4_on);
+        if (__any_sync(0xffffffffu, nbad > 0) && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
+        b_bytes = 512u * __popc(on);
+      }
       if (STAGE == 1 || sh) {
         const int row0 = sh ? t.n0 : a.grp_off[t.g] + t.n0;
         const bool in = row0 >= 0 && row0 < (sh ? a.T : a.tk);
@@ -306,6 +368,9 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
           if (box_row >= 0) tma_load_2d(sb, bmap, &full[stage], ks * 64, box_row, pol_x);
         }
         __syncwarp();
+        if (g4_on)
+          tma_gather4(sb + lane * 512, bmap, &full[stage], ks * 64, g4[0], g4[1], g4[2], g4[3],
+                      pol_x);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -370,7 +435,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit t = decode_unit<BN>(a, u);
-      const bool gather = STAGE == 0 && t.g >= 0;
+      const bool gather = STAGE == 0 && t.g >= 0 && t.nlen > kSmallTile;
       const uint8_t* src[kRowsPer];
 #pragma unroll
       for (int i = 0; i < kRowsPer; ++i) {
@@ -400,7 +465,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
         if (++q > kLag) {
           asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
           fence_proxy_async_smem();
-          mbar_arrive(&full[(q - 1 - kLag) % STAGES]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[(q - 1 - kLag) % STAGES]);
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -411,7 +477,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     // the last kLag stages (or, after an abort, every copy still in flight)
     asm volatile("cp.async.wait_all;" ::: "memory");
     fence_proxy_async_smem();
-    if (ok)
+    __syncwarp();
+    if (ok && lane == 0)
       for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2) mbar_arrive(&full[r2 % STAGES]);
   } else {
     // ------------------------------ epilogue ------------------------------
@@ -428,6 +495,27 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
       const int f = t.m * 128 + rrow;  // output column
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sh ? a.out_shared : a.out_routed);
       const int ld = sh ? a.ld_shared : a.ld_routed;
+      // output row of tile column lane + 32*i, looked up once per unit (-1: not stored)
+      long long orows[BN / 32];
+      const int base = sh ? 0 : a.grp_off[t.g];
+#pragma unroll
+      for (int i = 0; i < BN / 32; ++i) {
+        const int p = lane + 32 * i;
+        long long o = -1;
+        if (p < t.nlen) {
+          if (sh) {
+            o = t.n0 + p;
+          } else if (STAGE == 0) {
+            o = base + t.n0 + p;
+            if (o < 0 || o >= a.tk) o = -1;
+          } else {
+            const int ci = base + t.n0 + p;
+            o = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+            if (o >= a.recv_rows) o = -1;
+          }
+        }
+        orows[i] = o;
+      }
       for (int c0 = 0; c0 < t.nlen; c0 += 16) {
         uint32_t ra[16], rb[16];
         tmem_ld16(tb + c0, ra);
@@ -435,20 +523,9 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int p = c0 + j;
-          if (p >= t.nlen) break;
-          long long orow;
-          if (sh) {
-            orow = t.n0 + p;
-          } else if (STAGE == 0) {
-            orow = a.grp_off[t.g] + t.n0 + p;
-            if (orow < 0 || orow >= a.tk) continue;
-          } else {
-            const int ci = a.grp_off[t.g] + t.n0 + p;
-            if (ci < 0 || ci >= a.tk) continue;
-            orow = a.row_list[ci];
-            if (orow < 0 || orow >= a.recv_rows) continue;
-          }
+          const int p = c0 + j;   // c0 is a multiple of 16: column p is lane p % 32 of group p / 32
+          const long long orow = __shfl_sync(0xffffffffu, orows[(c0 >> 5) & (BN / 32 - 1)], p & 31);
+          if (p >= t.nlen || orow < 0) continue;
           float val;
           if (S::NA == 2) val = silu(__uint_as_float(ra[j])) * __uint_as_float(rb[j]);
           else val = __uint_as_float(ra[j]);
@@ -539,11 +616,21 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
   }
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
   const size_t stage = (size_t)c.R * c.E * sizeof(int32_t);
+  const int32_t* grp_n = reinterpret_cast<const int32_t*>(ws + L.grp_n);
+  const int32_t* grp_off = reinterpret_cast<const int32_t*>(ws + L.grp_off);
   ffn_plan_kernel<<<1, kPlanThreads, stage <= kPlanStageBytes ? stage : 0, st>>>(
       counts, reinterpret_cast<int32_t*>(ws + L.grp_n), reinterpret_cast<int32_t*>(ws + L.grp_off),
       reinterpret_cast<int32_t*>(ws + L.n_tiles), reinterpret_cast<Tile*>(ws + L.tiles),
-      reinterpret_cast<int32_t*>(ws + L.row_list), status, c.E, c.R, cap_of(c), L.bn,
-      L.max_tiles, c.T * c.k);
+      reinterpret_cast<int32_t*>(ws + L.run_start), reinterpret_cast<int32_t*>(ws + L.run_pre),
+      status, c.E, c.R, cap_of(c), L.bn, L.max_tiles, c.T * c.k);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int tk = c.T * c.k;
+  const int blocks = (tk + 255) / 256 < 4 * 152 ? (tk + 255) / 256 : 4 * 152;
+  ffn_rows_kernel<<<blocks, 256, 0, st>>>(
+      grp_n, grp_off, reinterpret_cast<const int32_t*>(ws + L.run_start),
+      reinterpret_cast<const int32_t*>(ws + L.run_pre), reinterpret_cast<int32_t*>(ws + L.row_list),
+      status, c.E, c.R, tk);
   return cudaGetLastError();
 }
 

@@ -157,8 +157,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      // the TMA lane's expect_tx arrival, plus one per gather thread (gate/up)
-      mbar_init(&full[i], 1 + Fp8Threads<STAGE>::kGather);
+      // the TMA lane's expect_tx arrival, plus one per gather warp (gate/up)
+      mbar_init(&full[i], 1 + Fp8Threads<STAGE>::kGather / 32);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -315,7 +315,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
         if (++q > kLag) {
           asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
           fence_proxy_async_smem();
-          mbar_arrive(&full[(q - 1 - kLag) % STAGES]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[(q - 1 - kLag) % STAGES]);
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -326,7 +327,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     // the last kLag stages (or, after an abort, every copy still in flight)
     asm volatile("cp.async.wait_all;" ::: "memory");
     fence_proxy_async_smem();
-    if (ok)
+    __syncwarp();
+    if (ok && lane == 0)
       for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2) mbar_arrive(&full[r2 % STAGES]);
   } else {
     // ------------------------------ promoters / epilogue ------------------------------
@@ -415,23 +417,27 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
         tc_fence_after();
         const uint32_t tb = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + pb * S::ACC_COLS +
                             part * 32;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[16];
-          tmem_ld16(tb + c * 16, v);
+        // two tensor-memory loads in flight per wait: the gate columns, then the up columns
+        {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(tb, v0);
+          tmem_ld16(tb + 16, v1);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc0[c * 16 + j] = fmaf(__uint_as_float(v[j]), s0, acc0[c * 16 + j]);
+          for (int j = 0; j < 16; ++j) {
+            acc0[j] = fmaf(__uint_as_float(v0[j]), s0, acc0[j]);
+            acc0[16 + j] = fmaf(__uint_as_float(v1[j]), s0, acc0[16 + j]);
+          }
         }
         if (S::NB == 2) {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(tb + 128, v0);
+          tmem_ld16(tb + 144, v1);
+          tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t v[16];
-            tmem_ld16(tb + 128 + c * 16, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc1[c * 16 + j] = fmaf(__uint_as_float(v[j]), s1, acc1[c * 16 + j]);
+          for (int j = 0; j < 16; ++j) {
+            acc1[j] = fmaf(__uint_as_float(v0[j]), s1, acc1[j]);
+            acc1[16 + j] = fmaf(__uint_as_float(v1[j]), s1, acc1[16 + j]);
           }
         }
         tc_fence_before();

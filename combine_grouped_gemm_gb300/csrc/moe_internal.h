@@ -36,6 +36,8 @@ struct WsLayout {
   size_t hs_scales;   // e4m3: fp32 [T][d_ff_shared/128]
   size_t xq;          // e4m3: quantised shared-expert input [T][d]
   size_t xq_scales;   // e4m3: fp32 [T][d/128]
+  size_t run_start;   // int32 [R][E]: receive row of the first row source s sent expert e
+  size_t run_pre;     // int32 [R][E]: rows of expert e from sources before s
   size_t total;
   int bn;             // token-tile width of the expert GEMMs
   int max_tiles;      // bound on routed tiles: E + T*k/bn

@@ -45,6 +45,15 @@ __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16
 
   const int tid = threadIdx.x;
   const int tx = tid % (BE / TN), ty = tid / (BE / TN);
+  // Thread tile rows / columns. With 8 per side they are two groups of 4 consecutive entries,
+  // half a tile apart, so each group is one conflict-free 16-byte shared load; otherwise rows
+  // are consecutive and columns strided by the thread count along the row.
+  auto row_of = [&](int ty_, int i) {
+    return TM == 8 ? (i < 4 ? ty_ * 4 + i : BT / 2 + ty_ * 4 + (i - 4)) : ty_ * TM + i;
+  };
+  auto col_of = [&](int tx_, int j) {
+    return TN == 8 ? (j < 4 ? tx_ * 4 + j : BE / 2 + tx_ * 4 + (j - 4)) : tx_ + j * (BE / TN);
+  };
   const int e0 = blockIdx.x * BE, t0 = blockIdx.y * BT, c = blockIdx.z;
   const int L = d / kRouteChunks;
   const int kbeg = c * L;
@@ -120,9 +129,9 @@ __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16
     for (int kk = 0; kk < BK; ++kk) {
       float a[TM], b[TN];
 #pragma unroll
-      for (int i = 0; i < TM; ++i) a[i] = xs[buf][kk][ty * TM + i];
+      for (int i = 0; i < TM; ++i) a[i] = xs[buf][kk][row_of(ty, i)];
 #pragma unroll
-      for (int j = 0; j < TN; ++j) b[j] = ws[buf][kk][tx + j * (BE / TN)];
+      for (int j = 0; j < TN; ++j) b[j] = ws[buf][kk][col_of(tx, j)];
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -134,11 +143,11 @@ __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16
 
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
-    const int t = t0 + ty * TM + i;
+    const int t = t0 + row_of(ty, i);
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < TN; ++j) {
-      const int e = e0 + tx + j * (BE / TN);
+      const int e = e0 + col_of(tx, j);
       if (e < E) partials[((size_t)c * T + t) * E + e] = acc[i][j];
     }
   }
