@@ -92,6 +92,10 @@ def algorithmic(cfg, counts):
     b["ffn_down"] = (touched * (d * F * bw + sc_w2) + (d * Fs * bw + sc_w2 if Fs else 0)
                      + (tk + rows_sh) * (F * ba + sc_h) + (tk + rows_sh) * d * 2)
     b["combine"] = tk * d * 2 + (T * d * 2 if Fs else 0) + T * d * 2 + 8 * tk
+    # schedule: counts in, per-expert tables and the row list out (+ the shared expert's input
+    # quantised on the e4m3 path)
+    b["ffn_setup"] = 4 * cfg.R * E * 3 + 8 * E + 4 * tk + (
+        T * d * 2 + T * d + T * (d // 128) * 4 if cfg.act == "fp8" and Fs else 0)
     f = {"route": 2 * T * d * E, "ffn_gate_up": 2 * (tk + rows_sh) * 2 * F * d,
          "ffn_down": 2 * (tk + rows_sh) * F * d}
     return b, f, touched

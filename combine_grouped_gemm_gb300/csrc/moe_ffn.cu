@@ -424,7 +424,11 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     // the 128-byte-swizzled layout (chunk j of row p at chunk j ^ (p % 8) = j ^ gt/8).
     // Completion is observed kLag stages late: wait for the copies, make them visible to the
     // async proxy, then arrive on that stage's barrier.
-    constexpr int kLag = STAGES - 1;
+    // kLag = STAGES - 2: the arrival for stage q waits only for stage q+kLag to be free, i.e.
+    // for the MMAs of k-step q-2, so two k-steps of MMAs can be in flight.
+    constexpr int kLag = STAGES - 2;
+    static_assert(kLag >= 1, "needs at least three stages");
+    uint32_t with_copies = 0;  // bit i: k-step q-1-i issued copies (arrival still owed)
     constexpr int kRowsPer = BN / 8;
     const int gt = threadIdx.x - 192;
     const int j = gt & 7, rg = gt >> 3;
@@ -462,7 +466,14 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
                          "l"(src[i] + ks * 128)
                          : "memory");
         asm volatile("cp.async.commit_group;" ::: "memory");
-        if (++q > kLag) {
+        // a k-step without copies (nothing to gather in this unit) is arrived for at once;
+        // one with copies kLag k-steps later, once its copies have landed
+        with_copies = (with_copies << 1) | (gather ? 1u : 0u);
+        if (!gather) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[q % STAGES]);
+        }
+        if (++q > kLag && ((with_copies >> kLag) & 1u)) {
           asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
           fence_proxy_async_smem();
           __syncwarp();
@@ -479,7 +490,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (ok && lane == 0)
-      for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2) mbar_arrive(&full[r2 % STAGES]);
+      for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2)
+        if ((with_copies >> (q - 1 - r2)) & 1u) mbar_arrive(&full[r2 % STAGES]);
   } else {
     // ------------------------------ epilogue ------------------------------
     const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31

@@ -109,6 +109,18 @@ struct Fp8Threads {
 // of the next kRing-1 k-steps in flight with cp.async.
 constexpr int kRing = 4;
 
+// (a0, a1) += (x0, x1) * s as one packed fp32x2 fused multiply-add (two IEEE fmas).
+__device__ __forceinline__ void ffma2(float& a0, float& a1, uint32_t x0, uint32_t x1, float s) {
+  asm("{\n\t.reg .b64 d, x, w;\n\t"
+      "mov.b64 d, {%0, %1};\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 w, {%4, %4};\n\t"
+      "fma.rn.f32x2 d, x, w, d;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(x0), "r"(x1), "f"(s));
+}
+
 __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
@@ -127,7 +139,10 @@ struct Fp8Shape {
   static constexpr int B_BYTES = 128 * 128;          // 128 weight rows x 128 e4m3
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   static constexpr int ACC_COLS = NB * 128;          // partial accumulator columns per buffer
-  static constexpr int TMEM_COLS = 2 * ACC_COLS;     // two partial buffers
+  // partial buffers: as many as tensor memory holds (2 for gate/up, 4 for down), so the tensor
+  // core can run that many K blocks ahead of the promoters
+  static constexpr int NBUF = 512 / ACC_COLS;
+  static constexpr int TMEM_COLS = NBUF * ACC_COLS;
   // stages + barriers (512 B) + amax exchange [2][4][32][4] floats (4 KB)
   // + scale ring [kRing][3][kPromoThreads] floats (24 KB) + alignment slack
   static constexpr int RING_OFF = STAGES * STAGE_BYTES + 512 + 4096;
@@ -147,9 +162,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* pfull = empty + STAGES;    // [2] partial buffer written
-  uint64_t* pempty = pfull + 2;        // [2] partial buffer read
-  uint64_t* xbar = pempty + 2;         // [4] amax exchange of the two warps on one lane quarter
+  uint64_t* pfull = empty + STAGES;    // [NBUF] partial buffer written
+  uint64_t* pempty = pfull + S::NBUF;  // [NBUF] partial buffer read
+  uint64_t* xbar = pempty + S::NBUF;   // [4] amax exchange of the warps on one lane quarter
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* amax_x = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES + 512);  // [2][4][32][4]
@@ -161,7 +176,7 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       mbar_init(&full[i], 1 + Fp8Threads<STAGE>::kGather / 32);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < S::NBUF; ++i) {
       mbar_init(&pfull[i], 1);
       mbar_init(&pempty[i], kPromoThreads);
     }
@@ -246,8 +261,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         for (int ks = 0; ks < a.k_steps; ++ks, ++pk) {
-          const uint32_t pb = pk & 1u;
-          if (!mbar_wait(&pempty[pb], ((pk >> 1) & 1u) ^ 1u, abort_flag, a.status) ||
+          const uint32_t pb = pk % S::NBUF;
+          if (!mbar_wait(&pempty[pb], ((pk / S::NBUF) & 1u) ^ 1u, abort_flag, a.status) ||
               !mbar_wait(&full[stage], phase, abort_flag, a.status)) {
             ok = false;
             break;
@@ -276,7 +291,11 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     // into the 128-byte-swizzled layout the MMA descriptor expects (chunk j of row p at
     // chunk j ^ (p % 8) = j ^ gt/8). Completion is observed kLag stages late: wait for the
     // copies, make them visible to the async proxy, then arrive on that stage's barrier.
-    constexpr int kLag = STAGES - 1;
+    // kLag = STAGES - 2: the arrival for stage q waits only for stage q+kLag to be free, i.e.
+    // for the MMAs of k-step q-2, so two k-steps of MMAs can be in flight.
+    constexpr int kLag = STAGES - 2;
+    static_assert(kLag >= 1, "needs at least three stages");
+    uint32_t with_copies = 0;  // bit i: k-step q-1-i issued copies (arrival still owed)
     const int gt = threadIdx.x - (64 + kPromoThreads);
     const int j = gt & 7, rg = gt >> 3;
     const uint32_t dst_off = static_cast<uint32_t>(rg * 128 + ((j ^ rg) << 4));
@@ -312,7 +331,14 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
                          "l"(src[i] + ks * 128)
                          : "memory");
         cp_async_commit();
-        if (++q > kLag) {
+        // a k-step without copies (nothing to gather in this unit) is arrived for at once;
+        // one with copies kLag k-steps later, once its copies have landed
+        with_copies = (with_copies << 1) | (gather ? 1u : 0u);
+        if (!gather) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[q % STAGES]);
+        }
+        if (++q > kLag && ((with_copies >> kLag) & 1u)) {
           asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
           fence_proxy_async_smem();
           __syncwarp();
@@ -329,7 +355,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (ok && lane == 0)
-      for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2) mbar_arrive(&full[r2 % STAGES]);
+      for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2)
+        if ((with_copies >> (q - 1 - r2)) & 1u) mbar_arrive(&full[r2 % STAGES]);
   } else {
     // ------------------------------ promoters / epilogue ------------------------------
     const int quarter = warp & 3;
@@ -409,24 +436,25 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
         const float s0 = xsv * slot[kPromoThreads];
         const float s1 = S::NB == 2 ? xsv * slot[2 * kPromoThreads] : 0.0f;
         prefetch_one();
-        const uint32_t pb = pk & 1u;
-        if (!mbar_wait(&pfull[pb], (pk >> 1) & 1u, abort_flag, a.status)) {
+        const uint32_t pb = pk % S::NBUF;
+        if (!mbar_wait(&pfull[pb], (pk / S::NBUF) & 1u, abort_flag, a.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t tb = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + pb * S::ACC_COLS +
                             part * 32;
-        // two tensor-memory loads in flight per wait: the gate columns, then the up columns
+        // two tensor-memory loads in flight per wait: the gate columns, then the up columns;
+        // packed fp32x2 FMAs
         {
           uint32_t v0[16], v1[16];
           tmem_ld16(tb, v0);
           tmem_ld16(tb + 16, v1);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            acc0[j] = fmaf(__uint_as_float(v0[j]), s0, acc0[j]);
-            acc0[16 + j] = fmaf(__uint_as_float(v1[j]), s0, acc0[16 + j]);
+          for (int j = 0; j < 16; j += 2) {
+            ffma2(acc0[j], acc0[j + 1], v0[j], v0[j + 1], s0);
+            ffma2(acc0[16 + j], acc0[17 + j], v1[j], v1[j + 1], s0);
           }
         }
         if (S::NB == 2) {
@@ -435,9 +463,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
           tmem_ld16(tb + 144, v1);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            acc1[j] = fmaf(__uint_as_float(v0[j]), s1, acc1[j]);
-            acc1[16 + j] = fmaf(__uint_as_float(v1[j]), s1, acc1[16 + j]);
+          for (int j = 0; j < 16; j += 2) {
+            ffma2(acc1[j], acc1[j + 1], v0[j], v0[j + 1], s1);
+            ffma2(acc1[16 + j], acc1[17 + j], v1[j], v1[j + 1], s1);
           }
         }
         tc_fence_before();
