@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
+      mbar_init(&tempty[i], 4);   // one arrival per epilogue warp
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -545,7 +545,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
     }
   }
 

@@ -80,35 +80,6 @@ __device__ __forceinline__ Unit8 decode_unit8(const Fp8Args& a, int u) {
   return r;
 }
 
-// 32 lanes x 32 bits, 32 consecutive columns.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-}
-
-constexpr int kPromoWarps = 16;                  // 4 per tensor-memory lane quarter
-constexpr int kPromoThreads = kPromoWarps * 32;
-// Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies.
-constexpr int kGatherWarps = 2;
-constexpr int kGatherThreads = kGatherWarps * 32;
-template <int STAGE>
-struct Fp8Threads {
-  static constexpr int kGather = STAGE == 0 ? kGatherThreads : 0;
-  static constexpr int kAll = 64 + kPromoThreads + kGather;
-};
-// Scale prefetch ring: each promoter thread keeps the (token scale, gate/weight scale, up scale)
-// of the next kRing-1 k-steps in flight with cp.async.
-constexpr int kRing = 4;
-
 // (a0, a1) += (x0, x1) * s as one packed fp32x2 fused multiply-add (two IEEE fmas).
 __device__ __forceinline__ void ffma2(float& a0, float& a1, uint32_t x0, uint32_t x1, float s) {
   asm("{\n\t.reg .b64 d, x, w;\n\t"
@@ -144,9 +115,10 @@ struct Fp8Shape {
   static constexpr int NBUF = 512 / ACC_COLS;
   static constexpr int TMEM_COLS = NBUF * ACC_COLS;
   // stages + barriers (512 B) + amax exchange [2][4][32][4] floats (4 KB)
-  // + scale ring [kRing][3][kPromoThreads] floats (24 KB) + alignment slack
+  // + scale ring: token scales [kRing][kPromoThreads] and weight scales [kRing][kPromoWarps][2]
+  // floats + alignment slack
   static constexpr int RING_OFF = STAGES * STAGE_BYTES + 512 + 4096;
-  static constexpr int SMEM = RING_OFF + kRing * 3 * kPromoThreads * 4 + 1024;
+  static constexpr int SMEM = RING_OFF + kRing * (kPromoThreads + 2 * kPromoWarps) * 4 + 1024;
   static_assert(TMEM_COLS <= 512, "tensor memory");
 };
 
@@ -178,9 +150,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     }
     for (int i = 0; i < S::NBUF; ++i) {
       mbar_init(&pfull[i], 1);
-      mbar_init(&pempty[i], kPromoThreads);
+      mbar_init(&pempty[i], kPromoWarps);   // one arrival per promoter warp
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 4 * 32);
+    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 4);   // the four warps of a lane quarter
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -364,7 +336,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     const int r = quarter * 32 + lane;     // token row of the tile (tensor-memory lane)
     const int kb_n = a.k_steps;
     const int pid = threadIdx.x - 64;      // 0 .. kPromoThreads-1
-    float* ring = reinterpret_cast<float*>(smem + S::RING_OFF);
+    const int pw = pid >> 5;               // promoter warp 0 .. kPromoWarps-1
+    float* ring = reinterpret_cast<float*>(smem + S::RING_OFF);           // token scales
+    float* wring = ring + kRing * kPromoThreads;                         // weight scales
 
     // Scale sources of one unit for this thread: its token row's scale row and the two weight
     // block scale rows (gate, up); a lane past the unit's rows reads the weight row instead
@@ -402,10 +376,13 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     uint32_t pk = 0;
     auto prefetch_one = [&]() {
       if (pu < units) {
-        float* slot = ring + ((pk + kRing - 1) % kRing) * 3 * kPromoThreads + pid;
-        cp_async4(slot, ps.xs + pks);
-        cp_async4(slot + kPromoThreads, ps.w0 + pks);
-        if (S::NB == 2) cp_async4(slot + 2 * kPromoThreads, ps.w0 + w_up + pks);
+        const uint32_t r8 = (pk + kRing - 1) % kRing;
+        cp_async4(ring + r8 * kPromoThreads + pid, ps.xs + pks);
+        if (lane == 0) {   // the two weight scales are the same for the whole warp
+          float* wslot = wring + (r8 * kPromoWarps + pw) * 2;
+          cp_async4(wslot, ps.w0 + pks);
+          if (S::NB == 2) cp_async4(wslot + 1, ps.w0 + w_up + pks);
+        }
         if (++pks == kb_n) {
           pks = 0;
           pu += gridDim.x;
@@ -431,10 +408,11 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       bool ok = true;
       for (int ks = 0; ks < kb_n; ++ks, ++pk) {
         cp_async_wait_ring();               // this k-step's scales have landed
-        const float* slot = ring + (pk % kRing) * 3 * kPromoThreads + pid;
-        const float xsv = slot[0];
-        const float s0 = xsv * slot[kPromoThreads];
-        const float s1 = S::NB == 2 ? xsv * slot[2 * kPromoThreads] : 0.0f;
+        __syncwarp();                       // (lane 0's weight-scale copies included)
+        const float xsv = ring[(pk % kRing) * kPromoThreads + pid];
+        const float* wslot = wring + ((pk % kRing) * kPromoWarps + pw) * 2;
+        const float s0 = xsv * wslot[0];
+        const float s1 = S::NB == 2 ? xsv * wslot[1] : 0.0f;
         prefetch_one();
         const uint32_t pb = pk % S::NBUF;
         if (!mbar_wait(&pfull[pb], (pk / S::NBUF) & 1u, abort_flag, a.status)) {
@@ -469,7 +447,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&pempty[pb]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty[pb]);
       }
       if (!ok) break;
 
@@ -486,7 +465,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
         // meets a partner's pending read)
         float* slot = amax_x + (((it & 1u) * 4 + quarter) * 32 + lane) * 4;
         slot[part] = amax;
-        mbar_arrive(&xbar[quarter]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xbar[quarter]);
         if (!mbar_wait(&xbar[quarter], it & 1u, abort_flag, a.status)) break;
         amax = fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
         const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;

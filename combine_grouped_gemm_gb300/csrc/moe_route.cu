@@ -24,6 +24,19 @@
 namespace moe {
 namespace {
 
+// (c0, c1) = (x0 * a + c0, x1 * a + c1): one packed fp32x2 fused multiply-add, i.e. two IEEE
+// fmas each rounded once, exactly as two __fmaf_rn calls.
+__device__ __forceinline__ void fma2_bcast(float& c0, float& c1, float x0, float x1, float a) {
+  asm("{\n\t.reg .b64 d, x, w;\n\t"
+      "mov.b64 d, {%0, %1};\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 w, {%4, %4};\n\t"
+      "fma.rn.f32x2 d, x, w, d;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(x0), "f"(x1), "f"(a));
+}
+
 // ---------------------------------------------------------------------------------------
 // Partial logits: partials[c][t][e] = sum over the c-th chunk of d of x[t][i] * w[e][i],
 // one sequential FMA chain per (c, t, e).
@@ -133,9 +146,16 @@ __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16
 #pragma unroll
       for (int j = 0; j < TN; ++j) b[j] = ws[buf][kk][col_of(tx, j)];
 #pragma unroll
-      for (int i = 0; i < TM; ++i)
+      for (int i = 0; i < TM; ++i) {
+        if constexpr (TN % 2 == 0) {
+          // packed fp32x2 FMAs: two independent IEEE fmas, the same chain per output
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+          for (int j = 0; j < TN; j += 2) fma2_bcast(acc[i][j], acc[i][j + 1], b[j], b[j + 1], a[i]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < TN; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+        }
+      }
     }
     if (step + 1 < nsteps) stash(buf ^ 1);
     __syncthreads();
