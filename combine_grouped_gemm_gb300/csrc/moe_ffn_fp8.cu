@@ -80,6 +80,20 @@ __device__ __forceinline__ Unit8 decode_unit8(const Fp8Args& a, int u) {
   return r;
 }
 
+constexpr int kPromoWarps = 16;                  // 4 per tensor-memory lane quarter
+constexpr int kPromoThreads = kPromoWarps * 32;
+// Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies.
+constexpr int kGatherWarps = 2;
+constexpr int kGatherThreads = kGatherWarps * 32;
+template <int STAGE>
+struct Fp8Threads {
+  static constexpr int kGather = STAGE == 0 ? kGatherThreads : 0;
+  static constexpr int kAll = 64 + kPromoThreads + kGather;
+};
+// Scale prefetch ring: each promoter thread keeps its token scale (and lane 0 its warp's two
+// weight scales) for the next kRing-1 k-steps in flight with cp.async.
+constexpr int kRing = 4;
+
 // (a0, a1) += (x0, x1) * s as one packed fp32x2 fused multiply-add (two IEEE fmas).
 __device__ __forceinline__ void ffma2(float& a0, float& a1, uint32_t x0, uint32_t x1, float s) {
   asm("{\n\t.reg .b64 d, x, w;\n\t"
