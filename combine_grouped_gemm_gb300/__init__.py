@@ -220,7 +220,7 @@ class Buffers(dict):
         self["topk_w"] = torch.empty((T, k), dtype=torch.float32, device=device)
         self["recv"] = torch.empty((s["recv_rows"], d),
                                    dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
-        self["recv_scales"] = (torch.empty((s["recv_rows"], d // 128), dtype=torch.float32,
+        self["recv_scales"] = (torch.empty((d // 128, s["recv_rows"]), dtype=torch.float32,
                                            device=device) if fp8 else None)
         self["counts"] = torch.empty((R, E), dtype=torch.int32, device=device)
         self["row_of"] = torch.empty((T, k), dtype=torch.int32, device=device)

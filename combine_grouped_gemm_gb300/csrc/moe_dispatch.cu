@@ -156,10 +156,11 @@ __global__ void __launch_bounds__(128) dispatch_copy_bf16_kernel(
 
 // e4m3 payload: 16 threads per 128-column block, 8 columns per thread. amax over the block,
 // scale = amax/448 (1 if amax is 0), code = e4m3(x / scale) with IEEE division, nearest even,
-// saturating. The codes and the scale are written to each of the token's rows.
+// saturating. The codes and the scale are written to each of the token's rows; the scales are
+// block-major, recv_scales[block][row] with sc_ld rows per block.
 __global__ void __launch_bounds__(128) dispatch_copy_e4m3_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ row_of, uint2* __restrict__ recv,
-    float* __restrict__ recv_scales, int d, int k, int slice_vecs) {
+    float* __restrict__ recv_scales, long long sc_ld, int d, int k, int slice_vecs) {
   __shared__ int32_t rows[32];
   const int t = blockIdx.x;
   // row_of == nullptr: quantise token t into row t (the shared expert's input)
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(128) dispatch_copy_e4m3_kernel(
         const int row = rows[i];
         if (row < 0) continue;
         recv[(size_t)row * vpr + v] = make_uint2(lo, hi);
-        if (leader) recv_scales[(size_t)row * (d / 128) + v / 16] = scale;
+        if (leader) recv_scales[(long long)(v / 16) * sc_ld + row] = scale;
       }
     }
   }
@@ -226,7 +227,7 @@ cudaError_t launch_quant_rows_e4m3(const void* x, int T, int d, void* out, float
   int nslice, slice_vecs;
   copy_grid(T, d, &nslice, &slice_vecs);
   dispatch_copy_e4m3_kernel<<<dim3(T, nslice), 128, 0, st>>>(
-      static_cast<const uint4*>(x), nullptr, static_cast<uint2*>(out), scales, d, 1, slice_vecs);
+      static_cast<const uint4*>(x), nullptr, static_cast<uint2*>(out), scales, T, d, 1, slice_vecs);
   return cudaGetLastError();
 }
 
@@ -253,8 +254,9 @@ cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk
   dim3 grid(c.T, nslice);
   if (c.act_dtype == MOE_FP8_E4M3) {
     dispatch_copy_e4m3_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x), row_of,
-                                                    static_cast<uint2*>(recv), recv_scales, c.d,
-                                                    c.k, slice_vecs);
+                                                    static_cast<uint2*>(recv), recv_scales,
+                                                    (long long)c.R * c.R * cap, c.d, c.k,
+                                                    slice_vecs);
   } else {
     dispatch_copy_bf16_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x), row_of,
                                                     static_cast<uint4*>(recv), c.d, c.k,

@@ -39,14 +39,17 @@ struct Fp8Args {
   int k_steps;                  // K / 128
   int b_rows_routed;            // weight rows per routed expert (2F or d)
   int b_up_routed, b_up_shared; // offset of the up rows (gate/up) or 0
-  const float* a_sc_routed;     // token scales of routed A rows [rows][K/128]
-  const float* a_sc_shared;     // token scales of shared A rows [T][K/128]
+  // Token scales are block-major, [K/128][rows]: the scales of one K block for consecutive
+  // rows are consecutive, so a warp's 32 rows read one or two cache lines per k-step.
+  const float* a_sc_routed;     // token scales of routed A rows [K/128][a_sc_ld_routed]
+  const float* a_sc_shared;     // token scales of shared A rows [K/128][T]
+  int a_sc_ld_routed;           // rows per K block of a_sc_routed
   const float* w_sc_routed;     // [E][b_rows_routed/128][K/128]
   const float* w_sc_shared;     // [b_rows_shared/128][K/128]
   void* out_routed;             // gate/up: e4m3 h [tk][F]; down: bf16 ebuf [recv rows][d]
-  float* out_sc_routed;         // gate/up: h scales [tk][F/128]
+  float* out_sc_routed;         // gate/up: h scales, block-major [F/128][tk]
   void* out_shared;             // gate/up: e4m3 hs [T][Fs]; down: bf16 shared_out [T][d]
-  float* out_sc_shared;
+  float* out_sc_shared;         // gate/up: hs scales, block-major [Fs/128][T]
   int ld_routed, ld_shared;     // output row length (elements)
   long long out_rows_routed;    // bound of routed output row indices
   int box_routed, box_shared;   // rows per box of the contiguous token-row maps
@@ -292,29 +295,32 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit8 t = decode_unit8(a, u);
       const bool gather = STAGE == 0 && t.g >= 0;
-      const uint8_t* src[16];
+      // receive row of each of the thread's 16 tile rows (-1: none), 32-bit to save registers
+      int src[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int p = rg + 8 * i;
-        src[i] = nullptr;
+        src[i] = -1;
         if (gather && p < t.nlen) {
           const int ci = a.grp_off[t.g] + t.n0 + p;
           const long long row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
-          if (row >= 0 && row < a.a_rows_routed) src[i] = a.gather_base + row * a.gather_ld + j * 16;
+          if (row >= 0 && row < a.a_rows_routed) src[i] = static_cast<int>(row);
           else raise_status(a.status, MOE_DEV_BOUNDS);
         }
       }
+      const uint8_t* gsrc = a.gather_base + j * 16;
       for (int ks = 0; ks < a.k_steps; ++ks) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
           ok = false;
           break;
         }
         const uint32_t sa = smem_addr(smem + stage * S::STAGE_BYTES) + dst_off;
+        const uint8_t* gk = gsrc + ks * 128;
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          if (src[i])
+          if (src[i] >= 0)
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa + i * 1024),
-                         "l"(src[i] + ks * 128)
+                         "l"(gk + (long long)src[i] * a.gather_ld)
                          : "memory");
         cp_async_commit();
         // a k-step without copies (nothing to gather in this unit) is arrived for at once;
@@ -354,12 +360,13 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     float* ring = reinterpret_cast<float*>(smem + S::RING_OFF);           // token scales
     float* wring = ring + kRing * kPromoThreads;                         // weight scales
 
-    // Scale sources of one unit for this thread: its token row's scale row and the two weight
-    // block scale rows (gate, up); a lane past the unit's rows reads the weight row instead
-    // (its results are never stored).
+    // Scale sources of one unit for this thread: its token row's scale column (block-major,
+    // stride xs_ld per K block) and the two weight block scale rows (gate, up); a lane past the
+    // unit's rows reads row 0's scales instead (its results are never stored).
     struct Src {
       const float* xs;
       const float* w0;   // the up block's row is w0 + w_up
+      int xs_ld;
     };
     const int w_up = (STAGE == 0 ? a.b_up_routed : 0) / 128 * kb_n;  // routed and shared alike
     auto sources = [&](int u) -> Src {
@@ -380,18 +387,20 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
                             : a.w_sc_routed + (size_t)t.g * (a.b_rows_routed / 128) * kb_n;
       Src q;
       q.w0 = wsc + (size_t)t.m * kb_n;
-      q.xs = arow >= 0 ? (sh ? a.a_sc_shared : a.a_sc_routed) + arow * kb_n : q.w0;
+      q.xs = (sh ? a.a_sc_shared : a.a_sc_routed) + (arow >= 0 ? arow : 0);
+      q.xs_ld = sh ? a.T : a.a_sc_ld_routed;
       return q;
     };
     // prefetch cursor: unit pu, k-step pks (runs kRing-1 k-steps ahead of consumption)
     int pu = blockIdx.x, pks = 0;
-    Src ps = pu < units ? sources(pu) : Src{nullptr, nullptr};
+    Src ps = pu < units ? sources(pu) : Src{nullptr, nullptr, 0};
     // the cursor's stream position is always pk + kRing - 1 (pk: consumed k-steps)
     uint32_t pk = 0;
     auto prefetch_one = [&]() {
       if (pu < units) {
         const uint32_t r8 = (pk + kRing - 1) % kRing;
-        cp_async4(ring + r8 * kPromoThreads + pid, ps.xs + pks);
+        cp_async4(ring + r8 * kPromoThreads + pid, ps.xs);
+        ps.xs += ps.xs_ld;
         if (lane == 0) {   // the two weight scales are the same for the whole warp
           float* wslot = wring + (r8 * kPromoWarps + pw) * 2;
           cp_async4(wslot, ps.w0 + pks);
@@ -506,10 +515,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
               }
               reinterpret_cast<uint4*>(out)[q] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            if (part == 0) {
+            if (part == 0) {   // block-major: consecutive lanes write consecutive rows
               float* osc = sh ? a.out_sc_shared : a.out_sc_routed;
-              const int nblk = (sh ? a.ld_shared : a.ld_routed) / 128;
-              osc[orow * nblk + t.m] = scale;
+              osc[(long long)t.m * (sh ? a.T : a.tk) + orow] = scale;
             }
           }
         }
@@ -566,6 +574,7 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
   a.status = reinterpret_cast<uint32_t*>(ws + L.status);
   a.n_shared_tiles = has_shared ? (c.T + 127) / 128 : 0;
   a.out_rows_routed = recv_rows;
+  if (recv_rows > 0x7fffffffLL) return cudaErrorNotSupported;   // 32-bit scale-row strides
   CUtensorMap mA, mAs, mB, mBs;
   bool ok = true;
   if (stage == 0) {
@@ -577,6 +586,7 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     a.b_up_routed = F;
     a.b_up_shared = Fs;
     a.a_sc_routed = recv_scales;
+    a.a_sc_ld_routed = static_cast<int>(recv_rows);
     a.a_sc_shared = reinterpret_cast<const float*>(ws + L.xq_scales);
     a.w_sc_routed = w.w13_scales;
     a.w_sc_shared = w.ws13_scales;
@@ -606,6 +616,7 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     a.b_up_routed = 0;
     a.b_up_shared = 0;
     a.a_sc_routed = reinterpret_cast<const float*>(ws + L.h_scales);
+    a.a_sc_ld_routed = tk;
     a.a_sc_shared = reinterpret_cast<const float*>(ws + L.hs_scales);
     a.w_sc_routed = w.w2_scales;
     a.w_sc_shared = w.ws2_scales;

@@ -31,11 +31,11 @@ struct WsLayout {
   size_t tiles;       // Tile [max_tiles]
   size_t row_list;    // int32 [T*k]: receive row of each compact row
   size_t h;           // SwiGLU intermediate of routed rows: [T*k][d_ff] (bf16 or e4m3)
-  size_t h_scales;    // e4m3: fp32 [T*k][d_ff/128]
+  size_t h_scales;    // e4m3: fp32, block-major [d_ff/128][T*k]
   size_t hs;          // shared expert intermediate: [T][d_ff_shared]
-  size_t hs_scales;   // e4m3: fp32 [T][d_ff_shared/128]
+  size_t hs_scales;   // e4m3: fp32, block-major [d_ff_shared/128][T]
   size_t xq;          // e4m3: quantised shared-expert input [T][d]
-  size_t xq_scales;   // e4m3: fp32 [T][d/128]
+  size_t xq_scales;   // e4m3: fp32, block-major [d/128][T]
   size_t run_start;   // int32 [R][E]: receive row of the first row source s sent expert e
   size_t run_pre;     // int32 [R][E]: rows of expert e from sources before s
   size_t total;

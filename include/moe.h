@@ -82,7 +82,8 @@ typedef struct moe_sizes {
   int32_t cap;              /* rows per (destination rank, source rank) segment:
                                (T/R) * min(k, E/R), the most one source can send one rank */
   size_t recv_bytes;        /* recv: [R][R][cap][d], bf16 (2 B) or e4m3 (1 B) elements */
-  size_t recv_scale_bytes;  /* e4m3 only: recv_scales [R][R][cap][d/128] fp32; else 0 */
+  size_t recv_scale_bytes;  /* e4m3 only: recv_scales fp32, block-major [d/128][recv_rows]
+                               (scale of block b of row j at b * recv_rows + j); else 0 */
   size_t ebuf_bytes;        /* ebuf: expert outputs, bf16 [R][R][cap][d] (same rows as recv) */
   size_t ws_bytes;          /* ws: scratch workspace (status word, router partials, tile
                                schedule, SwiGLU intermediates) */
@@ -154,7 +155,8 @@ int moe_route_noalloc(const moe_cfg* cfg, const void* x, const float* w_gate, co
  * earlier tokens of s that chose e]. No count is exchanged before the rows are written.
  * bf16: recv[row] = x[t]. e4m3: x[t] is quantised once per 128-column block (scale =
  * amax/448, or 1 if amax is 0; code = e4m3(x/scale), nearest even, saturating) and written to
- * each of its rows with recv_scales[row][d/128].
+ * each of its rows; the block scales are block-major, recv_scales[b * recv_rows + row], so the
+ * expert GEMMs read one K block's scales for consecutive rows from consecutive addresses.
  * Inputs x bf16 [T][d], topk_idx int32 [T][k] (entries in [0, E), distinct per token).
  * Outputs recv (see moe_sizes), recv_scales (e4m3 only, else NULL), counts int32 [R][E],
  * row_of int32 [T][k] (receive row of each choice), src_tok int32 [recv_rows] (token of each

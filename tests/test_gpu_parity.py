@@ -168,7 +168,8 @@ def test_dispatch_e4m3_codes_and_scales_bit_exact():
     q, sc = oracle.dispatch_payload(host_bits(inp["x"]), row_of, src_tok.size, fp8=True)
     filled = src_tok >= 0
     assert np.array_equal(b["recv"].cpu().numpy()[filled], q[filled])
-    assert np.array_equal(b["recv_scales"].cpu().numpy()[filled], sc[filled])
+    # the library's scales are block-major [d/128][rows]
+    assert np.array_equal(b["recv_scales"].cpu().numpy().T[filled], sc[filled])
 
 
 @pytest.mark.parametrize("name", ["dsv3_skew_prefill", "dsv3_fp8_prefill"])
@@ -219,7 +220,7 @@ def test_dispatch_invariants_large(name):
         toks = tok[rows]
         q, sc = oracle.quant_rows_e4m3(oracle.bf16_to_f32(x[toks]))
         assert np.array_equal(b["recv"][ro.reshape(-1)[rows]].cpu().numpy(), q)
-        assert np.array_equal(b["recv_scales"][ro.reshape(-1)[rows]].cpu().numpy(), sc)
+        assert np.array_equal(b["recv_scales"][:, ro.reshape(-1)[rows]].cpu().numpy().T, sc)
     else:
         assert np.array_equal(host_bits(b["recv"][ro.reshape(-1)[rows]]), x[tok[rows]])
 
