@@ -16,11 +16,15 @@
 // Two partial buffers in tensor memory alternate so the tensor core computes block kb+1 while
 // the promoter warps read block kb.
 //
-// Roles (576 threads, one CTA per SM, persistent over the unit list):
-//   warp 0       TMA producer (token rows gathered four at a time or one box; weight tiles)
+// Roles (640 threads, one CTA per SM, persistent over the unit list):
+//   warp 0       TMA producer (weight tiles; contiguous token rows as one box)
 //   warp 1       tensor-memory allocation; lane 0 issues the MMAs
 //   warps 2..17  promoters / epilogue: warp w owns lanes 32*(w%4).. and the column quarter
 //                (w-2)/4 of each accumulator (32 columns of gate and of up)
+//   warps 18,19  copy warps: per k-step the tile's 128 token scales and its weight scales into
+//                a shared-memory scale ring, and (gate/up, routed units) the token rows
+// Every global load of the k-step loop is issued by the producer or the copy warps, so the
+// promoters' loop holds only barrier waits, shared-memory reads, tensor-memory loads and FMAs.
 #include "moe_device.cuh"
 
 namespace moe {
@@ -85,17 +89,19 @@ __device__ __forceinline__ Unit8 decode_unit8(const Fp8Args& a, int u) {
 
 constexpr int kPromoWarps = 16;                  // 4 per tensor-memory lane quarter
 constexpr int kPromoThreads = kPromoWarps * 32;
-// Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies.
+// Copy warps: token scales and weight scales of every k-step, and (gate/up) the routed token
+// rows, with cp.async.
 constexpr int kGatherWarps = 2;
 constexpr int kGatherThreads = kGatherWarps * 32;
 template <int STAGE>
 struct Fp8Threads {
-  static constexpr int kGather = STAGE == 0 ? kGatherThreads : 0;
+  static constexpr int kGather = kGatherThreads;
   static constexpr int kAll = 64 + kPromoThreads + kGather;
 };
-// Scale prefetch ring: each promoter thread keeps its token scale (and lane 0 its warp's two
-// weight scales) for the next kRing-1 k-steps in flight with cp.async.
-constexpr int kRing = 4;
+// Scale ring: slot q % kScaleSlots holds k-step q's 128 token scales and its two weight scales
+// (gate, up), written by the copy warps and released by the promoter warps.
+constexpr int kScaleSlots = 8;
+constexpr int kSlotFloats = 132;   // 128 token scales + 2 weight scales, padded to 16 bytes
 
 // (a0, a1) += (x0, x1) * s as one packed fp32x2 fused multiply-add (two IEEE fmas).
 __device__ __forceinline__ void ffma2(float& a0, float& a1, uint32_t x0, uint32_t x1, float s) {
@@ -113,11 +119,11 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_ring() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 2) : "memory");
+// The hardware arrives on bar once every cp.async this thread has issued so far has landed;
+// the arrival counts as one of the barrier's expected arrivals.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
 }
 
 template <int STAGE, int STAGES>
@@ -132,10 +138,9 @@ struct Fp8Shape {
   static constexpr int NBUF = 512 / ACC_COLS;
   static constexpr int TMEM_COLS = NBUF * ACC_COLS;
   // stages + barriers (512 B) + amax exchange [2][4][32][4] floats (4 KB)
-  // + scale ring: token scales [kRing][kPromoThreads] and weight scales [kRing][kPromoWarps][2]
-  // floats + alignment slack
+  // + scale ring [kScaleSlots][kSlotFloats] floats + alignment slack
   static constexpr int RING_OFF = STAGES * STAGE_BYTES + 512 + 4096;
-  static constexpr int SMEM = RING_OFF + kRing * (kPromoThreads + 2 * kPromoWarps) * 4 + 1024;
+  static constexpr int SMEM = RING_OFF + kScaleSlots * kSlotFloats * 4 + 1024;
   static_assert(TMEM_COLS <= 512, "tensor memory");
 };
 
@@ -154,15 +159,17 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
   uint64_t* pfull = empty + STAGES;    // [NBUF] partial buffer written
   uint64_t* pempty = pfull + S::NBUF;  // [NBUF] partial buffer read
   uint64_t* xbar = pempty + S::NBUF;   // [4] amax exchange of the warps on one lane quarter
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
+  uint64_t* sfull = xbar + 4;          // [kScaleSlots] scale slot written
+  uint64_t* sempty = sfull + kScaleSlots;   // [kScaleSlots] scale slot read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + kScaleSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* amax_x = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES + 512);  // [2][4][32][4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      // the TMA lane's expect_tx arrival, plus one per gather warp (gate/up)
-      mbar_init(&full[i], 1 + Fp8Threads<STAGE>::kGather / 32);
+      // the TMA lane's expect_tx arrival, plus one per copy thread
+      mbar_init(&full[i], 1 + Fp8Threads<STAGE>::kGather);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < S::NBUF; ++i) {
@@ -170,6 +177,10 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       mbar_init(&pempty[i], kPromoWarps);   // one arrival per promoter warp
     }
     for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 4);   // the four warps of a lane quarter
+    for (int i = 0; i < kScaleSlots; ++i) {
+      mbar_init(&sfull[i], kGatherThreads);   // one cp.async arrival per copy thread
+      mbar_init(&sempty[i], kPromoWarps);     // one arrival per promoter warp
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -256,6 +267,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
             ok = false;
             break;
           }
+          // gate/up: the gathered token rows were written by cp.async (generic proxy); the
+          // fence orders them, observed through the barrier, before the MMA's reads
+          if (STAGE == 0) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sa = smem_addr(smem + stage * S::STAGE_BYTES);
           const uint32_t sb = sa + S::A_BYTES;
@@ -275,26 +289,27 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     }
     __syncwarp();
   } else if (warp >= 2 + kPromoWarps) {
-    // ------------------------------ token-row gather (gate/up) ------------------------------
-    // Thread gt copies 16-byte chunk j = gt % 8 of rows p = gt/8 + 8i (i < 16) of the tile
-    // into the 128-byte-swizzled layout the MMA descriptor expects (chunk j of row p at
-    // chunk j ^ (p % 8) = j ^ gt/8). Completion is observed kLag stages late: wait for the
-    // copies, make them visible to the async proxy, then arrive on that stage's barrier.
-    // kLag = STAGES - 2: the arrival for stage q waits only for stage q+kLag to be free, i.e.
-    // for the MMAs of k-step q-2, so two k-steps of MMAs can be in flight.
-    constexpr int kLag = STAGES - 2;
-    static_assert(kLag >= 1, "needs at least three stages");
-    uint32_t with_copies = 0;  // bit i: k-step q-1-i issued copies (arrival still owed)
+    // ------------------------------ copy warps ------------------------------
+    // Per k-step: the tile's 128 token scales (thread gt: rows gt and gt + 64) and the two
+    // weight block scales (thread 0) into the scale ring, and, for routed gate/up units, the
+    // token rows: thread gt copies 16-byte chunk j = gt % 8 of rows p = gt/8 + 8i (i < 16) into
+    // the 128-byte-swizzled layout the MMA descriptor expects (chunk j of row p at chunk
+    // j ^ (p % 8) = j ^ gt/8). Each thread then arms arrivals on the stage's full barrier and
+    // on the scale slot's barrier, which the hardware performs once its copies have landed.
+    // The MMA thread puts a proxy fence between its wait and its tensor-core reads.
     const int gt = threadIdx.x - (64 + kPromoThreads);
     const int j = gt & 7, rg = gt >> 3;
     const uint32_t dst_off = static_cast<uint32_t>(rg * 128 + ((j ^ rg) << 4));
+    float* sring = reinterpret_cast<float*>(smem + S::RING_OFF);
+    const int kb_n = a.k_steps;
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t q = 0;  // k-steps issued
+    uint32_t q = 0;   // k-steps issued (scale ring position)
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit8 t = decode_unit8(a, u);
-      const bool gather = STAGE == 0 && t.g >= 0;
+      const bool sh = t.g < 0;
+      const bool gather = STAGE == 0 && !sh;
       // receive row of each of the thread's 16 tile rows (-1: none), 32-bit to save registers
       int src[16];
 #pragma unroll
@@ -308,118 +323,78 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
           else raise_status(a.status, MOE_DEV_BOUNDS);
         }
       }
+      // scale rows of tile rows gt and gt + 64 (-1: past the tile's rows)
+      long long srow[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int p = gt + 64 * h;
+        srow[h] = -1;
+        if (p < t.nlen) {
+          long long row;
+          if (sh) {
+            row = t.n0 + p;
+          } else {
+            const int ci = a.grp_off[t.g] + t.n0 + p;
+            row = ci;   // down: compact row of h
+            if (STAGE == 0) row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+          }
+          const long long bound = sh ? a.T : (STAGE == 0 ? a.a_rows_routed : a.tk);
+          if (row >= 0 && row < bound) srow[h] = row;
+          else raise_status(a.status, MOE_DEV_BOUNDS);
+        }
+      }
+      const float* xs = sh ? a.a_sc_shared : a.a_sc_routed;
+      const long long xs_ld = sh ? a.T : a.a_sc_ld_routed;
+      const float* wsc = (sh ? a.w_sc_shared
+                             : a.w_sc_routed + (size_t)t.g * (a.b_rows_routed / 128) * kb_n) +
+                         (size_t)t.m * kb_n;
+      const int w_up = (sh ? a.b_up_shared : a.b_up_routed) / 128 * kb_n;
       const uint8_t* gsrc = a.gather_base + j * 16;
-      for (int ks = 0; ks < a.k_steps; ++ks) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
+      for (int ks = 0; ks < kb_n; ++ks, ++q) {
+        const uint32_t slot = q % kScaleSlots;
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status) ||
+            !mbar_wait(&sempty[slot], ((q / kScaleSlots) & 1u) ^ 1u, abort_flag, a.status)) {
           ok = false;
           break;
         }
-        const uint32_t sa = smem_addr(smem + stage * S::STAGE_BYTES) + dst_off;
-        const uint8_t* gk = gsrc + ks * 128;
+        if (gather) {
+          const uint32_t sa = smem_addr(smem + stage * S::STAGE_BYTES) + dst_off;
+          const uint8_t* gk = gsrc + ks * 128;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (src[i] >= 0)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa + i * 1024),
-                         "l"(gk + (long long)src[i] * a.gather_ld)
-                         : "memory");
-        cp_async_commit();
-        // a k-step without copies (nothing to gather in this unit) is arrived for at once;
-        // one with copies kLag k-steps later, once its copies have landed
-        with_copies = (with_copies << 1) | (gather ? 1u : 0u);
-        if (!gather) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[q % STAGES]);
+          for (int i = 0; i < 16; ++i)
+            if (src[i] >= 0)
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa + i * 1024),
+                           "l"(gk + (long long)src[i] * a.gather_ld)
+                           : "memory");
         }
-        if (++q > kLag && ((with_copies >> kLag) & 1u)) {
-          asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[(q - 1 - kLag) % STAGES]);
+        float* sl = sring + slot * kSlotFloats;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (srow[h] >= 0) cp_async4(sl + gt + 64 * h, xs + ks * xs_ld + srow[h]);
+        if (gt == 0) {
+          cp_async4(sl + 128, wsc + ks);
+          if (S::NB == 2) cp_async4(sl + 129, wsc + w_up + ks);
         }
+        // the arrivals count as expected arrivals of both barriers (a thread with nothing to
+        // copy arrives as soon as its earlier copies have landed)
+        cp_async_arrive(&full[stage]);
+        cp_async_arrive(&sfull[slot]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    // the last kLag stages (or, after an abort, every copy still in flight)
+    // after an abort: copies still in flight land before the CTA exits
     asm volatile("cp.async.wait_all;" ::: "memory");
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (ok && lane == 0)
-      for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2)
-        if ((with_copies >> (q - 1 - r2)) & 1u) mbar_arrive(&full[r2 % STAGES]);
   } else {
     // ------------------------------ promoters / epilogue ------------------------------
     const int quarter = warp & 3;
     const int part = (warp - 2) >> 2;      // columns 32*part .. 32*part+31 of each accumulator
     const int r = quarter * 32 + lane;     // token row of the tile (tensor-memory lane)
     const int kb_n = a.k_steps;
-    const int pid = threadIdx.x - 64;      // 0 .. kPromoThreads-1
-    const int pw = pid >> 5;               // promoter warp 0 .. kPromoWarps-1
-    float* ring = reinterpret_cast<float*>(smem + S::RING_OFF);           // token scales
-    float* wring = ring + kRing * kPromoThreads;                         // weight scales
-
-    // Scale sources of one unit for this thread: its token row's scale column (block-major,
-    // stride xs_ld per K block) and the two weight block scale rows (gate, up); a lane past the
-    // unit's rows reads row 0's scales instead (its results are never stored).
-    struct Src {
-      const float* xs;
-      const float* w0;   // the up block's row is w0 + w_up
-      int xs_ld;
-    };
-    const int w_up = (STAGE == 0 ? a.b_up_routed : 0) / 128 * kb_n;  // routed and shared alike
-    auto sources = [&](int u) -> Src {
-      const Unit8 t = decode_unit8(a, u);
-      const bool sh = t.g < 0;
-      long long arow = -1;
-      if (r < t.nlen) {
-        if (sh) arow = t.n0 + r;
-        else if (STAGE == 0) {
-          const int ci = a.grp_off[t.g] + t.n0 + r;
-          arow = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
-        } else {
-          arow = a.grp_off[t.g] + t.n0 + r;
-        }
-        if (!sh && (arow < 0 || arow >= a.a_rows_routed)) arow = -1;
-      }
-      const float* wsc = sh ? a.w_sc_shared
-                            : a.w_sc_routed + (size_t)t.g * (a.b_rows_routed / 128) * kb_n;
-      Src q;
-      q.w0 = wsc + (size_t)t.m * kb_n;
-      q.xs = (sh ? a.a_sc_shared : a.a_sc_routed) + (arow >= 0 ? arow : 0);
-      q.xs_ld = sh ? a.T : a.a_sc_ld_routed;
-      return q;
-    };
-    // prefetch cursor: unit pu, k-step pks (runs kRing-1 k-steps ahead of consumption)
-    int pu = blockIdx.x, pks = 0;
-    Src ps = pu < units ? sources(pu) : Src{nullptr, nullptr, 0};
-    // the cursor's stream position is always pk + kRing - 1 (pk: consumed k-steps)
-    uint32_t pk = 0;
-    auto prefetch_one = [&]() {
-      if (pu < units) {
-        const uint32_t r8 = (pk + kRing - 1) % kRing;
-        cp_async4(ring + r8 * kPromoThreads + pid, ps.xs);
-        ps.xs += ps.xs_ld;
-        if (lane == 0) {   // the two weight scales are the same for the whole warp
-          float* wslot = wring + (r8 * kPromoWarps + pw) * 2;
-          cp_async4(wslot, ps.w0 + pks);
-          if (S::NB == 2) cp_async4(wslot + 1, ps.w0 + w_up + pks);
-        }
-        if (++pks == kb_n) {
-          pks = 0;
-          pu += gridDim.x;
-          if (pu < units) ps = sources(pu);
-        }
-      }
-      cp_async_commit();   // an empty group past the end keeps the group count uniform
-    };
-    // prime the ring: stream positions 0 .. kRing-2
-    for (int i = 0; i < kRing - 1; ++i) {
-      pk = static_cast<uint32_t>(i) - (kRing - 1);   // so that pk + kRing - 1 == i
-      prefetch_one();
-    }
-    pk = 0;
+    const float* sring = reinterpret_cast<const float*>(smem + S::RING_OFF);
+    uint32_t pk = 0;   // k-steps consumed (partial-buffer and scale-ring position)
     uint32_t it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
       const Unit8 t = decode_unit8(a, u);
@@ -430,14 +405,16 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = 0.0f;
       bool ok = true;
       for (int ks = 0; ks < kb_n; ++ks, ++pk) {
-        cp_async_wait_ring();               // this k-step's scales have landed
-        __syncwarp();                       // (lane 0's weight-scale copies included)
-        const float xsv = ring[(pk % kRing) * kPromoThreads + pid];
-        const float* wslot = wring + ((pk % kRing) * kPromoWarps + pw) * 2;
-        const float s0 = xsv * wslot[0];
-        const float s1 = S::NB == 2 ? xsv * wslot[1] : 0.0f;
-        prefetch_one();
+        const uint32_t slot = pk % kScaleSlots;
         const uint32_t pb = pk % S::NBUF;
+        if (!mbar_wait(&sfull[slot], (pk / kScaleSlots) & 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const float* sl = sring + slot * kSlotFloats;
+        const float xsv = sl[r];
+        const float s0 = xsv * sl[128];
+        const float s1 = S::NB == 2 ? xsv * sl[129] : 0.0f;
         if (!mbar_wait(&pfull[pb], (pk / S::NBUF) & 1u, abort_flag, a.status)) {
           ok = false;
           break;
@@ -471,7 +448,10 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pempty[pb]);
+        if (lane == 0) {
+          mbar_arrive(&pempty[pb]);
+          mbar_arrive(&sempty[slot]);
+        }
       }
       if (!ok) break;
 
