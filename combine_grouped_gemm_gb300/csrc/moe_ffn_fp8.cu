@@ -98,9 +98,14 @@ struct Fp8Threads {
   static constexpr int kGather = kGatherThreads;
   static constexpr int kAll = 64 + kPromoThreads + kGather;
 };
-// Scale ring: slot q % kScaleSlots holds k-step q's 128 token scales and its two weight scales
-// (gate, up), written by the copy warps and released by the promoter warps.
-constexpr int kScaleSlots = 8;
+// Scale ring: slot q % SLOTS holds k-step q's 128 token scales and its two weight scales (gate,
+// up). It needs no barriers of its own:
+//  - filled: the copy warps' cp.async arrivals on the stage's full barrier fire only after their
+//    scale copies have landed; the MMA waits on that barrier before it commits the partial
+//    buffer the promoters wait for;
+//  - released: with SLOTS = STAGES + NBUF, a copy warp overwrites the slot of k-step q only
+//    after the stage of k-step q + NBUF has been consumed by the MMA, which waited for the
+//    promoters to release the partial buffer of k-step q (and so to finish reading its slot).
 constexpr int kSlotFloats = 132;   // 128 token scales + 2 weight scales, padded to 16 bytes
 
 // (a0, a1) += (x0, x1) * s as one packed fp32x2 fused multiply-add (two IEEE fmas).
@@ -137,10 +142,11 @@ struct Fp8Shape {
   // core can run that many K blocks ahead of the promoters
   static constexpr int NBUF = 512 / ACC_COLS;
   static constexpr int TMEM_COLS = NBUF * ACC_COLS;
+  static constexpr int SLOTS = STAGES + NBUF;        // scale ring slots
   // stages + barriers (512 B) + amax exchange [2][4][32][4] floats (4 KB)
-  // + scale ring [kScaleSlots][kSlotFloats] floats + alignment slack
+  // + scale ring [SLOTS][kSlotFloats] floats + alignment slack
   static constexpr int RING_OFF = STAGES * STAGE_BYTES + 512 + 4096;
-  static constexpr int SMEM = RING_OFF + kScaleSlots * kSlotFloats * 4 + 1024;
+  static constexpr int SMEM = RING_OFF + SLOTS * kSlotFloats * 4 + 1024;
   static_assert(TMEM_COLS <= 512, "tensor memory");
 };
 
@@ -159,9 +165,7 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
   uint64_t* pfull = empty + STAGES;    // [NBUF] partial buffer written
   uint64_t* pempty = pfull + S::NBUF;  // [NBUF] partial buffer read
   uint64_t* xbar = pempty + S::NBUF;   // [4] amax exchange of the warps on one lane quarter
-  uint64_t* sfull = xbar + 4;          // [kScaleSlots] scale slot written
-  uint64_t* sempty = sfull + kScaleSlots;   // [kScaleSlots] scale slot read
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + kScaleSlots);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* amax_x = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES + 512);  // [2][4][32][4]
 
@@ -177,10 +181,6 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       mbar_init(&pempty[i], kPromoWarps);   // one arrival per promoter warp
     }
     for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 4);   // the four warps of a lane quarter
-    for (int i = 0; i < kScaleSlots; ++i) {
-      mbar_init(&sfull[i], kGatherThreads);   // one cp.async arrival per copy thread
-      mbar_init(&sempty[i], kPromoWarps);     // one arrival per promoter warp
-    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -294,9 +294,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     // weight block scales (thread 0) into the scale ring, and, for routed gate/up units, the
     // token rows: thread gt copies 16-byte chunk j = gt % 8 of rows p = gt/8 + 8i (i < 16) into
     // the 128-byte-swizzled layout the MMA descriptor expects (chunk j of row p at chunk
-    // j ^ (p % 8) = j ^ gt/8). Each thread then arms arrivals on the stage's full barrier and
-    // on the scale slot's barrier, which the hardware performs once its copies have landed.
-    // The MMA thread puts a proxy fence between its wait and its tensor-core reads.
+    // j ^ (p % 8) = j ^ gt/8). Each thread then arms an arrival on the stage's full barrier,
+    // which the hardware performs once its copies have landed. The MMA thread puts a proxy
+    // fence between its wait and its tensor-core reads.
     const int gt = threadIdx.x - (64 + kPromoThreads);
     const int j = gt & 7, rg = gt >> 3;
     const uint32_t dst_off = static_cast<uint32_t>(rg * 128 + ((j ^ rg) << 4));
@@ -351,9 +351,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       const int w_up = (sh ? a.b_up_shared : a.b_up_routed) / 128 * kb_n;
       const uint8_t* gsrc = a.gather_base + j * 16;
       for (int ks = 0; ks < kb_n; ++ks, ++q) {
-        const uint32_t slot = q % kScaleSlots;
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status) ||
-            !mbar_wait(&sempty[slot], ((q / kScaleSlots) & 1u) ^ 1u, abort_flag, a.status)) {
+        const uint32_t slot = q % S::SLOTS;
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
           ok = false;
           break;
         }
@@ -375,10 +374,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
           cp_async4(sl + 128, wsc + ks);
           if (S::NB == 2) cp_async4(sl + 129, wsc + w_up + ks);
         }
-        // the arrivals count as expected arrivals of both barriers (a thread with nothing to
-        // copy arrives as soon as its earlier copies have landed)
+        // counts as one of the barrier's expected arrivals (a thread with nothing to copy
+        // arrives as soon as its earlier copies have landed)
         cp_async_arrive(&full[stage]);
-        cp_async_arrive(&sfull[slot]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -405,20 +403,16 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = 0.0f;
       bool ok = true;
       for (int ks = 0; ks < kb_n; ++ks, ++pk) {
-        const uint32_t slot = pk % kScaleSlots;
         const uint32_t pb = pk % S::NBUF;
-        if (!mbar_wait(&sfull[slot], (pk / kScaleSlots) & 1u, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
-        const float* sl = sring + slot * kSlotFloats;
-        const float xsv = sl[r];
-        const float s0 = xsv * sl[128];
-        const float s1 = S::NB == 2 ? xsv * sl[129] : 0.0f;
         if (!mbar_wait(&pfull[pb], (pk / S::NBUF) & 1u, abort_flag, a.status)) {
           ok = false;
           break;
         }
+        // the k-step's scales (filled before the stage's full barrier fired; see the ring)
+        const float* sl = sring + (pk % S::SLOTS) * kSlotFloats;
+        const float xsv = sl[r];
+        const float s0 = xsv * sl[128];
+        const float s1 = S::NB == 2 ? xsv * sl[129] : 0.0f;
         tc_fence_after();
         const uint32_t tb = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + pb * S::ACC_COLS +
                             part * 32;
@@ -448,10 +442,7 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&pempty[pb]);
-          mbar_arrive(&sempty[slot]);
-        }
+        if (lane == 0) mbar_arrive(&pempty[pb]);
       }
       if (!ok) break;
 
