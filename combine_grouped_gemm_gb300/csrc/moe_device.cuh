@@ -238,5 +238,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+// The same with the fast division (about 2 ulp): for an intermediate that is rounded to e4m3
+// right after (large negative g: the denominator overflows to infinity and the result is 0).
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 }  // namespace moe

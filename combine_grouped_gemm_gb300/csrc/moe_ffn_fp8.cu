@@ -394,10 +394,32 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     const float* sring = reinterpret_cast<const float*>(smem + S::RING_OFF);
     uint32_t pk = 0;   // k-steps consumed (partial-buffer and scale-ring position)
     uint32_t it = 0;
+    // The schedule entry of the next unit and its group's row offset are loaded one unit ahead,
+    // so these dependent global loads overlap a unit's k-steps instead of starting the next.
+    Unit8 tn{0, 0, 0, 0};
+    int goff_n = 0;
+    if (blockIdx.x < units) {
+      tn = decode_unit8(a, blockIdx.x);
+      goff_n = tn.g >= 0 ? a.grp_off[tn.g] : 0;
+    }
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
-      const Unit8 t = decode_unit8(a, u);
+      const Unit8 t = tn;
+      const int goff = goff_n;
+      const int un = u + gridDim.x;
+      if (un < units) tn = decode_unit8(a, un);
       const bool sh = t.g < 0;
       const bool live = r < t.nlen;
+      // down: this lane's output row (the receive row), loaded now and used in the epilogue
+      long long orow_down = -1;
+      if (STAGE == 1 && live) {
+        if (sh) {
+          orow_down = t.n0 + r;
+        } else {
+          const int ci = goff + t.n0 + r;
+          const long long row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
+          orow_down = (row >= 0 && row < a.out_rows_routed) ? row : -1;
+        }
+      }
       float acc0[32], acc1[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = 0.0f;
@@ -445,13 +467,14 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
         if (lane == 0) mbar_arrive(&pempty[pb]);
       }
       if (!ok) break;
+      if (un < units) goff_n = tn.g >= 0 ? a.grp_off[tn.g] : 0;   // used at the next unit
 
       // ---- epilogue of the unit ----
       if (STAGE == 0) {
         float amax = 0.0f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          acc0[j] = silu(acc0[j]) * acc1[j];
+          acc0[j] = silu_fast(acc0[j]) * acc1[j];
           amax = fmaxf(amax, fabsf(acc0[j]));
         }
         // the 128-column block of h is split over the four warps of this lane quarter:
@@ -465,7 +488,7 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
         amax = fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
         const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
         if (live) {
-          long long orow = sh ? (long long)t.n0 + r : (long long)a.grp_off[t.g] + t.n0 + r;
+          long long orow = sh ? (long long)t.n0 + r : (long long)goff + t.n0 + r;
           const bool in = sh || (orow >= 0 && orow < a.tk);
           if (in) {
             uint8_t* out = static_cast<uint8_t*>(sh ? a.out_shared : a.out_routed) +
@@ -493,17 +516,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
           }
         }
       } else if (live) {
-        long long orow;
-        bool in = true;
-        if (sh) {
-          orow = t.n0 + r;
-        } else {
-          const int ci = a.grp_off[t.g] + t.n0 + r;
-          in = ci >= 0 && ci < a.tk;
-          orow = in ? a.row_list[ci] : -1;
-          in = in && orow >= 0 && orow < a.out_rows_routed;
-        }
-        if (in) {
+        const long long orow = orow_down;
+        if (orow >= 0) {
           uint4* out = reinterpret_cast<uint4*>(
               static_cast<__nv_bfloat16*>(sh ? a.out_shared : a.out_routed) +
               orow * (sh ? a.ld_shared : a.ld_routed) + t.m * 128 + part * 32);
