@@ -38,11 +38,11 @@ struct Fp8Args {
   int tk;
   long long a_rows_routed;      // bound of routed A row indices
   int T;
-  int mt_routed, mt_shared;     // 128-row weight tiles per group
+  int mt_routed, mt_shared;     // weight tiles (units along N) per group
   int n_shared_tiles;
   int k_steps;                  // K / 128
   int b_rows_routed;            // weight rows per routed expert (2F or d)
-  int b_up_routed, b_up_shared; // offset of the up rows (gate/up) or 0
+  int b_up_routed, b_up_shared; // offset of a unit's second weight tile (gate/up: the up rows)
   // Token scales are block-major, [K/128][rows]: the scales of one K block for consecutive
   // rows are consecutive, so a warp's 32 rows read one or two cache lines per k-step.
   const float* a_sc_routed;     // token scales of routed A rows [K/128][a_sc_ld_routed]
@@ -131,15 +131,17 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
                : "memory");
 }
 
-template <int STAGE, int STAGES>
+template <int NB_, int STAGES>
 struct Fp8Shape {
-  static constexpr int NB = STAGE == 0 ? 2 : 1;      // weight tiles per stage (gate, up)
+  // weight tiles per stage: gate/up 2 (gate, up); down 2 (two adjacent 128-column tiles of the
+  // output) when d is a multiple of 256, else 1
+  static constexpr int NB = NB_;
   static constexpr int A_BYTES = 128 * 128;          // 128 token rows x 128 e4m3
   static constexpr int B_BYTES = 128 * 128;          // 128 weight rows x 128 e4m3
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   static constexpr int ACC_COLS = NB * 128;          // partial accumulator columns per buffer
-  // partial buffers: as many as tensor memory holds (2 for gate/up, 4 for down), so the tensor
-  // core can run that many K blocks ahead of the promoters
+  // partial buffers: as many as tensor memory holds (2 for N = 256, 4 for N = 128), so the
+  // tensor core can run that many K blocks ahead of the promoters
   static constexpr int NBUF = 512 / ACC_COLS;
   static constexpr int TMEM_COLS = NBUF * ACC_COLS;
   static constexpr int SLOTS = STAGES + NBUF;        // scale ring slots
@@ -150,13 +152,16 @@ struct Fp8Shape {
   static_assert(TMEM_COLS <= 512, "tensor memory");
 };
 
-template <int STAGE, int STAGES>
+template <int STAGE, int NB, int STAGES>
 __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
     ffn_gemm_e4m3_kernel(const Fp8Args a, const __grid_constant__ CUtensorMap mapA,
                          const __grid_constant__ CUtensorMap mapAs,
                          const __grid_constant__ CUtensorMap mapB,
                          const __grid_constant__ CUtensorMap mapBs) {
-  using S = Fp8Shape<STAGE, STAGES>;
+  using S = Fp8Shape<NB, STAGES>;
+  // weight rows between consecutive units' first tiles: gate/up 128 (a unit's second tile is
+  // the up projection, F rows further); down NB x 128 (adjacent output tiles)
+  constexpr int kStep = STAGE == 0 ? 128 : NB * 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       const bool sh = t.g < 0;
       const CUtensorMap* amap = sh ? &mapAs : &mapA;
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
-      const int brow0 = (sh ? 0 : t.g * a.b_rows_routed) + t.m * 128;
+      const int brow0 = (sh ? 0 : t.g * a.b_rows_routed) + t.m * kStep;
       const int brow1 = brow0 + (sh ? a.b_up_shared : a.b_up_routed);
       // Token rows: routed gate/up rows are gathered by the gather warps (cp.async); the shared
       // expert's rows (x, contiguous) and the down projection's rows (h, contiguous) are one
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       const long long xs_ld = sh ? a.T : a.a_sc_ld_routed;
       const float* wsc = (sh ? a.w_sc_shared
                              : a.w_sc_routed + (size_t)t.g * (a.b_rows_routed / 128) * kb_n) +
-                         (size_t)t.m * kb_n;
+                         (size_t)t.m * (kStep / 128) * kb_n;
       const int w_up = (sh ? a.b_up_shared : a.b_up_routed) / 128 * kb_n;
       const uint8_t* gsrc = a.gather_base + j * 16;
       for (int ks = 0; ks < kb_n; ++ks, ++q) {
@@ -518,14 +523,19 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       } else if (live) {
         const long long orow = orow_down;
         if (orow >= 0) {
-          uint4* out = reinterpret_cast<uint4*>(
-              static_cast<__nv_bfloat16*>(sh ? a.out_shared : a.out_routed) +
-              orow * (sh ? a.ld_shared : a.ld_routed) + t.m * 128 + part * 32);
+          __nv_bfloat16* orow_p = static_cast<__nv_bfloat16*>(sh ? a.out_shared : a.out_routed) +
+                                  orow * (sh ? a.ld_shared : a.ld_routed) + t.m * (NB * 128) +
+                                  part * 32;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int j = q * 8;
-            out[q] = make_uint4(pack_bf16x2(acc0[j], acc0[j + 1]), pack_bf16x2(acc0[j + 2], acc0[j + 3]),
-                                pack_bf16x2(acc0[j + 4], acc0[j + 5]), pack_bf16x2(acc0[j + 6], acc0[j + 7]));
+          for (int h = 0; h < NB; ++h) {   // the unit's first and (NB = 2) second 128 columns
+            const float* acc = h ? acc1 : acc0;
+            uint4* out = reinterpret_cast<uint4*>(orow_p + h * 128);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int j = q * 8;
+              out[q] = make_uint4(pack_bf16x2(acc[j], acc[j + 1]), pack_bf16x2(acc[j + 2], acc[j + 3]),
+                                  pack_bf16x2(acc[j + 4], acc[j + 5]), pack_bf16x2(acc[j + 6], acc[j + 7]));
+            }
           }
         }
       }
@@ -593,13 +603,14 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     }
   } else {
     if (has_shared && Fs != F) return cudaErrorNotSupported;
+    const int nb = d % 256 == 0 ? 2 : 1;   // output columns per unit: nb x 128
     a.a_rows_routed = tk;
-    a.mt_routed = d / 128;
-    a.mt_shared = has_shared ? d / 128 : 0;
+    a.mt_routed = d / (nb * 128);
+    a.mt_shared = has_shared ? d / (nb * 128) : 0;
     a.k_steps = F / 128;
     a.b_rows_routed = d;
-    a.b_up_routed = 0;
-    a.b_up_shared = 0;
+    a.b_up_routed = nb == 2 ? 128 : 0;
+    a.b_up_shared = nb == 2 ? 128 : 0;
     a.a_sc_routed = reinterpret_cast<const float*>(ws + L.h_scales);
     a.a_sc_ld_routed = tk;
     a.a_sc_shared = reinterpret_cast<const float*>(ws + L.hs_scales);
@@ -625,14 +636,20 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
   if (!ok) return cudaErrorInvalidValue;
   cudaError_t err;
   if (stage == 0) {
-    using S = Fp8Shape<0, 4>;
-    auto kern = ffn_gemm_e4m3_kernel<0, 4>;
+    using S = Fp8Shape<2, 4>;
+    auto kern = ffn_gemm_e4m3_kernel<0, 2, 4>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (err != cudaSuccess) return err;
     kern<<<sm_count(), Fp8Threads<0>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+  } else if (d % 256 == 0) {
+    using S = Fp8Shape<2, 4>;
+    auto kern = ffn_gemm_e4m3_kernel<1, 2, 4>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (err != cudaSuccess) return err;
+    kern<<<sm_count(), Fp8Threads<1>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
   } else {
     using S = Fp8Shape<1, 6>;
-    auto kern = ffn_gemm_e4m3_kernel<1, 6>;
+    auto kern = ffn_gemm_e4m3_kernel<1, 1, 6>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (err != cudaSuccess) return err;
     kern<<<sm_count(), Fp8Threads<1>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);

@@ -421,9 +421,13 @@ def test_gate_up_intermediate_and_schedule(cfg):
 TOL_FP8 = 6e-2
 FP8_HOT = dataclasses.replace(HOT, name="hot_fp8", act="fp8", w="fp8", d=256, d_ff=256,
                               d_ff_shared=256)
+# d = 3 x 128: the down projection takes one 128-column output tile per unit (d not a multiple
+# of 256), the other shapes two
+FP8_ODD = dataclasses.replace(SMALL, name="odd_fp8", act="fp8", w="fp8", d=384, d_ff=256,
+                              d_ff_shared=256)
 
 
-@pytest.mark.parametrize("cfg", [FP8_SMALL, FP8_HOT], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [FP8_SMALL, FP8_HOT, FP8_ODD], ids=lambda c: c.name)
 def test_fp8_expert_rows_and_layer(cfg):
     inp, W = inputs(cfg)
     m = moe()
