@@ -120,18 +120,31 @@ KERNEL_NAMES = {"ffn_gate_up": "ffn_gemm_{}_kernel<0> (gate/up + SwiGLU)",
                 "combine": "combine_kernel", "ffn_setup": "ffn_plan_kernel + ffn_rows_kernel"}
 
 
+# The router's dot products are exact-order fp32 FMAs on the CUDA cores (no tensor cores), so its
+# compute roof is the fp32 FMA rate: 152 SMs x 128 FMA lanes x 2 flops x 2.07 GHz (the maximum
+# SM clock; a packed fp32x2 FMA occupies two lanes).
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 def roofline(cfg, stage, ms, bytes_, flops, pk):
-    """Roofline entry of one stage: the binding roof is the one whose ideal time is longer —
-    HBM (algorithmic bytes / measured copy bandwidth) or the tensor cores (flops / the dtype's
-    peak: measured bf16 burst, e4m3 = 2x that by the nominal ratio)."""
+    """Roofline entry of one stage: the binding roof is the one whose ideal time is longest —
+    HBM (algorithmic bytes / measured copy bandwidth), the tensor cores for the expert GEMMs
+    (flops / the dtype's peak: measured bf16 burst, e4m3 = 2x that by the nominal ratio) or the
+    fp32 FMA rate for the router."""
     tc_peak = pk["bf16"] * (2.0 if cfg.w == "fp8" else 1.0)
     t_hbm = bytes_[stage] / (pk["hbm"] * 1e9)
     t_tc = flops.get(stage, 0) / (tc_peak * 1e12) if stage in ("ffn_gate_up", "ffn_down") else 0.0
+    t_alu = flops.get(stage, 0) / (ALU_FP32_TFLOPS * 1e12) if stage == "route" else 0.0
     name = KERNEL_NAMES[stage].format("e4m3" if cfg.w == "fp8" else "bf16")
     base = {"kernel": name, "launch_ms": round(ms, 4),
             "traffic": measured_traffic(stage, cfg.name),
             "algorithmic_bytes_per_launch": bytes_[stage],
             "algorithmic_flops_per_launch": flops.get(stage, 0)}
+    if t_alu > t_hbm:
+        ach = flops[stage] / (ms * 1e-3) / 1e12
+        return {**base, "bound": "alu", "achieved": round(ach, 1), "peak": round(ALU_FP32_TFLOPS, 1),
+                "unit": "TFLOP/s", "frac": round(ach / ALU_FP32_TFLOPS, 4),
+                "peak_source": "derived: fp32 FMA lanes x 2 x max SM clock"}
     if t_tc > t_hbm:
         ach = flops[stage] / (ms * 1e-3) / 1e12
         return {**base, "bound": "tensor", "achieved": round(ach, 1), "peak": tc_peak,
@@ -368,7 +381,7 @@ def main():
             "layer_hbm_frac": round(layer_bytes / (r["ms"] * 1e-3) / 1e9 / pk["hbm"], 4),
             "stages_roofline": {n: {k2: v2 for k2, v2 in roofline(cfg, n, r["stage_ms"][n], b, f, pk).items()
                                     if k2 in ("bound", "achieved", "unit", "frac")}
-                                for n in ("ffn_gate_up", "ffn_down")},
+                                for n in ("route", "dispatch", "ffn_gate_up", "ffn_down", "combine")},
             "experts_touched": touched,
             "imbalance_factor": round(float(np.bincount(
                 np.repeat(np.arange(cfg.E), r["counts"].sum(0)), minlength=cfg.E)

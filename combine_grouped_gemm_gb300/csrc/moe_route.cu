@@ -41,11 +41,15 @@ __device__ __forceinline__ void fma2_bcast(float& c0, float& c1, float x0, float
 // Partial logits: partials[c][t][e] = sum over the c-th chunk of d of x[t][i] * w[e][i],
 // one sequential FMA chain per (c, t, e).
 // CTA tile BT tokens x BE experts of one chunk; thread tile TM x TN; k-steps of BK columns,
-// staged through shared memory (k-major, so the compute loop reads conflict-free) with the next
-// step's global loads held in registers while the current step computes.
+// staged through (dynamic) shared memory, k-major so the compute loop reads conflict-free, with
+// the next step's global loads held in registers while the current step computes.
 // ---------------------------------------------------------------------------------------
 template <int BT, int BE, int TM, int TN, int BK>
-__global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16* __restrict__ x,
+constexpr int partials_smem_bytes() { return 2 * BK * (BT + BE) * 4; }
+
+// Thread tiles of up to 64 outputs run two CTAs per SM (at most 128 registers a thread).
+template <int BT, int BE, int TM, int TN, int BK>
+__global__ void __launch_bounds__(256, TM * TN <= 64 ? 2 : 1) route_partials_kernel(const __nv_bfloat16* __restrict__ x,
                                                              const float* __restrict__ wg,
                                                              float* __restrict__ partials, int T,
                                                              int d, int E) {
@@ -53,19 +57,21 @@ __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16
   constexpr int XV = BT * BK / 8;            // 16-byte vectors of x per step (8 bf16)
   constexpr int WV = BE * BK / 4;            // 16-byte vectors of w per step (4 floats)
   constexpr int NX = (XV + 255) / 256, NW = (WV + 255) / 256;
-  __shared__ __align__(16) float xs[2][BK][BT];
-  __shared__ __align__(16) float ws[2][BK][BE];
+  extern __shared__ __align__(16) float rsm[];
+  float (*xs)[BK][BT] = reinterpret_cast<float (*)[BK][BT]>(rsm);
+  float (*ws)[BK][BE] = reinterpret_cast<float (*)[BK][BE]>(rsm + 2 * BK * BT);
 
   const int tid = threadIdx.x;
   const int tx = tid % (BE / TN), ty = tid / (BE / TN);
-  // Thread tile rows / columns. With 8 per side they are two groups of 4 consecutive entries,
-  // half a tile apart, so each group is one conflict-free 16-byte shared load; otherwise rows
-  // are consecutive and columns strided by the thread count along the row.
+  // Thread tile rows / columns. With a multiple of 4 per side they are groups of 4 consecutive
+  // entries, one group per BT/(TM/4) rows (BE/(TN/4) columns), so each group is one
+  // conflict-free 16-byte shared load; otherwise rows are consecutive and columns strided by
+  // the thread count along the row.
   auto row_of = [&](int ty_, int i) {
-    return TM == 8 ? (i < 4 ? ty_ * 4 + i : BT / 2 + ty_ * 4 + (i - 4)) : ty_ * TM + i;
+    return TM % 4 == 0 ? (i / 4) * (BT / (TM / 4)) + ty_ * 4 + (i % 4) : ty_ * TM + i;
   };
   auto col_of = [&](int tx_, int j) {
-    return TN == 8 ? (j < 4 ? tx_ * 4 + j : BE / 2 + tx_ * 4 + (j - 4)) : tx_ + j * (BE / TN);
+    return TN % 4 == 0 ? (j / 4) * (BE / (TN / 4)) + tx_ * 4 + (j % 4) : tx_ + j * (BE / TN);
   };
   const int e0 = blockIdx.x * BE, t0 = blockIdx.y * BT, c = blockIdx.z;
   const int L = d / kRouteChunks;
@@ -173,21 +179,27 @@ __global__ void __launch_bounds__(256) route_partials_kernel(const __nv_bfloat16
   }
 }
 
-// MAXBK caps the k-step so the static shared memory (2 x BK x (BT + BE) floats) stays within
-// 48 KB.
+// The k-step is BK columns, the largest of MAXBK, 16, 8 that divides a chunk.
+template <int BT, int BE, int TM, int TN, int BK>
+cudaError_t launch_partials_bk(const __nv_bfloat16* x, const float* wg, float* partials, int T,
+                               int d, int E, cudaStream_t st) {
+  constexpr int smem = partials_smem_bytes<BT, BE, TM, TN, BK>();
+  auto kern = route_partials_kernel<BT, BE, TM, TN, BK>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  dim3 grid((E + BE - 1) / BE, (T + BT - 1) / BT, kRouteChunks);
+  kern<<<grid, 256, smem, st>>>(x, wg, partials, T, d, E);
+  return cudaGetLastError();
+}
+
 template <int BT, int BE, int TM, int TN, int MAXBK>
 cudaError_t launch_partials(const __nv_bfloat16* x, const float* wg, float* partials, int T, int d,
                             int E, cudaStream_t st) {
-  static_assert(2 * MAXBK * (BT + BE) * 4 <= 48 * 1024, "static shared memory");
   const int L = d / kRouteChunks;
-  dim3 grid((E + BE - 1) / BE, (T + BT - 1) / BT, kRouteChunks);
   if (MAXBK >= 32 && L % 32 == 0)
-    route_partials_kernel<BT, BE, TM, TN, (MAXBK >= 32 ? 32 : 16)><<<grid, 256, 0, st>>>(x, wg, partials, T, d, E);
-  else if (L % 16 == 0)
-    route_partials_kernel<BT, BE, TM, TN, 16><<<grid, 256, 0, st>>>(x, wg, partials, T, d, E);
-  else
-    route_partials_kernel<BT, BE, TM, TN, 8><<<grid, 256, 0, st>>>(x, wg, partials, T, d, E);
-  return cudaGetLastError();
+    return launch_partials_bk<BT, BE, TM, TN, (MAXBK >= 32 ? 32 : 16)>(x, wg, partials, T, d, E, st);
+  if (L % 16 == 0) return launch_partials_bk<BT, BE, TM, TN, 16>(x, wg, partials, T, d, E, st);
+  return launch_partials_bk<BT, BE, TM, TN, 8>(x, wg, partials, T, d, E, st);
 }
 
 // e^z by Cody-Waite reduction and a degree-7 Taylor polynomial (see the file comment).
@@ -216,7 +228,7 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
 }
 
 // ---------------------------------------------------------------------------------------
-// Selection: one CTA (256 threads) per token.
+// Selection for small batches: one CTA (256 threads) per token.
 //  1. thread e: the 16 chunk partials of expert e (coalesced across threads), pairwise tree,
 //     sigmoid, selection key v = s + bias;
 //  2. warp w: scores of groups w, w+8, ...: the two largest keys of the group by a warp-wide
@@ -227,7 +239,7 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
 // ---------------------------------------------------------------------------------------
 constexpr int kSelThreads = 256;
 
-__global__ void __launch_bounds__(kSelThreads) route_select_kernel(
+__global__ void __launch_bounds__(kSelThreads) route_select_cta_kernel(
     const float* __restrict__ partials, const float* __restrict__ bias,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int E, int k,
     int n_group, int topk_group, float route_scale) {
@@ -324,6 +336,117 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Selection for large batches: one warp per token, several tokens per CTA; each warp has its own shared-memory
+// scratch. The operations and their order are those of the file comment:
+//  1. lane l, experts e = l, l+32, ...: the 16 chunk partials (coalesced across lanes), pairwise
+//     tree, sigmoid, selection key v = s + bias;
+//  2. per group: the two largest keys by a warp-wide top-2 merge (values only: equal keys give
+//     equal scores whichever expert carries them);
+//  3. lane g: rank of group g among all groups -> kept or not;
+//  4. k rounds of a warp-wide argmax over the eligible experts (key desc, index asc), then the
+//     weights from the raw sigmoid scores in selection order.
+// ---------------------------------------------------------------------------------------
+__host__ __device__ constexpr int sel_scratch_floats(int E) { return 2 * E + 64 + 64 + 32; }
+
+__global__ void __launch_bounds__(256) route_select_kernel(
+    const float* __restrict__ partials, const float* __restrict__ bias,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int E, int k,
+    int n_group, int topk_group, float route_scale) {
+  extern __shared__ float sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;   // whole warps only: no block-wide barrier follows
+  float* s = sm + warp * sel_scratch_floats(E);        // [E] sigmoid scores
+  float* v = s + E;                                    // [E] selection keys
+  float* gscore = v + E;                               // [64]
+  int* keep = reinterpret_cast<int*>(gscore + 64);     // [64]
+  float* sel_s = reinterpret_cast<float*>(keep + 64);  // [32]
+
+#pragma unroll 4
+  for (int e = lane; e < E; e += 32) {
+    float p[kRouteChunks];
+#pragma unroll
+    for (int c = 0; c < kRouteChunks; ++c) p[c] = partials[((size_t)c * T + t) * E + e];
+#pragma unroll
+    for (int w = kRouteChunks; w > 1; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w / 2; ++j) p[j] = __fadd_rn(p[2 * j], p[2 * j + 1]);
+    const float si = __fdiv_rn(1.0f, __fadd_rn(1.0f, route_exp(-p[0])));
+    s[e] = si;
+    v[e] = __fadd_rn(si, bias[e]);
+  }
+  __syncwarp();
+
+  const int gs = E / n_group;
+  for (int g = 0; g < n_group; ++g) {
+    float a = -INFINITY, b = -INFINITY;  // this lane's two largest keys of group g
+    for (int e = g * gs + lane; e < (g + 1) * gs; e += 32) {
+      const float x = v[e];
+      if (x > a) {
+        b = a;
+        a = x;
+      } else if (x > b) {
+        b = x;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float c = __shfl_xor_sync(0xffffffffu, a, off);
+      const float d = __shfl_xor_sync(0xffffffffu, b, off);
+      const float hi = fmaxf(a, c);
+      b = fmaxf(fminf(a, c), fmaxf(b, d));
+      a = hi;
+    }
+    if (lane == 0) gscore[g] = gs >= 2 ? __fadd_rn(a, b) : a;
+  }
+  __syncwarp();
+  for (int g = lane; g < n_group; g += 32) {
+    int rank = 0;
+    for (int h = 0; h < n_group; ++h) rank += ranks_before(gscore[h], h, gscore[g], g) ? 1 : 0;
+    keep[g] = rank < topk_group;
+  }
+  __syncwarp();
+
+  uint32_t taken = 0;  // bit q: expert lane + 32*q already chosen (E <= 1024)
+  int sel_e = -1;      // lane i (< k) keeps the i-th choice
+  for (int i = 0; i < k; ++i) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int q = 0, e = lane; e < E; ++q, e += 32) {
+      if ((taken >> q) & 1u) continue;
+      if (!keep[e / gs]) continue;
+      if (be == 0x7fffffff || ranks_before(v[e], e, bv, be)) {
+        bv = v[e];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (oe != 0x7fffffff && (be == 0x7fffffff || ranks_before(ov, oe, bv, be))) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == i) sel_e = be;
+  }
+  if (lane < k) sel_s[lane] = s[sel_e];
+  __syncwarp();
+  if (lane == 0) {
+    float sum = 0.0f;
+    for (int i = 0; i < k; ++i) sum = __fadd_rn(sum, sel_s[i]);
+    for (int i = 0; i < k; ++i) sel_s[i] = __fmul_rn(__fdiv_rn(sel_s[i], sum), route_scale);
+  }
+  __syncwarp();
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = sel_e;
+    topk_w[(size_t)t * k + lane] = sel_s[lane];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, const float* bias,
@@ -337,9 +460,22 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
                         ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st)
                         : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st);
   if (err != cudaSuccess) return err;
-  const size_t smem = (size_t)(2 * c.E + 64 + 64 + 32) * sizeof(float);
-  route_select_kernel<<<c.T, kSelThreads, smem, st>>>(partials, bias, topk_idx, topk_w, c.T, c.E,
-                                                      c.k, c.n_group, c.topk_group, c.route_scale);
+  if (c.T < 1024) {   // a CTA per token keeps every expert's loads in flight at once
+    const size_t smem1 = (size_t)sel_scratch_floats(c.E) * sizeof(float);
+    route_select_cta_kernel<<<c.T, kSelThreads, smem1, st>>>(partials, bias, topk_idx, topk_w, c.T,
+                                                             c.E, c.k, c.n_group, c.topk_group,
+                                                             c.route_scale);
+    return cudaGetLastError();
+  }
+  // one warp per token; CTAs of up to 8 warps, fewer when T is small so the tokens still spread
+  // over the SMs
+  const int wpc = c.T >= 2432 ? 8 : c.T >= 1216 ? 4 : 2;
+  const size_t smem = (size_t)wpc * sel_scratch_floats(c.E) * sizeof(float);
+  err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  if (err != cudaSuccess) return err;
+  route_select_kernel<<<(c.T + wpc - 1) / wpc, 32 * wpc, smem, st>>>(
+      partials, bias, topk_idx, topk_w, c.T, c.E, c.k, c.n_group, c.topk_group, c.route_scale);
   return cudaGetLastError();
 }
 
