@@ -267,8 +267,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      // the TMA lane's expect_tx arrival, plus one per gather warp (gate/up)
-      mbar_init(&full[i], 1 + GemmThreads<STAGE>::kGather / 32);
+      // the TMA lane's expect_tx arrival, plus one per gather thread (gate/up)
+      mbar_init(&full[i], 1 + GemmThreads<STAGE>::kGather);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -398,6 +398,9 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
             ok = false;
             break;
           }
+          // gate/up: token rows gathered by cp.async (generic proxy) are ordered, observed
+          // through the barrier, before the MMA's reads
+          if (STAGE == 0) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sa = smem_addr(smem + stage * S::STAGE_BYTES);
           const uint32_t sb = sa + S::NA * S::A_BYTES;
@@ -421,21 +424,16 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
   } else if (warp >= 6) {
     // ------------------------------ token-row gather (gate/up) ------------------------------
     // Thread gt copies 16-byte chunk j = gt % 8 of rows p = gt/8 + 8i of the token tile into
-    // the 128-byte-swizzled layout (chunk j of row p at chunk j ^ (p % 8) = j ^ gt/8).
-    // Completion is observed kLag stages late: wait for the copies, make them visible to the
-    // async proxy, then arrive on that stage's barrier.
-    // kLag = STAGES - 2: the arrival for stage q waits only for stage q+kLag to be free, i.e.
-    // for the MMAs of k-step q-2, so two k-steps of MMAs can be in flight.
-    constexpr int kLag = STAGES - 2;
-    static_assert(kLag >= 1, "needs at least three stages");
-    uint32_t with_copies = 0;  // bit i: k-step q-1-i issued copies (arrival still owed)
+    // the 128-byte-swizzled layout (chunk j of row p at chunk j ^ (p % 8) = j ^ gt/8), then arms
+    // an arrival on the stage's full barrier that the hardware performs once every copy the
+    // thread has issued so far has landed (a thread with nothing to copy arrives at once). The
+    // MMA thread puts a proxy fence between its wait and its tensor-core reads.
     constexpr int kRowsPer = BN / 8;
     const int gt = threadIdx.x - 192;
     const int j = gt & 7, rg = gt >> 3;
     const uint32_t dst_off = static_cast<uint32_t>(rg * 128 + ((j ^ rg) << 4));
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t q = 0;  // k-steps issued
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit t = decode_unit<BN>(a, u);
@@ -465,33 +463,17 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sb + i * 1024),
                          "l"(src[i] + ks * 128)
                          : "memory");
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        // a k-step without copies (nothing to gather in this unit) is arrived for at once;
-        // one with copies kLag k-steps later, once its copies have landed
-        with_copies = (with_copies << 1) | (gather ? 1u : 0u);
-        if (!gather) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[q % STAGES]);
-        }
-        if (++q > kLag && ((with_copies >> kLag) & 1u)) {
-          asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[(q - 1 - kLag) % STAGES]);
-        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                         smem_addr(&full[stage]))
+                     : "memory");
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    // the last kLag stages (or, after an abort, every copy still in flight)
+    // after an abort: copies still in flight land before the CTA exits
     asm volatile("cp.async.wait_all;" ::: "memory");
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (ok && lane == 0)
-      for (uint32_t r2 = (q > kLag ? q - kLag : 0); r2 < q; ++r2)
-        if ((with_copies >> (q - 1 - r2)) & 1u) mbar_arrive(&full[r2 % STAGES]);
   } else {
     // ------------------------------ epilogue ------------------------------
     const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31

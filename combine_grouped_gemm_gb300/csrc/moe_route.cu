@@ -57,9 +57,15 @@ __global__ void __launch_bounds__(256, TM * TN <= 64 ? 2 : 1) route_partials_ker
   constexpr int XV = BT * BK / 8;            // 16-byte vectors of x per step (8 bf16)
   constexpr int WV = BE * BK / 4;            // 16-byte vectors of w per step (4 floats)
   constexpr int NX = (XV + 255) / 256, NW = (WV + 255) / 256;
+  // static shared memory when the stages fit in 48 KB (addresses known at compile time),
+  // dynamic otherwise
+  constexpr int kSmemFloats = partials_smem_bytes<BT, BE, TM, TN, BK>() / 4;
+  constexpr bool kStatic = kSmemFloats * 4 <= 48 * 1024;
   extern __shared__ __align__(16) float rsm[];
-  float (*xs)[BK][BT] = reinterpret_cast<float (*)[BK][BT]>(rsm);
-  float (*ws)[BK][BE] = reinterpret_cast<float (*)[BK][BE]>(rsm + 2 * BK * BT);
+  __shared__ __align__(16) float rstat[kStatic ? kSmemFloats : 4];
+  float* const rbase = kStatic ? rstat : rsm;
+  float (*xs)[BK][BT] = reinterpret_cast<float (*)[BK][BT]>(rbase);
+  float (*ws)[BK][BE] = reinterpret_cast<float (*)[BK][BE]>(rbase + 2 * BK * BT);
 
   const int tid = threadIdx.x;
   const int tx = tid % (BE / TN), ty = tid / (BE / TN);
@@ -185,10 +191,14 @@ cudaError_t launch_partials_bk(const __nv_bfloat16* x, const float* wg, float* p
                                int d, int E, cudaStream_t st) {
   constexpr int smem = partials_smem_bytes<BT, BE, TM, TN, BK>();
   auto kern = route_partials_kernel<BT, BE, TM, TN, BK>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
+  // (the opt-in call only where needed: it costs host time right at the start of the layer)
+  if (smem > 48 * 1024) {
+    const cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+  }
   dim3 grid((E + BE - 1) / BE, (T + BT - 1) / BT, kRouteChunks);
-  kern<<<grid, 256, smem, st>>>(x, wg, partials, T, d, E);
+  kern<<<grid, 256, smem > 48 * 1024 ? smem : 0, st>>>(x, wg, partials, T, d, E);
   return cudaGetLastError();
 }
 
@@ -454,11 +464,14 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
                          cudaStream_t st) {
   (void)status;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  // Large batches: 128x128 tiles, 8x8 per thread. Small batches: 32x32 tiles, 2x2 per thread,
-  // so the 16 chunks x E/32 x T/32 grid still fills the GPU several CTAs per SM deep.
-  cudaError_t err = c.T >= 2048
-                        ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st)
-                        : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st);
+  // From 512 tokens: 128x128 tiles, 8x8 per thread. Below, smaller tiles (64x32 with 4x2 per
+  // thread, then 32x32 with 2x2) so the 16 chunks x E/BE x T/BT grid still fills the GPU
+  // several CTAs per SM deep. (Measured on the DSV3 router: 75 / 120 us at T = 512 / 1024 with
+  // 128x128 against 146 / 268 us with 32x32; 71 us at T = 256 with 64x32 against 85 us.)
+  cudaError_t err =
+      c.T >= 512   ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st)
+      : c.T >= 256 ? launch_partials<64, 32, 4, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
+                   : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st);
   if (err != cudaSuccess) return err;
   if (c.T < 1024) {   // a CTA per token keeps every expert's loads in flight at once
     const size_t smem1 = (size_t)sel_scratch_floats(c.E) * sizeof(float);
@@ -471,9 +484,11 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
   // over the SMs
   const int wpc = c.T >= 2432 ? 8 : c.T >= 1216 ? 4 : 2;
   const size_t smem = (size_t)wpc * sel_scratch_floats(c.E) * sizeof(float);
-  err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-  if (err != cudaSuccess) return err;
+  if (smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (err != cudaSuccess) return err;
+  }
   route_select_kernel<<<(c.T + wpc - 1) / wpc, 32 * wpc, smem, st>>>(
       partials, bias, topk_idx, topk_w, c.T, c.E, c.k, c.n_group, c.topk_group, c.route_scale);
   return cudaGetLastError();
