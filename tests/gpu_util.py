@@ -63,7 +63,7 @@ def ws_offsets(cfg):
         return (v + 255) // 256 * 256
     tk = cfg.T * cfg.k
     ab = 1 if cfg.act == "fp8" else 2
-    bn = 128 if tk >= 64 * cfg.E else 64
+    bn = 128 if (cfg.act == "fp8" or tk >= 16 * cfg.E) else 64
     max_tiles = cfg.E + (tk + bn - 1) // bn
     o = {}
     cur = 0
