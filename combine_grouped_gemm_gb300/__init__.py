@@ -67,6 +67,7 @@ def _load():
         "moe_layer": [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P],
         "moe_clear_status": [P, S],
         "moe_read_status": [P, P, S],
+        "moe_selftest_wait": [P, ctypes.c_int64, S],
         "moe_strerror": [I],
         "moe_abi_version": [],
         "moe_last_cuda_error": [],
@@ -82,8 +83,8 @@ _lib = _load()
 
 EXPORTED = ["moe_validate", "moe_query_sizes", "moe_route", "moe_route_noalloc", "moe_dispatch",
             "moe_expert_ffn",
-            "moe_combine", "moe_layer", "moe_clear_status", "moe_read_status", "moe_strerror",
-            "moe_abi_version", "moe_last_cuda_error"]
+            "moe_combine", "moe_layer", "moe_clear_status", "moe_read_status", "moe_selftest_wait",
+            "moe_strerror", "moe_abi_version", "moe_last_cuda_error"]
 
 
 def _check(fn, rc):
@@ -200,6 +201,12 @@ def read_status(ws, stream=None) -> int:
     st = ctypes.c_uint32(0)
     _check("moe_read_status", _lib.moe_read_status(_p(ws), ctypes.byref(st), _s(stream)))
     return st.value
+
+
+def selftest_wait(ws, limit_ns, stream=None):
+    """Launches the library's wait diagnostic (see moe_selftest_wait): a kernel whose bounded
+    waits run out after about limit_ns and set MOE_DEV_TIMEOUT in ws's status word."""
+    _check("moe_selftest_wait", _lib.moe_selftest_wait(_p(ws), int(limit_ns), _s(stream)))
 
 
 def abi_version() -> int:

@@ -69,16 +69,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed. Bounded: returns false (after
-// setting *abort and the status bit) when the wait outlives kWaitLimitNs, or at once when
-// another role of the CTA has already set *abort.
+// setting *abort and the status bit) when the wait outlives limit_ns (kWaitLimitNs unless
+// given), or at once when another role of the CTA has already set *abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
+                                          uint32_t* status, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_test(bar, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       raise_status(status, MOE_DEV_TIMEOUT);
       return false;

@@ -208,6 +208,16 @@ int moe_clear_status(void* ws, cudaStream_t stream);
  * bits). This is the one call that blocks the host. */
 int moe_read_status(const void* ws, uint32_t* status, cudaStream_t stream);
 
+/* Diagnostic of the device-side failure handling (the pages have no counterpart; it serves
+ * callers and tests that must see a kernel give up instead of hang). Launches one CTA in which
+ * one thread waits on a barrier that nothing ever completes, bounded by limit_ns, while a
+ * second thread waits on another such barrier with a limit three times as long. When the first
+ * wait runs out it ORs MOE_DEV_TIMEOUT into the status word of ws and raises the CTA's abort
+ * flag, on which the second wait returns at once; the kernel then ends (after about limit_ns,
+ * well before 3 x limit_ns) and the context stays usable. ws: any workspace of this library
+ * (only its status word is written). limit_ns: 1 us .. 10 s, else MOE_ERR_INVALID_ARG. */
+int moe_selftest_wait(void* ws, int64_t limit_ns, cudaStream_t stream);
+
 /* Static name of a return code. */
 const char* moe_strerror(int code);
 

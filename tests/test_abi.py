@@ -95,3 +95,8 @@ def test_null_and_misaligned_pointers_are_rejected_before_any_launch(moe):
     bad.T = 15
     assert L.moe_layer(ctypes.byref(bad), *([ok] * 14), None, None) == 1
     assert L.moe_read_status(None, None, None) == 1
+    # the wait diagnostic: no workspace, a misaligned one, or a limit outside 1 us .. 10 s
+    assert L.moe_selftest_wait(None, 10 ** 6, None) == 1
+    assert L.moe_selftest_wait(ok + 4, 10 ** 6, None) == 1
+    assert L.moe_selftest_wait(ok, 999, None) == 1
+    assert L.moe_selftest_wait(ok, 10 ** 10 + 1, None) == 1

@@ -316,6 +316,33 @@ def test_layer_all_tokens(cfg):
     assert _layer_tokens_check(cfg, np.arange(cfg.T), inp, W, y) <= TOL_BF16
 
 
+def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable():
+    """Failure handling on the device: a wait on a barrier that nothing completes gives up
+    after its limit, records MOE_DEV_TIMEOUT in the workspace status word and raises the CTA's
+    abort flag, on which a second wait (limit 3x) returns at once; afterwards a layer still
+    runs and matches the oracle."""
+    m = moe()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    m.clear_status(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    limit_ms = 50.0
+    e0.record()
+    m.selftest_wait(ws, int(limit_ms * 1e6))
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    assert m.read_status(ws) == m.MOE_DEV_TIMEOUT
+    assert limit_ms <= ms < 2.5 * limit_ms, ms   # the second wait left on the abort flag
+    m.clear_status(ws)
+    assert m.read_status(ws) == 0
+    cfg = synth.CONFIGS["tiny"]
+    inp, W = inputs(cfg)
+    lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y = lay(inp["x"])
+    assert m.read_status(lay.bufs["ws"]) == 0
+    assert _layer_tokens_check(cfg, np.arange(cfg.T), inp, W, y) <= TOL_BF16
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("cfg,n", [(synth.CONFIGS["dsv3_decode"], 4),
                                    (synth.CONFIGS["dsv3_sweep"].with_T(8), 8),
