@@ -237,6 +237,52 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
+// k rounds of a warp-wide argmax over the eligible experts of one token under the total order
+// (key desc, index asc); lane l holds candidates e = l + 32q. Each lane's best candidate is kept
+// between rounds and only the lane whose candidate was taken looks again, so a round is one
+// butterfly of shuffles (a strict total order: the argmax does not depend on how it is reduced).
+// Returns, in lane i < k, the i-th choice. E <= 1024.
+__device__ __forceinline__ int warp_topk(const float* v, const int* keep, int E, int gs, int k,
+                                         int lane) {
+  uint32_t elig = 0;   // bit q: candidate lane + 32q is in a kept group and not yet chosen
+  for (int q = 0, e = lane; e < E; ++q, e += 32)
+    if (keep[e / gs]) elig |= 1u << q;
+  auto lane_best = [&](float& bv, int& be) {
+    bv = -INFINITY;
+    be = 0x7fffffff;
+    for (uint32_t m = elig; m; m &= m - 1) {
+      const int e = lane + 32 * (__ffs(m) - 1);
+      if (be == 0x7fffffff || ranks_before(v[e], e, bv, be)) {
+        bv = v[e];
+        be = e;
+      }
+    }
+  };
+  float lv;
+  int le;
+  lane_best(lv, le);
+  int sel_e = -1;
+  for (int i = 0; i < k; ++i) {
+    float bv = lv;
+    int be = le;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (oe != 0x7fffffff && (be == 0x7fffffff || ranks_before(ov, oe, bv, be))) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) {
+      elig &= ~(1u << (be >> 5));
+      lane_best(lv, le);
+    }
+    if (lane == i) sel_e = be;
+  }
+  return sel_e;
+}
+
 // ---------------------------------------------------------------------------------------
 // Selection for small batches: one CTA (256 threads) per token.
 //  1. thread e: the 16 chunk partials of expert e (coalesced across threads), pairwise tree,
@@ -307,31 +353,7 @@ __global__ void __launch_bounds__(kSelThreads) route_select_cta_kernel(
   __syncthreads();
   if (warp != 0) return;
 
-  uint32_t taken = 0;  // bit q: expert lane + 32*q already chosen (E <= 1024)
-  int sel_e = -1;      // lane i (< k) keeps the i-th choice
-  for (int i = 0; i < k; ++i) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-    for (int q = 0, e = lane; e < E; ++q, e += 32) {
-      if ((taken >> q) & 1u) continue;
-      if (!keep[e / gs]) continue;
-      if (be == 0x7fffffff || ranks_before(v[e], e, bv, be)) {
-        bv = v[e];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (oe != 0x7fffffff && (be == 0x7fffffff || ranks_before(ov, oe, bv, be))) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == i) sel_e = be;
-  }
+  const int sel_e = warp_topk(v, keep, E, gs, k, lane);
   if (lane < k) sel_s[lane] = s[sel_e];
   __syncwarp();
   if (lane == 0) {
@@ -418,31 +440,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(
   }
   __syncwarp();
 
-  uint32_t taken = 0;  // bit q: expert lane + 32*q already chosen (E <= 1024)
-  int sel_e = -1;      // lane i (< k) keeps the i-th choice
-  for (int i = 0; i < k; ++i) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-    for (int q = 0, e = lane; e < E; ++q, e += 32) {
-      if ((taken >> q) & 1u) continue;
-      if (!keep[e / gs]) continue;
-      if (be == 0x7fffffff || ranks_before(v[e], e, bv, be)) {
-        bv = v[e];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (oe != 0x7fffffff && (be == 0x7fffffff || ranks_before(ov, oe, bv, be))) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == i) sel_e = be;
-  }
+  const int sel_e = warp_topk(v, keep, E, gs, k, lane);
   if (lane < k) sel_s[lane] = s[sel_e];
   __syncwarp();
   if (lane == 0) {
@@ -464,13 +462,15 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
                          cudaStream_t st) {
   (void)status;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  // From 512 tokens: 128x128 tiles, 8x8 per thread. Below, smaller tiles (64x32 with 4x2 per
-  // thread, then 32x32 with 2x2) so the 16 chunks x E/BE x T/BT grid still fills the GPU
-  // several CTAs per SM deep. (Measured on the DSV3 router: 75 / 120 us at T = 512 / 1024 with
-  // 128x128 against 146 / 268 us with 32x32; 71 us at T = 256 with 64x32 against 85 us.)
+  // The tile grows with T: larger thread tiles read shared memory less often per FMA (the small
+  // tiles are bound by it), smaller CTA tiles keep the 16 chunks x E/BE x T/BT grid several
+  // CTAs per SM deep. Measured on the DSV3 router (partials + selection, us): T = 8: 25 with
+  // 32x32; T = 64: 30 with 64x32 (32x32: 40); T = 128 / 256: 36 / 52 with 64x64 (32x32: 58 /
+  // 71); T = 512 / 1024: 75 / 114 with 128x128 (32x32: 146 / 268).
   cudaError_t err =
       c.T >= 512   ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st)
-      : c.T >= 256 ? launch_partials<64, 32, 4, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
+      : c.T >= 128 ? launch_partials<64, 64, 4, 4, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
+      : c.T >= 32  ? launch_partials<64, 32, 4, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
                    : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st);
   if (err != cudaSuccess) return err;
   if (c.T < 1024) {   // a CTA per token keeps every expert's loads in flight at once

@@ -81,9 +81,9 @@ def oracle_route(cfg, inp, tokens=None):
 # ------------------------------------------------------------------------------------------
 # Router
 # ------------------------------------------------------------------------------------------
-# T spans the three partial-dot tiles (32x32 below 256 tokens, 64x32 below 512, 128x128 from
-# there) and both selection kernels (a CTA per token below 1024 tokens, a warp per token from
-# there, 2 / 4 / 8 warps per CTA at 1024 / 1536 / 4096+ tokens)
+# T spans the four partial-dot tiles (32x32 below 32 tokens, 64x32 below 128, 64x64 below 512,
+# 128x128 from there) and both selection kernels (a CTA per token below 1024 tokens, a warp per
+# token from there, 2 / 4 / 8 warps per CTA at 1024 / 1536 / 4096+ tokens)
 ROUTE_FULL = [synth.CONFIGS["tiny"], SMALL, HOT, synth.CONFIGS["dsv3_decode"],
               synth.CONFIGS["dsv3_sweep"].with_T(8), synth.CONFIGS["dsv3_sweep"].with_T(256),
               synth.CONFIGS["dsv3_sweep"].with_T(1024), synth.CONFIGS["dsv3_sweep"].with_T(1536)]
