@@ -38,7 +38,11 @@ METRIC = "MoE layer µs & tokens/s vs tokens (1–16K); % of HBM / tensor roofli
 # route x2, dispatch x2, ffn schedule x2 (plan, row list), gate/up GEMM, down GEMM, combine
 # (+ the shared expert's input quantisation on the e4m3 path)
 def kernels_per_step(cfg):
-    return 9 + (1 if cfg.act == "fp8" and cfg.d_ff_shared else 0)
+    """Library kernels one layer step launches: route 2, dispatch 2, schedule 2 (1 when the
+    plan kernel fills the row list itself, up to 1024 rows), gate/up, down, combine, and for
+    e4m3 with a shared expert the quantisation of its input."""
+    sched = 1 if cfg.T * cfg.k <= 1024 else 2
+    return 7 + sched + (1 if cfg.act == "fp8" and cfg.d_ff_shared else 0)
 L2_BYTES = 129 * 2 ** 20
 
 

@@ -38,10 +38,11 @@ namespace {
 // ---------------------------------------------------------------------------------------
 // Tile schedule (one CTA)
 // ---------------------------------------------------------------------------------------
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 1024;             // upper bound; launched with E rounded up to 32
 constexpr size_t kPlanStageBytes = 48 * 1024;   // counts table staged in shared memory up to this
+constexpr int kPlanFusedRows = 1024;            // fill the row list in the plan CTA up to this T*k
 
-// Block-wide exclusive scan of one int per thread (blockDim.x == kPlanThreads).
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, <= 1024).
 __device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -54,7 +55,7 @@ __device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_sums[lane];
+    int w = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -71,15 +72,44 @@ __device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
   return ex;
 }
 
+// row_list[c] for every compact row c: its expert by binary search on the compact offsets,
+// its source run by a scan of the run prefixes, then the run's receive row plus the position.
+__device__ __forceinline__ void fill_rows(const int32_t* grp_n, const int32_t* grp_off,
+                                          const int32_t* run_start, const int32_t* run_pre,
+                                          int32_t* row_list, uint32_t* status, int E, int R,
+                                          int tk, int first, int stride) {
+  for (int c = first; c < tk; c += stride) {
+    int lo = 0, hi = E - 1;  // last expert whose compact offset is <= c
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (grp_off[mid] <= c) lo = mid;
+      else hi = mid - 1;
+    }
+    int e = lo;
+    while (e > 0 && grp_n[e] == 0) --e;  // an empty expert shares its offset with the next
+    while (e < E - 1 && c >= grp_off[e] + grp_n[e]) ++e;
+    const int p = c - grp_off[e];
+    if (p < 0 || p >= grp_n[e]) {
+      raise_status(status, MOE_DEV_BOUNDS);
+      row_list[c] = -1;
+      continue;
+    }
+    int s = 0;
+    while (s + 1 < R && run_pre[(s + 1) * E + e] <= p) ++s;
+    row_list[c] = run_start[s * E + e] + (p - run_pre[s * E + e]);
+  }
+}
+
 // From counts[R][E]: rows per expert and their compact offsets, the list of token tiles, and
 // for every (source, expert) run the receive row of its first row and the number of the
 // expert's rows from earlier sources (compact rows are expert-major, then source, then
-// position). The row list itself is filled by ffn_rows_kernel.
+// position). The row list itself is filled here for up to kPlanFusedRows rows, else by
+// ffn_rows_kernel.
 __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     const int32_t* __restrict__ counts, int32_t* __restrict__ grp_n, int32_t* __restrict__ grp_off,
     int32_t* __restrict__ n_tiles, Tile* __restrict__ tiles, int32_t* __restrict__ run_start,
-    int32_t* __restrict__ run_pre, uint32_t* status, int E, int R, int cap, int bn, int max_tiles,
-    int tk) {
+    int32_t* __restrict__ run_pre, int32_t* __restrict__ row_list, uint32_t* status, int E, int R,
+    int cap, int bn, int max_tiles, int tk) {
   __shared__ int warp_sums[33];
   __shared__ int rank_base[64];
   extern __shared__ int32_t cnt_s[];   // counts staged once: [R][E] when it fits, else unused
@@ -118,52 +148,60 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
 
   // per (source, expert) run: first receive row, rows from earlier sources
   int pre = 0;
-  for (int s = 0; s < R; ++s) {
-    const int c = act ? cnt(s) : 0;
-    int dummy;
-    const int ex = block_exclusive_scan(c, &dummy, warp_sums);
-    if (act && e % Er == 0) rank_base[e / Er] = ex;
-    __syncthreads();
-    if (act) {
-      const int r = e / Er;
-      const int in_seg = ex - rank_base[r];
-      if (in_seg + c > cap) raise_status(status, MOE_DEV_BOUNDS);
-      run_start[s * E + e] = (r * R + s) * cap + in_seg;
-      run_pre[s * E + e] = pre;
-      pre += c;
+  if (32 % Er == 0) {
+    // each destination rank's experts lie in one warp: a segmented warp scan per source
+    const int seg_lane = (threadIdx.x & 31) % Er;
+    for (int s = 0; s < R; ++s) {
+      const int c = act ? cnt(s) : 0;
+      int incl = c;
+      for (int o = 1; o < Er; o <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (seg_lane >= o) incl += nb;
+      }
+      if (act) {
+        const int r = e / Er;
+        const int in_seg = incl - c;
+        if (in_seg + c > cap) raise_status(status, MOE_DEV_BOUNDS);
+        run_start[s * E + e] = (r * R + s) * cap + in_seg;
+        run_pre[s * E + e] = pre;
+        pre += c;
+      }
     }
+  } else {
+    for (int s = 0; s < R; ++s) {
+      const int c = act ? cnt(s) : 0;
+      int dummy;
+      const int ex = block_exclusive_scan(c, &dummy, warp_sums);
+      if (act && e % Er == 0) rank_base[e / Er] = ex;
+      __syncthreads();
+      if (act) {
+        const int r = e / Er;
+        const int in_seg = ex - rank_base[r];
+        if (in_seg + c > cap) raise_status(status, MOE_DEV_BOUNDS);
+        run_start[s * E + e] = (r * R + s) * cap + in_seg;
+        run_pre[s * E + e] = pre;
+        pre += c;
+      }
+      __syncthreads();
+    }
+  }
+  // few rows: fill the row list here (the tables above are this CTA's own writes)
+  if (tk <= kPlanFusedRows) {
     __syncthreads();
+    fill_rows(grp_n, grp_off, run_start, run_pre, row_list, status, E, R, tk, threadIdx.x,
+              blockDim.x);
   }
 }
 
-// row_list[c] for every compact row c: its expert by binary search on the compact offsets,
-// its source run by a scan of the run prefixes, then the run's receive row plus the position.
+// The row list (see fill_rows), filled by a grid when there are many rows.
 __global__ void __launch_bounds__(256) ffn_rows_kernel(const int32_t* __restrict__ grp_n,
                                                        const int32_t* __restrict__ grp_off,
                                                        const int32_t* __restrict__ run_start,
                                                        const int32_t* __restrict__ run_pre,
                                                        int32_t* __restrict__ row_list,
                                                        uint32_t* status, int E, int R, int tk) {
-  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < tk; c += gridDim.x * blockDim.x) {
-    int lo = 0, hi = E - 1;  // last expert whose compact offset is <= c
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (grp_off[mid] <= c) lo = mid;
-      else hi = mid - 1;
-    }
-    int e = lo;
-    while (e > 0 && grp_n[e] == 0) --e;  // an empty expert shares its offset with the next
-    while (e < E - 1 && c >= grp_off[e] + grp_n[e]) ++e;
-    const int p = c - grp_off[e];
-    if (p < 0 || p >= grp_n[e]) {
-      raise_status(status, MOE_DEV_BOUNDS);
-      row_list[c] = -1;
-      continue;
-    }
-    int s = 0;
-    while (s + 1 < R && run_pre[(s + 1) * E + e] <= p) ++s;
-    row_list[c] = run_start[s * E + e] + (p - run_pre[s * E + e]);
-  }
+  fill_rows(grp_n, grp_off, run_start, run_pre, row_list, status, E, R, tk,
+            blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -613,14 +651,17 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
   const size_t stage = (size_t)c.R * c.E * sizeof(int32_t);
   const int32_t* grp_n = reinterpret_cast<const int32_t*>(ws + L.grp_n);
   const int32_t* grp_off = reinterpret_cast<const int32_t*>(ws + L.grp_off);
-  ffn_plan_kernel<<<1, kPlanThreads, stage <= kPlanStageBytes ? stage : 0, st>>>(
+  const int tk = c.T * c.k;
+  const int plan_threads = c.E <= 32 ? 32 : (c.E + 31) / 32 * 32;   // one thread per expert
+  ffn_plan_kernel<<<1, plan_threads, stage <= kPlanStageBytes ? stage : 0, st>>>(
       counts, reinterpret_cast<int32_t*>(ws + L.grp_n), reinterpret_cast<int32_t*>(ws + L.grp_off),
       reinterpret_cast<int32_t*>(ws + L.n_tiles), reinterpret_cast<Tile*>(ws + L.tiles),
       reinterpret_cast<int32_t*>(ws + L.run_start), reinterpret_cast<int32_t*>(ws + L.run_pre),
-      status, c.E, c.R, cap_of(c), L.bn, L.max_tiles, c.T * c.k);
+      reinterpret_cast<int32_t*>(ws + L.row_list), status, c.E, c.R, cap_of(c), L.bn,
+      L.max_tiles, tk);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const int tk = c.T * c.k;
+  if (tk <= kPlanFusedRows) return cudaSuccess;   // the plan CTA filled the row list
   const int blocks = (tk + 255) / 256 < 4 * 152 ? (tk + 255) / 256 : 4 * 152;
   ffn_rows_kernel<<<blocks, 256, 0, st>>>(
       grp_n, grp_off, reinterpret_cast<const int32_t*>(ws + L.run_start),

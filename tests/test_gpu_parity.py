@@ -32,6 +32,10 @@ def moe():
 # 3 down tiles, a shared expert with more rows than one token tile, 3 logical ranks.
 SMALL = synth.MoEConfig("small", T=96, d=384, E=12, k=3, n_group=4, topk_group=2, d_ff=640,
                         d_ff_shared=640, R=3, route_scale=2.5, seed=77)
+# 64 experts per logical rank: the schedule takes its block-wide scan path (the other shapes
+# have at most 32 experts per rank, one warp).
+ER64 = synth.MoEConfig("er64", T=64, d=256, E=128, k=4, n_group=4, topk_group=2, d_ff=128,
+                       d_ff_shared=128, R=2, route_scale=1.0, seed=11)
 # One expert receives every token (bias +10): several token tiles of one expert.
 HOT = synth.MoEConfig("hot", T=256, d=256, E=16, k=2, n_group=1, topk_group=1, d_ff=256,
                       d_ff_shared=256, R=2, route_scale=1.0, seed=5)
@@ -307,7 +311,7 @@ def _layer_tokens_check(cfg, tokens, inp, W, y):
     return err
 
 
-@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, HOT], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, HOT, ER64], ids=lambda c: c.name)
 def test_layer_all_tokens(cfg):
     inp, W = inputs(cfg)
     lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
@@ -400,7 +404,7 @@ def test_layer_events_are_recorded_in_order():
     assert all(b >= a for a, b in zip(times, times[1:]))
 
 
-@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, ER64], ids=lambda c: c.name)
 def test_gate_up_intermediate_and_schedule(cfg):
     """The expert schedule (compact rows expert-major, then source rank, then position) and the
     SwiGLU intermediate h of every compact row, before the down projection."""
