@@ -19,6 +19,8 @@
 //    sum taken in selection order.
 // Every operation is an explicitly rounded intrinsic (__fmaf_rn, __fadd_rn, __fmul_rn,
 // __fdiv_rn) so the compiler cannot contract or reorder it.
+#include <atomic>
+
 #include "moe_device.cuh"
 
 namespace moe {
@@ -210,6 +212,158 @@ cudaError_t launch_partials(const __nv_bfloat16* x, const float* wg, float* part
     return launch_partials_bk<BT, BE, TM, TN, (MAXBK >= 32 ? 32 : 16)>(x, wg, partials, T, d, E, st);
   if (L % 16 == 0) return launch_partials_bk<BT, BE, TM, TN, 16>(x, wg, partials, T, d, E, st);
   return launch_partials_bk<BT, BE, TM, TN, 8>(x, wg, partials, T, d, E, st);
+}
+
+// ---------------------------------------------------------------------------------------
+// Partial logits for small batches, the CTA's whole slice resident. With few tokens the grid
+// is only E/BE x 16 CTAs, and a kernel that stages one k-step at a time keeps a few KB in
+// flight per SM: it waits on memory latency, not bandwidth. Here the CTA's BT rows of x and BE
+// rows of w_gate over its chunk (L = d/16 columns) are all copied into shared memory at once
+// with 16-byte cp.async, in G commit groups along k (rows past T or E are zero-filled), and the
+// FMA chains run over each group as soon as it has landed. Nothing is overwritten, so the
+// groups need no barrier other than the one after each wait.
+// Shared layout: x rows [BT][L + 8] bf16, w rows [BE][L + 4] fp32, row-major with 16 bytes of
+// padding, so a quarter-warp's 16-byte reads of 8 consecutive w rows hit distinct banks (the
+// row stride is an odd number of 16-byte units when L % 8 == 0).
+// Thread tile: rows ty*TM + i (TM even: one packed fp32x2 FMA covers two tokens against one
+// weight), columns tx + j*(BE/TN). Every output is the same sequential chain over its chunk as
+// in the staged kernel.
+// ---------------------------------------------------------------------------------------
+__host__ __device__ constexpr size_t resident_smem_bytes(int BT, int BE, int L) {
+  return (size_t)BT * (L + 8) * 2 + (size_t)BE * (L + 4) * 4;
+}
+
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// wait until at most n of this thread's newest commit groups are still pending (n <= 3)
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else if (n == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+  else asm volatile("cp.async.wait_group 3;" ::: "memory");
+}
+
+template <int BT, int BE, int TM, int TN>
+__global__ void __launch_bounds__(256, 1) route_partials_resident_kernel(
+    const __nv_bfloat16* __restrict__ x, const float* __restrict__ wg, float* __restrict__ partials,
+    int T, int d, int E, int G) {
+  static_assert((BT / TM) * (BE / TN) == 256, "256 threads");
+  static_assert(TM % 2 == 0, "token pairs");
+  extern __shared__ __align__(16) unsigned char rres[];
+  const int tid = threadIdx.x;
+  const int e0 = blockIdx.x * BE, t0 = blockIdx.y * BT, c = blockIdx.z;
+  const int L = d / kRouteChunks, kbeg = c * L;
+  const int SX = L + 8, SW = L + 4;   // row strides (elements)
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(rres);
+  float* ws = reinterpret_cast<float*>(rres + (size_t)BT * SX * 2);
+
+  // issue every copy of the slice: group g covers columns [g*KG, (g+1)*KG)
+  const int KG = L / G, XV = KG / 8, WV = KG / 4;   // 16-byte vectors per row and group
+  for (int g = 0; g < G; ++g) {
+    const int kg = g * KG;
+    for (int q = tid; q < BT * XV; q += 256) {
+      const int r = q / XV, v = q - r * XV;   // consecutive threads: consecutive 16 bytes of a row
+      const int t = t0 + r;
+      const __nv_bfloat16* src = x + (size_t)(t < T ? t : 0) * d + kbeg + kg + v * 8;
+      cp_async16_zfill(xs + r * SX + kg + v * 8, src, t < T ? 16 : 0);
+    }
+    for (int q = tid; q < BE * WV; q += 256) {
+      const int r = q / WV, v = q - r * WV;
+      const int e = e0 + r;
+      const float* src = wg + (size_t)(e < E ? e : 0) * d + kbeg + kg + v * 4;
+      cp_async16_zfill(ws + r * SW + kg + v * 4, src, e < E ? 16 : 0);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+
+  const int tx = tid % (BE / TN), ty = tid / (BE / TN);
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+  const __nv_bfloat16* xrow = xs + (ty * TM) * SX;
+  const float* wrow = ws + tx * SW;
+
+  for (int g = 0; g < G; ++g) {
+    cp_async_wait_pending(G - 1 - g);
+    __syncthreads();   // every thread's copies of group g are visible
+    const int kend = (g + 1) * KG;
+    for (int k = g * KG; k < kend; k += 4) {
+      float a[TM][4], b[TN][4];
+#pragma unroll
+      for (int i = 0; i < TM; ++i) {
+        const uint2 u = *reinterpret_cast<const uint2*>(xrow + i * SX + k);
+        a[i][0] = bf16_lo(u.x);
+        a[i][1] = bf16_hi(u.x);
+        a[i][2] = bf16_lo(u.y);
+        a[i][3] = bf16_hi(u.y);
+      }
+#pragma unroll
+      for (int j = 0; j < TN; ++j) {
+        const float4 w = *reinterpret_cast<const float4*>(wrow + j * (BE / TN) * SW + k);
+        b[j][0] = w.x;
+        b[j][1] = w.y;
+        b[j][2] = w.z;
+        b[j][3] = w.w;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int i = 0; i < TM; i += 2)
+#pragma unroll
+          for (int j = 0; j < TN; ++j)
+            fma2_bcast(acc[i][j], acc[i + 1][j], a[i][kk], a[i + 1][kk], b[j][kk]);
+    }
+  }
+
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int t = t0 + ty * TM + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      const int e = e0 + tx + j * (BE / TN);
+      if (e < E) partials[((size_t)c * T + t) * E + e] = acc[i][j];
+    }
+  }
+}
+
+// Whether the resident kernel takes this shape: 16-byte aligned rows and chunks, and the slice
+// within the per-CTA shared memory limit.
+template <int BT, int BE>
+bool resident_fits(const void* x, const void* wg, int d) {
+  const int L = d / kRouteChunks;
+  return L % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(wg) & 15) == 0 &&
+         resident_smem_bytes(BT, BE, L) <= 227 * 1024;
+}
+
+template <int BT, int BE, int TM, int TN>
+cudaError_t launch_partials_resident(const __nv_bfloat16* x, const float* wg, float* partials,
+                                     int T, int d, int E, cudaStream_t st) {
+  auto kern = route_partials_resident_kernel<BT, BE, TM, TN>;
+  const int L = d / kRouteChunks;
+  const size_t smem = resident_smem_bytes(BT, BE, L);
+  // The shared-memory opt-in once per device for the largest size (the call costs host time
+  // right at the start of the layer): bit `dev` of `opted` is set once it is done.
+  static std::atomic<uint64_t> opted{0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (smem > 48 * 1024 && (dev >= 64 || !(opted.load(std::memory_order_relaxed) >> dev & 1))) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) opted.fetch_or(uint64_t(1) << dev, std::memory_order_relaxed);
+  }
+  const int G = L % 32 == 0 ? 4 : L % 16 == 0 ? 2 : 1;
+  dim3 grid((E + BE - 1) / BE, (T + BT - 1) / BT, kRouteChunks);
+  kern<<<grid, 256, smem, st>>>(x, wg, partials, T, d, E, G);
+  return cudaGetLastError();
 }
 
 // e^z by Cody-Waite reduction and a degree-7 Taylor polynomial (see the file comment).
@@ -464,14 +618,23 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   // The tile grows with T: larger thread tiles read shared memory less often per FMA (the small
   // tiles are bound by it), smaller CTA tiles keep the 16 chunks x E/BE x T/BT grid several
-  // CTAs per SM deep. Measured on the DSV3 router (partials + selection, us): T = 8: 25 with
-  // 32x32; T = 64: 30 with 64x32 (32x32: 40); T = 128 / 256: 36 / 52 with 64x64 (32x32: 58 /
-  // 71); T = 512 / 1024: 75 / 114 with 128x128 (32x32: 146 / 268).
-  cudaError_t err =
-      c.T >= 512   ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st)
-      : c.T >= 128 ? launch_partials<64, 64, 4, 4, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
-      : c.T >= 32  ? launch_partials<64, 32, 4, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
-                   : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st);
+  // CTAs per SM deep. Measured on the DSV3 router (partials + selection, us, gate weights in
+  // L2): T = 8 / 64 / 104 / 128: 21 / 25 / 31 / 31 with the resident slice (staged 32x32,
+  // 64x32, 64x32, 64x64: 25 / 29 / 39 / 35); T = 256: 52 with 64x64 (32x32: 71); T = 512 /
+  // 1024: 75 / 114 with 128x128 (32x32: 146 / 268).
+  // Up to 128 tokens the whole per-CTA slice is resident (its copies all in flight at once).
+  cudaError_t err;
+  if (c.T <= 32 && resident_fits<32, 32>(xb, w_gate, c.d))
+    err = launch_partials_resident<32, 32, 2, 2>(xb, w_gate, partials, c.T, c.d, c.E, st);
+  else if (c.T <= 64 && resident_fits<64, 32>(xb, w_gate, c.d))
+    err = launch_partials_resident<64, 32, 2, 4>(xb, w_gate, partials, c.T, c.d, c.E, st);
+  else if (c.T <= 128 && resident_fits<128, 32>(xb, w_gate, c.d))
+    err = launch_partials_resident<128, 32, 4, 4>(xb, w_gate, partials, c.T, c.d, c.E, st);
+  else
+    err = c.T >= 512   ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st)
+          : c.T >= 128 ? launch_partials<64, 64, 4, 4, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
+          : c.T >= 32  ? launch_partials<64, 32, 4, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
+                       : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st);
   if (err != cudaSuccess) return err;
   if (c.T < 1024) {   // a CTA per token keeps every expert's loads in flight at once
     const size_t smem1 = (size_t)sel_scratch_floats(c.E) * sizeof(float);

@@ -85,11 +85,13 @@ def oracle_route(cfg, inp, tokens=None):
 # ------------------------------------------------------------------------------------------
 # Router
 # ------------------------------------------------------------------------------------------
-# T spans the four partial-dot tiles (32x32 below 32 tokens, 64x32 below 128, 64x64 below 512,
-# 128x128 from there) and both selection kernels (a CTA per token below 1024 tokens, a warp per
-# token from there, 2 / 4 / 8 warps per CTA at 1024 / 1536 / 4096+ tokens)
+# T spans the partial-dot kernels (the resident slice with 32 / 64 / 128-token tiles up to 128
+# tokens, ragged at 40 and 104; staged 64x64 tiles below 512, 128x128 from there) and both
+# selection kernels (a CTA per token below 1024 tokens, a warp per token from there, 2 / 4 / 8
+# warps per CTA at 1024 / 1536 / 4096+ tokens)
 ROUTE_FULL = [synth.CONFIGS["tiny"], SMALL, HOT, synth.CONFIGS["dsv3_decode"],
-              synth.CONFIGS["dsv3_sweep"].with_T(8), synth.CONFIGS["dsv3_sweep"].with_T(256),
+              synth.CONFIGS["dsv3_sweep"].with_T(8), synth.CONFIGS["dsv3_sweep"].with_T(40),
+              synth.CONFIGS["dsv3_sweep"].with_T(104), synth.CONFIGS["dsv3_sweep"].with_T(256),
               synth.CONFIGS["dsv3_sweep"].with_T(1024), synth.CONFIGS["dsv3_sweep"].with_T(1536)]
 
 
