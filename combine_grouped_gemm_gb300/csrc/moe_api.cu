@@ -19,6 +19,7 @@ int cuda_fail(cudaError_t e) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
 }  // namespace
 
 int validate(const moe_cfg& c) {
@@ -194,11 +195,12 @@ int moe_expert_ffn(const moe_cfg* cfg, const void* recv, const float* recv_scale
   }
   const WsLayout L = ws_layout(c);
   char* wsp = static_cast<char*>(ws);
+  // the GEMMs follow this call's own kernels: programmatic launches
   cudaError_t e = launch_ffn_setup(c, L, counts, x, wsp, stream);
   if (e == cudaSuccess)
-    e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream);
+    e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, true);
   if (e == cudaSuccess)
-    e = launch_ffn_gemm(c, L, 1, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream);
+    e = launch_ffn_gemm(c, L, 1, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, true);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
@@ -255,25 +257,34 @@ int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const floa
   auto rec = [&](int i) -> cudaError_t {
     return events ? cudaEventRecord(events[i], stream) : cudaSuccess;
   };
+  // Without stage events every kernel after the first follows a kernel of this call directly
+  // and is launched programmatically (its CTAs become resident while the previous kernel
+  // runs; measured on the DSV3 layer: 20 us less per step at T = 64, 39 us at T = 4096). With
+  // events, each stage starts after its event as usual, so the events time the stages
+  // themselves.
+  const bool pdl = events == nullptr;
   cudaError_t e = rec(0);
   if (e == cudaSuccess)
     e = launch_route(c, x, w_gate, bias, topk_idx, topk_w,
                      reinterpret_cast<float*>(wsp + L.partials),
-                     reinterpret_cast<uint32_t*>(wsp + L.status), stream);
+                     reinterpret_cast<uint32_t*>(wsp + L.status), stream, pdl,
+                     c.d_ff_shared ? w->ws13 : nullptr,
+                     (size_t)2 * c.d_ff_shared * c.d * act_bytes(c));
   if (e == cudaSuccess) e = rec(1);
   if (e == cudaSuccess)
-    e = launch_dispatch(c, x, topk_idx, recv, recv_scales, counts, row_of, nullptr, stream);
+    e = launch_dispatch(c, x, topk_idx, recv, recv_scales, counts, row_of, nullptr, stream, pdl);
   if (e == cudaSuccess) e = rec(2);
-  if (e == cudaSuccess) e = launch_ffn_setup(c, L, counts, x, wsp, stream);
+  if (e == cudaSuccess) e = launch_ffn_setup(c, L, counts, x, wsp, stream, pdl);
   if (e == cudaSuccess) e = rec(3);
   if (e == cudaSuccess)
-    e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream);
+    e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, pdl);
   if (e == cudaSuccess) e = rec(4);
   if (e == cudaSuccess)
-    e = launch_ffn_gemm(c, L, 1, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream);
+    e = launch_ffn_gemm(c, L, 1, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, pdl);
   if (e == cudaSuccess) e = rec(5);
   if (e == cudaSuccess)
-    e = launch_combine(c, ebuf, row_of, topk_w, c.d_ff_shared ? shared_out : nullptr, y, stream);
+    e = launch_combine(c, ebuf, row_of, topk_w, c.d_ff_shared ? shared_out : nullptr, y, stream,
+                       pdl);
   if (e == cudaSuccess) e = rec(6);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }

@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
                                                       uint4* __restrict__ y, int d, int k,
                                                       int slice_vecs) {
   __shared__ int32_t rows[32];
+  pdl_wait();
+  pdl_trigger();
   __shared__ float wts[32];
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
@@ -77,17 +79,17 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
 
 cudaError_t launch_combine(const moe_cfg& c, const void* ebuf, const int32_t* row_of,
                            const float* topk_w, const void* shared_out, void* y,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool pdl) {
   const int vpr = c.d / 8;
   int nslice = 1;
   while (c.T * nslice < 2 * 152 && vpr / (nslice * 2) >= 128) nslice *= 2;
   const int slice_vecs = (vpr + nslice - 1) / nslice;
   nslice = (vpr + slice_vecs - 1) / slice_vecs;
   dim3 grid(c.T, nslice);
-  combine_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(ebuf), row_of, topk_w,
-                                       static_cast<const uint4*>(shared_out),
-                                       static_cast<uint4*>(y), c.d, c.k, slice_vecs);
-  return cudaGetLastError();
+  return launch_kernel(combine_kernel, grid, dim3(128), 0, st, pdl,
+                       static_cast<const uint4*>(ebuf), row_of, topk_w,
+                       static_cast<const uint4*>(shared_out), static_cast<uint4*>(y), c.d, c.k,
+                       slice_vecs);
 }
 
 }  // namespace moe

@@ -35,6 +35,39 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 }
 
 // ------------------------------------------------------------------------------------------
+// Programmatic dependent launch. The layer's kernels after the first are launched with
+// programmatic stream serialisation, so a kernel's CTAs may be resident before the previous
+// kernel in the stream has finished. Every kernel therefore starts with pdl_wait(): it returns
+// once the previous grid has completed and its memory writes are visible (at once when the
+// kernel was launched without the attribute), and nothing before it touches global memory or
+// tensor memory. pdl_trigger() then lets the next kernel's CTAs launch while this one runs.
+// Waiting CTAs are not free: letting the combine CTAs wait beside the e4m3 down GEMM for its
+// whole run made the DSV3 FP8 layer about 1% slower, so the GEMM kernels trigger only once
+// their last loads are issued.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// kern<<<grid, block, smem, st>>>(args...), with programmatic stream serialisation when pdl.
+template <typename... P, typename... A>
+cudaError_t launch_kernel(void (*kern)(P...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool pdl, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+  if (err != cudaSuccess) (void)cudaGetLastError();   // the error is returned, not left sticky
+  return err;
+}
+
+// ------------------------------------------------------------------------------------------
 // mbarrier
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -126,6 +159,24 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// Starts pulling [p, p + bytes) into L2 for a later kernel: 64 KB bulk prefetches, piece
+// part, part + nparts, ... issued by thread 0 of the calling CTA, evict-first like the weight
+// streams that will read them. Nothing waits for them. p must be 16-byte aligned (the host
+// checks).
+__device__ __forceinline__ void l2_warm(const void* p, size_t bytes, int part, int nparts) {
+  if (!p || threadIdx.x != 0) return;
+  constexpr size_t kPiece = 64 * 1024;
+  const size_t n = bytes & ~static_cast<size_t>(15);
+  const uint64_t pol = l2_policy_evict_first();
+  const char* base = static_cast<const char*>(p);
+  for (size_t off = (size_t)part * kPiece; off < n; off += (size_t)nparts * kPiece) {
+    const uint32_t len = static_cast<uint32_t>(n - off < kPiece ? n - off : kPiece);
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(base + off),
+                 "r"(len), "l"(pol)
+                 : "memory");
+  }
 }
 
 // ------------------------------------------------------------------------------------------

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(kIndexWarps * 32) dispatch_index_kernel(
   int32_t* run = smi;                                              // [16][E]
   uint32_t* mask = reinterpret_cast<uint32_t*>(run + kIndexWarps * E);  // [16][E]
   int32_t* off = reinterpret_cast<int32_t*>(mask + kIndexWarps * E);    // [E]
+  pdl_wait();
+  pdl_trigger();
 
   const int s = blockIdx.x;
   const int Ts = T / R, Er = E / R;
@@ -141,6 +143,8 @@ __global__ void __launch_bounds__(128) dispatch_copy_bf16_kernel(
     int d, int k, int slice_vecs) {
   __shared__ int32_t rows[32];
   const int t = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x < k) rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
   __syncthreads();
   const int vpr = d / 8;  // 16-byte vectors per row
@@ -163,6 +167,8 @@ __global__ void __launch_bounds__(128) dispatch_copy_e4m3_kernel(
     float* __restrict__ recv_scales, long long sc_ld, int d, int k, int slice_vecs) {
   __shared__ int32_t rows[32];
   const int t = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
   // row_of == nullptr: quantise token t into row t (the shared expert's input)
   if (threadIdx.x < k) rows[threadIdx.x] = row_of ? row_of[(size_t)t * k + threadIdx.x] : t;
   __syncthreads();
@@ -223,17 +229,17 @@ void copy_grid(int T, int d, int* nslice_out, int* slice_vecs_out) {
 }  // namespace
 
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int d, void* out, float* scales,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, bool pdl) {
   int nslice, slice_vecs;
   copy_grid(T, d, &nslice, &slice_vecs);
-  dispatch_copy_e4m3_kernel<<<dim3(T, nslice), 128, 0, st>>>(
-      static_cast<const uint4*>(x), nullptr, static_cast<uint2*>(out), scales, T, d, 1, slice_vecs);
-  return cudaGetLastError();
+  return launch_kernel(dispatch_copy_e4m3_kernel, dim3(T, nslice), dim3(128), 0, st, pdl,
+                       static_cast<const uint4*>(x), static_cast<const int32_t*>(nullptr),
+                       static_cast<uint2*>(out), scales, (long long)T, d, 1, slice_vecs);
 }
 
 cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk_idx, void* recv,
                             float* recv_scales, int32_t* counts, int32_t* row_of,
-                            int32_t* src_tok, cudaStream_t st) {
+                            int32_t* src_tok, cudaStream_t st, bool pdl) {
   const int cap = cap_of(c);
   cudaError_t err;
   if (src_tok) {
@@ -244,25 +250,25 @@ cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk
   err = cudaFuncSetAttribute(dispatch_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
   if (err != cudaSuccess) return err;
-  dispatch_index_kernel<<<c.R, kIndexWarps * 32, smem, st>>>(topk_idx, counts, row_of, src_tok,
-                                                             nullptr, c.T, c.E, c.k, c.R, cap);
-  err = cudaGetLastError();
+  // (after the memset the index kernel is launched as usual: its predecessor is not a kernel)
+  err = launch_kernel(dispatch_index_kernel, dim3(c.R), dim3(kIndexWarps * 32), smem, st,
+                      pdl && !src_tok,
+                      topk_idx, counts, row_of, src_tok, static_cast<uint32_t*>(nullptr), c.T,
+                      c.E, c.k, c.R, cap);
   if (err != cudaSuccess) return err;
 
   int nslice, slice_vecs;
   copy_grid(c.T, c.d, &nslice, &slice_vecs);
   dim3 grid(c.T, nslice);
   if (c.act_dtype == MOE_FP8_E4M3) {
-    dispatch_copy_e4m3_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x), row_of,
-                                                    static_cast<uint2*>(recv), recv_scales,
-                                                    (long long)c.R * c.R * cap, c.d, c.k,
-                                                    slice_vecs);
-  } else {
-    dispatch_copy_bf16_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x), row_of,
-                                                    static_cast<uint4*>(recv), c.d, c.k,
-                                                    slice_vecs);
+    return launch_kernel(dispatch_copy_e4m3_kernel, grid, dim3(128), 0, st, pdl,
+                         static_cast<const uint4*>(x), static_cast<const int32_t*>(row_of),
+                         static_cast<uint2*>(recv), recv_scales, (long long)c.R * c.R * cap, c.d,
+                         c.k, slice_vecs);
   }
-  return cudaGetLastError();
+  return launch_kernel(dispatch_copy_bf16_kernel, grid, dim3(128), 0, st, pdl,
+                       static_cast<const uint4*>(x), static_cast<const int32_t*>(row_of),
+                       static_cast<uint4*>(recv), c.d, c.k, slice_vecs);
 }
 
 }  // namespace moe

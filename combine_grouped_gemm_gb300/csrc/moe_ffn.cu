@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
   __shared__ int warp_sums[33];
   __shared__ int rank_base[64];
   extern __shared__ int32_t cnt_s[];   // counts staged once: [R][E] when it fits, else unused
+  pdl_wait();
+  pdl_trigger();
   const int e = threadIdx.x;
   const bool act = e < E;
   const int Er = E / R;
@@ -200,6 +202,8 @@ __global__ void __launch_bounds__(256) ffn_rows_kernel(const int32_t* __restrict
                                                        const int32_t* __restrict__ run_pre,
                                                        int32_t* __restrict__ row_list,
                                                        uint32_t* status, int E, int R, int tk) {
+  pdl_wait();
+  pdl_trigger();
   fill_rows(grp_n, grp_off, run_start, run_pre, row_list, status, E, R, tk,
             blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
 }
@@ -324,6 +328,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
       tma_prefetch_map(&mapBs);
     }
   }
+  // the previous kernel's outputs (schedule, activations) and its tensor memory are free from here
+  pdl_wait();
   if (warp == 1) {
     tmem_alloc(tmem_slot, S::TMEM_COLS);
     tmem_relinquish();
@@ -415,6 +421,9 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
         }
       }
     }
+    // Every load of this CTA is issued: the next kernel may start launching. (Not earlier: its
+    // CTAs would sit on the SMs, waiting, for the whole GEMM.)
+    pdl_trigger();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
@@ -580,14 +589,14 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
 
 template <int STAGE, int BN, int STAGES>
 cudaError_t run_gemm(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mAs,
-                     const CUtensorMap& mB, const CUtensorMap& mBs, cudaStream_t st) {
+                     const CUtensorMap& mB, const CUtensorMap& mBs, cudaStream_t st, bool pdl) {
   using S = GemmShape<STAGE, BN, STAGES>;
   auto kern = ffn_gemm_bf16_kernel<STAGE, BN, STAGES>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
   if (err != cudaSuccess) return err;
-  kern<<<sm_count(), GemmThreads<STAGE>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(sm_count()), dim3(GemmThreads<STAGE>::kAll), S::SMEM, st, pdl,
+                       a, mA, mAs, mB, mBs);
 }
 
 }  // namespace
@@ -641,10 +650,10 @@ int sm_count() {
 
 
 cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
-                             const void* x, char* ws, cudaStream_t st) {
+                             const void* x, char* ws, cudaStream_t st, bool pdl) {
   if (c.act_dtype == MOE_FP8_E4M3 && c.d_ff_shared) {
-    const cudaError_t err = launch_quant_rows_e4m3(x, c.T, c.d, ws + L.xq,
-                                                   reinterpret_cast<float*>(ws + L.xq_scales), st);
+    const cudaError_t err = launch_quant_rows_e4m3(
+        x, c.T, c.d, ws + L.xq, reinterpret_cast<float*>(ws + L.xq_scales), st, pdl);
     if (err != cudaSuccess) return err;
   }
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
@@ -653,28 +662,28 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
   const int32_t* grp_off = reinterpret_cast<const int32_t*>(ws + L.grp_off);
   const int tk = c.T * c.k;
   const int plan_threads = c.E <= 32 ? 32 : (c.E + 31) / 32 * 32;   // one thread per expert
-  ffn_plan_kernel<<<1, plan_threads, stage <= kPlanStageBytes ? stage : 0, st>>>(
+  cudaError_t err = launch_kernel(
+      ffn_plan_kernel, dim3(1), dim3(plan_threads), stage <= kPlanStageBytes ? stage : 0, st, pdl,
       counts, reinterpret_cast<int32_t*>(ws + L.grp_n), reinterpret_cast<int32_t*>(ws + L.grp_off),
       reinterpret_cast<int32_t*>(ws + L.n_tiles), reinterpret_cast<Tile*>(ws + L.tiles),
       reinterpret_cast<int32_t*>(ws + L.run_start), reinterpret_cast<int32_t*>(ws + L.run_pre),
       reinterpret_cast<int32_t*>(ws + L.row_list), status, c.E, c.R, cap_of(c), L.bn,
       L.max_tiles, tk);
-  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (tk <= kPlanFusedRows) return cudaSuccess;   // the plan CTA filled the row list
   const int blocks = (tk + 255) / 256 < 4 * 152 ? (tk + 255) / 256 : 4 * 152;
-  ffn_rows_kernel<<<blocks, 256, 0, st>>>(
-      grp_n, grp_off, reinterpret_cast<const int32_t*>(ws + L.run_start),
+  return launch_kernel(
+      ffn_rows_kernel, dim3(blocks), dim3(256), 0, st, pdl, grp_n, grp_off,
+      reinterpret_cast<const int32_t*>(ws + L.run_start),
       reinterpret_cast<const int32_t*>(ws + L.run_pre), reinterpret_cast<int32_t*>(ws + L.row_list),
       status, c.E, c.R, tk);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                             const float* recv_scales, const void* x, const moe_weights& w,
-                            void* ebuf, void* shared_out, char* ws, cudaStream_t st) {
+                            void* ebuf, void* shared_out, char* ws, cudaStream_t st, bool pdl) {
   if (c.act_dtype == MOE_FP8_E4M3)
-    return launch_ffn_gemm_e4m3(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st);
+    return launch_ffn_gemm_e4m3(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st, pdl);
   const int cap = cap_of(c);
   const long long recv_rows = (long long)c.R * c.R * cap;
   const int F = c.d_ff, Fs = c.d_ff_shared, d = c.d, tk = c.T * c.k;
@@ -744,11 +753,11 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
   if (!ok) return cudaErrorInvalidValue;
 
   if (L.bn == 64) {
-    if (stage == 0) return run_gemm<0, 64, 5>(a, mA, mAs, mB, mBs, st);
-    return run_gemm<1, 64, 8>(a, mA, mAs, mB, mBs, st);
+    if (stage == 0) return run_gemm<0, 64, 5>(a, mA, mAs, mB, mBs, st, pdl);
+    return run_gemm<1, 64, 8>(a, mA, mAs, mB, mBs, st, pdl);
   }
-  if (stage == 0) return run_gemm<0, 128, 4>(a, mA, mAs, mB, mBs, st);
-  return run_gemm<1, 128, 6>(a, mA, mAs, mB, mBs, st);
+  if (stage == 0) return run_gemm<0, 128, 4>(a, mA, mAs, mB, mBs, st, pdl);
+  return run_gemm<1, 128, 6>(a, mA, mAs, mB, mBs, st, pdl);
 }
 
 }  // namespace moe

@@ -197,6 +197,8 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       tma_prefetch_map(&mapBs);
     }
   }
+  // the previous kernel's outputs (schedule, activations) and its tensor memory are free from here
+  pdl_wait();
   if (warp == 1) {
     tmem_alloc(tmem_slot, S::TMEM_COLS);
     tmem_relinquish();
@@ -254,6 +256,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
         }
       }
     }
+    // Every load of this CTA is issued: the next kernel may start launching. (Not earlier: its
+    // CTAs would sit on the SMs, waiting, for the whole GEMM.)
+    pdl_trigger();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
 
 cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                                  const float* recv_scales, const moe_weights& w, void* ebuf,
-                                 void* shared_out, char* ws, cudaStream_t st) {
+                                 void* shared_out, char* ws, cudaStream_t st, bool pdl) {
   const int cap = cap_of(c);
   const long long recv_rows = (long long)c.R * c.R * cap;
   const int F = c.d_ff, Fs = c.d_ff_shared, d = c.d, tk = c.T * c.k;
@@ -640,21 +645,23 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     auto kern = ffn_gemm_e4m3_kernel<0, 2, 4>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (err != cudaSuccess) return err;
-    kern<<<sm_count(), Fp8Threads<0>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+    return launch_kernel(kern, dim3(sm_count()), dim3(Fp8Threads<0>::kAll), S::SMEM, st, pdl, a,
+                         mA, mAs, mB, mBs);
   } else if (d % 256 == 0) {
     using S = Fp8Shape<2, 4>;
     auto kern = ffn_gemm_e4m3_kernel<1, 2, 4>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (err != cudaSuccess) return err;
-    kern<<<sm_count(), Fp8Threads<1>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+    return launch_kernel(kern, dim3(sm_count()), dim3(Fp8Threads<1>::kAll), S::SMEM, st, pdl, a,
+                         mA, mAs, mB, mBs);
   } else {
     using S = Fp8Shape<1, 6>;
     auto kern = ffn_gemm_e4m3_kernel<1, 1, 6>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (err != cudaSuccess) return err;
-    kern<<<sm_count(), Fp8Threads<1>::kAll, S::SMEM, st>>>(a, mA, mAs, mB, mBs);
+    return launch_kernel(kern, dim3(sm_count()), dim3(Fp8Threads<1>::kAll), S::SMEM, st, pdl, a,
+                         mA, mAs, mB, mBs);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -51,36 +51,45 @@ inline int cap_of(const moe_cfg& c) {
 }
 inline size_t act_bytes(const moe_cfg& c) { return c.act_dtype == MOE_FP8_E4M3 ? 1 : 2; }
 
-// Kernel launchers. Each returns the launch error (cudaSuccess when enqueued).
+// launch_route's selection kernel also starts pulling [warm, warm + warm_bytes) into L2 (the
+// shared expert's gate/up weights, which the gate/up GEMM reads first) while the rest of the
+// routing runs with the memory system mostly idle.
+// Kernel launchers. Each returns the launch error (cudaSuccess when enqueued). With pdl the
+// launcher's kernels are launched programmatically: each may become resident while the
+// previous kernel in the stream is still running, and waits for it before touching memory
+// (launch_route's first kernel, which follows the caller's own work, is always launched as
+// usual).
 cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, const float* bias,
                          int32_t* topk_idx, float* topk_w, float* partials, uint32_t* status,
-                         cudaStream_t st);
+                         cudaStream_t st, bool pdl = false, const void* warm = nullptr,
+                         size_t warm_bytes = 0);
 
 cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk_idx, void* recv,
                             float* recv_scales, int32_t* counts, int32_t* row_of,
-                            int32_t* src_tok, cudaStream_t st);
+                            int32_t* src_tok, cudaStream_t st, bool pdl = false);
 
 cudaError_t launch_combine(const moe_cfg& c, const void* ebuf, const int32_t* row_of,
                            const float* topk_w, const void* shared_out, void* y,
-                           cudaStream_t st);
+                           cudaStream_t st, bool pdl = false);
 
 // Expert FFN set-up: tile schedule from counts (+ e4m3 quantisation of the shared input).
 cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
-                             const void* x, char* ws, cudaStream_t st);
+                             const void* x, char* ws, cudaStream_t st, bool pdl = false);
 
 // The two grouped GEMMs. stage: 0 = gate/up with the SwiGLU epilogue, 1 = down projection.
 cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                             const float* recv_scales, const void* x, const moe_weights& w,
-                            void* ebuf, void* shared_out, char* ws, cudaStream_t st);
+                            void* ebuf, void* shared_out, char* ws, cudaStream_t st,
+                            bool pdl = false);
 
 // e4m3 grouped GEMMs (non-swapped, per-128-K-block scale promotion), same stages.
 cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                                  const float* recv_scales, const moe_weights& w, void* ebuf,
-                                 void* shared_out, char* ws, cudaStream_t st);
+                                 void* shared_out, char* ws, cudaStream_t st, bool pdl = false);
 
 // 1x128 e4m3 quantisation of T rows of width d (the dispatch's rule), row t -> row t.
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int d, void* out, float* scales,
-                                   cudaStream_t st);
+                                   cudaStream_t st, bool pdl = false);
 
 // 2-D row-major tensor map [rows][cols] with a box of box_rows x 128 bytes, 128-byte swizzle.
 bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t cols,

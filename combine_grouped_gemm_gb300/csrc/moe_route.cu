@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(256, TM * TN <= 64 ? 2 : 1) route_partials_ker
                                                              float* __restrict__ partials, int T,
                                                              int d, int E) {
   static_assert((BT / TM) * (BE / TN) == 256, "256 threads");
+  pdl_wait();
+  pdl_trigger();
   constexpr int XV = BT * BK / 8;            // 16-byte vectors of x per step (8 bf16)
   constexpr int WV = BE * BK / 4;            // 16-byte vectors of w per step (4 floats)
   constexpr int NX = (XV + 255) / 256, NW = (WV + 255) / 256;
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(256, TM * TN <= 64 ? 2 : 1) route_partials_ker
 // The k-step is BK columns, the largest of MAXBK, 16, 8 that divides a chunk.
 template <int BT, int BE, int TM, int TN, int BK>
 cudaError_t launch_partials_bk(const __nv_bfloat16* x, const float* wg, float* partials, int T,
-                               int d, int E, cudaStream_t st) {
+                               int d, int E, cudaStream_t st, bool pdl) {
   constexpr int smem = partials_smem_bytes<BT, BE, TM, TN, BK>();
   auto kern = route_partials_kernel<BT, BE, TM, TN, BK>;
   // (the opt-in call only where needed: it costs host time right at the start of the layer)
@@ -200,18 +202,19 @@ cudaError_t launch_partials_bk(const __nv_bfloat16* x, const float* wg, float* p
     if (err != cudaSuccess) return err;
   }
   dim3 grid((E + BE - 1) / BE, (T + BT - 1) / BT, kRouteChunks);
-  kern<<<grid, 256, smem > 48 * 1024 ? smem : 0, st>>>(x, wg, partials, T, d, E);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(256), smem > 48 * 1024 ? smem : 0, st, pdl, x, wg,
+                       partials, T, d, E);
 }
 
 template <int BT, int BE, int TM, int TN, int MAXBK>
 cudaError_t launch_partials(const __nv_bfloat16* x, const float* wg, float* partials, int T, int d,
-                            int E, cudaStream_t st) {
+                            int E, cudaStream_t st, bool pdl) {
   const int L = d / kRouteChunks;
   if (MAXBK >= 32 && L % 32 == 0)
-    return launch_partials_bk<BT, BE, TM, TN, (MAXBK >= 32 ? 32 : 16)>(x, wg, partials, T, d, E, st);
-  if (L % 16 == 0) return launch_partials_bk<BT, BE, TM, TN, 16>(x, wg, partials, T, d, E, st);
-  return launch_partials_bk<BT, BE, TM, TN, 8>(x, wg, partials, T, d, E, st);
+    return launch_partials_bk<BT, BE, TM, TN, (MAXBK >= 32 ? 32 : 16)>(x, wg, partials, T, d, E, st,
+                                                                       pdl);
+  if (L % 16 == 0) return launch_partials_bk<BT, BE, TM, TN, 16>(x, wg, partials, T, d, E, st, pdl);
+  return launch_partials_bk<BT, BE, TM, TN, 8>(x, wg, partials, T, d, E, st, pdl);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -260,6 +263,8 @@ __global__ void __launch_bounds__(256, 1) route_partials_resident_kernel(
   const int SX = L + 8, SW = L + 4;   // row strides (elements)
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(rres);
   float* ws = reinterpret_cast<float*>(rres + (size_t)BT * SX * 2);
+  pdl_wait();
+  pdl_trigger();
 
   // issue every copy of the slice: group g covers columns [g*KG, (g+1)*KG)
   const int KG = L / G, XV = KG / 8, WV = KG / 4;   // 16-byte vectors per row and group
@@ -345,7 +350,7 @@ bool resident_fits(const void* x, const void* wg, int d) {
 
 template <int BT, int BE, int TM, int TN>
 cudaError_t launch_partials_resident(const __nv_bfloat16* x, const float* wg, float* partials,
-                                     int T, int d, int E, cudaStream_t st) {
+                                     int T, int d, int E, cudaStream_t st, bool pdl) {
   auto kern = route_partials_resident_kernel<BT, BE, TM, TN>;
   const int L = d / kRouteChunks;
   const size_t smem = resident_smem_bytes(BT, BE, L);
@@ -362,8 +367,7 @@ cudaError_t launch_partials_resident(const __nv_bfloat16* x, const float* wg, fl
   }
   const int G = L % 32 == 0 ? 4 : L % 16 == 0 ? 2 : 1;
   dim3 grid((E + BE - 1) / BE, (T + BT - 1) / BT, kRouteChunks);
-  kern<<<grid, 256, smem, st>>>(x, wg, partials, T, d, E, G);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(256), smem, st, pdl, x, wg, partials, T, d, E, G);
 }
 
 // e^z by Cody-Waite reduction and a degree-7 Taylor polynomial (see the file comment).
@@ -448,19 +452,27 @@ __device__ __forceinline__ int warp_topk(const float* v, const int* keep, int E,
 //     then the weights from the raw sigmoid scores in selection order.
 // ---------------------------------------------------------------------------------------
 constexpr int kSelThreads = 256;
+constexpr int kWarmCtas = 64;   // CTAs that issue the L2 warm-up (about 1 MB each for DSV3)
 
 __global__ void __launch_bounds__(kSelThreads) route_select_cta_kernel(
     const float* __restrict__ partials, const float* __restrict__ bias,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int E, int k,
-    int n_group, int topk_group, float route_scale) {
+    int n_group, int topk_group, float route_scale, const void* warm, size_t warm_bytes,
+    int warm_ctas) {
   extern __shared__ float sm[];
   float* s = sm;                 // [E] sigmoid scores
   float* v = s + E;              // [E] selection keys
   float* gscore = v + E;         // [64]
   int* keep = reinterpret_cast<int*>(gscore + 64);   // [64]
   float* sel_s = reinterpret_cast<float*>(keep + 64); // [32]
-  const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
+  if ((int)blockIdx.x < warm_ctas) {   // the first CTAs only start the L2 warm-up
+    l2_warm(warm, warm_bytes, blockIdx.x, warm_ctas);
+    return;
+  }
+  const int t = blockIdx.x - warm_ctas;
 
   for (int e = threadIdx.x; e < E; e += kSelThreads) {
     float p[kRouteChunks];
@@ -538,10 +550,17 @@ __host__ __device__ constexpr int sel_scratch_floats(int E) { return 2 * E + 64 
 __global__ void __launch_bounds__(256) route_select_kernel(
     const float* __restrict__ partials, const float* __restrict__ bias,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int E, int k,
-    int n_group, int topk_group, float route_scale) {
+    int n_group, int topk_group, float route_scale, const void* warm, size_t warm_bytes,
+    int warm_ctas) {
   extern __shared__ float sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  pdl_wait();
+  pdl_trigger();
+  if ((int)blockIdx.x < warm_ctas) {   // the first CTAs only start the L2 warm-up
+    l2_warm(warm, warm_bytes, blockIdx.x, warm_ctas);
+    return;
+  }
+  const int t = (blockIdx.x - warm_ctas) * (blockDim.x >> 5) + warp;
   if (t >= T) return;   // whole warps only: no block-wide barrier follows
   float* s = sm + warp * sel_scratch_floats(E);        // [E] sigmoid scores
   float* v = s + E;                                    // [E] selection keys
@@ -613,9 +632,14 @@ __global__ void __launch_bounds__(256) route_select_kernel(
 
 cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, const float* bias,
                          int32_t* topk_idx, float* topk_w, float* partials, uint32_t* status,
-                         cudaStream_t st) {
+                         cudaStream_t st, bool pdl, const void* warm, size_t warm_bytes) {
   (void)status;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (reinterpret_cast<uintptr_t>(warm) & 15) warm = nullptr;   // bulk prefetches need 16 bytes
+  if (!warm) warm_bytes = 0;
+  // extra CTAs at the front of the selection grid issue the warm-up on SMs of their own, off
+  // the selection's path
+  const int warm_ctas = warm_bytes ? kWarmCtas : 0;
   // The tile grows with T: larger thread tiles read shared memory less often per FMA (the small
   // tiles are bound by it), smaller CTA tiles keep the 16 chunks x E/BE x T/BT grid several
   // CTAs per SM deep. Measured on the DSV3 router (partials + selection, us, gate weights in
@@ -625,23 +649,22 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
   // Up to 128 tokens the whole per-CTA slice is resident (its copies all in flight at once).
   cudaError_t err;
   if (c.T <= 32 && resident_fits<32, 32>(xb, w_gate, c.d))
-    err = launch_partials_resident<32, 32, 2, 2>(xb, w_gate, partials, c.T, c.d, c.E, st);
+    err = launch_partials_resident<32, 32, 2, 2>(xb, w_gate, partials, c.T, c.d, c.E, st, false);
   else if (c.T <= 64 && resident_fits<64, 32>(xb, w_gate, c.d))
-    err = launch_partials_resident<64, 32, 2, 4>(xb, w_gate, partials, c.T, c.d, c.E, st);
+    err = launch_partials_resident<64, 32, 2, 4>(xb, w_gate, partials, c.T, c.d, c.E, st, false);
   else if (c.T <= 128 && resident_fits<128, 32>(xb, w_gate, c.d))
-    err = launch_partials_resident<128, 32, 4, 4>(xb, w_gate, partials, c.T, c.d, c.E, st);
+    err = launch_partials_resident<128, 32, 4, 4>(xb, w_gate, partials, c.T, c.d, c.E, st, false);
   else
-    err = c.T >= 512   ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st)
-          : c.T >= 128 ? launch_partials<64, 64, 4, 4, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
-          : c.T >= 32  ? launch_partials<64, 32, 4, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st)
-                       : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st);
+    err = c.T >= 512   ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st, false)
+          : c.T >= 128 ? launch_partials<64, 64, 4, 4, 32>(xb, w_gate, partials, c.T, c.d, c.E, st, false)
+          : c.T >= 32  ? launch_partials<64, 32, 4, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st, false)
+                       : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st, false);
   if (err != cudaSuccess) return err;
   if (c.T < 1024) {   // a CTA per token keeps every expert's loads in flight at once
     const size_t smem1 = (size_t)sel_scratch_floats(c.E) * sizeof(float);
-    route_select_cta_kernel<<<c.T, kSelThreads, smem1, st>>>(partials, bias, topk_idx, topk_w, c.T,
-                                                             c.E, c.k, c.n_group, c.topk_group,
-                                                             c.route_scale);
-    return cudaGetLastError();
+    return launch_kernel(route_select_cta_kernel, dim3(warm_ctas + c.T), dim3(kSelThreads), smem1,
+                         st, pdl, partials, bias, topk_idx, topk_w, c.T, c.E, c.k, c.n_group,
+                         c.topk_group, c.route_scale, warm, warm_bytes, warm_ctas);
   }
   // one warp per token; CTAs of up to 8 warps, fewer when T is small so the tokens still spread
   // over the SMs
@@ -652,9 +675,9 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
                                (int)smem);
     if (err != cudaSuccess) return err;
   }
-  route_select_kernel<<<(c.T + wpc - 1) / wpc, 32 * wpc, smem, st>>>(
-      partials, bias, topk_idx, topk_w, c.T, c.E, c.k, c.n_group, c.topk_group, c.route_scale);
-  return cudaGetLastError();
+  return launch_kernel(route_select_kernel, dim3(warm_ctas + (c.T + wpc - 1) / wpc), dim3(32 * wpc),
+                       smem, st, pdl, partials, bias, topk_idx, topk_w, c.T, c.E, c.k, c.n_group,
+                       c.topk_group, c.route_scale, warm, warm_bytes, warm_ctas);
 }
 
 }  // namespace moe

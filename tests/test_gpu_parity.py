@@ -392,6 +392,32 @@ def test_layer_equals_stage_calls_and_is_deterministic():
     assert torch.equal(y1, y3)
 
 
+@pytest.mark.parametrize("cfg", [SMALL, FP8_SMALL, synth.CONFIGS["dsv3_decode"]],
+                         ids=lambda c: c.name)
+def test_back_to_back_layers_match_single_calls(cfg):
+    # Layer calls queued one after another on the stream with no synchronisation: within a call
+    # every kernel after the first is launched programmatically and has to wait for its
+    # predecessor before it reads anything. Each call gets other tokens, so a read of the
+    # previous call's routing, schedule or activations would change its output.
+    inp, W = inputs(cfg)
+    lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    g = torch.Generator(device="cuda").manual_seed(cfg.seed + 7)
+    xs = [inp["x"]] + [torch.randn(tuple(inp["x"].shape), generator=g, device="cuda")
+                       .to(inp["x"].dtype) for _ in range(3)]
+    ref = []
+    for x in xs:
+        ref.append(lay(x).clone())
+        torch.cuda.synchronize()
+    outs = [torch.empty_like(ref[0]) for _ in xs]
+    for x, y in zip(xs, outs):
+        lay(x, y)
+    torch.cuda.synchronize()
+    assert moe().read_status(lay.bufs["ws"]) == 0
+    for a, b in zip(outs, ref):
+        assert torch.equal(a, b)
+    assert not torch.equal(ref[0], ref[1])
+
+
 def test_layer_events_are_recorded_in_order():
     cfg = SMALL
     inp, W = inputs(cfg)
