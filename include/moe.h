@@ -176,7 +176,8 @@ int moe_dispatch(const moe_cfg* cfg, const void* x, const int32_t* topk_idx, voi
  * counts: the dispatch's counts [R][E] (the only metadata; rows are located from it).
  * x: bf16 [T][d], the shared expert's input (NULL when d_ff_shared == 0). For e4m3 the shared
  * input is quantised here with the dispatch's rule. Rows of ebuf that hold no token are not
- * written. ws: workspace (holds the tile schedule and the SwiGLU intermediates). */
+ * written. ws: workspace (holds the tile schedule and the SwiGLU intermediates). The two
+ * GEMMs follow this call's own schedule kernels with programmatic launches (see moe_layer). */
 int moe_expert_ffn(const moe_cfg* cfg, const void* recv, const float* recv_scales,
                    const int32_t* counts, const void* x, const moe_weights* w, void* ebuf,
                    void* shared_out, void* ws, cudaStream_t stream);
@@ -194,7 +195,13 @@ int moe_combine(const moe_cfg* cfg, const void* ebuf, const int32_t* row_of,
  * Buffers as in those calls (src_tok is not produced). events: NULL, or MOE_LAYER_EVENTS
  * created events that are recorded on `stream` before the router, after the router, after
  * the dispatch, after the FFN set-up (schedule and shared-input quantisation), after the
- * gate/up GEMM, after the down GEMM, and after the combine. */
+ * gate/up GEMM, after the down GEMM, and after the combine.
+ * With events == NULL every kernel after the first is launched with programmatic stream
+ * serialisation: it may become resident while the previous kernel runs, and waits for that
+ * kernel to finish before it touches memory. The first kernel (the router's) starts after the
+ * work already on `stream`, as any launch. With events, the stages are launched one after
+ * another so that the events time them. With a shared expert, the router's selection kernel
+ * also starts prefetching w->ws13 into L2 (reads only; the gate/up GEMM reads it first). */
 int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const float* bias,
               const moe_weights* w, int32_t* topk_idx, float* topk_w, void* recv,
               float* recv_scales, int32_t* counts, int32_t* row_of, void* ebuf,
