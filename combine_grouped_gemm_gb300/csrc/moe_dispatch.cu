@@ -247,8 +247,7 @@ cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk
     if (err != cudaSuccess) return err;
   }
   const size_t smem = sizeof(int32_t) * (size_t)(2 * kIndexWarps + 1) * c.E;
-  err = cudaFuncSetAttribute(dispatch_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+  err = ensure_smem_limit(reinterpret_cast<const void*>(dispatch_index_kernel), smem);
   if (err != cudaSuccess) return err;
   // (after the memset the index kernel is launched as usual: its predecessor is not a kernel)
   err = launch_kernel(dispatch_index_kernel, dim3(c.R), dim3(kIndexWarps * 32), smem, st,

@@ -29,6 +29,7 @@
 // accumulator buffers hand over through tmem_full/tmem_empty mbarriers, so the epilogue of a
 // unit overlaps the main loop of the next. Every wait is bounded (see moe_device.cuh).
 #include <mutex>
+#include <vector>
 
 #include "moe_device.cuh"
 
@@ -592,8 +593,7 @@ cudaError_t run_gemm(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap
                      const CUtensorMap& mB, const CUtensorMap& mBs, cudaStream_t st, bool pdl) {
   using S = GemmShape<STAGE, BN, STAGES>;
   auto kern = ffn_gemm_bf16_kernel<STAGE, BN, STAGES>;
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+  const cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), S::SMEM);
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(sm_count()), dim3(GemmThreads<STAGE>::kAll), S::SMEM, st, pdl,
                        a, mA, mAs, mB, mBs);
@@ -639,6 +639,33 @@ bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64
          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+cudaError_t ensure_smem_limit(const void* kern, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  struct Entry {
+    const void* kern;
+    int dev;
+    size_t bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> set_so_far;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry* hit = nullptr;
+  for (Entry& en : set_so_far)
+    if (en.kern == kern && en.dev == dev) hit = &en;
+  if (hit && hit->bytes >= bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes));
+  if (err != cudaSuccess) return err;
+  if (hit)
+    hit->bytes = bytes;
+  else
+    set_so_far.push_back(Entry{kern, dev, bytes});
+  return cudaSuccess;
 }
 
 int sm_count() {

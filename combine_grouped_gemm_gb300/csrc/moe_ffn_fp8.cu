@@ -643,21 +643,21 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
   if (stage == 0) {
     using S = Fp8Shape<2, 4>;
     auto kern = ffn_gemm_e4m3_kernel<0, 2, 4>;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    err = ensure_smem_limit(reinterpret_cast<const void*>(kern), S::SMEM);
     if (err != cudaSuccess) return err;
     return launch_kernel(kern, dim3(sm_count()), dim3(Fp8Threads<0>::kAll), S::SMEM, st, pdl, a,
                          mA, mAs, mB, mBs);
   } else if (d % 256 == 0) {
     using S = Fp8Shape<2, 4>;
     auto kern = ffn_gemm_e4m3_kernel<1, 2, 4>;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    err = ensure_smem_limit(reinterpret_cast<const void*>(kern), S::SMEM);
     if (err != cudaSuccess) return err;
     return launch_kernel(kern, dim3(sm_count()), dim3(Fp8Threads<1>::kAll), S::SMEM, st, pdl, a,
                          mA, mAs, mB, mBs);
   } else {
     using S = Fp8Shape<1, 6>;
     auto kern = ffn_gemm_e4m3_kernel<1, 1, 6>;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    err = ensure_smem_limit(reinterpret_cast<const void*>(kern), S::SMEM);
     if (err != cudaSuccess) return err;
     return launch_kernel(kern, dim3(sm_count()), dim3(Fp8Threads<1>::kAll), S::SMEM, st, pdl, a,
                          mA, mAs, mB, mBs);

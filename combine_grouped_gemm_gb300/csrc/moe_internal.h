@@ -98,4 +98,9 @@ bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64
 // Streaming multiprocessors of the current device.
 int sm_count();
 
+// Raises kern's dynamic shared-memory limit on the current device to at least `bytes` (no-op up
+// to 48 KB). The runtime is called only the first time a kernel needs a larger size on a
+// device, so steady-state calls enqueue launches and nothing else.
+cudaError_t ensure_smem_limit(const void* kern, size_t bytes);
+
 }  // namespace moe

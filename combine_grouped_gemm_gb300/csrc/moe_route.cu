@@ -19,8 +19,6 @@
 //    sum taken in selection order.
 // Every operation is an explicitly rounded intrinsic (__fmaf_rn, __fadd_rn, __fmul_rn,
 // __fdiv_rn) so the compiler cannot contract or reorder it.
-#include <atomic>
-
 #include "moe_device.cuh"
 
 namespace moe {
@@ -195,12 +193,8 @@ cudaError_t launch_partials_bk(const __nv_bfloat16* x, const float* wg, float* p
                                int d, int E, cudaStream_t st, bool pdl) {
   constexpr int smem = partials_smem_bytes<BT, BE, TM, TN, BK>();
   auto kern = route_partials_kernel<BT, BE, TM, TN, BK>;
-  // (the opt-in call only where needed: it costs host time right at the start of the layer)
-  if (smem > 48 * 1024) {
-    const cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-  }
+  const cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
+  if (err != cudaSuccess) return err;
   dim3 grid((E + BE - 1) / BE, (T + BT - 1) / BT, kRouteChunks);
   return launch_kernel(kern, grid, dim3(256), smem > 48 * 1024 ? smem : 0, st, pdl, x, wg,
                        partials, T, d, E);
@@ -354,17 +348,8 @@ cudaError_t launch_partials_resident(const __nv_bfloat16* x, const float* wg, fl
   auto kern = route_partials_resident_kernel<BT, BE, TM, TN>;
   const int L = d / kRouteChunks;
   const size_t smem = resident_smem_bytes(BT, BE, L);
-  // The shared-memory opt-in once per device for the largest size (the call costs host time
-  // right at the start of the layer): bit `dev` of `opted` is set once it is done.
-  static std::atomic<uint64_t> opted{0};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  const cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  if (smem > 48 * 1024 && (dev >= 64 || !(opted.load(std::memory_order_relaxed) >> dev & 1))) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (err != cudaSuccess) return err;
-    if (dev < 64) opted.fetch_or(uint64_t(1) << dev, std::memory_order_relaxed);
-  }
   const int G = L % 32 == 0 ? 4 : L % 16 == 0 ? 2 : 1;
   dim3 grid((E + BE - 1) / BE, (T + BT - 1) / BT, kRouteChunks);
   return launch_kernel(kern, grid, dim3(256), smem, st, pdl, x, wg, partials, T, d, E, G);
@@ -670,11 +655,8 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
   // over the SMs
   const int wpc = c.T >= 2432 ? 8 : c.T >= 1216 ? 4 : 2;
   const size_t smem = (size_t)wpc * sel_scratch_floats(c.E) * sizeof(float);
-  if (smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-    if (err != cudaSuccess) return err;
-  }
+  err = ensure_smem_limit(reinterpret_cast<const void*>(route_select_kernel), smem);
+  if (err != cudaSuccess) return err;
   return launch_kernel(route_select_kernel, dim3(warm_ctas + (c.T + wpc - 1) / wpc), dim3(32 * wpc),
                        smem, st, pdl, partials, bias, topk_idx, topk_w, c.T, c.E, c.k, c.n_group,
                        c.topk_group, c.route_scale, warm, warm_bytes, warm_ctas);
