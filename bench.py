@@ -119,7 +119,7 @@ def peaks():
 
 KERNEL_NAMES = {"ffn_gate_up": "ffn_gemm_{}_kernel<0> (gate/up + SwiGLU)",
                 "ffn_down": "ffn_gemm_{}_kernel<1> (down)",
-                "route": "route_partials_kernel + route_select_kernel",
+                "route": "route_partials[_resident]_kernel + route_select[_cta]_kernel",
                 "dispatch": "dispatch_index_kernel + dispatch_copy_kernel",
                 "combine": "combine_kernel", "ffn_setup": "ffn_plan_kernel + ffn_rows_kernel"}
 

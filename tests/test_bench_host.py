@@ -1,0 +1,85 @@
+"""bench.py's host-side arithmetic on CPU: kernels counted per step, the binding roof of each
+stage with its achieved/peak/fraction fields, and the DRAM-traffic lookup that goes stale with
+its kernel source."""
+import hashlib
+import json
+
+import numpy as np
+import pytest
+
+import bench
+import synth
+
+C = synth.CONFIGS
+PEAKS = {"hbm": 6781.1, "bf16": 1907.9, "bf16_sustained": 1700.0, "source": "measured"}
+
+
+def test_kernels_per_step_follows_the_launch_structure():
+    # route 2, dispatch 2, plan (+ row-list kernel beyond 1024 rows), gate/up, down, combine
+    assert bench.kernels_per_step(C["tiny"]) == 8
+    assert bench.kernels_per_step(C["dsv3_decode"]) == 8                 # 512 rows
+    assert bench.kernels_per_step(C["dsv3_sweep"].with_T(128)) == 8      # 1024 rows
+    assert bench.kernels_per_step(C["dsv3_sweep"].with_T(256)) == 9      # 2048 rows
+    assert bench.kernels_per_step(C["dsv3_skew_prefill"]) == 9
+    # + the e4m3 quantisation of the shared expert's input
+    assert bench.kernels_per_step(C["dsv3_fp8_prefill"]) == 10
+
+
+def _counts(cfg, touched):
+    c = np.zeros((cfg.R, cfg.E), dtype=np.int64)
+    c[0, :touched] = 1
+    return c
+
+
+def test_touched_experts_scale_the_weight_bytes():
+    cfg = C["dsv3_decode"]
+    b1, _, t1 = bench.algorithmic(cfg, _counts(cfg, 100))
+    b2, _, t2 = bench.algorithmic(cfg, _counts(cfg, 101))
+    assert (t1, t2) == (100, 101)
+    # one more touched expert streams one more expert's gate/up and down weights
+    assert b2["ffn_gate_up"] - b1["ffn_gate_up"] == 2 * cfg.d_ff * cfg.d * 2
+    assert b2["ffn_down"] - b1["ffn_down"] == cfg.d * cfg.d_ff * 2
+    # e4m3 weights: half the bytes plus one fp32 scale per 128x128 block
+    f8 = C["dsv3_fp8_prefill"]
+    b8a, _, _ = bench.algorithmic(f8, _counts(f8, 100))
+    b8b, _, _ = bench.algorithmic(f8, _counts(f8, 101))
+    assert b8b["ffn_gate_up"] - b8a["ffn_gate_up"] == (2 * f8.d_ff * f8.d
+                                                       + (2 * f8.d_ff // 128) * (f8.d // 128) * 4)
+
+
+def test_binding_roof_per_stage():
+    dec = C["dsv3_decode"]
+    b, f, _ = bench.algorithmic(dec, _counts(dec, 135))
+    r = bench.roofline(dec, "ffn_gate_up", 1.15, b, f, PEAKS)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == PEAKS["hbm"]
+    assert r["achieved"] == pytest.approx(b["ffn_gate_up"] / 1.15e-3 / 1e9, rel=1e-4)
+    assert r["frac"] == pytest.approx(r["achieved"] / PEAKS["hbm"], rel=1e-3)
+    # the router: reading W_g binds at T=8, its fp32 FMAs from T of a few dozen on
+    small = C["dsv3_sweep"].with_T(8)
+    bs, fs, _ = bench.algorithmic(small, _counts(small, 50))
+    assert bench.roofline(small, "route", 0.02, bs, fs, PEAKS)["bound"] == "hbm"
+    ra = bench.roofline(dec, "route", 0.03, b, f, PEAKS)
+    assert ra["bound"] == "alu" and ra["peak"] == pytest.approx(80.5, abs=0.1)
+    assert ra["achieved"] == pytest.approx(f["route"] / 0.03e-3 / 1e12, abs=0.05)   # 0.1 rounding
+    # FP8 prefill GEMMs: the tensor roof, e4m3 = 2 x the measured bf16 burst
+    f8 = C["dsv3_fp8_prefill"]
+    b8, f8l, _ = bench.algorithmic(f8, _counts(f8, 256))
+    rt = bench.roofline(f8, "ffn_gate_up", 5.0, b8, f8l, PEAKS)
+    assert rt["bound"] == "tensor" and rt["peak"] == pytest.approx(2 * PEAKS["bf16"])
+    assert rt["frac"] == pytest.approx(f8l["ffn_gate_up"] / 5e-3 / 1e12 / (2 * PEAKS["bf16"]),
+                                       rel=1e-3)
+
+
+def test_traffic_lookup_goes_stale_with_its_kernel_source(tmp_path, monkeypatch):
+    src = tmp_path / "kernel.cu"
+    src.write_text("first version\n")
+    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"ffn_gate_up@w": {"source": "kernel.cu", "source_sha256_16": h,
+                           "dram_bytes_per_launch": 123}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_traffic("ffn_gate_up", "w") == 123
+    assert bench.measured_traffic("ffn_down", "w") is None
+    src.write_text("second version\n")
+    assert bench.measured_traffic("ffn_gate_up", "w") is None
