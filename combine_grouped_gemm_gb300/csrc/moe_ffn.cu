@@ -29,7 +29,6 @@
 // accumulator buffers hand over through tmem_full/tmem_empty mbarriers, so the epilogue of a
 // unit overlaps the main loop of the next. Every wait is bounded (see moe_device.cuh).
 #include <mutex>
-#include <vector>
 
 #include "moe_device.cuh"
 
@@ -646,25 +645,29 @@ cudaError_t ensure_smem_limit(const void* kern, size_t bytes) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
+  // a fixed table, so that no call allocates host memory either (when it is full the runtime
+  // is simply called every time)
   struct Entry {
     const void* kern;
     int dev;
     size_t bytes;
   };
+  constexpr int kEntries = 256;
   static std::mutex mu;
-  static std::vector<Entry> set_so_far;
+  static Entry set_so_far[kEntries];
+  static int used = 0;
   std::lock_guard<std::mutex> lock(mu);
   Entry* hit = nullptr;
-  for (Entry& en : set_so_far)
-    if (en.kern == kern && en.dev == dev) hit = &en;
+  for (int i = 0; i < used; ++i)
+    if (set_so_far[i].kern == kern && set_so_far[i].dev == dev) hit = &set_so_far[i];
   if (hit && hit->bytes >= bytes) return cudaSuccess;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes));
   if (err != cudaSuccess) return err;
   if (hit)
     hit->bytes = bytes;
-  else
-    set_so_far.push_back(Entry{kern, dev, bytes});
+  else if (used < kEntries)
+    set_so_far[used++] = Entry{kern, dev, bytes};
   return cudaSuccess;
 }
 
