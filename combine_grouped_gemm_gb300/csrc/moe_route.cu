@@ -49,10 +49,9 @@ constexpr int partials_smem_bytes() { return 2 * BK * (BT + BE) * 4; }
 
 // Thread tiles of up to 64 outputs run two CTAs per SM (at most 128 registers a thread).
 template <int BT, int BE, int TM, int TN, int BK>
-__global__ void __launch_bounds__(256, TM * TN <= 64 ? 2 : 1) route_partials_kernel(const __nv_bfloat16* __restrict__ x,
-                                                             const float* __restrict__ wg,
-                                                             float* __restrict__ partials, int T,
-                                                             int d, int E) {
+__global__ void __launch_bounds__(256, TM * TN <= 64 ? 2 : 1)
+    route_partials_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wg,
+                          float* __restrict__ partials, int T, int d, int E) {
   static_assert((BT / TM) * (BE / TN) == 256, "256 threads");
   pdl_wait();
   pdl_trigger();
@@ -164,7 +163,8 @@ __global__ void __launch_bounds__(256, TM * TN <= 64 ? 2 : 1) route_partials_ker
         if constexpr (TN % 2 == 0) {
           // packed fp32x2 FMAs: two independent IEEE fmas, the same chain per output
 #pragma unroll
-          for (int j = 0; j < TN; j += 2) fma2_bcast(acc[i][j], acc[i][j + 1], b[j], b[j + 1], a[i]);
+          for (int j = 0; j < TN; j += 2)
+            fma2_bcast(acc[i][j], acc[i][j + 1], b[j], b[j + 1], a[i]);
         } else {
 #pragma unroll
           for (int j = 0; j < TN; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
@@ -520,8 +520,8 @@ __global__ void __launch_bounds__(kSelThreads) route_select_cta_kernel(
 }
 
 // ---------------------------------------------------------------------------------------
-// Selection for large batches: one warp per token, several tokens per CTA; each warp has its own shared-memory
-// scratch. The operations and their order are those of the file comment:
+// Selection for large batches: one warp per token, several tokens per CTA; each warp has its own
+// shared-memory scratch. The operations and their order are those of the file comment:
 //  1. lane l, experts e = l, l+32, ...: the 16 chunk partials (coalesced across lanes), pairwise
 //     tree, sigmoid, selection key v = s + bias;
 //  2. per group: the two largest keys by a warp-wide top-2 merge (values only: equal keys give
@@ -632,18 +632,23 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
   // 64x32, 64x32, 64x64: 25 / 29 / 39 / 35); T = 256: 52 with 64x64 (32x32: 71); T = 512 /
   // 1024: 75 / 114 with 128x128 (32x32: 146 / 268).
   // Up to 128 tokens the whole per-CTA slice is resident (its copies all in flight at once).
+  // The partial-dot kernel follows the caller's own work, so it is launched as usual.
+  const int T = c.T, d = c.d, E = c.E;
   cudaError_t err;
-  if (c.T <= 32 && resident_fits<32, 32>(xb, w_gate, c.d))
-    err = launch_partials_resident<32, 32, 2, 2>(xb, w_gate, partials, c.T, c.d, c.E, st, false);
-  else if (c.T <= 64 && resident_fits<64, 32>(xb, w_gate, c.d))
-    err = launch_partials_resident<64, 32, 2, 4>(xb, w_gate, partials, c.T, c.d, c.E, st, false);
-  else if (c.T <= 128 && resident_fits<128, 32>(xb, w_gate, c.d))
-    err = launch_partials_resident<128, 32, 4, 4>(xb, w_gate, partials, c.T, c.d, c.E, st, false);
+  if (T <= 32 && resident_fits<32, 32>(xb, w_gate, d))
+    err = launch_partials_resident<32, 32, 2, 2>(xb, w_gate, partials, T, d, E, st, false);
+  else if (T <= 64 && resident_fits<64, 32>(xb, w_gate, d))
+    err = launch_partials_resident<64, 32, 2, 4>(xb, w_gate, partials, T, d, E, st, false);
+  else if (T <= 128 && resident_fits<128, 32>(xb, w_gate, d))
+    err = launch_partials_resident<128, 32, 4, 4>(xb, w_gate, partials, T, d, E, st, false);
+  else if (T >= 512)
+    err = launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, T, d, E, st, false);
+  else if (T >= 128)
+    err = launch_partials<64, 64, 4, 4, 32>(xb, w_gate, partials, T, d, E, st, false);
+  else if (T >= 32)
+    err = launch_partials<64, 32, 4, 2, 32>(xb, w_gate, partials, T, d, E, st, false);
   else
-    err = c.T >= 512   ? launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, c.T, c.d, c.E, st, false)
-          : c.T >= 128 ? launch_partials<64, 64, 4, 4, 32>(xb, w_gate, partials, c.T, c.d, c.E, st, false)
-          : c.T >= 32  ? launch_partials<64, 32, 4, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st, false)
-                       : launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, c.T, c.d, c.E, st, false);
+    err = launch_partials<32, 32, 2, 2, 32>(xb, w_gate, partials, T, d, E, st, false);
   if (err != cudaSuccess) return err;
   if (c.T < 1024) {   // a CTA per token keeps every expert's loads in flight at once
     const size_t smem1 = (size_t)sel_scratch_floats(c.E) * sizeof(float);
@@ -657,9 +662,9 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
   const size_t smem = (size_t)wpc * sel_scratch_floats(c.E) * sizeof(float);
   err = ensure_smem_limit(reinterpret_cast<const void*>(route_select_kernel), smem);
   if (err != cudaSuccess) return err;
-  return launch_kernel(route_select_kernel, dim3(warm_ctas + (c.T + wpc - 1) / wpc), dim3(32 * wpc),
-                       smem, st, pdl, partials, bias, topk_idx, topk_w, c.T, c.E, c.k, c.n_group,
-                       c.topk_group, c.route_scale, warm, warm_bytes, warm_ctas);
+  return launch_kernel(route_select_kernel, dim3(warm_ctas + (c.T + wpc - 1) / wpc),
+                       dim3(32 * wpc), smem, st, pdl, partials, bias, topk_idx, topk_w, c.T, c.E,
+                       c.k, c.n_group, c.topk_group, c.route_scale, warm, warm_bytes, warm_ctas);
 }
 
 }  // namespace moe
