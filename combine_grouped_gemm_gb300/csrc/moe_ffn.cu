@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     grp_off[e] = off;
     for (int j = 0; j < nt; ++j) {
       const int ti = toff + j;
-      if (ti < max_tiles) tiles[ti] = Tile{e, j * bn, min(bn, n - j * bn), 0};
+      if (ti < max_tiles) tiles[ti] = Tile{e, j * bn, min(bn, n - j * bn), nt};
     }
   }
   if (threadIdx.x == 0) {
@@ -242,8 +242,15 @@ struct Unit {
   int n0, nlen, m;
 };
 
-template <int BN>
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
+// Unit u -> (group, token tile, weight tile). Shared-expert units come first, token-tile-major.
+// A routed expert with nt token tiles owns units [mt*b, mt*(b+nt)), b = its first tile. The
+// gate/up stage takes them token-tile-major (unit mt*b + j*mt + m), so a token tile's rows are
+// reused by consecutive units. The down stage takes them weight-tile-major (unit
+// mt*b + m*nt + j): the nt units that read weight tile m run on adjacent CTAs at about the same
+// time, and on the skew workload this cut the down GEMM's DRAM reads from 10.56 to 8.50 GB
+// (the gate/up stage's traffic did not move with it). n_tiles: entries in the tile list.
+template <int BN, bool kWeightMajor>
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u, int n_tiles) {
   Unit r;
   const int us = a.n_shared_tiles * a.mt_shared;
   if (u < us) {
@@ -254,9 +261,20 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
     r.nlen = min(BN, a.T - r.n0);
   } else {
     const int v = u - us;
-    const int tt = v / a.mt_routed;
-    r.m = v - tt * a.mt_routed;
-    const Tile t = a.tiles[tt];
+    const int tt0 = v / a.mt_routed;   // a tile of the unit's expert (the ranges coincide)
+    const Tile t0 = a.tiles[tt0];
+    Tile t = t0;
+    if (!kWeightMajor) {
+      r.m = v - tt0 * a.mt_routed;
+    } else {
+      const int base = tt0 - t0.n0 / BN;
+      // (a list cut short at its bound, already reported, keeps every index inside it)
+      const int nt = max(1, min(t0.ntiles, n_tiles - base));
+      const int local = v - base * a.mt_routed;
+      r.m = local / nt;
+      const int j = local - r.m * nt;
+      if (base + j != tt0) t = a.tiles[base + j];
+    }
     r.g = t.group;
     r.n0 = t.n0;
     r.nlen = t.nlen;
@@ -339,7 +357,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int units = a.n_shared_tiles * a.mt_shared + (*a.n_tiles) * a.mt_routed;
+  const int n_tiles = *a.n_tiles;
+  const int units = a.n_shared_tiles * a.mt_shared + n_tiles * a.mt_routed;
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -349,7 +368,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit t = decode_unit<BN>(a, u);
+      const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
       const bool sh = t.g < 0;
       const CUtensorMap* amap = sh ? &mapAs : &mapA;
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
@@ -432,7 +451,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
       bool ok = true;
       int it = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
-        const Unit t = decode_unit<BN>(a, u);
+        const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
         const uint32_t n_pad = static_cast<uint32_t>(max(16, (t.nlen + 15) & ~15));
         const uint32_t idesc = idesc_bf16(128, n_pad);
         const int b = it & 1;
@@ -483,7 +502,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit t = decode_unit<BN>(a, u);
+      const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
       const bool gather = STAGE == 0 && t.g >= 0 && t.nlen > kSmallTile;
       const uint8_t* src[kRowsPer];
 #pragma unroll
@@ -527,7 +546,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     const int rrow = quarter * 32 + lane;
     int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
-      const Unit t = decode_unit<BN>(a, u);
+      const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
       const bool sh = t.g < 0;
       const int b = it & 1;
       if (!mbar_wait(&tfull[b], (it >> 1) & 1, abort_flag, a.status)) break;

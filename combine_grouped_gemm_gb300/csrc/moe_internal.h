@@ -13,12 +13,13 @@ namespace moe {
 // Router: d is cut into this many equal chunks, each summed as one sequential FMA chain.
 constexpr int kRouteChunks = 16;
 
-// One entry of the expert-GEMM tile schedule: rows [n0, n0+nlen) of group g.
+// One entry of the expert-GEMM tile schedule: rows [n0, n0+nlen) of group g, which has ntiles
+// token tiles in all (its entries are consecutive, n0 = j * bn for the j-th).
 struct Tile {
   int32_t group;
   int32_t n0;
   int32_t nlen;
-  int32_t pad;
+  int32_t ntiles;
 };
 
 // Byte offsets of the pieces of the workspace (all 256-byte aligned).
