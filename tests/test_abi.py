@@ -100,3 +100,22 @@ def test_null_and_misaligned_pointers_are_rejected_before_any_launch(moe):
     assert L.moe_selftest_wait(ok + 4, 10 ** 6, None) == 1
     assert L.moe_selftest_wait(ok, 999, None) == 1
     assert L.moe_selftest_wait(ok, 10 ** 10 + 1, None) == 1
+
+
+def test_noalloc_router_checks_before_any_launch(moe):
+    # every refusal of moe_route_noalloc comes before it touches the device
+    L = moe._lib
+    ok = 1 << 20
+    c = moe.make_cfg(synth.CONFIGS["tiny"])
+    assert L.moe_route_noalloc(None, ok, ok, ok, ok, ok, None) == 1
+    assert L.moe_route_noalloc(ctypes.byref(c), None, ok, ok, ok, ok, None) == 1
+    assert L.moe_route_noalloc(ctypes.byref(c), ok, ok, ok, ok + 4, ok, None) == 3
+    bad = moe.make_cfg(synth.CONFIGS["tiny"])
+    bad.T = 15                                              # T % R != 0
+    assert L.moe_route_noalloc(ctypes.byref(bad), ok, ok, ok, ok, ok, None) == 1
+    # 16 partials per token and expert: 512 tokens at 256 experts fill the fixed 8 MiB scratch,
+    # 520 do not fit
+    fits = moe.make_cfg(synth.CONFIGS["dsv3_sweep"].with_T(512))
+    big = moe.make_cfg(synth.CONFIGS["dsv3_sweep"].with_T(520))
+    assert 16 * fits.T * fits.E == 2 ** 21
+    assert L.moe_route_noalloc(ctypes.byref(big), ok, ok, ok, ok, ok, None) == 2
