@@ -450,6 +450,39 @@ def test_layer_captured_in_a_cuda_graph_replays_like_eager_calls(cfg):
     assert moe().read_status(lay.bufs["ws"]) == 0
 
 
+GUARD = 4096   # canary bytes on each side of a guarded buffer (keeps the 16-byte alignment)
+
+
+def _guarded(shape, dtype, store):
+    """A tensor of the given shape and dtype inside a byte buffer whose first and last GUARD
+    bytes hold the canary 0xA5; (buffer, payload bytes) is appended to store for the check."""
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    raw = torch.full((GUARD + n + GUARD,), 0xA5, dtype=torch.uint8, device="cuda")
+    store.append((raw, n))
+    return raw[GUARD:GUARD + n].view(dtype).view(shape)
+
+
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, FP8_SMALL], ids=lambda c: c.name)
+def test_layer_writes_stay_inside_every_buffer(cfg):
+    # Every buffer the layer writes (outputs, receive buffers, metadata, workspace) lies between
+    # two guard bands of a canary byte; two layer calls later the bands are untouched.
+    inp, W = inputs(cfg)
+    m = moe()
+    store, bufs = [], {}
+    for key, t in m.Buffers(cfg).items():
+        bufs[key] = None if t is None else _guarded(tuple(t.shape), t.dtype, store)
+    bufs["ws"].zero_()
+    y = _guarded((cfg.T, cfg.d), torch.bfloat16, store)
+    for _ in range(2):
+        m.layer(cfg, inp["x"], inp["w_gate"], inp["bias"], weight_dict(W), bufs, y)
+    torch.cuda.synchronize()
+    assert m.read_status(bufs["ws"]) == 0
+    for raw, n in store:
+        assert bool((raw[:GUARD] == 0xA5).all()) and bool((raw[GUARD + n:] == 0xA5).all())
+    y_ref = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))(inp["x"])
+    assert torch.equal(y, y_ref)
+
+
 def test_layer_events_are_recorded_in_order():
     cfg = SMALL
     inp, W = inputs(cfg)
