@@ -6,6 +6,15 @@
 
 #include "moe_internal.h"
 
+// NVTX ranges around the layer's stages, so a profiler's timeline (or `ncu --nvtx`) can tell
+// them apart. NVTX is header-only: without a profiler attached a range costs a pointer check.
+#if __has_include(<nvtx3/nvToolsExt.h>)
+#include <nvtx3/nvToolsExt.h>
+#define MOE_NVTX 1
+#else
+#define MOE_NVTX 0
+#endif
+
 namespace moe {
 
 namespace {
@@ -19,6 +28,24 @@ int cuda_fail(cudaError_t e) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// one NVTX range for the lifetime of the object (no-op without the NVTX header)
+struct StageRange {
+  explicit StageRange(const char* name) {
+#if MOE_NVTX
+    nvtxRangePushA(name);
+#else
+    (void)name;
+#endif
+  }
+  ~StageRange() {
+#if MOE_NVTX
+    nvtxRangePop();
+#endif
+  }
+  StageRange(const StageRange&) = delete;
+  StageRange& operator=(const StageRange&) = delete;
+};
 
 }  // namespace
 
@@ -263,28 +290,42 @@ int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const floa
   // events, each stage starts after its event as usual, so the events time the stages
   // themselves.
   const bool pdl = events == nullptr;
+  const StageRange layer_range("moe_layer");
   cudaError_t e = rec(0);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    const StageRange r("route");
     e = launch_route(c, x, w_gate, bias, topk_idx, topk_w,
                      reinterpret_cast<float*>(wsp + L.partials),
                      reinterpret_cast<uint32_t*>(wsp + L.status), stream, pdl,
                      c.d_ff_shared ? w->ws13 : nullptr,
                      (size_t)2 * c.d_ff_shared * c.d * act_bytes(c));
+  }
   if (e == cudaSuccess) e = rec(1);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    const StageRange r("dispatch");
     e = launch_dispatch(c, x, topk_idx, recv, recv_scales, counts, row_of, nullptr, stream, pdl);
+  }
   if (e == cudaSuccess) e = rec(2);
-  if (e == cudaSuccess) e = launch_ffn_setup(c, L, counts, x, wsp, stream, pdl);
+  if (e == cudaSuccess) {
+    const StageRange r("ffn_setup");
+    e = launch_ffn_setup(c, L, counts, x, wsp, stream, pdl);
+  }
   if (e == cudaSuccess) e = rec(3);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    const StageRange r("ffn_gate_up");
     e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, pdl);
+  }
   if (e == cudaSuccess) e = rec(4);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    const StageRange r("ffn_down");
     e = launch_ffn_gemm(c, L, 1, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, pdl);
+  }
   if (e == cudaSuccess) e = rec(5);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    const StageRange r("combine");
     e = launch_combine(c, ebuf, row_of, topk_w, c.d_ff_shared ? shared_out : nullptr, y, stream,
                        pdl);
+  }
   if (e == cudaSuccess) e = rec(6);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
