@@ -44,6 +44,7 @@ def kernels_per_step(cfg):
     sched = 1 if cfg.T * cfg.k <= 1024 else 2
     return 7 + sched + (1 if cfg.act == "fp8" and cfg.d_ff_shared else 0)
 L2_BYTES = 129 * 2 ** 20
+CPU_SAMPLE_SECONDS = 12.0   # target CPU time of the oracle sample behind cpu_baseline
 
 
 def parse():
@@ -404,15 +405,20 @@ def main():
                     "ms_per_step": round(r["ms_e2e"], 5)},
         }
         if world == 1 and not args.no_cpu_baseline:
-            n = args.cpu_sample or min(cfg.T, 8)
+            # a bounded sample: a 4-token probe sizes it to about CPU_SAMPLE_SECONDS of work
             rng = np.random.default_rng(0)
+            n0 = min(cfg.T, 4)
+            sec0 = oracle_sample(cfg, r["inp"], r["W"],
+                                 np.sort(rng.choice(cfg.T, n0, replace=False)))
+            n = args.cpu_sample or int(min(cfg.T, max(n0, round(CPU_SAMPLE_SECONDS * n0 / max(sec0, 1e-6)))))
             tokens = np.sort(rng.choice(cfg.T, n, replace=False))
             sec = oracle_sample(cfg, r["inp"], r["W"], tokens)
             out["cpu_baseline"] = {"value": round(n / sec, 4), "unit": "tokens/s", "cores": 1,
                                    "kind": "oracle",
                                    "sample": f"{n} of {cfg.T} tokens of {cfg.name}: route + "
                                              f"k experts + shared + combine per token, "
-                                             f"{sec:.1f} s single-threaded"}
+                                             f"{sec:.1f} s single-threaded (sized from a "
+                                             f"{n0}-token probe)"}
         else:
             out["cpu_baseline"] = None
         print(json.dumps(out), flush=True)
