@@ -410,7 +410,8 @@ def main():
             n0 = min(cfg.T, 4)
             sec0 = oracle_sample(cfg, r["inp"], r["W"],
                                  np.sort(rng.choice(cfg.T, n0, replace=False)))
-            n = args.cpu_sample or int(min(cfg.T, max(n0, round(CPU_SAMPLE_SECONDS * n0 / max(sec0, 1e-6)))))
+            per_token = max(sec0, 1e-6) / n0
+            n = args.cpu_sample or int(min(cfg.T, max(n0, round(CPU_SAMPLE_SECONDS / per_token))))
             tokens = np.sort(rng.choice(cfg.T, n, replace=False))
             sec = oracle_sample(cfg, r["inp"], r["W"], tokens)
             out["cpu_baseline"] = {"value": round(n / sec, 4), "unit": "tokens/s", "cores": 1,
