@@ -83,3 +83,29 @@ def test_traffic_lookup_goes_stale_with_its_kernel_source(tmp_path, monkeypatch)
     assert bench.measured_traffic("ffn_down", "w") is None
     src.write_text("second version\n")
     assert bench.measured_traffic("ffn_gate_up", "w") is None
+
+
+@pytest.mark.parametrize("rank", [0, 1])
+def test_reference_arm_under_two_ranks(rank):
+    # bench.py --impl reference as torchrun would start it with two ranks: rank 0 times the
+    # oracle and prints one JSON line, the other rank exits 0 without work
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="2", RANK=str(rank), LOCAL_RANK=str(rank),
+               MASTER_ADDR="127.0.0.1", MASTER_PORT="29533")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--workload", "tiny", "--steps", "2", "--warmup", "1"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    if rank:
+        assert lines == []
+        return
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["value"] > 0 and out["unit"] == "tokens/s"
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["value"] == out["value"]
+    assert out["e2e"] == {"value": out["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
