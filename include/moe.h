@@ -160,7 +160,10 @@ int moe_route_noalloc(const moe_cfg* cfg, const void* x, const float* w_gate, co
  * Inputs x bf16 [T][d], topk_idx int32 [T][k] (entries in [0, E), distinct per token).
  * Outputs recv (see moe_sizes), recv_scales (e4m3 only, else NULL), counts int32 [R][E],
  * row_of int32 [T][k] (receive row of each choice), src_tok int32 [recv_rows] (token of each
- * row, -1 for empty rows; NULL to skip). Receive rows that get no token are not written. */
+ * row, -1 for empty rows; NULL to skip). Receive rows that get no token are not written.
+ * Entries of topk_idx outside [0, E) are skipped (their row_of is -1). Repeated experts within
+ * a token are not checked: they can overflow a segment and write past recv. moe_route never
+ * produces either. */
 int moe_dispatch(const moe_cfg* cfg, const void* x, const int32_t* topk_idx, void* recv,
                  float* recv_scales, int32_t* counts, int32_t* row_of, int32_t* src_tok,
                  cudaStream_t stream);
@@ -187,7 +190,9 @@ int moe_expert_ffn(const moe_cfg* cfg, const void* recv, const float* recv_scale
  * combine). y[t] = bf16( sum_i topk_w[t][i] * ebuf[row_of[t][i]] + shared_out[t] ), summed in
  * fp32 in selection order. ebuf bf16 [recv_rows][d]; row_of int32 [T][k]; topk_w fp32
  * [T][k]; shared_out bf16 [T][d] or NULL; y bf16 [T][d]. Passing the receive buffer as ebuf
- * (bf16) gives route_scale * x: the identity-expert check of the dispatch/combine pair. */
+ * (bf16) gives route_scale * x: the identity-expert check of the dispatch/combine pair.
+ * Negative entries of row_of are skipped. Entries at or past recv_rows are not checked: they
+ * read past ebuf. moe_dispatch's row_of holds only valid rows and -1. */
 int moe_combine(const moe_cfg* cfg, const void* ebuf, const int32_t* row_of,
                 const float* topk_w, const void* shared_out, void* y, cudaStream_t stream);
 
