@@ -405,24 +405,7 @@ def main():
                     "ms_per_step": round(r["ms_e2e"], 5)},
         }
         if world == 1 and not args.no_cpu_baseline:
-            # a bounded sample: a 4-token probe sizes it to about CPU_SAMPLE_SECONDS of work
-            rng = np.random.default_rng(0)
-            n0 = min(cfg.T, 4)
-            sec0 = oracle_sample(cfg, r["inp"], r["W"],
-                                 np.sort(rng.choice(cfg.T, n0, replace=False)))
-            per_token = max(sec0, 1e-6) / n0
-            n = args.cpu_sample or int(min(cfg.T, max(n0, round(CPU_SAMPLE_SECONDS / per_token))))
-            tokens = np.sort(rng.choice(cfg.T, n, replace=False))
-            # in batches of 8 tokens, each copying only its own experts' weights to the host
-            # (outside the clock), so host memory stays at one batch's experts
-            sec = sum(oracle_sample(cfg, r["inp"], r["W"], tokens[i:i + 8])
-                      for i in range(0, n, 8))
-            out["cpu_baseline"] = {"value": round(n / sec, 4), "unit": "tokens/s", "cores": 1,
-                                   "kind": "oracle",
-                                   "sample": f"{n} of {cfg.T} tokens of {cfg.name}: route + "
-                                             f"k experts + shared + combine per token, "
-                                             f"{sec:.1f} s single-threaded (sized from a "
-                                             f"{n0}-token probe)"}
+            out["cpu_baseline"] = cpu_baseline(cfg, r["inp"], r["W"], args.cpu_sample)
         else:
             out["cpu_baseline"] = None
         print(json.dumps(out), flush=True)
@@ -430,6 +413,24 @@ def main():
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     return 0
+
+
+def cpu_baseline(cfg, inp, W, n_tokens=0, seconds=CPU_SAMPLE_SECONDS):
+    """The oracle on a bounded sample of the workload's tokens, single-threaded: a 4-token probe
+    sizes the sample to about `seconds` of CPU work (n_tokens > 0 fixes it instead). The sample
+    runs in batches of 8 tokens, each copying only its own experts' weights to the host outside
+    the clock, so host memory holds one batch's experts at a time."""
+    rng = np.random.default_rng(0)
+    n0 = min(cfg.T, 4)
+    sec0 = oracle_sample(cfg, inp, W, np.sort(rng.choice(cfg.T, n0, replace=False)))
+    per_token = max(sec0, 1e-6) / n0
+    n = n_tokens or int(min(cfg.T, max(n0, round(seconds / per_token))))
+    tokens = np.sort(rng.choice(cfg.T, n, replace=False))
+    sec = sum(oracle_sample(cfg, inp, W, tokens[i:i + 8]) for i in range(0, n, 8))
+    return {"value": round(n / sec, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {cfg.T} tokens of {cfg.name}: route + k experts + shared + "
+                      f"combine per token, {sec:.1f} s single-threaded (sized from a "
+                      f"{n0}-token probe)"}
 
 
 def run_reference(args, cfg, rank, world, local_rank):

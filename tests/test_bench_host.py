@@ -109,3 +109,16 @@ def test_reference_arm_under_two_ranks(rank):
     assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["value"] == out["value"]
     assert out["e2e"] == {"value": out["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_sizes_its_sample_from_the_probe():
+    cfg = C["tiny"]
+    inp = synth.make_router_inputs(cfg, "cpu")
+    W = synth.make_expert_weights(cfg, "cpu")
+    # a tiny layer: a second of oracle work covers every token
+    out = bench.cpu_baseline(cfg, inp, W, seconds=1.0)
+    assert out["kind"] == "oracle" and out["cores"] == 1 and out["value"] > 0
+    assert out["sample"].startswith(f"{cfg.T} of {cfg.T} tokens")
+    # a fixed size is taken as given, in batches of 8
+    out = bench.cpu_baseline(cfg, inp, W, n_tokens=11)
+    assert out["sample"].startswith(f"11 of {cfg.T} tokens")
