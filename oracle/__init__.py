@@ -54,9 +54,11 @@ _SIGS = {
     "oracle_dispatch_index": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "oracle_dispatch_payload": (None, [_I, _I, _I, _P, _P, _P, _P]),
     "oracle_quant_row_e4m3": (None, [_P, _I, _P, _P]),
-    "oracle_swiglu_row_bf16": (None, [_I, _I, _P, _P, _P, _P, _P]),
-    "oracle_swiglu_row_fp8": (None, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "oracle_combine": (None, [_I, _I, _I, _P, _P, _P, _P, _P]),
+    "oracle_swiglu_row_bf16": (None, [_I, _I, _P, _P, _P, _P, _P, _P]),
+    "oracle_swiglu_row_fp8": (None, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "oracle_combine": (None, [_I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "oracle_place_experts": (_I, [_I, _I, _I, _P, _I, _P, _P, _P]),
+    "oracle_dispatch_index_placed": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
     "oracle_logit": (_F, [_P, _P, _I]),
     "oracle_exp_array": (None, [_L, _P, _P]),
     "oracle_sigmoid_array": (None, [_L, _P, _P]),
@@ -225,10 +227,52 @@ def dispatch_payload(x_bits, row_of, n_rows, fp8=False):
 
 
 # ------------------------------------------------------------------------------------------
+# Redundant experts (reading R-k)
+# ------------------------------------------------------------------------------------------
+def place_experts(load, R, S, max_copies=8):
+    """Placement of E experts with R*S - E extra copies over R ranks of S slots, from estimated
+    loads [E]. Returns (slot_expert [R*S], n_copies [E], copy_slot [E][max_copies])."""
+    ld = _c(load, np.float64)
+    E = ld.size
+    se = np.empty(R * S, dtype=np.int32)
+    nc = np.empty(E, dtype=np.int32)
+    cs = np.empty((E, max_copies), dtype=np.int32)
+    if lib().oracle_place_experts(E, R, S, _ptr(ld), max_copies, _ptr(se), _ptr(nc), _ptr(cs)):
+        raise ValueError("oracle_place_experts: too few slots or too many copies")
+    return se, nc, cs
+
+
+def dispatch_index_placed(topk_idx, E, R, S, n_copies, copy_slot):
+    """The dispatch index over the slots of a placement: counts [R][R*S], row_of [T][k],
+    src_tok [R*R*cap] with cap = (T/R) * min(k, S)."""
+    ti = _c(topk_idx, np.int32)
+    nc = _c(n_copies, np.int32)
+    cs = _c(copy_slot, np.int32)
+    T, k = ti.shape
+    cap = (T // R) * min(k, S)
+    counts = np.empty((R, R * S), dtype=np.int32)
+    row_of = np.empty((T, k), dtype=np.int32)
+    src_tok = np.empty(R * R * cap, dtype=np.int32)
+    if lib().oracle_dispatch_index_placed(T, E, k, R, S, _ptr(ti), _ptr(nc), _ptr(cs),
+                                          cs.shape[1], _ptr(counts), _ptr(row_of),
+                                          _ptr(src_tok)):
+        raise ValueError("oracle_dispatch_index_placed: bad shape")
+    return counts, row_of, src_tok
+
+
+def rank_loads(counts, R):
+    """Rows each rank receives: counts [sources][slots] summed per destination rank (slots in
+    contiguous blocks of slots/R per rank)."""
+    c = np.asarray(counts, dtype=np.int64).sum(axis=0)
+    return c.reshape(R, -1).sum(axis=1)
+
+
+# ------------------------------------------------------------------------------------------
 # Experts and combine
 # ------------------------------------------------------------------------------------------
-def swiglu_row_bf16(x_row_bits, w13_bits, w2_bits):
-    """One bf16 row through one SwiGLU expert -> (out bf16 bits [d], h floats [F])."""
+def swiglu_row_bf16(x_row_bits, w13_bits, w2_bits, exact=False):
+    """One bf16 row through one SwiGLU expert -> (out bf16 bits [d], h floats [F]); with exact,
+    also the fp64 output before its rounding to bf16 [d]."""
     x = _c(x_row_bits, np.uint16)
     w13 = _c(w13_bits, np.uint16)
     w2 = _c(w2_bits, np.uint16)
@@ -236,12 +280,14 @@ def swiglu_row_bf16(x_row_bits, w13_bits, w2_bits):
     F = w13.shape[0] // 2
     out = np.empty(d, dtype=np.uint16)
     h = np.empty(F, dtype=np.float32)
-    lib().oracle_swiglu_row_bf16(d, F, _ptr(x), _ptr(w13), _ptr(w2), _ptr(out), _ptr(h))
-    return out, h
+    ox = np.empty(d, dtype=np.float64) if exact else None
+    lib().oracle_swiglu_row_bf16(d, F, _ptr(x), _ptr(w13), _ptr(w2), _ptr(out), _ptr(h), _ptr(ox))
+    return (out, h, ox) if exact else (out, h)
 
 
-def swiglu_row_fp8(xq, xs, w13q, w13s, w2q, w2s):
-    """One e4m3 row (codes + 1x128 scales) through one e4m3 expert -> (out bf16 [d], h [F])."""
+def swiglu_row_fp8(xq, xs, w13q, w13s, w2q, w2s, exact=False):
+    """One e4m3 row (codes + 1x128 scales) through one e4m3 expert -> (out bf16 [d], h [F]);
+    with exact, also the fp64 output before its rounding to bf16 [d]."""
     xq = _c(xq, np.uint8)
     xs = _c(xs, np.float32)
     w13q = _c(w13q, np.uint8)
@@ -252,12 +298,14 @@ def swiglu_row_fp8(xq, xs, w13q, w13s, w2q, w2s):
     F = w13q.shape[0] // 2
     out = np.empty(d, dtype=np.uint16)
     h = np.empty(F, dtype=np.float32)
+    ox = np.empty(d, dtype=np.float64) if exact else None
     lib().oracle_swiglu_row_fp8(d, F, _ptr(xq), _ptr(xs), _ptr(w13q), _ptr(w13s), _ptr(w2q),
-                                _ptr(w2s), _ptr(out), _ptr(h))
-    return out, h
+                                _ptr(w2s), _ptr(out), _ptr(h), _ptr(ox))
+    return (out, h, ox) if exact else (out, h)
 
 
-def combine(ebuf_bits, row_of, topk_w, shared_bits=None):
+def combine(ebuf_bits, row_of, topk_w, shared_bits=None, exact=False):
+    """y bf16 bits [T][d]; with exact, also the fp64 sums before their rounding [T][d]."""
     eb = _c(ebuf_bits, np.uint16)
     ro = _c(row_of, np.int32)
     w = _c(topk_w, np.float32)
@@ -265,8 +313,9 @@ def combine(ebuf_bits, row_of, topk_w, shared_bits=None):
     T, k = ro.shape
     d = eb.shape[1]
     y = np.empty((T, d), dtype=np.uint16)
-    lib().oracle_combine(T, d, k, _ptr(eb), _ptr(ro), _ptr(w), _ptr(sh), _ptr(y))
-    return y
+    yx = np.empty((T, d), dtype=np.float64) if exact else None
+    lib().oracle_combine(T, d, k, _ptr(eb), _ptr(ro), _ptr(w), _ptr(sh), _ptr(y), _ptr(yx))
+    return (y, yx) if exact else y
 
 
 # ------------------------------------------------------------------------------------------
@@ -293,8 +342,8 @@ def layer_tokens(cfg, x_bits, w_gate, bias, expert_weights, shared_weights, toke
     y[t] depends only on x[t] and the weights, so any subset of tokens can be computed alone.
     expert_weights: callable e -> dict(w13, w2, w13_s, w2_s) of host arrays (bf16 as uint16,
     e4m3 as uint8). shared_weights: dict(ws13, ws2, ws13_s, ws2_s) or None.
-    Returns dict with topk_idx, topk_w, y (bf16 bits [n][d]), expert_out (bf16 bits
-    [n][k][d]) and shared_out (bf16 bits [n][d] or None)."""
+    Returns dict with topk_idx, topk_w, y (bf16 bits [n][d]), y_exact (the fp64 sums y is rounded
+    from), expert_out (bf16 bits [n][k][d]) and shared_out (bf16 bits [n][d] or None)."""
     tokens = np.asarray(tokens, dtype=np.int64)
     xs = _c(x_bits[tokens], np.uint16)
     idx, w = route(xs, w_gate, bias, cfg.k, cfg.n_group, cfg.topk_group, cfg.route_scale)
@@ -325,5 +374,5 @@ def layer_tokens(cfg, x_bits, w_gate, bias, expert_weights, shared_weights, toke
             else:
                 sh[j], _ = swiglu_row_bf16(xs[j], S["ws13"], S["ws2"])
     rows = np.arange(n * cfg.k, dtype=np.int32).reshape(n, cfg.k)
-    y = combine(eo.reshape(n * cfg.k, d), rows, w, sh)
-    return dict(topk_idx=idx, topk_w=w, y=y, expert_out=eo, shared_out=sh)
+    y, y_exact = combine(eo.reshape(n * cfg.k, d), rows, w, sh, exact=True)
+    return dict(topk_idx=idx, topk_w=w, y=y, y_exact=y_exact, expert_out=eo, shared_out=sh)

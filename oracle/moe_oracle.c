@@ -44,6 +44,16 @@
  *       round-to-nearest-even and saturation of value/scale; weights e4m3 with one fp32 scale
  *       per 128x128 block.
  *  R-j  Combine: y = bf16(sum_i w_i * o_i + sh) with the sum taken in fp64 here.
+ *  R-k  Redundant experts ([SMoE] "Hot-Expert Skew", redundant experts; exercise 5,
+ *       imbalance_factor_replicated): a deployment has S expert slots on each of the R ranks
+ *       (R*S >= E). The R*S - E spare slots hold extra copies, given one at a time to the expert
+ *       with the largest estimated load per copy (ties: lower expert). Every copy carries an
+ *       equal share of its expert's load, and copies are placed largest first onto the least
+ *       loaded rank that still has a free slot (ties: lower expert, lower copy, lower rank);
+ *       a rank's slots are ordered by (expert, copy). Each source rank splits its own tokens of
+ *       an expert evenly over the copies: its j-th token of expert e (counted in token order)
+ *       goes to copy (j + s) mod copies(e), copies numbered in slot order. The receive layout
+ *       is R-g with slots in place of experts and cap = (T/R) * min(k, S).
  */
 #include <math.h>
 #include <stdint.h>
@@ -321,9 +331,10 @@ void oracle_dispatch_payload(int T, int d, int k, const uint16_t* x, const int32
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /* One input row through one bf16 SwiGLU expert. w13 [2F][d] (rows 0..F-1 gate, F..2F-1 up),
- * w2 [d][F]. out: bf16 [d]. h_out (nullable): the bf16-rounded intermediate, as floats [F]. */
+ * w2 [d][F]. out: bf16 [d]. h_out (nullable): the bf16-rounded intermediate, as floats [F].
+ * out_exact (nullable): the down projection's fp64 sums before their rounding to bf16 [d]. */
 void oracle_swiglu_row_bf16(int d, int F, const uint16_t* x, const uint16_t* w13,
-                            const uint16_t* w2, uint16_t* out, float* h_out) {
+                            const uint16_t* w2, uint16_t* out, float* h_out, double* out_exact) {
     double* xv = (double*)malloc(sizeof(double) * d);
     double* h = (double*)malloc(sizeof(double) * F);
     for (int c = 0; c < d; ++c) xv[c] = oracle_bf16_to_f32(x[c]);
@@ -343,16 +354,18 @@ void oracle_swiglu_row_bf16(int d, int F, const uint16_t* x, const uint16_t* w13
         const uint16_t* wd = w2 + (size_t)c * F;
         for (int f = 0; f < F; ++f) o += h[f] * oracle_bf16_to_f32(wd[f]);
         out[c] = oracle_f32_to_bf16((float)o);
+        if (out_exact) out_exact[c] = o;
     }
     free(xv); free(h);
 }
 
 /* One row through one e4m3 SwiGLU expert. xq [d] codes with xs [d/128] scales; w13q [2F][d]
  * with w13s [2F/128][d/128]; w2q [d][F] with w2s [d/128][F/128]. h is re-quantised 1x128 before
- * the down projection (reading R-i). out: bf16 [d]. h_out (nullable): dequantised h [F]. */
+ * the down projection (reading R-i). out: bf16 [d]. h_out (nullable): dequantised h [F].
+ * out_exact (nullable): the down projection's fp64 sums before their rounding to bf16 [d]. */
 void oracle_swiglu_row_fp8(int d, int F, const uint8_t* xq, const float* xs,
                            const uint8_t* w13q, const float* w13s, const uint8_t* w2q,
-                           const float* w2s, uint16_t* out, float* h_out) {
+                           const float* w2s, uint16_t* out, float* h_out, double* out_exact) {
     int db = d / 128, fb = F / 128;
     double* xv = (double*)malloc(sizeof(double) * d);
     float* hf = (float*)calloc((size_t)F, sizeof(float));
@@ -380,6 +393,7 @@ void oracle_swiglu_row_fp8(int d, int F, const uint8_t* xq, const float* xs,
         for (int f = 0; f < F; ++f)
             o += (double)hf[f] * ((double)oracle_e4m3_to_f32(w2q[(size_t)c * F + f]) * w2s[(c / 128) * fb + f / 128]);
         out[c] = oracle_f32_to_bf16((float)o);
+        if (out_exact) out_exact[c] = o;
     }
     free(xv); free(hf); free(hq); free(hs);
 }
@@ -390,9 +404,10 @@ void oracle_swiglu_row_fp8(int d, int F, const uint8_t* xq, const float* xs,
  * ------------------------------------------------------------------------------------------ */
 
 /* y[t] = bf16( sum_i topk_w[t][i] * ebuf[row_of[t][i]] + shared[t] ), sum in fp64.
- * ebuf bf16 [*][d] indexed by receive row; shared bf16 [T][d] or NULL. */
+ * ebuf bf16 [*][d] indexed by receive row; shared bf16 [T][d] or NULL. y_exact (nullable): the
+ * fp64 sums before their rounding to bf16 [T][d]. */
 void oracle_combine(int T, int d, int k, const uint16_t* ebuf, const int32_t* row_of,
-                    const float* topk_w, const uint16_t* shared, uint16_t* y) {
+                    const float* topk_w, const uint16_t* shared, uint16_t* y, double* y_exact) {
     for (int t = 0; t < T; ++t)
         for (int c = 0; c < d; ++c) {
             double acc = 0.0;
@@ -402,7 +417,125 @@ void oracle_combine(int T, int d, int k, const uint16_t* ebuf, const int32_t* ro
             }
             if (shared) acc += oracle_bf16_to_f32(shared[(size_t)t * d + c]);
             y[(size_t)t * d + c] = oracle_f32_to_bf16((float)acc);
+            if (y_exact) y_exact[(size_t)t * d + c] = acc;
         }
+}
+
+/* ------------------------------------------------------------------------------------------
+ * Redundant experts and their placement  [SMoE "Hot-Expert Skew": replicate the busiest
+ * experts on under-loaded GPUs and let the dispatch split their tokens over the replicas;
+ * exercise 5: each copy takes an equal share of its expert's load and copies are assigned,
+ * largest first, to the least-loaded rank (LPT). Reading R-k.]
+ * ------------------------------------------------------------------------------------------ */
+
+/* load [E] (estimated rows per expert), R ranks of S slots. Outputs: slot_expert [R*S] (expert
+ * held by each slot), n_copies [E], copy_slot [E][max_copies] (slot of each copy, ascending;
+ * unused entries -1). Returns 0, or -1 when R*S < E or some expert would need more than
+ * max_copies copies. */
+int oracle_place_experts(int E, int R, int S, const double* load, int max_copies,
+                         int32_t* slot_expert, int32_t* n_copies, int32_t* copy_slot) {
+    int P = R * S;
+    if (P < E || max_copies < 1) return -1;
+    for (int e = 0; e < E; ++e) n_copies[e] = 1;
+    /* the spare slots: one more copy at a time to the largest load per copy */
+    for (int extra = 0; extra < P - E; ++extra) {
+        int best = 0;
+        for (int e = 1; e < E; ++e)
+            if (load[e] / n_copies[e] > load[best] / n_copies[best]) best = e;
+        n_copies[best] += 1;
+        if (n_copies[best] > max_copies) return -1;
+    }
+    /* the copies, largest share first (ties: lower expert, lower copy) */
+    int* ce = (int*)malloc(sizeof(int) * P);
+    int* cc = (int*)malloc(sizeof(int) * P);
+    double* cl = (double*)malloc(sizeof(double) * P);
+    int n = 0;
+    for (int e = 0; e < E; ++e)
+        for (int c = 0; c < n_copies[e]; ++c) {
+            ce[n] = e; cc[n] = c; cl[n] = load[e] / n_copies[e]; ++n;
+        }
+    for (int a = 1; a < n; ++a) {               /* insertion sort: plain and stable */
+        int e = ce[a], c = cc[a];
+        double l = cl[a];
+        int b = a - 1;
+        while (b >= 0 && cl[b] < l) { ce[b + 1] = ce[b]; cc[b + 1] = cc[b]; cl[b + 1] = cl[b]; --b; }
+        ce[b + 1] = e; cc[b + 1] = c; cl[b + 1] = l;
+    }
+    /* LPT onto ranks with a free slot */
+    double* rank_load = (double*)calloc((size_t)R, sizeof(double));
+    int* rank_used = (int*)calloc((size_t)R, sizeof(int));
+    int* copy_rank = (int*)malloc(sizeof(int) * P);   /* rank of copy index (e, c), by list pos */
+    for (int a = 0; a < n; ++a) {
+        int r_best = -1;
+        for (int r = 0; r < R; ++r)
+            if (rank_used[r] < S && (r_best < 0 || rank_load[r] < rank_load[r_best])) r_best = r;
+        copy_rank[a] = r_best;
+        rank_load[r_best] += cl[a];
+        rank_used[r_best] += 1;
+    }
+    /* slots of each rank in (expert, copy) order */
+    for (int i = 0; i < E * max_copies; ++i) copy_slot[i] = -1;
+    for (int r = 0; r < R; ++r) {
+        int j = 0;
+        for (int e = 0; e < E; ++e)
+            for (int c = 0; c < n_copies[e]; ++c)
+                for (int a = 0; a < n; ++a)
+                    if (ce[a] == e && cc[a] == c && copy_rank[a] == r) {
+                        slot_expert[r * S + j] = e;
+                        ++j;
+                    }
+    }
+    /* copies of each expert numbered in slot order */
+    for (int e = 0; e < E; ++e) {
+        int c = 0;
+        for (int p = 0; p < P; ++p)
+            if (slot_expert[p] == e) copy_slot[e * max_copies + c++] = p;
+    }
+    free(ce); free(cc); free(cl); free(rank_load); free(rank_used); free(copy_rank);
+    return 0;
+}
+
+/* The dispatch index of R-g over the slots of a placement (R-k): counts [R][P] (rows source s
+ * sends to slot p), row_of [T][k], src_tok [R*R*cap] (nullable), cap = (T/R) * min(k, S),
+ * P = R*S. Returns 0, or -1 on a bad shape. */
+int oracle_dispatch_index_placed(int T, int E, int k, int R, int S, const int32_t* topk_idx,
+                                 const int32_t* n_copies, const int32_t* copy_slot,
+                                 int max_copies, int32_t* counts, int32_t* row_of,
+                                 int32_t* src_tok) {
+    if (T % R || R * S < E) return -1;
+    int Ts = T / R, P = R * S;
+    int cap = Ts * (k < S ? k : S);
+    int32_t* seen = (int32_t*)calloc((size_t)R * E, sizeof(int32_t));   /* j per (s, e) */
+    int32_t* slot_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
+    memset(counts, 0, sizeof(int32_t) * (size_t)R * P);
+    for (int t = 0; t < T; ++t) {               /* tokens in ascending order */
+        int s = t / Ts;
+        for (int i = 0; i < k; ++i) {
+            int e = topk_idx[(size_t)t * k + i];
+            int j = seen[s * E + e]++;
+            int c = (j + s) % n_copies[e];
+            int p = copy_slot[e * max_copies + c];
+            slot_of[(size_t)t * k + i] = p;
+            counts[(size_t)s * P + p] += 1;
+        }
+    }
+    if (src_tok)
+        for (long r = 0; r < (long)R * R * cap; ++r) src_tok[r] = -1;
+    int32_t* run = (int32_t*)calloc((size_t)R * P, sizeof(int32_t));
+    for (int t = 0; t < T; ++t) {
+        int s = t / Ts;
+        for (int i = 0; i < k; ++i) {
+            int p = slot_of[(size_t)t * k + i];
+            int r = p / S;
+            int off = 0;                        /* rows of earlier slots of rank r from s */
+            for (int q = r * S; q < p; ++q) off += counts[(size_t)s * P + q];
+            int row = (r * R + s) * cap + off + run[(size_t)s * P + p]++;
+            row_of[(size_t)t * k + i] = row;
+            if (src_tok) src_tok[row] = t;
+        }
+    }
+    free(seen); free(slot_of); free(run);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------------------------

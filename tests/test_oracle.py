@@ -300,6 +300,23 @@ def test_swiglu_bf16_is_a_dense_mlp_when_one_expert():
     assert mism <= 3
 
 
+def test_swiglu_bf16_exact_output_is_the_unrounded_down_projection():
+    """The fp64 output before rounding: the fp64 torch down projection of the same bf16 h (the
+    sums agree to fp64 rounding order), and its rounding (fp64 -> fp32 -> bf16) is the bf16
+    output bit for bit."""
+    d, F = 256, 128
+    x = synth.normal_bf16(8, synth.TAG_X, (4, d), 1.0)
+    w13 = synth.normal_bf16(8, synth.TAG_W13, (2 * F, d), 0.05)
+    w2 = synth.normal_bf16(8, synth.TAG_W2, (d, F), 0.05)
+    for t in range(4):
+        out, h, ox = oracle.swiglu_row_bf16(synth.bf16_bits(x[t]), synth.bf16_bits(w13),
+                                            synth.bf16_bits(w2), exact=True)
+        ref = (torch.from_numpy(h.astype(np.float64)) @ w2.double().T).numpy()
+        assert np.allclose(ox, ref, rtol=1e-12, atol=1e-12)
+        rounded = torch.from_numpy(ox).float().to(torch.bfloat16).view(torch.int16).numpy()
+        assert np.array_equal(rounded.view(np.uint16), out)
+
+
 def test_swiglu_bf16_gate_and_up_are_not_swapped():
     d, F = 128, 128
     x = np.full(d, 0x3f80, dtype=np.uint16)            # ones
@@ -339,10 +356,16 @@ def test_swiglu_fp8_matches_torch_dequantised_mlp():
         sc = blk.abs().amax(1) / 448.0
         hq = (blk / sc[:, None]).to(torch.float8_e4m3fn).double() * sc[:, None].double()
         ref = (w2 @ hq.reshape(-1)).float()
-        out, h = oracle.swiglu_row_fp8(xq[t], xs[t], W["w13"].numpy(), W["w13_s"].numpy(),
-                                       W["w2"].numpy(), W["w2_s"].numpy())
+        out, h, ox = oracle.swiglu_row_fp8(xq[t], xs[t], W["w13"].numpy(), W["w13_s"].numpy(),
+                                           W["w2"].numpy(), W["w2_s"].numpy(), exact=True)
         o = oracle.bf16_to_f32(out)
         assert np.abs(o - ref.numpy()).max() <= 2 ** -7 * np.abs(ref.numpy()).max() + 1e-6
+        # the unrounded output: the fp64 down projection of the oracle's own dequantised h,
+        # which rounds to the bf16 output
+        assert np.allclose(ox, (w2 @ torch.from_numpy(h.astype(np.float64))).numpy(),
+                           rtol=1e-12, atol=1e-12)
+        rounded = torch.from_numpy(ox).float().to(torch.bfloat16).view(torch.int16).numpy()
+        assert np.array_equal(rounded.view(np.uint16), out)
 
 
 def test_combine_identity_experts_return_scaled_x():
@@ -372,6 +395,12 @@ def test_combine_matches_numpy_weighted_sum():
     ref += oracle.bf16_to_f32(sh)
     refb = torch.from_numpy(ref).float().to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.abs(y.astype(np.int32) - refb.astype(np.int32)).max() <= 1
+    # the unrounded sums: numpy's fp64 weighted sum (to fp64 rounding order), rounding to y
+    y2, yx = oracle.combine(eb, ro, w, sh, exact=True)
+    assert np.array_equal(y2, y)
+    assert np.allclose(yx, ref, rtol=1e-13, atol=1e-13)
+    rounded = torch.from_numpy(yx).float().to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(rounded.view(np.uint16), y)
 
 
 # ------------------------------------------------------------------------------------------
@@ -441,3 +470,158 @@ def test_layer_tokens_composes_route_experts_combine():
         ref += float(w[t, i]) * oracle.bf16_to_f32(o)
     yb = torch.from_numpy(ref).float().to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.abs(out["y"][2].astype(np.int32) - yb.astype(np.int32)).max() <= 1
+
+
+# ------------------------------------------------------------------------------------------
+# Redundant experts and their placement (reading R-k)
+# ------------------------------------------------------------------------------------------
+def _placement_ok(slot_expert, n_copies, copy_slot, E, R, S):
+    assert slot_expert.shape == (R * S,)
+    assert (n_copies >= 1).all() and n_copies.sum() == R * S
+    assert np.array_equal(np.bincount(slot_expert, minlength=E), n_copies)
+    for e in range(E):
+        slots = copy_slot[e, :n_copies[e]]
+        assert (copy_slot[e, n_copies[e]:] == -1).all()
+        assert np.all(np.diff(slots) > 0) and (slot_expert[slots] == e).all()
+    for r in range(R):                      # a rank's slots in (expert, copy) order
+        assert np.all(np.diff(slot_expert[r * S:(r + 1) * S]) >= 0)
+
+
+def test_placement_of_equal_loads_without_spares_is_round_robin():
+    """Equal loads and no spare slot: LPT deals the experts out in index order, expert e to rank
+    e mod R, so rank r holds r, r+R, r+2R, ..."""
+    E, R = 24, 4
+    se, nc, cs = oracle.place_experts(np.ones(E), R, E // R)
+    _placement_ok(se, nc, cs, E, R, E // R)
+    assert np.array_equal(se.reshape(R, -1), np.arange(E).reshape(-1, R).T)
+
+
+def test_placement_spare_copies_go_to_the_heaviest_shares():
+    # one heavy expert among equals takes every spare slot while its share stays the largest
+    E, R, S = 8, 6, 2
+    load = np.ones(E)
+    load[5] = 40.0
+    se, nc, cs = oracle.place_experts(load, R, S)
+    _placement_ok(se, nc, cs, E, R, S)
+    assert nc[5] == 1 + (R * S - E) and (np.delete(nc, 5) == 1).all()
+    # its copies land on distinct ranks (each is larger than any other expert's load)
+    assert len({int(p) // S for p in cs[5, :nc[5]]}) == nc[5]
+
+
+def _brute_force_makespan(shares, R, S):
+    """Smallest possible maximum rank load over every assignment of the shares to R ranks of at
+    most S shares each."""
+    import itertools
+    best = np.inf
+    for assign in itertools.product(range(R), repeat=len(shares)):
+        if max(np.bincount(assign, minlength=R)) > S:
+            continue
+        loads = np.zeros(R)
+        for a, l in zip(assign, shares):
+            loads[a] += l
+        best = min(best, loads.max())
+    return best
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_placement_is_within_grahams_lpt_bound(seed):
+    """With slots to spare on every rank (no slot limit binds) the placement is LPT, whose
+    largest rank load is at most (4/3 - 1/(3R)) of the optimum (Graham, 1969); the optimum
+    comes from brute force over every assignment."""
+    rng = np.random.default_rng(seed)
+    E, R = 6, 3
+    S = 4                                   # 12 slots: 6 experts + 6 copies, <= 4 per rank
+    load = rng.integers(1, 60, E).astype(np.float64)
+    se, nc, cs = oracle.place_experts(load, R, S)
+    _placement_ok(se, nc, cs, E, R, S)
+    shares = np.concatenate([[load[e] / nc[e]] * nc[e] for e in range(E)])
+    rank_load = np.zeros(R)
+    for p, e in enumerate(se):
+        rank_load[p // S] += load[e] / nc[e]
+    opt = _brute_force_makespan(shares, R, S)
+    assert rank_load.max() <= (4 / 3 - 1 / (3 * R)) * opt + 1e-9
+    assert np.isclose(rank_load.sum(), load.sum())
+
+
+def _chapter_skewed_batch():
+    """The skewed decode batch of "Serving Mixture-of-Experts", Hot-Expert Skew section: 256
+    experts on 32 GPUs, 2048 tokens, top-8, experts 0..7 four times as popular (drawn with the
+    same seeded generator the chapter names)."""
+    rng = np.random.default_rng(0)
+    E, G, T, k = 256, 32, 2048, 8
+    rng.integers(0, E, size=(T, k))          # the chapter draws its uniform batch first
+    p = np.ones(E)
+    p[:8] *= 4
+    p /= p.sum()
+    return rng.choice(E, size=(T, k), p=p), E, G
+
+
+def test_replication_lowers_the_imbalance_of_the_chapters_skewed_batch():
+    """The chapter's claim (exercise 5): replicating the hot experts drops IF on its skewed
+    example. Contiguous placement IF > 1.5 (the chapter's printed bound); the LPT placement with
+    one spare slot per GPU, loads from that same batch, brings it close to 1."""
+    ids, E, G = _chapter_skewed_batch()
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    base = oracle.imbalance_factor(counts, G)
+    assert base > 1.5
+    S = E // G + 1
+    se, nc, cs = oracle.place_experts(counts.astype(np.float64), G, S)
+    _placement_ok(se, nc, cs, E, G, S)
+    assert (nc[:8] >= 2).all()               # every hot expert got a copy
+    rank = np.zeros(G)
+    for p, e in enumerate(se):
+        rank[p // S] += counts[e] / nc[e]
+    placed = rank.max() / rank.mean()
+    assert placed < base and placed < 1.1
+
+
+def test_placed_dispatch_with_one_copy_each_is_the_rank_major_layout():
+    """One copy per expert in expert order (slot e = expert e): the placed dispatch is the
+    dispatch of reading R-g, bit for bit."""
+    cfg = synth.CONFIGS["tiny"]
+    rng = np.random.default_rng(11)
+    ti = np.stack([rng.permutation(cfg.E)[:cfg.k] for _ in range(cfg.T)]).astype(np.int32)
+    nc = np.ones(cfg.E, np.int32)
+    cs = np.full((cfg.E, 4), -1, np.int32)
+    cs[:, 0] = np.arange(cfg.E)
+    c1, r1, s1 = oracle.dispatch_index_placed(ti, cfg.E, cfg.R, cfg.E // cfg.R, nc, cs)
+    c0, _, r0, s0 = oracle.dispatch_index(ti, cfg.E, cfg.R)
+    assert np.array_equal(c1, c0) and np.array_equal(r1, r0) and np.array_equal(s1, s0)
+
+
+def test_placed_dispatch_splits_each_sources_tokens_evenly_over_the_copies():
+    T, E, k, R, S = 64, 16, 4, 4, 6          # 24 slots: 8 copies to spare
+    rng = np.random.default_rng(3)
+    p = np.ones(E)
+    p[[2, 9]] = 12.0
+    p /= p.sum()
+    ti = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    load = np.bincount(ti.reshape(-1), minlength=E).astype(np.float64)
+    se, nc, cs = oracle.place_experts(load, R, S)
+    counts, row_of, src_tok = oracle.dispatch_index_placed(ti, E, R, S, nc, cs)
+    cap = (T // R) * min(k, S)
+    assert counts.sum() == T * k
+    assert len(np.unique(row_of)) == T * k and row_of.min() >= 0 and row_of.max() < R * R * cap
+    tok = np.repeat(np.arange(T), k)
+    assert np.array_equal(src_tok[row_of.reshape(-1)], tok)
+    Ts = T // R
+    for s in range(R):
+        for e in range(E):
+            got = counts[s, cs[e, :nc[e]]]
+            assert got.max() - got.min() <= 1          # even within one source
+            n_se = int((ti[s * Ts:(s + 1) * Ts] == e).sum())
+            assert got.sum() == n_se
+            # the j-th token of source s for expert e went to copy (j + s) mod copies
+            js = [(t, i) for t in range(s * Ts, (s + 1) * Ts) for i in range(k) if ti[t, i] == e]
+            for j, (t, i) in enumerate(js):
+                slot = cs[e, (j + s) % nc[e]]
+                seg = row_of[t, i] // cap
+                assert seg == (slot // S) * R + s
+    # rows land in the segment of the slot's rank, packed from 0
+    seg_fill = np.bincount(row_of.reshape(-1) // cap, minlength=R * R)
+    assert np.array_equal(seg_fill.reshape(R, R).T.reshape(-1),
+                          counts.reshape(R, R, S).sum(2).reshape(-1))
+    # replication lowered the rank-level imbalance of this batch
+    contiguous = oracle.imbalance_factor(load, R)
+    placed = oracle.rank_loads(counts, R)
+    assert placed.max() / placed.mean() < contiguous
