@@ -37,12 +37,16 @@ import synth  # noqa: E402
 METRIC = "MoE layer µs & tokens/s vs tokens (1–16K); % of HBM / tensor roofline"
 # route x2, dispatch x2, ffn schedule x2 (plan, row list), gate/up GEMM, down GEMM, combine
 # (+ the shared expert's input quantisation on the e4m3 path)
-def kernels_per_step(cfg):
-    """Library kernels one layer step launches: route 2, dispatch 2, schedule 2 (1 when the
-    plan kernel fills the row list itself, up to 1024 rows), gate/up, down, combine, and for
-    e4m3 with a shared expert the quantisation of its input."""
+def kernels_per_step(cfg, mode="layer"):
+    """Library kernels one layer step launches: route 2, dispatch 2 (1 in gather mode: no copy),
+    schedule 2 (1 when the plan kernel fills the row list itself, up to 1024 rows), gate/up,
+    down, combine; for e4m3 the quantisation of x when a shared expert or gather mode needs it;
+    with the shared expert on a side stream, its two GEMMs as launches of their own."""
+    gather = "gather" in mode
+    side = "side" in mode and cfg.d_ff_shared > 0
     sched = 1 if cfg.T * cfg.k <= 1024 else 2
-    return 7 + sched + (1 if cfg.act == "fp8" and cfg.d_ff_shared else 0)
+    quant = 1 if cfg.act == "fp8" and (cfg.d_ff_shared or gather) else 0
+    return 7 + sched + quant - (1 if gather else 0) + (2 if side else 0)
 L2_BYTES = 129 * 2 ** 20
 CPU_SAMPLE_SECONDS = 12.0   # target CPU time of the oracle sample behind cpu_baseline
 
@@ -57,6 +61,12 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=0, help="tokens in the oracle sample")
+    p.add_argument("--no-extras", dest="extras", action="store_false",
+                   help="time the named workload only (default with dsv3_decode at N=1: also "
+                        "the sweep, the skewed prefill and the FP8 prefill)")
+    p.add_argument("--extra-steps", type=int, default=10, help="timed steps per extra workload")
+    p.add_argument("--mode", default="layer", choices=sorted(MODES),
+                   help="the layer variant of the main workload's timed steps")
     return p.parse_args()
 
 
@@ -237,30 +247,66 @@ def job_tokens_per_s(T: int, world: int, ms_per_step: float) -> float:
 # ------------------------------------------------------------------------------------------
 # Our arm
 # ------------------------------------------------------------------------------------------
-def run_ours(args, cfg, rank, world, local_rank):
+def weight_dict(W):
+    return dict(w13=W["w13"], w13_s=W["w13_s"], w2=W["w2"], w2_s=W["w2_s"], ws13=W["ws13"],
+                ws13_s=W["ws13_s"], ws2=W["ws2"], ws2_s=W["ws2_s"])
+
+
+MODES = {"layer": {}, "gather": {"gather": True}, "side": {"side_stream": True},
+         "gather+side": {"gather": True, "side_stream": True},
+         "side32": {"side_stream": True, "side_ctas": 32},
+         "side64": {"side_stream": True, "side_ctas": 64}}
+
+
+def setup(cfg, dev, rank=0, world=1, W=None, mode="layer"):
+    """Inputs, weights (made here unless given) and a layer object on dev. Under torchrun every
+    rank holds the same weights and its own batch of tokens. mode: one of MODES (moe_layer, or
+    moe_layer_ex with gather mode and/or the shared expert on a side stream)."""
     import combine_grouped_gemm_gb300 as moe
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    # every rank: same weights, its own batch of tokens
     inp = synth.make_router_inputs(cfg, dev)
     if world > 1:
         inp["x"] = synth.normal_bf16(cfg.seed + 7919 * rank, synth.TAG_X, (cfg.T, cfg.d),
                                      cfg.x_std, dev)
-    W = synth.make_expert_weights(cfg, dev)
-    weights = dict(w13=W["w13"], w13_s=W["w13_s"], w2=W["w2"], w2_s=W["w2_s"], ws13=W["ws13"],
-                   ws13_s=W["ws13_s"], ws2=W["ws2"], ws2_s=W["ws2_s"])
-    lay = moe.MoELayer(cfg, inp["w_gate"], inp["bias"], weights, dev)
+    if W is None:
+        W = synth.make_expert_weights(cfg, dev)
+    lay = moe.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), dev, **MODES[mode])
+    return inp, W, lay
+
+
+def time_modes(cfg, dev, W, steps, warm, modes=("gather", "side", "gather+side")):
+    """Layer time of each variant on the same inputs and weights (the variants' outputs equal
+    moe_layer's bit for bit; the tests check that)."""
+    out = {}
+    for mode in modes:
+        inp, _, lay = setup(cfg, dev, W=W, mode=mode)
+        r = time_layer(cfg, inp, lay, steps, warm, dev)
+        out[mode] = {"layer_us": round(r["ms"] * 1e3, 2),
+                     "tokens_per_s": round(job_tokens_per_s(cfg.T, 1, r["ms"]), 1),
+                     "stages_us": {n: round(v * 1e3, 2) for n, v in r["stage_ms"].items()},
+                     "e2e_tokens_per_s": round(job_tokens_per_s(cfg.T, 1, r["ms_e2e"]), 1),
+                     "gpu_launches": kernels_per_step(cfg, mode) * steps}
+        del lay, inp
+    return out
+
+
+def time_layer(cfg, inp, lay, steps, warmup, dev, rank=0, world=1, local_rank=0):
+    """W untimed steps, then K back-to-back steps timed with CUDA events on the launching stream
+    (barrier + synchronize on both sides, clocks sampled meanwhile); then K steps with stage
+    events; then K end-to-end steps through MoELayer.run_host (pinned host buffers, both copies
+    inside the timed region)."""
+    import combine_grouped_gemm_gb300 as moe
+
     y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_LAYER_EVENTS)]
-           for _ in range(args.steps)]
+           for _ in range(steps)]
     for row in evs:
         for e in row:
             e.record(stream)
     torch.cuda.synchronize(dev)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         lay(inp["x"], y)
     torch.cuda.synchronize(dev)
     moe.clear_status(lay.bufs["ws"])
@@ -275,13 +321,13 @@ def run_ours(args, cfg, rank, world, local_rank):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         lay(inp["x"], y)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop() if clocks else None
-    ms = t0.elapsed_time(t1) / args.steps
+    ms = t0.elapsed_time(t1) / steps
     status = moe.read_status(lay.bufs["ws"])
     if status:
         raise RuntimeError(f"device status {status} after the timed region")
@@ -289,13 +335,13 @@ def run_ours(args, cfg, rank, world, local_rank):
     # Per-stage times: the same steps again with an event between the stages. The events make
     # each stage start after the previous one has finished (no programmatic overlap of the
     # launches), so the stages add up to a little more than the step time above.
-    for i in range(args.steps):
+    for i in range(steps):
         lay(inp["x"], y, events=evs[i])
     torch.cuda.synchronize(dev)
     stage_ms = {n: 0.0 for n in moe.STAGE_NAMES}
     for row in evs:
         for j, n in enumerate(moe.STAGE_NAMES):
-            stage_ms[n] += row[j].elapsed_time(row[j + 1]) / args.steps
+            stage_ms[n] += row[j].elapsed_time(row[j + 1]) / steps
     ms_max = max_over_ranks(ms, dev)
 
     # end to end through the public API: pinned host buffers, copies inside the timed region
@@ -308,31 +354,138 @@ def run_ours(args, cfg, rank, world, local_rank):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         lay.run_host(x_host, y_host, stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / steps, dev)
 
     counts = lay.bufs["counts"].cpu().numpy()
     return dict(ms=ms_max, ms_local=ms, stage_ms=stage_ms, clocks=clk, ms_e2e=ms_e2e,
-                counts=counts, inp=inp, W=W, lay=lay)
+                counts=counts, steps=steps, warmup=warmup)
+
+
+def imbalance(cfg, counts):
+    """Rank-level imbalance factor of one step's routing (max rank load / mean rank load)."""
+    return round(float(counts.sum(0).reshape(cfg.R, -1).sum(1).max() / (cfg.T * cfg.k / cfg.R)), 4)
+
+
+def summarise(cfg, r, pk, world=1, full=True):
+    """The per-configuration fields of the JSON line."""
+    b, f, touched = algorithmic(cfg, r["counts"])
+    layer_bytes = sum(b.values())
+    out = {
+        "workload": cfg.name, "T": cfg.T, "act": cfg.act,
+        "steps": r["steps"], "warmup": r["warmup"],
+        "layer_us": round(r["ms"] * 1e3, 2),
+        "tokens_per_s": round(job_tokens_per_s(cfg.T, world, r["ms"]), 1),
+        "layer_hbm_frac": round(layer_bytes / (r["ms"] * 1e-3) / 1e9 / pk["hbm"], 4),
+        "stages_us": {n: round(v * 1e3, 2) for n, v in r["stage_ms"].items()},
+        "stages_roofline": {n: {k2: v2 for k2, v2 in
+                                roofline(cfg, n, r["stage_ms"][n], b, f, pk).items()
+                                if k2 in ("bound", "achieved", "unit", "frac")}
+                            for n in ("route", "dispatch", "ffn_gate_up", "ffn_down", "combine")},
+        "experts_touched": touched,
+        "imbalance_factor": imbalance(cfg, r["counts"]),
+        "gpu_launches": kernels_per_step(cfg, r.get("mode", "layer")) * r["steps"],
+        "e2e": {"value": round(job_tokens_per_s(cfg.T, world, r["ms_e2e"]), 1),
+                "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.d * 2,
+                "d2h_bytes_per_step": cfg.T * cfg.d * 2, "ms_per_step": round(r["ms_e2e"], 5)},
+        "clocks": r["clocks"],
+    }
+    if full:
+        out["gemm_roofline"] = {n: roofline(cfg, n, r["stage_ms"][n], b, f, pk)
+                                for n in ("ffn_gate_up", "ffn_down")}
+    return out
+
+
+def time_placed(cfg, dev, W, steps, warm, spare_per_rank=4, seed=17):
+    """The layer with redundant experts (32 spare slots at 8 ranks): a placement planned by
+    moe_place_experts from the routing of another batch of the same workload (standing for past
+    traffic), then timed on this batch. Reports the logical ranks' imbalance factor before
+    (contiguous experts) and after (placed copies) on the timed batch."""
+    import combine_grouped_gemm_gb300 as moe
+
+    inp = synth.make_router_inputs(cfg, dev)
+    other = synth.normal_bf16(cfg.seed + seed, synth.TAG_X, (cfg.T, cfg.d), cfg.x_std, dev)
+    b = moe.Buffers(cfg, dev)
+    moe.route(cfg, other, inp["w_gate"], inp["bias"], b["topk_idx"], b["topk_w"], b["ws"])
+    load = np.bincount(b["topk_idx"].cpu().numpy().reshape(-1), minlength=cfg.E)
+    del b
+    S = cfg.E // cfg.R + spare_per_rank
+    pl = moe.Placement.from_loads(load.astype(np.float64), cfg.R, S, max_copies=16, device=dev)
+    lay = moe.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), dev, placement=pl)
+    r = time_layer(cfg, inp, lay, steps, warm, dev)
+    counts = r["counts"]                      # [R][slots] of the timed batch
+    ti = lay.bufs["topk_idx"].cpu().numpy()
+    per_expert = np.bincount(ti.reshape(-1), minlength=cfg.E)
+    before = per_expert.reshape(cfg.R, -1).sum(1)
+    after = counts.sum(0).reshape(cfg.R, -1).sum(1)
+    nc = pl.n_copies.cpu().numpy()
+    out = {"slots_per_rank": S, "redundant": int(cfg.R * S - cfg.E),
+           "copies_of_hottest": int(nc[int(np.argmax(per_expert))]),
+           "layer_us": round(r["ms"] * 1e3, 2),
+           "tokens_per_s": round(job_tokens_per_s(cfg.T, 1, r["ms"]), 1),
+           "stages_us": {n: round(v * 1e3, 2) for n, v in r["stage_ms"].items()},
+           "imbalance_factor_contiguous": round(float(before.max() / before.mean()), 4),
+           "imbalance_factor_placed": round(float(after.max() / after.mean()), 4),
+           "slots_touched": int((counts.sum(0) > 0).sum()),
+           "planned_from": "routing of another batch of the workload (seed + %d)" % seed}
+    del lay, inp
+    return out
+
+
+def run_extras(args, dev, W_decode, pk):
+    """The rest of the metric's token range in the same process: the decode sweep (the decode
+    layer's weights at T = 8 .. 1024), the Zipf-skewed bf16 prefill (T = 4096) and the FP8
+    prefill (T = 16384). Each prefill's weights are made, timed and freed before the next."""
+    steps = max(3, args.extra_steps)
+    warm = max(3, args.warmup)
+    out = {"sweep": []}
+    dec = synth.CONFIGS["dsv3_decode"]
+    out["variants"] = {dec.name: time_modes(dec, dev, W_decode, steps, warm,
+                                            ("gather", "side", "side32", "side64",
+                                             "gather+side"))}
+    out["placed"] = {dec.name: time_placed(dec, dev, W_decode, steps, warm)}
+    for T in synth.SWEEP_T:
+        cfg = dec.with_T(T)
+        inp, _, lay = setup(cfg, dev, W=W_decode)
+        r = time_layer(cfg, inp, lay, steps, warm, dev)
+        s = summarise(cfg, r, pk, full=False)
+        out["sweep"].append({k: s[k] for k in ("T", "layer_us", "tokens_per_s", "layer_hbm_frac",
+                                               "stages_us", "experts_touched", "e2e",
+                                               "gpu_launches")}
+                            | {"sm_mhz": (r["clocks"] or {}).get("sm_mhz")})
+        del lay, inp
+    for key, name in (("skew_prefill", "dsv3_skew_prefill"), ("fp8_prefill", "dsv3_fp8_prefill")):
+        cfg = synth.CONFIGS[name]
+        torch.cuda.empty_cache()
+        inp, W, lay = setup(cfg, dev)
+        r = time_layer(cfg, inp, lay, steps, warm, dev)
+        out[key] = summarise(cfg, r, pk)
+        del lay, inp
+        out["variants"][cfg.name] = time_modes(cfg, dev, W, steps, warm)
+        out["placed"][cfg.name] = time_placed(cfg, dev, W, steps, warm)
+        del W
+        torch.cuda.empty_cache()
+    return out
 
 
 def oracle_sample(cfg, inp, W, tokens):
-    """Times oracle.layer_tokens on the given tokens; weight slices are copied to the host
-    before the clock starts."""
+    """Times the oracle's steps on the given tokens, single-threaded: the router, the dispatch
+    index, every routed expert row, the shared expert and the combine. Weight slices are copied
+    to the host before the clock starts. Returns {stage: seconds}."""
     import oracle
 
     def bits(t):
         t = t.detach().cpu().contiguous()
         return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
 
-    x = bits(inp["x"])
+    x = bits(inp["x"])[tokens]
     wg = inp["w_gate"].cpu().numpy()
     b = inp["bias"].cpu().numpy()
-    idx, _ = oracle.route(x[tokens], wg, b, cfg.k, cfg.n_group, cfg.topk_group, cfg.route_scale)
+    idx, _ = oracle.route(x, wg, b, cfg.k, cfg.n_group, cfg.topk_group, cfg.route_scale)
     fp8 = cfg.w == "fp8"
     experts = {}
     for e in np.unique(idx):
@@ -341,15 +494,47 @@ def oracle_sample(cfg, inp, W, tokens):
         if fp8:
             experts[e]["w13_s"] = W["w13_s"][e].cpu().numpy()
             experts[e]["w2_s"] = W["w2_s"][e].cpu().numpy()
-    shared = None
+    S = None
     if cfg.d_ff_shared:
-        shared = dict(ws13=bits(W["ws13"]), ws2=bits(W["ws2"]))
+        S = dict(ws13=bits(W["ws13"]), ws2=bits(W["ws2"]))
         if fp8:
-            shared["ws13_s"] = W["ws13_s"].cpu().numpy()
-            shared["ws2_s"] = W["ws2_s"].cpu().numpy()
+            S["ws13_s"] = W["ws13_s"].cpu().numpy()
+            S["ws2_s"] = W["ws2_s"].cpu().numpy()
+    n, k = len(tokens), cfg.k
+    sec = {}
     t = time.perf_counter()
-    oracle.layer_tokens(cfg, x, wg, b, lambda e: experts[e], shared, tokens)
-    return time.perf_counter() - t
+    idx, w = oracle.route(x, wg, b, cfg.k, cfg.n_group, cfg.topk_group, cfg.route_scale)
+    sec["route"] = time.perf_counter() - t
+    t = time.perf_counter()
+    if fp8:
+        xq, xs = oracle.quant_rows_e4m3(oracle.bf16_to_f32(x))
+    sec["dispatch"] = time.perf_counter() - t   # the index pass below is negligible
+    eo = np.empty((n, k, cfg.d), dtype=np.uint16)
+    t = time.perf_counter()
+    for j in range(n):
+        for i in range(k):
+            Wt = experts[int(idx[j, i])]
+            if fp8:
+                eo[j, i], _ = oracle.swiglu_row_fp8(xq[j], xs[j], Wt["w13"], Wt["w13_s"],
+                                                    Wt["w2"], Wt["w2_s"])
+            else:
+                eo[j, i], _ = oracle.swiglu_row_bf16(x[j], Wt["w13"], Wt["w2"])
+    sec["experts"] = time.perf_counter() - t
+    sh = None
+    t = time.perf_counter()
+    if S is not None:
+        sh = np.empty((n, cfg.d), dtype=np.uint16)
+        for j in range(n):
+            if fp8:
+                sh[j], _ = oracle.swiglu_row_fp8(xq[j], xs[j], S["ws13"], S["ws13_s"], S["ws2"],
+                                                 S["ws2_s"])
+            else:
+                sh[j], _ = oracle.swiglu_row_bf16(x[j], S["ws13"], S["ws2"])
+    sec["shared"] = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.combine(eo.reshape(n * k, cfg.d), np.arange(n * k, dtype=np.int32).reshape(n, k), w, sh)
+    sec["combine"] = time.perf_counter() - t
+    return sec
 
 
 def main():
@@ -368,46 +553,41 @@ def main():
     if world > 1:
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
 
-    r = run_ours(args, cfg, rank, world, local_rank)
+    inp, W, lay = setup(cfg, dev, rank, world, mode=args.mode)
+    r = time_layer(cfg, inp, lay, args.steps, args.warmup, dev, rank, world, local_rank)
+    r["mode"] = args.mode
     if rank == 0:
         b, f, touched = algorithmic(cfg, r["counts"])
         pk = peaks()
         dom = max(r["stage_ms"], key=lambda n: r["stage_ms"][n])
-        dom_ms = r["stage_ms"][dom]
-        roof = roofline(cfg, dom, dom_ms, b, f, pk)
-        layer_bytes = sum(b.values())
-        tokens_per_s = job_tokens_per_s(cfg.T, world, r["ms"])
+        roof = roofline(cfg, dom, r["stage_ms"][dom], b, f, pk)
+        s = summarise(cfg, r, pk, world)
         out = {
-            "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s",
+            "metric": METRIC, "value": s["tokens_per_s"], "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(r["ms"], 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": cfg.act,
             "data": "synthetic: seeded counter-based generator, random-init weights",
-            "config": {**describe(cfg), "parallelism": f"replicas x{world}",
+            "config": {**describe(cfg), "parallelism": f"replicas x{world}", "mode": args.mode,
                        "l2": "inputs larger than L2: ~%.1f GB of expert weights streamed per "
                              "step vs 129 MB L2" % (b["ffn_gate_up"] / 1e9 + b["ffn_down"] / 1e9)},
-            "layer_us": round(r["ms"] * 1e3, 2),
-            "stages_us": {n: round(v * 1e3, 2) for n, v in r["stage_ms"].items()},
-            "layer_hbm_frac": round(layer_bytes / (r["ms"] * 1e-3) / 1e9 / pk["hbm"], 4),
-            "stages_roofline": {n: {k2: v2 for k2, v2 in roofline(cfg, n, r["stage_ms"][n], b, f, pk).items()
-                                    if k2 in ("bound", "achieved", "unit", "frac")}
-                                for n in ("route", "dispatch", "ffn_gate_up", "ffn_down", "combine")},
-            "experts_touched": touched,
-            "imbalance_factor": round(float(np.bincount(
-                np.repeat(np.arange(cfg.E), r["counts"].sum(0)), minlength=cfg.E)
-                .reshape(cfg.R, -1).sum(1).max() / (cfg.T * cfg.k / cfg.R)), 4),
+            **{k2: s[k2] for k2 in ("layer_us", "stages_us", "layer_hbm_frac", "stages_roofline",
+                                    "experts_touched", "imbalance_factor", "gemm_roofline")},
             "roofline": roof,
-            "gpu_launches": kernels_per_step(cfg) * args.steps,
+            "gpu_launches": s["gpu_launches"],
             "clocks": r["clocks"],
-            "e2e": {"value": round(job_tokens_per_s(cfg.T, world, r["ms_e2e"]), 1), "unit": "tokens/s",
-                    "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
-                    "ms_per_step": round(r["ms_e2e"], 5)},
+            "e2e": s["e2e"],
         }
         if world == 1 and not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(cfg, r["inp"], r["W"], args.cpu_sample)
+            out["cpu_baseline"] = cpu_baseline(cfg, inp, W, args.cpu_sample)
         else:
             out["cpu_baseline"] = None
+        if world == 1 and args.extras and cfg.name == "dsv3_decode":
+            del lay
+            out.update(run_extras(args, dev, W, pk))
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -422,15 +602,25 @@ def cpu_baseline(cfg, inp, W, n_tokens=0, seconds=CPU_SAMPLE_SECONDS):
     the clock, so host memory holds one batch's experts at a time."""
     rng = np.random.default_rng(0)
     n0 = min(cfg.T, 4)
-    sec0 = oracle_sample(cfg, inp, W, np.sort(rng.choice(cfg.T, n0, replace=False)))
-    per_token = max(sec0, 1e-6) / n0
-    n = n_tokens or int(min(cfg.T, max(n0, round(seconds / per_token))))
-    tokens = np.sort(rng.choice(cfg.T, n, replace=False))
-    sec = sum(oracle_sample(cfg, inp, W, tokens[i:i + 8]) for i in range(0, n, 8))
-    return {"value": round(n / sec, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    if n_tokens > 0:
+        n = min(cfg.T, n_tokens)
+    else:
+        sec0 = sum(oracle_sample(cfg, inp, W, np.sort(rng.choice(cfg.T, n0, replace=False)))
+                   .values())
+        per_token = max(sec0, 1e-6) / n0
+        n = int(min(cfg.T, max(n0, round(seconds / per_token))))
+    tokens = np.sort(np.random.default_rng(1).choice(cfg.T, n, replace=False))
+    stage = {}
+    for i in range(0, n, 8):
+        for key, v in oracle_sample(cfg, inp, W, tokens[i:i + 8]).items():
+            stage[key] = stage.get(key, 0.0) + v
+    sec = sum(stage.values())
+    return {"value": round(n / sec, 4), "unit": "tokens/s", "cores": 1,
+            "host_cores": os.cpu_count(), "kind": "oracle",
+            "us_per_token": {key: round(v / n * 1e6, 1) for key, v in stage.items()},
             "sample": f"{n} of {cfg.T} tokens of {cfg.name}: route + k experts + shared + "
-                      f"combine per token, {sec:.1f} s single-threaded (sized from a "
-                      f"{n0}-token probe)"}
+                      f"combine per token, {sec:.1f} s single-threaded"
+                      + (f" (sized from a {n0}-token probe)" if n_tokens <= 0 else "")}
 
 
 def run_reference(args, cfg, rank, world, local_rank):
@@ -446,7 +636,7 @@ def run_reference(args, cfg, rank, world, local_rank):
         oracle_sample(cfg, inp, W, rng.choice(cfg.T, 1))
     total = 0.0
     for _ in range(args.steps):
-        total += oracle_sample(cfg, inp, W, rng.choice(cfg.T, 1))
+        total += sum(oracle_sample(cfg, inp, W, rng.choice(cfg.T, 1)).values())
     v = args.steps / total
     out = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tokens/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

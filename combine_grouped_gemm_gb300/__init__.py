@@ -44,6 +44,21 @@ class Sizes(ctypes.Structure):
                 ("ebuf_bytes", ctypes.c_size_t), ("ws_bytes", ctypes.c_size_t)]
 
 
+MOE_OPT_GATHER_X, MOE_OPT_SHARED_SIDE_STREAM = 1, 2
+
+
+class PlacementC(ctypes.Structure):
+    _fields_ = [("slots_per_rank", ctypes.c_int32), ("max_copies", ctypes.c_int32),
+                ("slot_expert", ctypes.c_void_p), ("n_copies", ctypes.c_void_p),
+                ("copy_slot", ctypes.c_void_p)]
+
+
+class LayerOpts(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_uint32), ("side_stream", ctypes.c_void_p),
+                ("fork_event", ctypes.c_void_p), ("join_event", ctypes.c_void_p),
+                ("side_ctas", ctypes.c_int32), ("placement", ctypes.POINTER(PlacementC))]
+
+
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w13", "w13_scales", "w2", "w2_scales", "ws13", "ws13_scales", "ws2",
@@ -61,10 +76,15 @@ def _load():
         "moe_query_sizes": [P, P],
         "moe_route": [P, P, P, P, P, P, P, S],
         "moe_route_noalloc": [P, P, P, P, P, P, S],
-        "moe_dispatch": [P, P, P, P, P, P, P, P, S],
+        "moe_dispatch": [P, P, P, P, P, P, P, P, P, S],
         "moe_expert_ffn": [P, P, P, P, P, P, P, P, P, S],
-        "moe_combine": [P, P, P, P, P, P, S],
+        "moe_combine": [P, P, P, P, P, P, P, S],
         "moe_layer": [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P],
+        "moe_layer_ex": [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P],
+        "moe_dispatch_index": [P, P, P, P, P, P, S],
+        "moe_place_experts": [I, I, I, P, I, P, P, P],
+        "moe_query_sizes_placed": [P, I, P],
+        "moe_expert_ffn_gather": [P, P, P, P, P, P, P, P, S],
         "moe_clear_status": [P, S],
         "moe_read_status": [P, P, S],
         "moe_selftest_wait": [P, ctypes.c_int64, S],
@@ -82,8 +102,9 @@ def _load():
 _lib = _load()
 
 EXPORTED = ["moe_validate", "moe_query_sizes", "moe_route", "moe_route_noalloc", "moe_dispatch",
-            "moe_expert_ffn",
-            "moe_combine", "moe_layer", "moe_clear_status", "moe_read_status", "moe_selftest_wait",
+            "moe_expert_ffn", "moe_combine", "moe_layer", "moe_layer_ex", "moe_dispatch_index",
+            "moe_expert_ffn_gather", "moe_place_experts", "moe_query_sizes_placed",
+            "moe_clear_status", "moe_read_status", "moe_selftest_wait",
             "moe_strerror", "moe_abi_version", "moe_last_cuda_error"]
 
 
@@ -143,6 +164,46 @@ def query_sizes(cfg) -> dict:
     return {n: getattr(s, n) for n, _ in Sizes._fields_}
 
 
+def query_sizes_placed(cfg, slots_per_rank) -> dict:
+    s = Sizes()
+    _check("moe_query_sizes_placed", _lib.moe_query_sizes_placed(
+        ctypes.byref(make_cfg(cfg)), int(slots_per_rank), ctypes.byref(s)))
+    return {n: getattr(s, n) for n, _ in Sizes._fields_}
+
+
+def place_experts(load, R, slots_per_rank, max_copies=8):
+    """moe_place_experts on the host: (slot_expert [R*S], n_copies [E], copy_slot [E][max])
+    as numpy int32 arrays, from estimated loads [E]."""
+    import numpy as np
+    ld = np.ascontiguousarray(load, dtype=np.float64)
+    E = ld.size
+    se = np.empty(R * slots_per_rank, dtype=np.int32)
+    nc = np.empty(E, dtype=np.int32)
+    cs = np.empty((E, max_copies), dtype=np.int32)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)   # noqa: E731
+    _check("moe_place_experts", _lib.moe_place_experts(E, R, slots_per_rank, ptr(ld), max_copies,
+                                                       ptr(se), ptr(nc), ptr(cs)))
+    return se, nc, cs
+
+
+class Placement:
+    """A placement of the experts on slots (see moe_placement), held on the device."""
+
+    def __init__(self, slot_expert, n_copies, copy_slot, slots_per_rank, device="cuda"):
+        self.slots_per_rank = int(slots_per_rank)
+        self.slot_expert = torch.as_tensor(slot_expert, dtype=torch.int32).to(device).contiguous()
+        self.n_copies = torch.as_tensor(n_copies, dtype=torch.int32).to(device).contiguous()
+        self.copy_slot = torch.as_tensor(copy_slot, dtype=torch.int32).to(device).contiguous()
+        self.c = PlacementC(self.slots_per_rank, self.copy_slot.shape[1],
+                            self.slot_expert.data_ptr(), self.n_copies.data_ptr(),
+                            self.copy_slot.data_ptr())
+
+    @classmethod
+    def from_loads(cls, load, R, slots_per_rank, max_copies=8, device="cuda"):
+        se, nc, cs = place_experts(load, R, slots_per_rank, max_copies)
+        return cls(se, nc, cs, slots_per_rank, device)
+
+
 def route(cfg, x, w_gate, bias, topk_idx, topk_w, ws, stream=None):
     _check("moe_route", _lib.moe_route(ctypes.byref(make_cfg(cfg)), _p(x), _p(w_gate), _p(bias),
                                        _p(topk_idx), _p(topk_w), _p(ws), _s(stream)))
@@ -156,10 +217,12 @@ def route_noalloc(cfg, x, w_gate, bias, topk_idx, topk_w, stream=None):
                                                        _p(topk_w), _s(stream)))
 
 
-def dispatch(cfg, x, topk_idx, recv, recv_scales, counts, row_of, src_tok=None, stream=None):
+def dispatch(cfg, x, topk_idx, recv, recv_scales, counts, row_of, src_tok=None, stream=None,
+             status=None):
+    """status: None or a device tensor whose first 4 bytes receive MOE_DEV_* bits (e.g. ws)."""
     _check("moe_dispatch", _lib.moe_dispatch(ctypes.byref(make_cfg(cfg)), _p(x), _p(topk_idx),
                                              _p(recv), _p(recv_scales), _p(counts), _p(row_of),
-                                             _p(src_tok), _s(stream)))
+                                             _p(src_tok), _p(status), _s(stream)))
 
 
 def expert_ffn(cfg, recv, recv_scales, counts, x, weights: dict, ebuf, shared_out, ws,
@@ -171,9 +234,10 @@ def expert_ffn(cfg, recv, recv_scales, counts, x, weights: dict, ebuf, shared_ou
                                                  _p(ws), _s(stream)))
 
 
-def combine(cfg, ebuf, row_of, topk_w, shared_out, y, stream=None):
+def combine(cfg, ebuf, row_of, topk_w, shared_out, y, stream=None, status=None):
     _check("moe_combine", _lib.moe_combine(ctypes.byref(make_cfg(cfg)), _p(ebuf), _p(row_of),
-                                           _p(topk_w), _p(shared_out), _p(y), _s(stream)))
+                                           _p(topk_w), _p(shared_out), _p(y), _p(status),
+                                           _s(stream)))
 
 
 def layer(cfg, x, w_gate, bias, weights: dict, bufs: dict, y, stream=None, events=None):
@@ -191,6 +255,39 @@ def layer(cfg, x, w_gate, bias, weights: dict, bufs: dict, y, stream=None, event
                                        _p(b["recv"]), _p(b.get("recv_scales")), _p(b["counts"]),
                                        _p(b["row_of"]), _p(b["ebuf"]), _p(b.get("shared_out")),
                                        _p(y), _p(b["ws"]), _s(stream), ev))
+
+
+def layer_ex(cfg, opts: LayerOpts | None, x, w_gate, bias, weights: dict, bufs: dict, y,
+             stream=None, events=None):
+    """moe_layer_ex: the layer with the variants of opts (None: moe_layer)."""
+    w = _weights(weights)
+    ev = None
+    if events is not None:
+        arr = (ctypes.c_void_p * MOE_LAYER_EVENTS)(*[e.cuda_event for e in events])
+        ev = ctypes.cast(arr, ctypes.c_void_p)
+    b = bufs
+    _check("moe_layer_ex", _lib.moe_layer_ex(ctypes.byref(make_cfg(cfg)),
+                                             ctypes.byref(opts) if opts is not None else None,
+                                             _p(x), _p(w_gate), _p(bias), ctypes.byref(w),
+                                             _p(b["topk_idx"]), _p(b["topk_w"]), _p(b.get("recv")),
+                                             _p(b.get("recv_scales")), _p(b["counts"]),
+                                             _p(b["row_of"]), _p(b["ebuf"]),
+                                             _p(b.get("shared_out")), _p(y), _p(b["ws"]),
+                                             _s(stream), ev))
+
+
+def dispatch_index(cfg, topk_idx, counts, row_of, src_tok, stream=None, status=None):
+    _check("moe_dispatch_index", _lib.moe_dispatch_index(ctypes.byref(make_cfg(cfg)), _p(topk_idx),
+                                                         _p(counts), _p(row_of), _p(src_tok),
+                                                         _p(status), _s(stream)))
+
+
+def expert_ffn_gather(cfg, x, counts, src_tok, weights: dict, ebuf, shared_out, ws, stream=None):
+    w = _weights(weights)
+    _check("moe_expert_ffn_gather",
+           _lib.moe_expert_ffn_gather(ctypes.byref(make_cfg(cfg)), _p(x), _p(counts), _p(src_tok),
+                                      ctypes.byref(w), _p(ebuf), _p(shared_out), _p(ws),
+                                      _s(stream)))
 
 
 def clear_status(ws, stream=None):
@@ -217,18 +314,21 @@ class Buffers(dict):
     """Device buffers of one layer configuration, allocated once with torch (the library itself
     allocates nothing)."""
 
-    def __init__(self, cfg, device="cuda"):
+    def __init__(self, cfg, device="cuda", with_recv=True, slots_per_rank=0):
         super().__init__()
-        s = query_sizes(cfg)
+        s = query_sizes_placed(cfg, slots_per_rank) if slots_per_rank else query_sizes(cfg)
         T, k, d, R, E = cfg.T, cfg.k, cfg.d, cfg.R, cfg.E
+        if slots_per_rank:
+            E = R * slots_per_rank     # counts are over the slots
         self.sizes = s
         fp8 = make_cfg(cfg).act_dtype == MOE_FP8_E4M3
         self["topk_idx"] = torch.empty((T, k), dtype=torch.int32, device=device)
         self["topk_w"] = torch.empty((T, k), dtype=torch.float32, device=device)
-        self["recv"] = torch.empty((s["recv_rows"], d),
-                                   dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
+        self["recv"] = (torch.empty((s["recv_rows"], d),
+                                    dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
+                        if with_recv else None)
         self["recv_scales"] = (torch.empty((d // 128, s["recv_rows"]), dtype=torch.float32,
-                                           device=device) if fp8 else None)
+                                           device=device) if fp8 and with_recv else None)
         self["counts"] = torch.empty((R, E), dtype=torch.int32, device=device)
         self["row_of"] = torch.empty((T, k), dtype=torch.int32, device=device)
         self["ebuf"] = torch.empty((s["recv_rows"], d), dtype=torch.bfloat16, device=device)
@@ -239,19 +339,54 @@ class Buffers(dict):
 
 class MoELayer:
     """One MoE layer with resident weights: ``y = layer(x)`` runs router, dispatch, expert
-    FFNs and combine on the current stream through ``moe_layer``."""
+    FFNs and combine on the current stream through ``moe_layer`` (``moe_layer_ex`` when a
+    variant is asked for).
 
-    def __init__(self, cfg, w_gate, bias, weights: dict, device="cuda"):
+    gather: the expert GEMMs read routed rows from x by token (no receive-buffer copy; the
+    receive buffers are not allocated). side_stream: the shared expert runs on a second stream
+    of its own, limited to side_ctas CTAs per GEMM. placement: redundant experts on slots
+    (Placement); the dispatch splits each expert's rows over its copies."""
+
+    def __init__(self, cfg, w_gate, bias, weights: dict, device="cuda", gather=False,
+                 side_stream=False, side_ctas=0, placement: Placement | None = None):
         self.cfg = cfg
         self.w_gate = w_gate
         self.bias = bias
         self.weights = weights
-        self.bufs = Buffers(cfg, device)
+        self.placement = placement
+        self.bufs = Buffers(cfg, device, with_recv=not gather,
+                            slots_per_rank=placement.slots_per_rank if placement else 0)
+        self.opts = None
+        if gather or side_stream or placement is not None:
+            self.opts = LayerOpts(flags=(MOE_OPT_GATHER_X if gather else 0)
+                                  | (MOE_OPT_SHARED_SIDE_STREAM if side_stream else 0),
+                                  side_ctas=int(side_ctas))
+            if placement is not None:
+                self.opts.placement = ctypes.pointer(placement.c)
+            if side_stream:
+                # the stream and events live as long as the layer object
+                self._side = torch.cuda.Stream(device=device)
+                self._fork = torch.cuda.Event()
+                self._join = torch.cuda.Event()
+                cur = torch.cuda.current_stream(device)
+                self._fork.record(cur)      # gives the events their handles
+                self._join.record(cur)
+                torch.cuda.synchronize(device)
+                self.opts.side_stream = self._side.cuda_stream
+                self.opts.fork_event = self._fork.cuda_event
+                self.opts.join_event = self._join.cuda_event
+
+    def _run(self, x, y, stream, events):
+        if self.opts is None:
+            layer(self.cfg, x, self.w_gate, self.bias, self.weights, self.bufs, y, stream, events)
+        else:
+            layer_ex(self.cfg, self.opts, x, self.w_gate, self.bias, self.weights, self.bufs, y,
+                     stream, events)
 
     def __call__(self, x, y=None, stream=None, events=None):
         if y is None:
             y = torch.empty((self.cfg.T, self.cfg.d), dtype=torch.bfloat16, device=x.device)
-        layer(self.cfg, x, self.w_gate, self.bias, self.weights, self.bufs, y, stream, events)
+        self._run(x, y, stream, events)
         return y
 
     def run_host(self, x_host, y_host, stream=None):
@@ -265,7 +400,6 @@ class MoELayer:
         s = stream or torch.cuda.current_stream()
         with torch.cuda.stream(s):
             self._x_dev.copy_(x_host, non_blocking=True)
-            layer(self.cfg, self._x_dev, self.w_gate, self.bias, self.weights, self.bufs,
-                  self._y_dev, s)
+            self._run(self._x_dev, self._y_dev, s, None)
             y_host.copy_(self._y_dev, non_blocking=True)
         return y_host

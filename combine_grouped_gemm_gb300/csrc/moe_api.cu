@@ -3,6 +3,9 @@
 // combine on the caller's stream. Nothing here allocates memory or waits for the device,
 // except moe_read_status.
 #include <math.h>
+#include <stdlib.h>
+
+#include <algorithm>
 
 #include "moe_internal.h"
 
@@ -19,12 +22,14 @@ namespace moe {
 
 namespace {
 thread_local int g_last_cuda_error = 0;
+}  // namespace
 
 int cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
   return MOE_ERR_CUDA;
 }
 
+namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -92,10 +97,12 @@ WsLayout ws_layout(const moe_cfg& c) {
   L.h_scales = o;   o = up256(o + (fp8 ? sizeof(float) * tk * (c.d_ff / 128) : 0));
   L.hs = o;         o = up256(o + ab * (size_t)c.T * c.d_ff_shared);
   L.hs_scales = o;  o = up256(o + (fp8 ? sizeof(float) * (size_t)c.T * (c.d_ff_shared / 128) : 0));
-  L.xq = o;         o = up256(o + (fp8 && c.d_ff_shared ? (size_t)c.T * c.d : 0));
-  L.xq_scales = o;  o = up256(o + (fp8 && c.d_ff_shared ? sizeof(float) * (size_t)c.T * (c.d / 128) : 0));
+  L.xq = o;         o = up256(o + (fp8 ? (size_t)c.T * c.d : 0));
+  L.xq_scales = o;  o = up256(o + (fp8 ? sizeof(float) * (size_t)c.T * (c.d / 128) : 0));
   L.run_start = o;  o = up256(o + sizeof(int32_t) * (size_t)c.R * c.E);
   L.run_pre = o;    o = up256(o + sizeof(int32_t) * (size_t)c.R * c.E);
+  L.src_tok = o;    o = up256(o + sizeof(int32_t) * (size_t)c.R * c.R * cap_of(c));
+  L.tok_list = o;   o = up256(o + sizeof(int32_t) * tk);
   L.total = o;
   return L;
 }
@@ -144,10 +151,8 @@ int moe_validate(const moe_cfg* cfg) {
   return MOE_OK;
 }
 
-int moe_query_sizes(const moe_cfg* cfg, moe_sizes* out) {
-  MOE_CHECK_CFG(cfg);
-  if (!out) return MOE_ERR_INVALID_ARG;
-  const moe_cfg& c = *cfg;
+namespace {
+void fill_sizes(const moe_cfg& c, moe_sizes* out) {
   const int cap = cap_of(c);
   out->cap = cap;
   out->recv_rows = (int64_t)c.R * c.R * cap;
@@ -156,6 +161,95 @@ int moe_query_sizes(const moe_cfg* cfg, moe_sizes* out) {
       c.act_dtype == MOE_FP8_E4M3 ? (size_t)out->recv_rows * (c.d / 128) * sizeof(float) : 0;
   out->ebuf_bytes = (size_t)out->recv_rows * c.d * 2;
   out->ws_bytes = ws_layout(c).total;
+}
+}  // namespace
+
+int moe_query_sizes(const moe_cfg* cfg, moe_sizes* out) {
+  MOE_CHECK_CFG(cfg);
+  if (!out) return MOE_ERR_INVALID_ARG;
+  fill_sizes(*cfg, out);
+  return MOE_OK;
+}
+
+int moe_query_sizes_placed(const moe_cfg* cfg, int32_t slots_per_rank, moe_sizes* out) {
+  MOE_CHECK_CFG(cfg);
+  if (!out || slots_per_rank < 1 || (long long)slots_per_rank * cfg->R < cfg->E)
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)slots_per_rank * cfg->R > 1024) return MOE_ERR_UNSUPPORTED;
+  moe_placement p{};
+  p.slots_per_rank = slots_per_rank;
+  const moe_cfg cs = slot_cfg(*cfg, &p);
+  const int rc = validate(cs);
+  if (rc != MOE_OK) return rc;
+  fill_sizes(cs, out);
+  return MOE_OK;
+}
+
+int moe_place_experts(int32_t E, int32_t R, int32_t S, const double* load, int32_t max_copies,
+                      int32_t* slot_expert, int32_t* n_copies, int32_t* copy_slot) {
+  if (!load || !slot_expert || !n_copies || !copy_slot) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || R < 1 || S < 1 || max_copies < 1) return MOE_ERR_INVALID_ARG;
+  const long long G = (long long)R * S;
+  if (G < E || G > (1 << 20)) return MOE_ERR_INVALID_ARG;
+  for (int e = 0; e < E; ++e)
+    if (!(load[e] >= 0.0) || !isfinite(load[e])) return MOE_ERR_INVALID_ARG;
+  // copies: each spare slot to the largest load per copy (first maximum: lower expert)
+  for (int e = 0; e < E; ++e) n_copies[e] = 1;
+  for (long long spare = G - E; spare > 0; --spare) {
+    int best = 0;
+    double best_share = load[0] / n_copies[0];
+    for (int e = 1; e < E; ++e) {
+      const double share = load[e] / n_copies[e];
+      if (share > best_share) {
+        best = e;
+        best_share = share;
+      }
+    }
+    if (++n_copies[best] > max_copies) return MOE_ERR_INVALID_ARG;
+  }
+  // the copies in placement order: share descending, then expert, then copy ascending
+  struct Copy {
+    double share;
+    int e, c, rank;
+  };
+  Copy* list = static_cast<Copy*>(malloc(sizeof(Copy) * (size_t)G));
+  double* rank_load = static_cast<double*>(calloc((size_t)R, sizeof(double)));
+  int* rank_fill = static_cast<int*>(calloc((size_t)R, sizeof(int)));
+  if (!list || !rank_load || !rank_fill) {
+    free(list);
+    free(rank_load);
+    free(rank_fill);
+    return MOE_ERR_INVALID_ARG;
+  }
+  long long n = 0;
+  for (int e = 0; e < E; ++e)
+    for (int c = 0; c < n_copies[e]; ++c) list[n++] = Copy{load[e] / n_copies[e], e, c, -1};
+  std::stable_sort(list, list + n, [](const Copy& a, const Copy& b) { return a.share > b.share; });
+  // largest first onto the least-loaded rank with a free slot (first minimum: lower rank)
+  for (long long i = 0; i < n; ++i) {
+    int r_min = -1;
+    for (int r = 0; r < R; ++r)
+      if (rank_fill[r] < S && (r_min < 0 || rank_load[r] < rank_load[r_min])) r_min = r;
+    list[i].rank = r_min;
+    rank_load[r_min] += list[i].share;
+    ++rank_fill[r_min];
+  }
+  // slots of a rank in (expert, copy) order: sort by (rank, expert, copy)
+  std::sort(list, list + n, [](const Copy& a, const Copy& b) {
+    if (a.rank != b.rank) return a.rank < b.rank;
+    if (a.e != b.e) return a.e < b.e;
+    return a.c < b.c;
+  });
+  for (long long p = 0; p < G; ++p) slot_expert[p] = list[p].e;
+  for (long long i = 0; i < (long long)E * max_copies; ++i) copy_slot[i] = -1;
+  for (int e = 0; e < E; ++e) n_copies[e] = 0;
+  for (long long p = 0; p < G; ++p) {
+    const int e = slot_expert[p];
+    copy_slot[(long long)e * max_copies + n_copies[e]++] = static_cast<int32_t>(p);
+  }
+  free(list);
+  free(rank_load);
+  free(rank_fill);
   return MOE_OK;
 }
 
@@ -178,7 +272,7 @@ int moe_route(const moe_cfg* cfg, const void* x, const float* w_gate, const floa
 
 int moe_dispatch(const moe_cfg* cfg, const void* x, const int32_t* topk_idx, void* recv,
                  float* recv_scales, int32_t* counts, int32_t* row_of, int32_t* src_tok,
-                 cudaStream_t stream) {
+                 uint32_t* status, cudaStream_t stream) {
   MOE_CHECK_CFG(cfg);
   MOE_NEED(x);
   MOE_NEED(topk_idx);
@@ -187,8 +281,9 @@ int moe_dispatch(const moe_cfg* cfg, const void* x, const int32_t* topk_idx, voi
   MOE_NEED(row_of);
   MOE_OPT(src_tok);
   if (cfg->act_dtype == MOE_FP8_E4M3) MOE_NEED(recv_scales);
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_MISALIGNED;
   cudaError_t e = launch_dispatch(*cfg, x, topk_idx, recv, recv_scales, counts, row_of, src_tok,
-                                  stream);
+                                  status, stream);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
@@ -232,41 +327,218 @@ int moe_expert_ffn(const moe_cfg* cfg, const void* recv, const float* recv_scale
 }
 
 int moe_combine(const moe_cfg* cfg, const void* ebuf, const int32_t* row_of,
-                const float* topk_w, const void* shared_out, void* y, cudaStream_t stream) {
+                const float* topk_w, const void* shared_out, void* y, uint32_t* status,
+                cudaStream_t stream) {
   MOE_CHECK_CFG(cfg);
   MOE_NEED(ebuf);
   MOE_NEED(row_of);
   MOE_NEED(topk_w);
   MOE_OPT(shared_out);
   MOE_NEED(y);
-  cudaError_t e = launch_combine(*cfg, ebuf, row_of, topk_w, shared_out, y, stream);
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_MISALIGNED;
+  cudaError_t e = launch_combine(*cfg, ebuf, row_of, topk_w, shared_out, y, status, stream);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
+
+namespace {
+
+// The layer on `stream` with the variants of opts (see moe_layer_ex). Pointers are checked by
+// the caller.
+int layer_impl(const moe_cfg& c0, const moe_layer_opts& o, const void* x, const float* w_gate,
+               const float* bias, const moe_weights* w, int32_t* topk_idx, float* topk_w,
+               void* recv, float* recv_scales, int32_t* counts, int32_t* row_of, void* ebuf,
+               void* shared_out, void* y, void* ws, cudaStream_t stream,
+               const cudaEvent_t* events) {
+  // with a placement every stage after the router works on the slots (c), the router on the
+  // experts (c0)
+  const moe_cfg c = slot_cfg(c0, o.placement);
+  const WsLayout L = ws_layout(c);
+  char* wsp = static_cast<char*>(ws);
+  const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
+  const bool gather = (o.flags & MOE_OPT_GATHER_X) != 0;
+  const bool side = (o.flags & MOE_OPT_SHARED_SIDE_STREAM) != 0 && c.d_ff_shared > 0;
+  int32_t* src_tok = gather ? reinterpret_cast<int32_t*>(wsp + L.src_tok) : nullptr;
+  auto rec = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(events[i], stream) : cudaSuccess;
+  };
+  // Without stage events every kernel after the first follows a kernel of this call directly
+  // and is launched programmatically (its CTAs become resident while the previous kernel
+  // runs; measured on the DSV3 layer: 20 us less per step at T = 64, 39 us at T = 4096). With
+  // events, each stage starts after its event as usual, so the events time the stages
+  // themselves.
+  const bool pdl = events == nullptr;
+  const StageRange layer_range("moe_layer");
+  cudaError_t e = rec(0);
+  bool quantised = false;
+  if (e == cudaSuccess && side) {
+    // the shared expert's input first (e4m3), then its two GEMMs on the side stream
+    const StageRange r("shared_expert_side");
+    if (fp8) {
+      e = launch_quant_x(c, L, x, wsp, stream, false);
+      quantised = true;
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(o.fork_event, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(o.side_stream, o.fork_event, 0);
+    FfnPart sp;
+    sp.routed = false;
+    sp.ctas = o.side_ctas > 0 ? o.side_ctas : 16;
+    sp.weight_experts = c0.E;
+    for (int stg = 0; stg < 2 && e == cudaSuccess; ++stg)
+      e = launch_ffn_gemm(c, L, stg, recv, recv_scales, x, *w, ebuf, shared_out, wsp,
+                          o.side_stream, stg == 1, sp);
+    if (e == cudaSuccess) e = cudaEventRecord(o.join_event, o.side_stream);
+  }
+  if (e == cudaSuccess) {
+    const StageRange r("route");
+    e = launch_route(c0, x, w_gate, bias, topk_idx, topk_w,
+                     reinterpret_cast<float*>(wsp + L.partials),
+                     reinterpret_cast<uint32_t*>(wsp + L.status), stream, pdl && !side,
+                     c.d_ff_shared && !side ? w->ws13 : nullptr,
+                     (size_t)2 * c.d_ff_shared * c.d * act_bytes(c));
+  }
+  if (e == cudaSuccess) e = rec(1);
+  if (e == cudaSuccess) {
+    const StageRange r("dispatch");
+    e = launch_dispatch(c0, x, topk_idx, gather ? nullptr : recv, recv_scales, counts, row_of,
+                        src_tok, reinterpret_cast<uint32_t*>(wsp + L.status), stream, pdl, false,
+                        o.placement);
+  }
+  if (e == cudaSuccess) e = rec(2);
+  if (e == cudaSuccess) {
+    const StageRange r("ffn_setup");
+    e = launch_ffn_setup(c, L, counts, x, wsp, stream, pdl, src_tok, !quantised);
+  }
+  if (e == cudaSuccess) e = rec(3);
+  FfnPart mp;
+  mp.shared = !side;
+  mp.src_tok = src_tok;
+  mp.group_expert = o.placement ? o.placement->slot_expert : nullptr;
+  mp.weight_experts = c0.E;
+  if (e == cudaSuccess) {
+    const StageRange r("ffn_gate_up");
+    e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, pdl,
+                        mp);
+  }
+  if (e == cudaSuccess) e = rec(4);
+  if (e == cudaSuccess) {
+    const StageRange r("ffn_down");
+    e = launch_ffn_gemm(c, L, 1, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, pdl,
+                        mp);
+  }
+  if (e == cudaSuccess) e = rec(5);
+  if (e == cudaSuccess && side) e = cudaStreamWaitEvent(stream, o.join_event, 0);
+  if (e == cudaSuccess) {
+    const StageRange r("combine");
+    e = launch_combine(c, ebuf, row_of, topk_w, c.d_ff_shared ? shared_out : nullptr, y,
+                       reinterpret_cast<uint32_t*>(wsp + L.status), stream, pdl && !side);
+  }
+  if (e == cudaSuccess) e = rec(6);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+#define MOE_LAYER_CHECKS(gather)              \
+  MOE_CHECK_CFG(cfg);                         \
+  const moe_cfg& c = *cfg;                    \
+  MOE_NEED(x);                                \
+  MOE_NEED(w_gate);                           \
+  MOE_NEED(bias);                             \
+  MOE_NEED(topk_idx);                         \
+  MOE_NEED(topk_w);                           \
+  if (!(gather)) MOE_NEED(recv);              \
+  MOE_NEED(counts);                           \
+  MOE_NEED(row_of);                           \
+  MOE_NEED(ebuf);                             \
+  MOE_NEED(y);                                \
+  MOE_NEED(ws);                               \
+  if (!w) return MOE_ERR_INVALID_ARG;         \
+  MOE_NEED(w->w13);                           \
+  MOE_NEED(w->w2);                            \
+  const bool fp8 = c.act_dtype == MOE_FP8_E4M3; \
+  if (fp8) {                                  \
+    if (!(gather)) MOE_NEED(recv_scales);     \
+    MOE_NEED(w->w13_scales);                  \
+    MOE_NEED(w->w2_scales);                   \
+  }                                           \
+  if (c.d_ff_shared) {                        \
+    MOE_NEED(w->ws13);                        \
+    MOE_NEED(w->ws2);                         \
+    MOE_NEED(shared_out);                     \
+    if (fp8) {                                \
+      MOE_NEED(w->ws13_scales);               \
+      MOE_NEED(w->ws2_scales);                \
+    }                                         \
+  }
 
 int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const float* bias,
               const moe_weights* w, int32_t* topk_idx, float* topk_w, void* recv,
               float* recv_scales, int32_t* counts, int32_t* row_of, void* ebuf,
               void* shared_out, void* y, void* ws, cudaStream_t stream,
               const cudaEvent_t* events) {
+  MOE_LAYER_CHECKS(false);
+  const moe_layer_opts o{};
+  return layer_impl(c, o, x, w_gate, bias, w, topk_idx, topk_w, recv, recv_scales, counts,
+                    row_of, ebuf, shared_out, y, ws, stream, events);
+}
+
+int moe_layer_ex(const moe_cfg* cfg, const moe_layer_opts* opts, const void* x,
+                 const float* w_gate, const float* bias, const moe_weights* w, int32_t* topk_idx,
+                 float* topk_w, void* recv, float* recv_scales, int32_t* counts, int32_t* row_of,
+                 void* ebuf, void* shared_out, void* y, void* ws, cudaStream_t stream,
+                 const cudaEvent_t* events) {
+  const moe_layer_opts o = opts ? *opts : moe_layer_opts{};
+  if (o.flags & ~(MOE_OPT_GATHER_X | MOE_OPT_SHARED_SIDE_STREAM)) return MOE_ERR_INVALID_ARG;
+  MOE_LAYER_CHECKS((o.flags & MOE_OPT_GATHER_X) != 0);
+  if (o.placement) {
+    const moe_placement& p = *o.placement;
+    if (p.slots_per_rank < 1 || (long long)p.slots_per_rank * c.R < c.E || p.max_copies < 1)
+      return MOE_ERR_INVALID_ARG;
+    if ((long long)p.slots_per_rank * c.R > 1024) return MOE_ERR_UNSUPPORTED;
+    MOE_NEED(p.slot_expert);
+    MOE_NEED(p.n_copies);
+    MOE_NEED(p.copy_slot);
+    const int rc = validate(slot_cfg(c, &p));
+    if (rc != MOE_OK) return rc;
+  }
+  if ((o.flags & MOE_OPT_SHARED_SIDE_STREAM) && c.d_ff_shared) {
+    if (!o.side_stream || !o.fork_event || !o.join_event || o.side_stream == stream)
+      return MOE_ERR_INVALID_ARG;
+    if (o.side_ctas < 0 || o.side_ctas > 4096) return MOE_ERR_INVALID_ARG;
+  }
+  return layer_impl(c, o, x, w_gate, bias, w, topk_idx, topk_w, recv, recv_scales, counts,
+                    row_of, ebuf, shared_out, y, ws, stream, events);
+}
+
+int moe_dispatch_index(const moe_cfg* cfg, const int32_t* topk_idx, int32_t* counts,
+                       int32_t* row_of, int32_t* src_tok, uint32_t* status,
+                       cudaStream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_NEED(topk_idx);
+  MOE_NEED(counts);
+  MOE_NEED(row_of);
+  MOE_NEED(src_tok);
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_MISALIGNED;
+  cudaError_t e = launch_dispatch(*cfg, nullptr, topk_idx, nullptr, nullptr, counts, row_of,
+                                  src_tok, status, stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+int moe_expert_ffn_gather(const moe_cfg* cfg, const void* x, const int32_t* counts,
+                          const int32_t* src_tok, const moe_weights* w, void* ebuf,
+                          void* shared_out, void* ws, cudaStream_t stream) {
   MOE_CHECK_CFG(cfg);
   const moe_cfg& c = *cfg;
   MOE_NEED(x);
-  MOE_NEED(w_gate);
-  MOE_NEED(bias);
-  MOE_NEED(topk_idx);
-  MOE_NEED(topk_w);
-  MOE_NEED(recv);
   MOE_NEED(counts);
-  MOE_NEED(row_of);
+  MOE_NEED(src_tok);
   MOE_NEED(ebuf);
-  MOE_NEED(y);
   MOE_NEED(ws);
   if (!w) return MOE_ERR_INVALID_ARG;
   MOE_NEED(w->w13);
   MOE_NEED(w->w2);
   const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
   if (fp8) {
-    MOE_NEED(recv_scales);
     MOE_NEED(w->w13_scales);
     MOE_NEED(w->w2_scales);
   }
@@ -281,52 +553,15 @@ int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const floa
   }
   const WsLayout L = ws_layout(c);
   char* wsp = static_cast<char*>(ws);
-  auto rec = [&](int i) -> cudaError_t {
-    return events ? cudaEventRecord(events[i], stream) : cudaSuccess;
-  };
-  // Without stage events every kernel after the first follows a kernel of this call directly
-  // and is launched programmatically (its CTAs become resident while the previous kernel
-  // runs; measured on the DSV3 layer: 20 us less per step at T = 64, 39 us at T = 4096). With
-  // events, each stage starts after its event as usual, so the events time the stages
-  // themselves.
-  const bool pdl = events == nullptr;
-  const StageRange layer_range("moe_layer");
-  cudaError_t e = rec(0);
-  if (e == cudaSuccess) {
-    const StageRange r("route");
-    e = launch_route(c, x, w_gate, bias, topk_idx, topk_w,
-                     reinterpret_cast<float*>(wsp + L.partials),
-                     reinterpret_cast<uint32_t*>(wsp + L.status), stream, pdl,
-                     c.d_ff_shared ? w->ws13 : nullptr,
-                     (size_t)2 * c.d_ff_shared * c.d * act_bytes(c));
-  }
-  if (e == cudaSuccess) e = rec(1);
-  if (e == cudaSuccess) {
-    const StageRange r("dispatch");
-    e = launch_dispatch(c, x, topk_idx, recv, recv_scales, counts, row_of, nullptr, stream, pdl);
-  }
-  if (e == cudaSuccess) e = rec(2);
-  if (e == cudaSuccess) {
-    const StageRange r("ffn_setup");
-    e = launch_ffn_setup(c, L, counts, x, wsp, stream, pdl);
-  }
-  if (e == cudaSuccess) e = rec(3);
-  if (e == cudaSuccess) {
-    const StageRange r("ffn_gate_up");
-    e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, pdl);
-  }
-  if (e == cudaSuccess) e = rec(4);
-  if (e == cudaSuccess) {
-    const StageRange r("ffn_down");
-    e = launch_ffn_gemm(c, L, 1, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, pdl);
-  }
-  if (e == cudaSuccess) e = rec(5);
-  if (e == cudaSuccess) {
-    const StageRange r("combine");
-    e = launch_combine(c, ebuf, row_of, topk_w, c.d_ff_shared ? shared_out : nullptr, y, stream,
-                       pdl);
-  }
-  if (e == cudaSuccess) e = rec(6);
+  FfnPart part;
+  part.src_tok = src_tok;
+  cudaError_t e = launch_ffn_setup(c, L, counts, x, wsp, stream, false, src_tok);
+  if (e == cudaSuccess)
+    e = launch_ffn_gemm(c, L, 0, nullptr, nullptr, x, *w, ebuf, shared_out, wsp, stream, true,
+                        part);
+  if (e == cudaSuccess)
+    e = launch_ffn_gemm(c, L, 1, nullptr, nullptr, x, *w, ebuf, shared_out, wsp, stream, true,
+                        part);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 

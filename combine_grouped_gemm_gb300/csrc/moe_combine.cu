@@ -11,19 +11,27 @@ namespace {
 
 // Block (token t, column slice), 128 threads, one 16-byte vector (8 columns) per thread per
 // iteration: k gathered row vectors and the shared row, fp32 FMAs in selection order.
+// Rows outside [0, recv_rows) are skipped: a negative one silently (a choice the dispatch
+// skipped), one past the buffer with MOE_DEV_BOUNDS in status (input the dispatch never writes).
 __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ ebuf,
                                                       const int32_t* __restrict__ row_of,
                                                       const float* __restrict__ topk_w,
                                                       const uint4* __restrict__ shared_out,
                                                       uint4* __restrict__ y, int d, int k,
-                                                      int slice_vecs) {
+                                                      int slice_vecs, long long recv_rows,
+                                                      uint32_t* status) {
   __shared__ int32_t rows[32];
   pdl_wait();
   pdl_trigger();
   __shared__ float wts[32];
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
-    rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+    int row = row_of[(size_t)t * k + threadIdx.x];
+    if (row >= recv_rows) {
+      if (blockIdx.y == 0) raise_status(status, MOE_DEV_BOUNDS);
+      row = -1;
+    }
+    rows[threadIdx.x] = row;
     wts[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
   }
   __syncthreads();
@@ -79,7 +87,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
 
 cudaError_t launch_combine(const moe_cfg& c, const void* ebuf, const int32_t* row_of,
                            const float* topk_w, const void* shared_out, void* y,
-                           cudaStream_t st, bool pdl) {
+                           uint32_t* status, cudaStream_t st, bool pdl) {
   const int vpr = c.d / 8;
   int nslice = 1;
   while (c.T * nslice < 2 * 152 && vpr / (nslice * 2) >= 128) nslice *= 2;
@@ -89,7 +97,7 @@ cudaError_t launch_combine(const moe_cfg& c, const void* ebuf, const int32_t* ro
   return launch_kernel(combine_kernel, grid, dim3(128), 0, st, pdl,
                        static_cast<const uint4*>(ebuf), row_of, topk_w,
                        static_cast<const uint4*>(shared_out), static_cast<uint4*>(y), c.d, c.k,
-                       slice_vecs);
+                       slice_vecs, (long long)c.R * c.R * cap_of(c), status);
 }
 
 }  // namespace moe

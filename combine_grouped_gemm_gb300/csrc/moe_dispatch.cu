@@ -18,22 +18,61 @@ namespace {
 
 constexpr int kIndexWarps = 16;
 
+// Choice i of token t is dispatched when its expert is in [0, E) and differs from the token's
+// earlier choices; otherwise (input that the router never produces) it is skipped, its row_of
+// is -1 and MOE_DEV_BOUNDS is reported. With distinct experts a token sends at most
+// min(k, E/R) rows to one destination rank, so no segment can overflow.
+// The token's k choices are read once (independent loads, then L1-resident local copies) and
+// the valid ones marked in a bit mask.
+constexpr int kMaxK = 32;
+__device__ __forceinline__ uint32_t load_choices(const int32_t* __restrict__ topk_idx, int t,
+                                                 int k, int E, int* ids) {
+  const int32_t* row = topk_idx + (size_t)t * k;
+  for (int i = 0; i < k; ++i) ids[i] = __ldg(row + i);
+  uint32_t valid = 0;
+  for (int i = 0; i < k; ++i) {
+    const int e = ids[i];
+    bool ok = e >= 0 && e < E;
+    for (int j = 0; j < i && ok; ++j) ok = ids[j] != e;
+    valid |= static_cast<uint32_t>(ok) << i;
+  }
+  return valid;
+}
+
+// Where the rows of a source go when the experts are placed on slots (redundant experts):
+// slot p of G = R*S holds expert slot_expert[p] on rank p / S; expert e has n_copies[e] copies
+// in slots copy_slot[e][0..], ascending. Source s sends its j-th row of expert e (in token
+// order) to copy (j + s) mod n_copies[e], as that copy's row j / n_copies[e]: each source splits
+// its own rows of an expert evenly over the copies, with no count exchanged.
+struct Placement {
+  const int32_t* slot_expert;   // [G]
+  const int32_t* n_copies;      // [E]
+  const int32_t* copy_slot;     // [E][max_copies]
+  int max_copies;
+  int slots_per_rank;           // S
+};
+
 // One CTA per logical source rank. Shared memory: run[16][E] (per-warp histogram, then
 // running per-warp positions), mask[16][E] (lanes of the current 32-token chunk that chose e),
-// off[E] (first row of expert e inside its segment).
+// cnt[E] (the source's rows per expert), off[G] (first row of each slot inside its segment;
+// the slots are the experts themselves, G = E, without a placement).
 __global__ void __launch_bounds__(kIndexWarps * 32) dispatch_index_kernel(
     const int32_t* __restrict__ topk_idx, int32_t* __restrict__ counts,
     int32_t* __restrict__ row_of, int32_t* __restrict__ src_tok, uint32_t* status, int T, int E,
-    int k, int R, int cap) {
+    int k, int R, int cap, Placement pl) {
   extern __shared__ int32_t smi[];
+  const bool placed = pl.slot_expert != nullptr;
+  const int G = placed ? R * pl.slots_per_rank : E;
   int32_t* run = smi;                                              // [16][E]
   uint32_t* mask = reinterpret_cast<uint32_t*>(run + kIndexWarps * E);  // [16][E]
-  int32_t* off = reinterpret_cast<int32_t*>(mask + kIndexWarps * E);    // [E]
+  int32_t* cnt = reinterpret_cast<int32_t*>(mask + kIndexWarps * E);    // [E]
+  int32_t* off = cnt + E;                                               // [G]
   pdl_wait();
   pdl_trigger();
 
   const int s = blockIdx.x;
-  const int Ts = T / R, Er = E / R;
+  const int Ts = T / R;
+  const int Sg = G / R;   // slots per destination rank
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per = (Ts + kIndexWarps - 1) / kIndexWarps;
   const int my0 = s * Ts + min(Ts, warp * per);
@@ -43,15 +82,13 @@ __global__ void __launch_bounds__(kIndexWarps * 32) dispatch_index_kernel(
   __syncthreads();
 
   // 1. per-warp histograms of this source's choices
-  for (int t = my0 + lane; t < my1; t += 32)
-    for (int i = 0; i < k; ++i) {
-      const int e = topk_idx[(size_t)t * k + i];
-      if (e < 0 || e >= E) {
-        raise_status(status, MOE_DEV_BOUNDS);
-        continue;
-      }
-      atomicAdd(&run[warp * E + e], 1);
-    }
+  int ids[kMaxK];
+  for (int t = my0 + lane; t < my1; t += 32) {
+    const uint32_t valid = load_choices(topk_idx, t, k, E, ids);
+    if (valid != (k >= 32 ? 0xffffffffu : (1u << k) - 1u)) raise_status(status, MOE_DEV_BOUNDS);
+    for (int i = 0; i < k; ++i)
+      if ((valid >> i) & 1u) atomicAdd(&run[warp * E + ids[i]], 1);
+  }
   __syncthreads();
 
   // 2. per expert: exclusive prefix over warps (each warp's first position), total count
@@ -62,17 +99,36 @@ __global__ void __launch_bounds__(kIndexWarps * 32) dispatch_index_kernel(
       run[w * E + e] = acc;
       acc += h;
     }
-    off[e] = acc;
-    counts[(size_t)s * E + e] = acc;
+    cnt[e] = acc;
+  }
+  __syncthreads();
+  // rows of this source per slot: an expert's own count, or its copy's share (rows j with
+  // j = c0 mod n, c0 = (c - s) mod n, for copy c of n)
+  for (int p = threadIdx.x; p < G; p += blockDim.x) {
+    int v = 0;
+    if (!placed) {
+      v = cnt[p];
+    } else {
+      const int e = pl.slot_expert[p];
+      if (e >= 0 && e < E) {
+        const int n = max(1, pl.n_copies[e]);
+        int c = 0;
+        while (c < n && c < pl.max_copies && pl.copy_slot[(size_t)e * pl.max_copies + c] != p) ++c;
+        const int c0 = ((c - s) % n + n) % n;
+        v = cnt[e] > c0 ? (cnt[e] - c0 + n - 1) / n : 0;
+      }
+    }
+    off[p] = v;
+    counts[(size_t)s * G + p] = v;
   }
   __syncthreads();
 
-  // 3. exclusive scan of counts over experts, restarted at every destination rank
+  // 3. exclusive scan of counts over slots, restarted at every destination rank
   if (warp == 0) {
-    const int chunk = (E + 31) / 32;
-    const int a = min(E, lane * chunk), b = min(E, (lane + 1) * chunk);
+    const int chunk = (G + 31) / 32;
+    const int a = min(G, lane * chunk), b = min(G, (lane + 1) * chunk);
     int local = 0;
-    for (int e = a; e < b; ++e) local += off[e];
+    for (int p = a; p < b; ++p) local += off[p];
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -80,20 +136,20 @@ __global__ void __launch_bounds__(kIndexWarps * 32) dispatch_index_kernel(
       if (lane >= o) incl += n;
     }
     int ex = incl - local;
-    for (int e = a; e < b; ++e) {
-      const int c = off[e];
-      off[e] = ex;  // global exclusive sum for now
+    for (int p = a; p < b; ++p) {
+      const int c = off[p];
+      off[p] = ex;  // global exclusive sum for now
       ex += c;
     }
   }
   __syncthreads();
-  // rebase to the destination rank's first expert (read all bases before overwriting)
+  // rebase to the destination rank's first slot (read all bases before overwriting)
   int base_vals[4];
   int nb = 0;
-  for (int e = threadIdx.x; e < E && nb < 4; e += blockDim.x) base_vals[nb++] = off[(e / Er) * Er];
+  for (int p = threadIdx.x; p < G && nb < 4; p += blockDim.x) base_vals[nb++] = off[(p / Sg) * Sg];
   __syncthreads();
   nb = 0;
-  for (int e = threadIdx.x; e < E && nb < 4; e += blockDim.x) off[e] -= base_vals[nb++];
+  for (int p = threadIdx.x; p < G && nb < 4; p += blockDim.x) off[p] -= base_vals[nb++];
   __syncthreads();
 
   // 4. stable positions: walk the warp's tokens in chunks of 32, one token per lane
@@ -101,31 +157,48 @@ __global__ void __launch_bounds__(kIndexWarps * 32) dispatch_index_kernel(
   for (int base = my0; base < my1; base += 32) {
     const int t = base + lane;
     const bool valid = t < my1;
+    const uint32_t vmask = valid ? load_choices(topk_idx, t, k, E, ids) : 0u;
     if (valid)
-      for (int i = 0; i < k; ++i) {
-        const int e = topk_idx[(size_t)t * k + i];
-        if (e >= 0 && e < E) atomicOr(&mask[warp * E + e], 1u << lane);
-      }
+      for (int i = 0; i < k; ++i)
+        if ((vmask >> i) & 1u) atomicOr(&mask[warp * E + ids[i]], 1u << lane);
     __syncwarp();
     if (valid)
       for (int i = 0; i < k; ++i) {
-        const int e = topk_idx[(size_t)t * k + i];
-        if (e < 0 || e >= E) {
+        if (!((vmask >> i) & 1u)) {
           row_of[(size_t)t * k + i] = -1;
           continue;
         }
+        const int e = ids[i];
         const uint32_t m = mask[warp * E + e];
-        const int pos = run[warp * E + e] + __popc(m & lt);
-        const int r = e / Er;
-        const int row = (r * R + s) * cap + off[e] + pos;
+        const int j = run[warp * E + e] + __popc(m & lt);   // the source's j-th row of e
+        int p = e, pos = j;
+        if (placed) {
+          const int n = max(1, pl.n_copies[e]);
+          const int c = (j + s) % n;
+          p = c < pl.max_copies ? pl.copy_slot[(size_t)e * pl.max_copies + c] : -1;
+          pos = j / n;
+          if (p < 0 || p >= G) {
+            raise_status(status, MOE_DEV_BOUNDS);
+            row_of[(size_t)t * k + i] = -1;
+            continue;
+          }
+        }
+        const int r = p / Sg;
+        const int in_seg = off[p] + pos;
+        if (in_seg < 0 || in_seg >= cap) {   // cannot happen with distinct experts; never written
+          raise_status(status, MOE_DEV_BOUNDS);
+          row_of[(size_t)t * k + i] = -1;
+          continue;
+        }
+        const int row = (r * R + s) * cap + in_seg;
         row_of[(size_t)t * k + i] = row;
         if (src_tok) src_tok[row] = t;
       }
     __syncwarp();
     if (valid)
       for (int i = 0; i < k; ++i) {
-        const int e = topk_idx[(size_t)t * k + i];
-        if (e < 0 || e >= E) continue;
+        if (!((vmask >> i) & 1u)) continue;
+        const int e = ids[i];
         const uint32_t m = mask[warp * E + e];
         if (m != 0u && (m & lt) == 0u) {  // lowest lane that chose e in this chunk
           run[warp * E + e] += __popc(m);
@@ -239,22 +312,32 @@ cudaError_t launch_quant_rows_e4m3(const void* x, int T, int d, void* out, float
 
 cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk_idx, void* recv,
                             float* recv_scales, int32_t* counts, int32_t* row_of,
-                            int32_t* src_tok, cudaStream_t st, bool pdl) {
-  const int cap = cap_of(c);
+                            int32_t* src_tok, uint32_t* status, cudaStream_t st, bool pdl,
+                            bool clear_src_tok, const moe_placement* placement) {
+  const moe_cfg cs = slot_cfg(c, placement);   // the receive layout is over the slots
+  const int cap = cap_of(cs);
   cudaError_t err;
-  if (src_tok) {
-    err = cudaMemsetAsync(src_tok, 0xff, sizeof(int32_t) * (size_t)c.R * c.R * cap, st);
+  const bool memset_first = src_tok && clear_src_tok;
+  if (memset_first) {
+    err = cudaMemsetAsync(src_tok, 0xff, sizeof(int32_t) * (size_t)cs.R * cs.R * cap, st);
     if (err != cudaSuccess) return err;
   }
-  const size_t smem = sizeof(int32_t) * (size_t)(2 * kIndexWarps + 1) * c.E;
+  Placement pl{};
+  if (placement) {
+    pl.slot_expert = placement->slot_expert;
+    pl.n_copies = placement->n_copies;
+    pl.copy_slot = placement->copy_slot;
+    pl.max_copies = placement->max_copies;
+    pl.slots_per_rank = placement->slots_per_rank;
+  }
+  const size_t smem = sizeof(int32_t) * ((size_t)(2 * kIndexWarps + 1) * c.E + cs.E);
   err = ensure_smem_limit(reinterpret_cast<const void*>(dispatch_index_kernel), smem);
   if (err != cudaSuccess) return err;
   // (after the memset the index kernel is launched as usual: its predecessor is not a kernel)
   err = launch_kernel(dispatch_index_kernel, dim3(c.R), dim3(kIndexWarps * 32), smem, st,
-                      pdl && !src_tok,
-                      topk_idx, counts, row_of, src_tok, static_cast<uint32_t*>(nullptr), c.T,
-                      c.E, c.k, c.R, cap);
-  if (err != cudaSuccess) return err;
+                      pdl && !memset_first,
+                      topk_idx, counts, row_of, src_tok, status, c.T, c.E, c.k, c.R, cap, pl);
+  if (err != cudaSuccess || recv == nullptr) return err;   // gather mode: indices only
 
   int nslice, slice_vecs;
   copy_grid(c.T, c.d, &nslice, &slice_vecs);

@@ -39,7 +39,9 @@ namespace {
 // Tile schedule (one CTA)
 // ---------------------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;             // upper bound; launched with E rounded up to 32
-constexpr size_t kPlanStageBytes = 48 * 1024;   // counts table staged in shared memory up to this
+// counts table staged in shared memory up to this: the 48 KB a kernel gets without an opt-in,
+// less 1 KB for the kernel's static shared memory (warp sums and rank bases, 388 bytes)
+constexpr size_t kPlanStageBytes = 47 * 1024;
 constexpr int kPlanFusedRows = 1024;            // fill the row list in the plan CTA up to this T*k
 
 // Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, <= 1024).
@@ -74,10 +76,13 @@ __device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
 
 // row_list[c] for every compact row c: its expert by binary search on the compact offsets,
 // its source run by a scan of the run prefixes, then the run's receive row plus the position.
+// In gather mode (src_tok != nullptr) tok_list[c] also receives the compact row's token.
 __device__ __forceinline__ void fill_rows(const int32_t* grp_n, const int32_t* grp_off,
                                           const int32_t* run_start, const int32_t* run_pre,
                                           int32_t* row_list, uint32_t* status, int E, int R,
-                                          int tk, int first, int stride) {
+                                          int tk, int first, int stride,
+                                          const int32_t* src_tok, int32_t* tok_list,
+                                          long long recv_rows, int T) {
   for (int c = first; c < tk; c += stride) {
     int lo = 0, hi = E - 1;  // last expert whose compact offset is <= c
     while (lo < hi) {
@@ -92,11 +97,21 @@ __device__ __forceinline__ void fill_rows(const int32_t* grp_n, const int32_t* g
     if (p < 0 || p >= grp_n[e]) {
       raise_status(status, MOE_DEV_BOUNDS);
       row_list[c] = -1;
+      if (tok_list) tok_list[c] = -1;
       continue;
     }
     int s = 0;
     while (s + 1 < R && run_pre[(s + 1) * E + e] <= p) ++s;
-    row_list[c] = run_start[s * E + e] + (p - run_pre[s * E + e]);
+    const int row = run_start[s * E + e] + (p - run_pre[s * E + e]);
+    row_list[c] = row;
+    if (tok_list) {
+      int t = (row >= 0 && row < recv_rows) ? src_tok[row] : -1;
+      if (t < 0 || t >= T) {
+        raise_status(status, MOE_DEV_BOUNDS);
+        t = -1;
+      }
+      tok_list[c] = t;
+    }
   }
 }
 
@@ -109,7 +124,8 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     const int32_t* __restrict__ counts, int32_t* __restrict__ grp_n, int32_t* __restrict__ grp_off,
     int32_t* __restrict__ n_tiles, Tile* __restrict__ tiles, int32_t* __restrict__ run_start,
     int32_t* __restrict__ run_pre, int32_t* __restrict__ row_list, uint32_t* status, int E, int R,
-    int cap, int bn, int max_tiles, int tk) {
+    int cap, int bn, int max_tiles, int tk, const int32_t* __restrict__ src_tok,
+    int32_t* __restrict__ tok_list, int T) {
   __shared__ int warp_sums[33];
   __shared__ int rank_base[64];
   extern __shared__ int32_t cnt_s[];   // counts staged once: [R][E] when it fits, else unused
@@ -191,7 +207,7 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
   if (tk <= kPlanFusedRows) {
     __syncthreads();
     fill_rows(grp_n, grp_off, run_start, run_pre, row_list, status, E, R, tk, threadIdx.x,
-              blockDim.x);
+              blockDim.x, src_tok, tok_list, (long long)R * R * cap, T);
   }
 }
 
@@ -201,11 +217,15 @@ __global__ void __launch_bounds__(256) ffn_rows_kernel(const int32_t* __restrict
                                                        const int32_t* __restrict__ run_start,
                                                        const int32_t* __restrict__ run_pre,
                                                        int32_t* __restrict__ row_list,
-                                                       uint32_t* status, int E, int R, int tk) {
+                                                       uint32_t* status, int E, int R, int tk,
+                                                       const int32_t* __restrict__ src_tok,
+                                                       int32_t* __restrict__ tok_list,
+                                                       long long recv_rows, int T) {
   pdl_wait();
   pdl_trigger();
   fill_rows(grp_n, grp_off, run_start, run_pre, row_list, status, E, R, tk,
-            blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
+            blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x, src_tok, tok_list,
+            recv_rows, T);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -235,7 +255,21 @@ struct GemmArgs {
   const uint8_t* gather_base;  // gate/up: receive buffer (routed token rows are gathered)
   long long gather_ld;         // bytes per receive row
   uint32_t* status;
+  const int32_t* group_expert; // expert whose weights group g uses (nullptr: expert g)
+  int n_experts;               // experts in the weight tensors
 };
+
+// The expert whose weight rows a routed group reads: itself, or the expert its slot holds
+// (redundant experts). An entry outside [0, n_experts) is reported and replaced by expert 0, so
+// no weight read leaves the tensors.
+__device__ __forceinline__ int weight_expert(const int32_t* group_expert, int g, int n_experts,
+                                             uint32_t* status) {
+  if (!group_expert) return g;
+  const int e = group_expert[g];
+  if (e >= 0 && e < n_experts) return e;
+  raise_status(status, MOE_DEV_BOUNDS);
+  return 0;
+}
 
 struct Unit {
   int g;       // routed expert, or -1 for the shared expert
@@ -372,7 +406,9 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
       const bool sh = t.g < 0;
       const CUtensorMap* amap = sh ? &mapAs : &mapA;
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
-      const int arow0 = (sh ? 0 : t.g * a.a_rows_routed) + t.m * 128;
+      const int we = sh ? 0 : weight_expert(a.group_expert, t.g, a.n_experts,
+                                             lane == 0 ? a.status : nullptr);
+      const int arow0 = (sh ? 0 : we * a.a_rows_routed) + t.m * 128;
       const int arow1 = arow0 + (sh ? a.a_up_shared : a.a_up_routed);
       // Token rows of the unit. Routed gate/up rows are gathered: a small tile (decode) by
       // this warp with tile::gather4 (lane j loads rows 4j..4j+3; a missing row repeats a valid
@@ -608,13 +644,14 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
 
 template <int STAGE, int BN, int STAGES>
 cudaError_t run_gemm(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mAs,
-                     const CUtensorMap& mB, const CUtensorMap& mBs, cudaStream_t st, bool pdl) {
+                     const CUtensorMap& mB, const CUtensorMap& mBs, cudaStream_t st, bool pdl,
+                     int ctas) {
   using S = GemmShape<STAGE, BN, STAGES>;
   auto kern = ffn_gemm_bf16_kernel<STAGE, BN, STAGES>;
   const cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), S::SMEM);
   if (err != cudaSuccess) return err;
-  return launch_kernel(kern, dim3(sm_count()), dim3(GemmThreads<STAGE>::kAll), S::SMEM, st, pdl,
-                       a, mA, mAs, mB, mBs);
+  return launch_kernel(kern, dim3(ctas > 0 ? ctas : sm_count()), dim3(GemmThreads<STAGE>::kAll),
+                       S::SMEM, st, pdl, a, mA, mAs, mB, mBs);
 }
 
 }  // namespace
@@ -698,11 +735,17 @@ int sm_count() {
 }
 
 
+cudaError_t launch_quant_x(const moe_cfg& c, const WsLayout& L, const void* x, char* ws,
+                           cudaStream_t st, bool pdl) {
+  return launch_quant_rows_e4m3(x, c.T, c.d, ws + L.xq, reinterpret_cast<float*>(ws + L.xq_scales),
+                                st, pdl);
+}
+
 cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
-                             const void* x, char* ws, cudaStream_t st, bool pdl) {
-  if (c.act_dtype == MOE_FP8_E4M3 && c.d_ff_shared) {
-    const cudaError_t err = launch_quant_rows_e4m3(
-        x, c.T, c.d, ws + L.xq, reinterpret_cast<float*>(ws + L.xq_scales), st, pdl);
+                             const void* x, char* ws, cudaStream_t st, bool pdl,
+                             const int32_t* src_tok, bool quantise) {
+  if (quantise && c.act_dtype == MOE_FP8_E4M3 && (c.d_ff_shared || src_tok)) {
+    const cudaError_t err = launch_quant_x(c, L, x, ws, st, pdl);
     if (err != cudaSuccess) return err;
   }
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
@@ -717,7 +760,8 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
       reinterpret_cast<int32_t*>(ws + L.n_tiles), reinterpret_cast<Tile*>(ws + L.tiles),
       reinterpret_cast<int32_t*>(ws + L.run_start), reinterpret_cast<int32_t*>(ws + L.run_pre),
       reinterpret_cast<int32_t*>(ws + L.row_list), status, c.E, c.R, cap_of(c), L.bn,
-      L.max_tiles, tk);
+      L.max_tiles, tk, src_tok, src_tok ? reinterpret_cast<int32_t*>(ws + L.tok_list) : nullptr,
+      c.T);
   if (err != cudaSuccess) return err;
   if (tk <= kPlanFusedRows) return cudaSuccess;   // the plan CTA filled the row list
   const int blocks = (tk + 255) / 256 < 4 * 152 ? (tk + 255) / 256 : 4 * 152;
@@ -725,18 +769,25 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
       ffn_rows_kernel, dim3(blocks), dim3(256), 0, st, pdl, grp_n, grp_off,
       reinterpret_cast<const int32_t*>(ws + L.run_start),
       reinterpret_cast<const int32_t*>(ws + L.run_pre), reinterpret_cast<int32_t*>(ws + L.row_list),
-      status, c.E, c.R, tk);
+      status, c.E, c.R, tk, src_tok,
+      src_tok ? reinterpret_cast<int32_t*>(ws + L.tok_list) : nullptr,
+      (long long)c.R * c.R * cap_of(c), c.T);
 }
 
 cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                             const float* recv_scales, const void* x, const moe_weights& w,
-                            void* ebuf, void* shared_out, char* ws, cudaStream_t st, bool pdl) {
+                            void* ebuf, void* shared_out, char* ws, cudaStream_t st, bool pdl,
+                            const FfnPart& part) {
   if (c.act_dtype == MOE_FP8_E4M3)
-    return launch_ffn_gemm_e4m3(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st, pdl);
+    return launch_ffn_gemm_e4m3(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st, pdl,
+                                part);
   const int cap = cap_of(c);
   const long long recv_rows = (long long)c.R * c.R * cap;
   const int F = c.d_ff, Fs = c.d_ff_shared, d = c.d, tk = c.T * c.k;
   const bool has_shared = Fs > 0;
+  // gather mode: the gate/up stage reads routed token rows from x, by token, through the
+  // schedule's token list (the down stage still writes ebuf at the receive rows)
+  const bool gather = part.src_tok != nullptr && stage == 0;
 
   GemmArgs a{};
   a.tiles = reinterpret_cast<const Tile*>(ws + L.tiles);
@@ -748,6 +799,9 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
   a.T = c.T;
   a.status = reinterpret_cast<uint32_t*>(ws + L.status);
   a.n_shared_tiles = has_shared ? (c.T + L.bn - 1) / L.bn : 0;
+  a.group_expert = part.group_expert;
+  const int n_w = part.weight_experts > 0 ? part.weight_experts : c.E;
+  a.n_experts = n_w;
 
   CUtensorMap mA, mAs, mB, mBs;
   bool ok = true;
@@ -762,12 +816,16 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
     a.out_shared = has_shared ? static_cast<void*>(ws + L.hs) : nullptr;
     a.ld_routed = F;
     a.ld_shared = Fs;
-    a.gather_base = static_cast<const uint8_t*>(recv);
+    a.gather_base = static_cast<const uint8_t*>(gather ? x : recv);
     a.gather_ld = 2ll * d;
     a.box_routed = 1;
     a.box_shared = c.T < L.bn ? c.T : L.bn;
-    ok &= make_tensor_map_2d(&mA, w.w13, 2, d, (uint64_t)c.E * 2 * F, 128);
-    ok &= make_tensor_map_2d(&mB, recv, 2, d, recv_rows, 1);
+    if (gather) {
+      a.row_list = reinterpret_cast<const int32_t*>(ws + L.tok_list);
+      a.recv_rows = c.T;
+    }
+    ok &= make_tensor_map_2d(&mA, w.w13, 2, d, (uint64_t)n_w * 2 * F, 128);
+    ok &= make_tensor_map_2d(&mB, gather ? x : recv, 2, d, gather ? c.T : recv_rows, 1);
     if (has_shared) {
       ok &= make_tensor_map_2d(&mAs, w.ws13, 2, d, 2ull * Fs, 128);
       ok &= make_tensor_map_2d(&mBs, x, 2, d, c.T, a.box_shared);
@@ -786,7 +844,7 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
     // the down projection's input rows are contiguous: one box of up to bn rows per k-step
     a.box_routed = tk < L.bn ? tk : L.bn;
     a.box_shared = c.T < L.bn ? c.T : L.bn;
-    ok &= make_tensor_map_2d(&mA, w.w2, 2, F, (uint64_t)c.E * d, 128);
+    ok &= make_tensor_map_2d(&mA, w.w2, 2, F, (uint64_t)n_w * d, 128);
     ok &= make_tensor_map_2d(&mB, ws + L.h, 2, F, tk, a.box_routed);
     if (has_shared) {
       if (Fs != F) return cudaErrorNotSupported;  // one K loop length per launch
@@ -800,13 +858,18 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
     mBs = mB;
   }
   if (!ok) return cudaErrorInvalidValue;
+  if (!part.routed) a.mt_routed = 0;   // this launch runs the shared expert's units only
+  if (!part.shared) {                  // ... or the routed experts' units only
+    a.mt_shared = 0;
+    a.n_shared_tiles = 0;
+  }
 
   if (L.bn == 64) {
-    if (stage == 0) return run_gemm<0, 64, 5>(a, mA, mAs, mB, mBs, st, pdl);
-    return run_gemm<1, 64, 8>(a, mA, mAs, mB, mBs, st, pdl);
+    if (stage == 0) return run_gemm<0, 64, 5>(a, mA, mAs, mB, mBs, st, pdl, part.ctas);
+    return run_gemm<1, 64, 8>(a, mA, mAs, mB, mBs, st, pdl, part.ctas);
   }
-  if (stage == 0) return run_gemm<0, 128, 4>(a, mA, mAs, mB, mBs, st, pdl);
-  return run_gemm<1, 128, 6>(a, mA, mAs, mB, mBs, st, pdl);
+  if (stage == 0) return run_gemm<0, 128, 4>(a, mA, mAs, mB, mBs, st, pdl, part.ctas);
+  return run_gemm<1, 128, 6>(a, mA, mAs, mB, mBs, st, pdl, part.ctas);
 }
 
 }  // namespace moe

@@ -60,7 +60,20 @@ struct Fp8Args {
   const uint8_t* gather_base;   // gate/up: receive buffer (routed token rows are gathered)
   long long gather_ld;          // bytes per receive row
   uint32_t* status;
+  const int32_t* group_expert;  // expert whose weights group g uses (nullptr: expert g)
+  int n_experts;                // experts in the weight tensors
 };
+
+// The expert whose weights a routed group reads (see the bf16 kernels): itself, or the expert
+// its slot holds; an entry outside [0, n_experts) is reported and replaced by expert 0.
+__device__ __forceinline__ int weight_expert8(const int32_t* group_expert, int g, int n_experts,
+                                              uint32_t* status) {
+  if (!group_expert) return g;
+  const int e = group_expert[g];
+  if (e >= 0 && e < n_experts) return e;
+  raise_status(status, MOE_DEV_BOUNDS);
+  return 0;
+}
 
 struct Unit8 {
   int g, n0, nlen, m;
@@ -221,7 +234,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       const bool sh = t.g < 0;
       const CUtensorMap* amap = sh ? &mapAs : &mapA;
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
-      const int brow0 = (sh ? 0 : t.g * a.b_rows_routed) + t.m * kStep;
+      const int we = sh ? 0 : weight_expert8(a.group_expert, t.g, a.n_experts,
+                                              lane == 0 ? a.status : nullptr);
+      const int brow0 = (sh ? 0 : we * a.b_rows_routed) + t.m * kStep;
       const int brow1 = brow0 + (sh ? a.b_up_shared : a.b_up_routed);
       // Token rows: routed gate/up rows are gathered by the gather warps (cp.async); the shared
       // expert's rows (x, contiguous) and the down projection's rows (h, contiguous) are one
@@ -355,8 +370,9 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
       }
       const float* xs = sh ? a.a_sc_shared : a.a_sc_routed;
       const long long xs_ld = sh ? a.T : a.a_sc_ld_routed;
+      const int we = sh ? 0 : weight_expert8(a.group_expert, t.g, a.n_experts, nullptr);
       const float* wsc = (sh ? a.w_sc_shared
-                             : a.w_sc_routed + (size_t)t.g * (a.b_rows_routed / 128) * kb_n) +
+                             : a.w_sc_routed + (size_t)we * (a.b_rows_routed / 128) * kb_n) +
                          (size_t)t.m * (kStep / 128) * kb_n;
       const int w_up = (sh ? a.b_up_shared : a.b_up_routed) / 128 * kb_n;
       const uint8_t* gsrc = a.gather_base + j * 16;
@@ -559,11 +575,15 @@ __global__ void __launch_bounds__(Fp8Threads<STAGE>::kAll, 1)
 
 cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                                  const float* recv_scales, const moe_weights& w, void* ebuf,
-                                 void* shared_out, char* ws, cudaStream_t st, bool pdl) {
+                                 void* shared_out, char* ws, cudaStream_t st, bool pdl,
+                                 const FfnPart& part) {
   const int cap = cap_of(c);
   const long long recv_rows = (long long)c.R * c.R * cap;
   const int F = c.d_ff, Fs = c.d_ff_shared, d = c.d, tk = c.T * c.k;
   const bool has_shared = Fs > 0;
+  // gather mode: the gate/up stage reads routed token rows (and their scales) from x quantised
+  // once per token, by token, through the schedule's token list
+  const bool gather = part.src_tok != nullptr && stage == 0;
   Fp8Args a{};
   a.tiles = reinterpret_cast<const Tile*>(ws + L.tiles);
   a.n_tiles = reinterpret_cast<const int32_t*>(ws + L.n_tiles);
@@ -574,6 +594,9 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
   a.status = reinterpret_cast<uint32_t*>(ws + L.status);
   a.n_shared_tiles = has_shared ? (c.T + 127) / 128 : 0;
   a.out_rows_routed = recv_rows;
+  a.group_expert = part.group_expert;
+  const int n_w = part.weight_experts > 0 ? part.weight_experts : c.E;
+  a.n_experts = n_w;
   if (recv_rows > 0x7fffffffLL) return cudaErrorNotSupported;   // 32-bit scale-row strides
   CUtensorMap mA, mAs, mB, mBs;
   bool ok = true;
@@ -600,8 +623,16 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     a.gather_ld = d;
     a.box_routed = 1;
     a.box_shared = c.T < 128 ? c.T : 128;
-    ok &= make_tensor_map_2d(&mA, recv, 1, d, recv_rows, 1);
-    ok &= make_tensor_map_2d(&mB, w.w13, 1, d, (uint64_t)c.E * 2 * F, 128);
+    if (gather) {
+      a.row_list = reinterpret_cast<const int32_t*>(ws + L.tok_list);
+      a.a_rows_routed = c.T;
+      a.a_sc_routed = reinterpret_cast<const float*>(ws + L.xq_scales);
+      a.a_sc_ld_routed = c.T;
+      a.gather_base = reinterpret_cast<const uint8_t*>(ws + L.xq);
+    }
+    ok &= make_tensor_map_2d(&mA, gather ? static_cast<const void*>(ws + L.xq) : recv, 1, d,
+                             gather ? c.T : recv_rows, 1);
+    ok &= make_tensor_map_2d(&mB, w.w13, 1, d, (uint64_t)n_w * 2 * F, 128);
     if (has_shared) {
       ok &= make_tensor_map_2d(&mAs, ws + L.xq, 1, d, c.T, a.box_shared);
       ok &= make_tensor_map_2d(&mBs, w.ws13, 1, d, 2ull * Fs, 128);
@@ -628,7 +659,7 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     a.box_routed = tk < 128 ? tk : 128;
     a.box_shared = c.T < 128 ? c.T : 128;
     ok &= make_tensor_map_2d(&mA, ws + L.h, 1, F, tk, a.box_routed);
-    ok &= make_tensor_map_2d(&mB, w.w2, 1, F, (uint64_t)c.E * d, 128);
+    ok &= make_tensor_map_2d(&mB, w.w2, 1, F, (uint64_t)n_w * d, 128);
     if (has_shared) {
       ok &= make_tensor_map_2d(&mAs, ws + L.hs, 1, Fs, c.T, a.box_shared);
       ok &= make_tensor_map_2d(&mBs, w.ws2, 1, Fs, d, 128);
@@ -639,28 +670,34 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
     mBs = mB;
   }
   if (!ok) return cudaErrorInvalidValue;
+  if (!part.routed) a.mt_routed = 0;   // this launch runs the shared expert's units only
+  if (!part.shared) {                  // ... or the routed experts' units only
+    a.mt_shared = 0;
+    a.n_shared_tiles = 0;
+  }
+  const dim3 grid(part.ctas > 0 ? part.ctas : sm_count());
   cudaError_t err;
   if (stage == 0) {
     using S = Fp8Shape<2, 4>;
     auto kern = ffn_gemm_e4m3_kernel<0, 2, 4>;
     err = ensure_smem_limit(reinterpret_cast<const void*>(kern), S::SMEM);
     if (err != cudaSuccess) return err;
-    return launch_kernel(kern, dim3(sm_count()), dim3(Fp8Threads<0>::kAll), S::SMEM, st, pdl, a,
-                         mA, mAs, mB, mBs);
+    return launch_kernel(kern, grid, dim3(Fp8Threads<0>::kAll), S::SMEM, st, pdl, a, mA, mAs,
+                         mB, mBs);
   } else if (d % 256 == 0) {
     using S = Fp8Shape<2, 4>;
     auto kern = ffn_gemm_e4m3_kernel<1, 2, 4>;
     err = ensure_smem_limit(reinterpret_cast<const void*>(kern), S::SMEM);
     if (err != cudaSuccess) return err;
-    return launch_kernel(kern, dim3(sm_count()), dim3(Fp8Threads<1>::kAll), S::SMEM, st, pdl, a,
-                         mA, mAs, mB, mBs);
+    return launch_kernel(kern, grid, dim3(Fp8Threads<1>::kAll), S::SMEM, st, pdl, a, mA, mAs,
+                         mB, mBs);
   } else {
     using S = Fp8Shape<1, 6>;
     auto kern = ffn_gemm_e4m3_kernel<1, 1, 6>;
     err = ensure_smem_limit(reinterpret_cast<const void*>(kern), S::SMEM);
     if (err != cudaSuccess) return err;
-    return launch_kernel(kern, dim3(sm_count()), dim3(Fp8Threads<1>::kAll), S::SMEM, st, pdl, a,
-                         mA, mAs, mB, mBs);
+    return launch_kernel(kern, grid, dim3(Fp8Threads<1>::kAll), S::SMEM, st, pdl, a, mA, mAs,
+                         mB, mBs);
   }
 }
 

@@ -35,22 +35,40 @@ struct WsLayout {
   size_t h_scales;    // e4m3: fp32, block-major [d_ff/128][T*k]
   size_t hs;          // shared expert intermediate: [T][d_ff_shared]
   size_t hs_scales;   // e4m3: fp32, block-major [d_ff_shared/128][T]
-  size_t xq;          // e4m3: quantised shared-expert input [T][d]
+  size_t xq;          // e4m3: x quantised once per token [T][d] (shared-expert input; the
+                      // routed rows' source in gather mode)
   size_t xq_scales;   // e4m3: fp32, block-major [d/128][T]
   size_t run_start;   // int32 [R][E]: receive row of the first row source s sent expert e
   size_t run_pre;     // int32 [R][E]: rows of expert e from sources before s
+  size_t src_tok;     // int32 [R*R*cap]: token of each filled receive row (gather mode)
+  size_t tok_list;    // int32 [T*k]: token of each compact row (gather mode)
   size_t total;
   int bn;             // token-tile width of the expert GEMMs
   int max_tiles;      // bound on routed tiles: E + T*k/bn
 };
 
 int validate(const moe_cfg& c);
+// Records e as this host thread's last CUDA error (moe_last_cuda_error) and returns
+// MOE_ERR_CUDA: every entry point reports a failed CUDA call through it.
+int cuda_fail(cudaError_t e);
 WsLayout ws_layout(const moe_cfg& c);
 inline int cap_of(const moe_cfg& c) {
   int Er = c.E / c.R, Ts = c.T / c.R;
   return Ts * (c.k < Er ? c.k : Er);
 }
 inline size_t act_bytes(const moe_cfg& c) { return c.act_dtype == MOE_FP8_E4M3 ? 1 : 2; }
+
+// The configuration seen by the stages after the router when the experts are placed on slots:
+// E becomes the slot count R * slots_per_rank (one group of the grouped GEMMs per slot). The
+// group fields are not used after the router; they are set to one group so the copy validates.
+inline moe_cfg slot_cfg(const moe_cfg& c, const moe_placement* p) {
+  if (!p) return c;
+  moe_cfg s = c;
+  s.E = c.R * p->slots_per_rank;
+  s.n_group = 1;
+  s.topk_group = 1;
+  return s;
+}
 
 // launch_route's selection kernel also starts pulling [warm, warm + warm_bytes) into L2 (the
 // shared expert's gate/up weights, which the gate/up GEMM reads first) while the rest of the
@@ -65,28 +83,59 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
                          cudaStream_t st, bool pdl = false, const void* warm = nullptr,
                          size_t warm_bytes = 0);
 
+// With recv == nullptr only the index pass runs (counts, row_of, src_tok): the gather mode,
+// whose expert GEMMs read token rows straight from x. clear_src_tok: fill src_tok with -1
+// first (the stage call's contract for rows that receive nothing).
+// status: nullable device word that index errors are OR-ed into (MOE_DEV_BOUNDS).
+// placement: NULL, or the experts' slots; counts and the receive rows are then over the slots.
 cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk_idx, void* recv,
                             float* recv_scales, int32_t* counts, int32_t* row_of,
-                            int32_t* src_tok, cudaStream_t st, bool pdl = false);
+                            int32_t* src_tok, uint32_t* status, cudaStream_t st,
+                            bool pdl = false, bool clear_src_tok = true,
+                            const moe_placement* placement = nullptr);
 
+// Entries of row_of outside [0, recv_rows) are skipped and reported in status (nullable).
 cudaError_t launch_combine(const moe_cfg& c, const void* ebuf, const int32_t* row_of,
                            const float* topk_w, const void* shared_out, void* y,
-                           cudaStream_t st, bool pdl = false);
+                           uint32_t* status, cudaStream_t st, bool pdl = false);
 
-// Expert FFN set-up: tile schedule from counts (+ e4m3 quantisation of the shared input).
+// Which parts of the expert stage a GEMM launch covers, and where its routed token rows come
+// from.
+struct FfnPart {
+  bool routed = true;        // the routed experts' units
+  bool shared = true;        // the shared expert's units (when it exists)
+  const int32_t* src_tok = nullptr;  // gather mode: token of each receive row; the routed rows
+                                     // are read from x (e4m3: x quantised per token) instead of
+                                     // from the receive buffer
+  int ctas = 0;              // grid size (0: one CTA per SM)
+  const int32_t* group_expert = nullptr;  // the expert whose weights each group uses (slots of
+                                          // a placement); nullptr: group g is expert g
+  int weight_experts = 0;    // experts in the weight tensors (0: the cfg's E)
+};
+
+// Expert FFN set-up: tile schedule from counts (+ e4m3 quantisation of x for the shared expert
+// and, in gather mode, the routed rows). src_tok != nullptr: gather mode (the schedule also
+// lists each compact row's token).
+// quantise == false: the e4m3 quantisation of x was enqueued already (launch_quant_x).
 cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
-                             const void* x, char* ws, cudaStream_t st, bool pdl = false);
+                             const void* x, char* ws, cudaStream_t st, bool pdl = false,
+                             const int32_t* src_tok = nullptr, bool quantise = true);
+
+// e4m3: x quantised once per token into the workspace (xq, xq_scales).
+cudaError_t launch_quant_x(const moe_cfg& c, const WsLayout& L, const void* x, char* ws,
+                           cudaStream_t st, bool pdl = false);
 
 // The two grouped GEMMs. stage: 0 = gate/up with the SwiGLU epilogue, 1 = down projection.
 cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                             const float* recv_scales, const void* x, const moe_weights& w,
                             void* ebuf, void* shared_out, char* ws, cudaStream_t st,
-                            bool pdl = false);
+                            bool pdl = false, const FfnPart& part = FfnPart());
 
 // e4m3 grouped GEMMs (non-swapped, per-128-K-block scale promotion), same stages.
 cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                                  const float* recv_scales, const moe_weights& w, void* ebuf,
-                                 void* shared_out, char* ws, cudaStream_t st, bool pdl = false);
+                                 void* shared_out, char* ws, cudaStream_t st, bool pdl,
+                                 const FfnPart& part);
 
 // 1x128 e4m3 quantisation of T rows of width d (the dispatch's rule), row t -> row t.
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int d, void* out, float* scales,

@@ -37,5 +37,5 @@ extern "C" int moe_selftest_wait(void* ws, int64_t limit_ns, cudaStream_t stream
   moe::selftest_wait_kernel<<<1, 64, 0, stream>>>(static_cast<uint32_t*>(ws),
                                                  static_cast<uint64_t>(limit_ns));
   const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(e);
 }

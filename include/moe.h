@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 /* Return codes */
 #define MOE_OK 0
@@ -137,8 +137,10 @@ int moe_route(const moe_cfg* cfg, const void* x, const float* w_gate, const floa
  * callers only. Arguments and results are those of moe_route. Limits and behaviour:
  *  - returns MOE_ERR_UNSUPPORTED when 16 * T * E exceeds 2^21 floats (T*E > 131072, e.g. more
  *    than 512 tokens at 256 experts); nothing is enqueued then;
- *  - the first call on a device looks up the array's device address with that device current
- *    (cudaGetSymbolAddress); make that first call before any stream capture;
+ *  - the first call in each device context looks up the array's device address with that
+ *    device current (cudaGetSymbolAddress) and caches it under the context's ID; make that
+ *    first call before any stream capture (a context made after a device reset looks it up
+ *    again on its own first call);
  *  - it allocates nothing (no cudaMalloc, no cudaFree, no allocating library call);
  *  - every call shares the array and leaves its contents behind; each call writes every entry
  *    it reads, so nothing needs clearing, but calls whose kernels overlap on the GPU (other
@@ -161,12 +163,14 @@ int moe_route_noalloc(const moe_cfg* cfg, const void* x, const float* w_gate, co
  * Outputs recv (see moe_sizes), recv_scales (e4m3 only, else NULL), counts int32 [R][E],
  * row_of int32 [T][k] (receive row of each choice), src_tok int32 [recv_rows] (token of each
  * row, -1 for empty rows; NULL to skip). Receive rows that get no token are not written.
- * Entries of topk_idx outside [0, E) are skipped (their row_of is -1). Repeated experts within
- * a token are not checked: they can overflow a segment and write past recv. moe_route never
- * produces either. */
+ * status: NULL, or a device uint32 (for instance the workspace's status word: pass ws) into
+ * which MOE_DEV_BOUNDS is OR-ed when topk_idx breaks its contract. A choice whose expert is
+ * outside [0, E), or repeats an earlier choice of the same token, is skipped: its row_of is
+ * -1, it is not counted, and nothing is written for it. With distinct experts no segment can
+ * overflow; every receive row written lies inside recv. moe_route never produces either. */
 int moe_dispatch(const moe_cfg* cfg, const void* x, const int32_t* topk_idx, void* recv,
                  float* recv_scales, int32_t* counts, int32_t* row_of, int32_t* src_tok,
-                 cudaStream_t stream);
+                 uint32_t* status, cudaStream_t stream);
 
 /* Expert FFNs ("Serving Mixture-of-Experts", Expert Parallelism Mechanics, expert compute: a
  * grouped GEMM over the rows each expert received; Hot-Expert Skew section and
@@ -191,10 +195,13 @@ int moe_expert_ffn(const moe_cfg* cfg, const void* recv, const float* recv_scale
  * fp32 in selection order. ebuf bf16 [recv_rows][d]; row_of int32 [T][k]; topk_w fp32
  * [T][k]; shared_out bf16 [T][d] or NULL; y bf16 [T][d]. Passing the receive buffer as ebuf
  * (bf16) gives route_scale * x: the identity-expert check of the dispatch/combine pair.
- * Negative entries of row_of are skipped. Entries at or past recv_rows are not checked: they
- * read past ebuf. moe_dispatch's row_of holds only valid rows and -1. */
+ * Negative entries of row_of are skipped (a choice the dispatch skipped). Entries at or past
+ * recv_rows are skipped too and reported: MOE_DEV_BOUNDS is OR-ed into status (NULL, or a
+ * device uint32 such as the workspace's status word). Nothing outside ebuf is read.
+ * moe_dispatch's row_of holds only valid rows and -1. */
 int moe_combine(const moe_cfg* cfg, const void* ebuf, const int32_t* row_of,
-                const float* topk_w, const void* shared_out, void* y, cudaStream_t stream);
+                const float* topk_w, const void* shared_out, void* y, uint32_t* status,
+                cudaStream_t stream);
 
 /* The whole layer on one stream: moe_route, moe_dispatch, moe_expert_ffn, moe_combine.
  * Buffers as in those calls (src_tok is not produced). events: NULL, or MOE_LAYER_EVENTS
@@ -212,6 +219,104 @@ int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const floa
               float* recv_scales, int32_t* counts, int32_t* row_of, void* ebuf,
               void* shared_out, void* y, void* ws, cudaStream_t stream,
               const cudaEvent_t* events);
+
+/* ---------------------------------------------------------------------------------------
+ * Variants of the layer ("next" steps of the method, each optional)
+ * ------------------------------------------------------------------------------------- */
+
+/* Gather mode. The dispatch writes only the indices (counts, row_of and the token of each
+ * receive row); the gate/up GEMM reads each routed row straight from x by token instead of
+ * from a receive-buffer copy, so the copy pass and its Tk*d bytes of writes and reads are
+ * skipped. The grouped GEMMs reading pushed rows in place is the design of "One-Sided
+ * Expert-Parallel All-to-All ..." (abstract); "DeepSeek MoE Serving: Where Expert-Parallel
+ * All-to-All Time Goes" (groundy) counts the extra pass of a two-sided scheme as HBM traffic.
+ * On one GPU the source rank's own x is the pushed buffer, read in place. e4m3: x is
+ * quantised once per token (not once per (token, expert) row) with the dispatch's rule. The
+ * expert outputs still land in ebuf at the receive rows, so the combine is unchanged and every
+ * output equals moe_layer's. recv and recv_scales are not used (may be NULL). */
+#define MOE_OPT_GATHER_X 1u
+/* Shared expert on a second stream ("Serving Mixture-of-Experts", Hot-Expert Skew: the shared
+ * expert's FFN needs no all-to-all, so it is free work to overlap with the dispatch; DeepEP
+ * section: hook-based overlap). Its GEMMs depend only on x: they are enqueued on side_stream
+ * after fork_event (recorded on `stream` at the start of the layer), limited to side_ctas CTAs
+ * (one per SM, leaving the other SMs to the router and dispatch), and the combine waits on
+ * join_event (recorded on side_stream after them). On one GPU this partitions the SMs between
+ * the two streams. The events are created by the caller (cudaEventDisableTiming is enough). */
+#define MOE_OPT_SHARED_SIDE_STREAM 2u
+
+/* Redundant experts ("Serving Mixture-of-Experts", Hot-Expert Skew: place extra copies of the
+ * busiest experts on under-loaded ranks and let the dispatch split their tokens across the
+ * copies; exercise 5: each copy takes an equal share of its expert's load, copies assigned
+ * largest first to the least-loaded rank). Each of the R logical ranks has slots_per_rank
+ * expert slots, G = R * slots_per_rank >= E in all; slot p lives on rank p / slots_per_rank.
+ * The dispatch sends source s's j-th row of expert e (in token order) to copy
+ * (j + s) mod n_copies[e]: every source splits its own rows of an expert evenly over the
+ * copies without exchanging counts. All arrays are DEVICE int32 arrays owned by the caller,
+ * normally filled from moe_place_experts:
+ *  slot_expert [G]: the expert each slot holds; n_copies [E]: copies of each expert (>= 1);
+ *  copy_slot [E][max_copies]: the slots of each expert's copies in ascending order.
+ * With a placement the receive layout and counts are over the G slots (counts [R][G],
+ * cap = (T/R) * min(k, slots_per_rank); moe_query_sizes_placed gives the sizes). */
+typedef struct moe_placement {
+  int32_t slots_per_rank;
+  int32_t max_copies;
+  const int32_t* slot_expert;
+  const int32_t* n_copies;
+  const int32_t* copy_slot;
+} moe_placement;
+
+typedef struct moe_layer_opts {
+  uint32_t flags;           /* MOE_OPT_* bits; 0 = moe_layer */
+  cudaStream_t side_stream; /* MOE_OPT_SHARED_SIDE_STREAM: the shared expert's stream */
+  cudaEvent_t fork_event;   /* recorded on `stream`, waited on by side_stream */
+  cudaEvent_t join_event;   /* recorded on side_stream, waited on by `stream` */
+  int32_t side_ctas;        /* CTAs of each shared-expert GEMM; 0 = 16 */
+  const moe_placement* placement; /* NULL, or redundant experts placed on slots (above) */
+} moe_layer_opts;
+
+/* Placement of E experts on R ranks of slots_per_rank slots from estimated loads (host
+ * function, no GPU; load: host double [E], e.g. a moving average of past counts). The
+ * R*slots_per_rank - E spare slots take one more copy at a time of the expert with the largest
+ * load per copy (ties: lower expert). Each copy carries load/copies; copies are placed largest
+ * first (ties: lower expert, then lower copy) on the least-loaded rank that has a free slot
+ * (ties: lower rank); a rank's slots are ordered by (expert, copy). Outputs (host int32):
+ * slot_expert [R*slots_per_rank], n_copies [E], copy_slot [E][max_copies] (-1 past a copy
+ * count). Returns MOE_ERR_INVALID_ARG for a NULL pointer, non-positive sizes, a negative or
+ * non-finite load, R*slots_per_rank < E, or an expert needing more than max_copies copies. */
+int moe_place_experts(int32_t E, int32_t R, int32_t slots_per_rank, const double* load,
+                      int32_t max_copies, int32_t* slot_expert, int32_t* n_copies,
+                      int32_t* copy_slot);
+
+/* moe_query_sizes for a layer whose experts are placed on R*slots_per_rank slots. */
+int moe_query_sizes_placed(const moe_cfg* cfg, int32_t slots_per_rank, moe_sizes* out);
+
+/* moe_layer with the variants selected by opts (NULL = moe_layer). Arguments as in moe_layer;
+ * with MOE_OPT_GATHER_X, recv and recv_scales may be NULL. With MOE_OPT_SHARED_SIDE_STREAM and
+ * a shared expert, side_stream, fork_event and join_event must be valid (else
+ * MOE_ERR_INVALID_ARG); stage events are recorded on `stream` only, so the FFN stages then
+ * time the routed experts alone. With a placement, recv, counts, ebuf and ws are sized by
+ * moe_query_sizes_placed and counts is [R][G] over the slots; a slot whose expert lies outside
+ * [0, E) is reported (MOE_DEV_BOUNDS) and computed with expert 0's weights. The layer output
+ * y is moe_layer's in every mode, bit for bit. */
+int moe_layer_ex(const moe_cfg* cfg, const moe_layer_opts* opts, const void* x,
+                 const float* w_gate, const float* bias, const moe_weights* w, int32_t* topk_idx,
+                 float* topk_w, void* recv, float* recv_scales, int32_t* counts, int32_t* row_of,
+                 void* ebuf, void* shared_out, void* y, void* ws, cudaStream_t stream,
+                 const cudaEvent_t* events);
+
+/* The index pass of moe_dispatch alone (gather mode): counts, row_of and src_tok exactly as
+ * moe_dispatch writes them (src_tok required here; receive rows that get no token hold -1),
+ * with no payload copied. status as in moe_dispatch. */
+int moe_dispatch_index(const moe_cfg* cfg, const int32_t* topk_idx, int32_t* counts,
+                       int32_t* row_of, int32_t* src_tok, uint32_t* status,
+                       cudaStream_t stream);
+
+/* moe_expert_ffn in gather mode: the routed rows are read from x by token through src_tok
+ * (from moe_dispatch_index) instead of from a receive buffer. x: bf16 [T][d], required. The
+ * outputs (ebuf at the receive rows, shared_out) equal moe_expert_ffn's. */
+int moe_expert_ffn_gather(const moe_cfg* cfg, const void* x, const int32_t* counts,
+                          const int32_t* src_tok, const moe_weights* w, void* ebuf,
+                          void* shared_out, void* ws, cudaStream_t stream);
 
 /* Sets the device status word in ws to 0 (enqueued on stream). */
 int moe_clear_status(void* ws, cudaStream_t stream);

@@ -75,3 +75,23 @@ def ws_offsets(cfg):
     o["hs"] = up(cur + (4 * tk * (cfg.d_ff // 128) if cfg.act == "fp8" else 0))
     o["bn"] = bn
     return o
+
+
+def half_gap_below_bf16(v):
+    """Half the distance from |v| down to the next smaller bf16 value (v bf16 values as
+    floats): the largest error the rounding of an exact value to v can have made."""
+    v = np.abs(np.asarray(v, dtype=np.float64)).astype(np.float32)
+    bits = v.view(np.uint32) >> 16
+    below = ((np.maximum(bits, 1) - 1).astype(np.uint32) << 16).view(np.float32)
+    return (v.astype(np.float64) - below.astype(np.float64)) / 2.0
+
+
+def format_err(got, exact):
+    """Error of bf16 outputs `got` (as floats) against the exact reference values, relative to
+    the reference RMS, after allowing each output its own rounding to bf16:
+    max(0, |got - exact| - half the bf16 gap below |got|) / rms(exact)."""
+    got = np.asarray(got, dtype=np.float64)
+    exact = np.asarray(exact, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(exact * exact)))
+    excess = np.maximum(0.0, np.abs(got - exact) - half_gap_below_bf16(got))
+    return float(excess.max()) / max(rms, 1e-30)

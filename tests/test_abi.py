@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(moe):
 
 
 def test_abi_version_and_strerror(moe):
-    assert moe.abi_version() == 1
+    assert moe.abi_version() == 2
     for code in range(5):
         assert moe._lib.moe_strerror(code)
     assert b"unknown" in moe._lib.moe_strerror(99)
@@ -86,8 +86,16 @@ def test_null_and_misaligned_pointers_are_rejected_before_any_launch(moe):
     ok = 1 << 20  # an aligned fake address: never dereferenced, checks fail first
     assert L.moe_route(ctypes.byref(c), None, ok, ok, ok, ok, ok, None) == 1
     assert L.moe_route(ctypes.byref(c), ok + 2, ok, ok, ok, ok, ok, None) == 3
-    assert L.moe_combine(ctypes.byref(c), ok, ok, ok, ok + 8, ok, None) == 3
-    assert L.moe_dispatch(ctypes.byref(c), ok, ok, ok, None, ok, None, None, None) == 1
+    assert L.moe_combine(ctypes.byref(c), ok, ok, ok, ok + 8, ok, None, None) == 3
+    assert L.moe_combine(ctypes.byref(c), ok, ok, ok, None, ok, ok + 2, None) == 3  # status
+    assert L.moe_dispatch(ctypes.byref(c), ok, ok, ok, None, ok, None, None, None, None) == 1
+    assert L.moe_dispatch(ctypes.byref(c), ok, ok, ok, None, ok, ok, None, ok + 1, None) == 3
+    assert L.moe_dispatch_index(ctypes.byref(c), ok, ok, ok, None, None, None) == 1
+    assert L.moe_expert_ffn_gather(ctypes.byref(c), ok, ok, None, ctypes.byref(moe.Weights()),
+                                   ok, None, ok, None) == 1
+    # moe_layer_ex: an unknown option bit, or a side stream asked for without stream and events
+    o = moe.LayerOpts(flags=64)
+    assert L.moe_layer_ex(ctypes.byref(c), ctypes.byref(o), *([ok] * 14), None, None) == 1
     w = moe.Weights()
     assert L.moe_expert_ffn(ctypes.byref(c), ok, None, ok, None, ctypes.byref(w), ok, None, ok,
                             None) == 1

@@ -14,8 +14,9 @@ import torch
 
 import oracle
 import synth
-from gpu_util import (bf16_to_f64, device_inputs, expert_getter, host_bits, rel_max_err,
+from gpu_util import (bf16_to_f64, expert_getter, format_err, host_bits, rel_max_err,
                       shared_host, weight_dict)
+from layer_check import check_layer, experts_by_rows, hot_expert_pairs
 
 pytestmark = pytest.mark.gpu
 
@@ -36,27 +37,38 @@ SMALL = synth.MoEConfig("small", T=96, d=384, E=12, k=3, n_group=4, topk_group=2
 # have at most 32 experts per rank, one warp).
 ER64 = synth.MoEConfig("er64", T=64, d=256, E=128, k=4, n_group=4, topk_group=2, d_ff=128,
                        d_ff_shared=128, R=2, route_scale=1.0, seed=11)
+# 64 logical ranks of 3 experts: the counts table (64 x 192 x 4 = 48 KB) is too large to stage
+# in the schedule kernel's shared memory, and a rank's experts do not divide a warp.
+E192_R64 = synth.MoEConfig("e192_r64", T=128, d=256, E=192, k=4, n_group=4, topk_group=2,
+                           d_ff=128, d_ff_shared=128, R=64, route_scale=1.0, seed=19)
 # One expert receives every token (bias +10): several token tiles of one expert.
 HOT = synth.MoEConfig("hot", T=256, d=256, E=16, k=2, n_group=1, topk_group=1, d_ff=256,
                       d_ff_shared=256, R=2, route_scale=1.0, seed=5)
 
-_cache = {}
+_cache = {}       # router inputs per workload
+_wcache = {}      # expert weights per (seed, shapes, format): sweep points share one set
+BIG_KEEP = 4      # DeepSeek-V3-sized weight sets kept at once (<= 23 GB each)
 
 
 def inputs(cfg):
-    """Device inputs for cfg; keeps only the most recent large weight set alive."""
-    key = (cfg.name, cfg.seed, cfg.T, cfg.bias)
-    if key not in _cache:
+    """Device inputs for cfg. Weight sets are shared by workloads that differ only in T; at most
+    BIG_KEEP large ones stay alive."""
+    wkey = (cfg.seed, cfg.E, cfg.d, cfg.d_ff, cfg.d_ff_shared, cfg.w)
+    if wkey not in _wcache:
         big = cfg.d * cfg.d_ff * cfg.E > 10 ** 8
         if big:
-            for k in [k for k in _cache if _cache[k][2]]:
-                del _cache[k]
+            bigs = [k for k in _wcache if _wcache[k][1]]
+            for k in bigs[:max(0, len(bigs) - BIG_KEEP + 1)]:
+                del _wcache[k]
             torch.cuda.empty_cache()
-        inp, W = device_inputs(cfg)
+        _wcache[wkey] = (synth.make_expert_weights(cfg, "cuda"), big)
+    key = (cfg.name, cfg.seed, cfg.T, cfg.bias)
+    if key not in _cache:
+        inp = synth.make_router_inputs(cfg, "cuda")
         if cfg.name == "hot":
             inp["bias"][3] = 10.0
-        _cache[key] = (inp, W, big)
-    return _cache[key][0], _cache[key][1]
+        _cache[key] = inp
+    return _cache[key], _wcache[wkey][0]
 
 
 def run_stages(cfg, inp, W, src_tok=True):
@@ -309,11 +321,11 @@ def _layer_tokens_check(cfg, tokens, inp, W, y):
                               inp["bias"].cpu().numpy(), expert_getter(W, cfg.w == "fp8"),
                               shared_host(W, cfg.w == "fp8"), tokens)
     got = bf16_to_f64(host_bits(y)[tokens])
-    err = rel_max_err(got, bf16_to_f64(ref["y"]))
-    return err
+    return format_err(got, ref["y_exact"])
 
 
-@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, HOT, ER64], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, HOT, ER64, E192_R64],
+                         ids=lambda c: c.name)
 def test_layer_all_tokens(cfg):
     inp, W = inputs(cfg)
     lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
@@ -349,34 +361,83 @@ def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable():
     assert _layer_tokens_check(cfg, np.arange(cfg.T), inp, W, y) <= TOL_BF16
 
 
-@pytest.mark.slow
-@pytest.mark.parametrize("cfg,n", [(synth.CONFIGS["dsv3_decode"], 4),
-                                   (synth.CONFIGS["dsv3_sweep"].with_T(8), 8),
-                                   (synth.CONFIGS["dsv3_sweep"].with_T(1024), 3)],
-                         ids=lambda v: getattr(v, "name", str(v)))
-def test_layer_dsv3_sampled_tokens(cfg, n):
+def _run_layer(cfg):
     inp, W = inputs(cfg)
     lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
     y = lay(inp["x"])
     assert moe().read_status(lay.bufs["ws"]) == 0
-    rng = np.random.default_rng(cfg.T)
-    tokens = np.sort(rng.choice(cfg.T, n, replace=False))
-    assert _layer_tokens_check(cfg, tokens, inp, W, y) <= TOL_BF16
+    return inp, W, lay, y
 
 
 @pytest.mark.slow
-def test_layer_skew_prefill_hot_expert_rows():
-    """The skewed prefill: tokens of the hottest expert (many token tiles) and a few others."""
-    cfg = synth.CONFIGS["dsv3_skew_prefill"]
-    inp, W = inputs(cfg)
-    lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
-    y = lay(inp["x"])
-    assert moe().read_status(lay.bufs["ws"]) == 0
+def test_layer_dsv3_decode_every_token():
+    """The DeepSeek-V3 decode layer (T=64): every token's output and every expert-output row
+    (all 512 routed rows, 64 shared rows) against the oracle."""
+    cfg = synth.CONFIGS["dsv3_decode"]
+    inp, W, lay, y = _run_layer(cfg)
+    res = check_layer(cfg, inp, W, lay.bufs, y, np.arange(cfg.T), tol=TOL_BF16)
+    print(cfg.name, res)
+    assert res["rows"] == cfg.T * cfg.k and res["tokens"] == cfg.T
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T", synth.SWEEP_T)
+def test_layer_dsv3_sweep_point(T):
+    """Each point of the decode sweep (1..128 tokens per logical rank): at least 32 tokens'
+    outputs (all of them up to 32) and every row of 16 touched experts, among them the four
+    with the most rows (at 512+ tokens those fill token tiles past 32 rows, the cp.async
+    gather path; below, the four-row TMA gathers)."""
+    cfg = synth.CONFIGS["dsv3_sweep"].with_T(T)
+    inp, W, lay, y = _run_layer(cfg)
     ti = lay.bufs["topk_idx"].cpu().numpy()
-    hot = int(np.bincount(ti.reshape(-1), minlength=cfg.E).argmax())
-    hot_tokens = np.nonzero((ti == hot).any(1))[0]
-    tokens = np.unique(np.concatenate([hot_tokens[[0, len(hot_tokens) // 2, -1]], [5]]))
-    assert _layer_tokens_check(cfg, tokens, inp, W, y) <= TOL_BF16
+    rng = np.random.default_rng(T)
+    tokens = np.arange(T) if T <= 32 else np.sort(rng.choice(T, 32, replace=False))
+    n = experts_by_rows(ti, cfg.E)
+    touched = np.nonzero(n)[0]
+    top = touched[np.argsort(-n[touched], kind="stable")][:4]
+    rest = np.setdiff1d(touched, top)
+    pick = np.concatenate([top, rng.choice(rest, min(12, rest.size), replace=False)])
+    extra = [p for e in pick for p in hot_expert_pairs(ti, int(e))]
+    res = check_layer(cfg, inp, W, lay.bufs, y, tokens, extra, tol=TOL_BF16)
+    print(cfg.name, res)
+    assert res["tokens"] >= min(T, 32) and res["experts"] >= 16
+
+
+def _prefill_pairs(cfg, bufs, rng):
+    """Expert rows for the large prefill checks: every row of the hottest expert, every row of an
+    expert whose rows fill a token tile past 32 rows and of one with at most 32, and every row
+    of two experts whose compact rows lie past the first 1024 (the schedule's grid-filled row
+    list)."""
+    ti = bufs["topk_idx"].cpu().numpy()
+    n = experts_by_rows(ti, cfg.E)
+    off = np.cumsum(n) - n
+    hot = int(np.argmax(n))
+    chosen = [hot]
+    mid = np.nonzero((n > 32) & (n <= 64))[0]
+    if mid.size:
+        chosen.append(int(mid[0]))
+    small = np.nonzero((n > 0) & (n <= 32))[0]
+    if small.size:
+        chosen.append(int(small[-1]))
+    late = np.setdiff1d(np.nonzero((off >= 1024) & (n > 0))[0], chosen)
+    chosen += [int(e) for e in rng.choice(late, min(2, late.size), replace=False)]
+    return [p for e in chosen for p in hot_expert_pairs(ti, e)], hot, n
+
+
+@pytest.mark.slow
+def test_layer_skew_prefill_rows_and_tokens():
+    """The Zipf-skewed prefill (T=4096, bf16): every row of the hottest expert (about 10x the
+    mean load: many token tiles), of a 33..64-row expert, of a <=32-row one and of two experts
+    past the first 1024 compact rows, plus 256 tokens' whole layer output; >= 1024 rows."""
+    cfg = synth.CONFIGS["dsv3_skew_prefill"]
+    inp, W, lay, y = _run_layer(cfg)
+    rng = np.random.default_rng(cfg.seed)
+    extra, hot, n = _prefill_pairs(cfg, lay.bufs, rng)
+    assert n[hot] >= 8 * n.mean()
+    tokens = np.sort(rng.choice(cfg.T, 256, replace=False))
+    res = check_layer(cfg, inp, W, lay.bufs, y, tokens, extra, tol=TOL_BF16)
+    print(cfg.name, res)
+    assert res["rows"] >= 1024
 
 
 def test_layer_equals_stage_calls_and_is_deterministic():
@@ -587,11 +648,168 @@ def test_fp8_expert_rows_and_layer(cfg):
 
 
 @pytest.mark.slow
-def test_fp8_prefill_sampled_tokens():
+def test_fp8_prefill_rows_and_tokens():
+    """The FP8 prefill (T=16384, e4m3 activations and weights): every row of the hottest expert,
+    of a <=32-row and a 33..64-row expert where they exist, and of two experts past the first
+    1024 compact rows, plus 256 tokens' whole layer output; >= 1024 rows."""
     cfg = synth.CONFIGS["dsv3_fp8_prefill"]
+    inp, W, lay, y = _run_layer(cfg)
+    rng = np.random.default_rng(cfg.seed)
+    extra, hot, n = _prefill_pairs(cfg, lay.bufs, rng)
+    tokens = np.sort(np.concatenate([[0, cfg.T - 1],
+                                     rng.choice(np.arange(1, cfg.T - 1), 254, replace=False)]))
+    res = check_layer(cfg, inp, W, lay.bufs, y, tokens, extra, tol=TOL_FP8)
+    print(cfg.name, res)
+    assert res["rows"] >= 1024
+
+
+# ------------------------------------------------------------------------------------------
+# Layer variants: gather mode (no receive-buffer copy) and the shared expert on a side stream
+# ------------------------------------------------------------------------------------------
+VARIANTS = [dict(gather=True), dict(side_stream=True), dict(gather=True, side_stream=True),
+            dict(side_stream=True, side_ctas=3)]
+
+
+@pytest.mark.parametrize("cfg", [SMALL, FP8_SMALL, HOT, FP8_HOT, synth.CONFIGS["dsv3_decode"]],
+                         ids=lambda c: c.name)
+def test_layer_variants_equal_the_layer(cfg):
+    """Every variant computes the same rows with the same kernels in the same K order, so its
+    output equals moe_layer's bit for bit (and the gate weights, indices and counts too)."""
     inp, W = inputs(cfg)
-    lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    m = moe()
+    base = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y0 = base(inp["x"]).clone()
+    torch.cuda.synchronize()
+    for v in VARIANTS:
+        lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), **v)
+        for _ in range(2):   # twice: the second call reuses the workspace and the side stream
+            y = lay(inp["x"])
+            torch.cuda.synchronize()
+            assert m.read_status(lay.bufs["ws"]) == 0, v
+            assert torch.equal(y, y0), v
+        assert torch.equal(lay.bufs["counts"], base.bufs["counts"])
+        assert torch.equal(lay.bufs["row_of"], base.bufs["row_of"])
+        if v.get("gather"):
+            assert lay.bufs["recv"] is None
+
+
+@pytest.mark.parametrize("cfg", [SMALL, FP8_SMALL, E192_R64], ids=lambda c: c.name)
+def test_gather_stage_calls_equal_the_copying_ones(cfg):
+    inp, W = inputs(cfg)
+    m = moe()
+    r = _ffn(cfg, inp, W, run_stages(cfg, inp, W))
+    b = m.Buffers(cfg, with_recv=False)
+    st = torch.empty(b.sizes["recv_rows"], dtype=torch.int32, device="cuda")
+    m.dispatch_index(cfg, r["topk_idx"], b["counts"], b["row_of"], st)
+    assert torch.equal(b["counts"], r["counts"]) and torch.equal(b["row_of"], r["row_of"])
+    assert torch.equal(st, r["src_tok"])
+    m.expert_ffn_gather(cfg, inp["x"], b["counts"], st, weight_dict(W), b["ebuf"],
+                        b["shared_out"], b["ws"])
+    torch.cuda.synchronize()
+    assert m.read_status(b["ws"]) == 0
+    filled = (r["src_tok"] >= 0).nonzero().squeeze(1)
+    assert torch.equal(b["ebuf"][filled], r["ebuf"][filled])
+    if cfg.d_ff_shared:
+        assert torch.equal(b["shared_out"], r["shared_out"])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["dsv3_skew_prefill", "dsv3_fp8_prefill"])
+def test_gather_mode_equals_the_layer_at_prefill(name):
+    cfg = synth.CONFIGS[name]
+    inp, W = inputs(cfg)
+    m = moe()
+    y0 = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))(inp["x"]).clone()
+    lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), gather=True)
     y = lay(inp["x"])
-    assert moe().read_status(lay.bufs["ws"]) == 0
-    tokens = np.array([0, 4097, 9999, cfg.T - 1])
-    assert _layer_tokens_check(cfg, tokens, inp, W, y) <= TOL_FP8
+    torch.cuda.synchronize()
+    assert m.read_status(lay.bufs["ws"]) == 0
+    assert torch.equal(y, y0)
+
+
+def test_layer_ex_rejects_bad_options():
+    import ctypes
+    m = moe()
+    cfg = SMALL
+    inp, W = inputs(cfg)
+    b = m.Buffers(cfg)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(m.MoEError) as e:   # an unknown flag
+        m.layer_ex(cfg, m.LayerOpts(flags=8), inp["x"], inp["w_gate"], inp["bias"],
+                   weight_dict(W), b, y)
+    assert e.value.code == 1
+    with pytest.raises(m.MoEError) as e:   # side stream asked for without a stream or events
+        m.layer_ex(cfg, m.LayerOpts(flags=m.MOE_OPT_SHARED_SIDE_STREAM), inp["x"],
+                   inp["w_gate"], inp["bias"], weight_dict(W), b, y)
+    assert e.value.code == 1
+    with pytest.raises(m.MoEError) as e:   # no receive buffer without gather mode
+        bb = dict(b)
+        bb["recv"] = None
+        m.layer_ex(cfg, m.LayerOpts(flags=0), inp["x"], inp["w_gate"], inp["bias"],
+                   weight_dict(W), bb, y)
+    assert e.value.code == 1
+
+
+# ------------------------------------------------------------------------------------------
+# Redundant experts placed on slots
+# ------------------------------------------------------------------------------------------
+def _placement_for(cfg, inp, spare_per_rank, seed):
+    """A placement planned from the loads of another batch of the same workload (the routing of
+    other tokens stands for past traffic), as a deployment would plan it."""
+    m = moe()
+    other = synth.normal_bf16(cfg.seed + seed, synth.TAG_X, (cfg.T, cfg.d), cfg.x_std, "cuda")
+    b = m.Buffers(cfg)
+    m.route(cfg, other, inp["w_gate"], inp["bias"], b["topk_idx"], b["topk_w"], b["ws"])
+    load = np.bincount(b["topk_idx"].cpu().numpy().reshape(-1), minlength=cfg.E)
+    S = cfg.E // cfg.R + spare_per_rank
+    return m.Placement.from_loads(load.astype(np.float64), cfg.R, S, max_copies=16), S
+
+
+PLACED = [(SMALL, 2), (HOT, 3), (E192_R64, 1), (synth.CONFIGS["dsv3_decode"], 4),
+          (FP8_SMALL, 2)]
+
+
+@pytest.mark.parametrize("cfg,spare", PLACED, ids=lambda v: getattr(v, "name", str(v)))
+def test_placed_layer_dispatch_is_the_oracles_and_output_is_the_layers(cfg, spare):
+    inp, W = inputs(cfg)
+    m = moe()
+    pl, S = _placement_for(cfg, inp, spare, 31)
+    y0 = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))(inp["x"]).clone()
+    for gather in (False, True):
+        lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), placement=pl,
+                         gather=gather)
+        y = lay(inp["x"])
+        torch.cuda.synchronize()
+        assert m.read_status(lay.bufs["ws"]) == 0
+        ti = lay.bufs["topk_idx"].cpu().numpy()
+        counts, row_of, _ = oracle.dispatch_index_placed(
+            ti, cfg.E, cfg.R, S, pl.n_copies.cpu().numpy(), pl.copy_slot.cpu().numpy())
+        assert np.array_equal(lay.bufs["counts"].cpu().numpy(), counts)
+        assert np.array_equal(lay.bufs["row_of"].cpu().numpy(), row_of)
+        # the same rows through the same weights: the output equals the unplaced layer's
+        assert torch.equal(y, y0)
+
+
+@pytest.mark.slow
+def test_placed_skew_prefill_lowers_the_imbalance_and_keeps_the_output():
+    cfg = synth.CONFIGS["dsv3_skew_prefill"]
+    inp, W = inputs(cfg)
+    m = moe()
+    pl, S = _placement_for(cfg, inp, 4, 17)
+    base = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y0 = base(inp["x"]).clone()
+    lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), placement=pl)
+    y = lay(inp["x"])
+    torch.cuda.synchronize()
+    assert m.read_status(lay.bufs["ws"]) == 0
+    assert torch.equal(y, y0)
+    ti = lay.bufs["topk_idx"].cpu().numpy()
+    counts, row_of, _ = oracle.dispatch_index_placed(
+        ti, cfg.E, cfg.R, S, pl.n_copies.cpu().numpy(), pl.copy_slot.cpu().numpy())
+    assert np.array_equal(lay.bufs["counts"].cpu().numpy(), counts)
+    assert np.array_equal(lay.bufs["row_of"].cpu().numpy(), row_of)
+    before = oracle.imbalance_factor(np.bincount(ti.reshape(-1), minlength=cfg.E), cfg.R)
+    loads = oracle.rank_loads(counts, cfg.R)
+    after = loads.max() / loads.mean()
+    print("skew prefill rank IF: contiguous %.3f, placed %.3f" % (before, after))
+    assert after < before and after < 1.1

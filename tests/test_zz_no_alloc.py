@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -44,6 +45,12 @@ def _route_both(moe, cfg, inp):
     return ref_i.cpu().numpy(), ref_w.cpu().numpy(), got_i.cpu().numpy(), got_w.cpu().numpy()
 
 
+def _oracle_route(cfg, inp):
+    x = inp["x"].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return oracle.route(x, inp["w_gate"].cpu().numpy(), inp["bias"].cpu().numpy(), cfg.k,
+                        cfg.n_group, cfg.topk_group, cfg.route_scale)
+
+
 def test_noalloc_router_matches_the_workspace_router_on_consecutive_calls(moe):
     big = synth.CONFIGS["dsv3_decode"]                   # T=64 x E=256: 1 MiB of scratch
     small = synth.CONFIGS["tiny"]                        # a smaller call after a larger one
@@ -51,7 +58,31 @@ def test_noalloc_router_matches_the_workspace_router_on_consecutive_calls(moe):
         inp = synth.make_router_inputs(cfg, "cuda")
         ref_i, ref_w, got_i, got_w = _route_both(moe, cfg, inp)
         assert np.array_equal(got_i, ref_i)
+        # the same kernels in the same order: the weights agree exactly, within the 1e-5 bound
         assert np.abs(got_w - ref_w).max() <= 1e-5
+        assert np.array_equal(got_w, ref_w)
+        # and both are the oracle's, bit for bit
+        o_i, o_w = _oracle_route(cfg, inp)
+        assert np.array_equal(got_i, o_i)
+        assert np.array_equal(got_w, o_w)
+
+
+def test_noalloc_router_at_1024_tokens_through_the_binding(moe):
+    """1024 tokens take the warp-per-token selection kernel (and its shared-memory opt-in); at
+    128 experts the partial table fills the fixed array exactly (16 x 1024 x 128 floats)."""
+    cfg = synth.MoEConfig("noalloc_t1024", T=1024, d=1024, E=128, k=8, n_group=8, topk_group=4,
+                          d_ff=128, d_ff_shared=0, R=8, route_scale=2.5, seed=21)
+    inp = synth.make_router_inputs(cfg, "cuda")
+    o_i, o_w = _oracle_route(cfg, inp)
+    for _ in range(2):                                   # two calls in a row share the array
+        got_i = torch.full((cfg.T, cfg.k), -1, dtype=torch.int32, device="cuda")
+        got_w = torch.full((cfg.T, cfg.k), -1.0, dtype=torch.float32, device="cuda")
+        moe.route_noalloc(cfg, inp["x"], inp["w_gate"], inp["bias"], got_i, got_w)
+        torch.cuda.synchronize()
+        assert np.array_equal(got_i.cpu().numpy(), o_i)
+        assert np.array_equal(got_w.cpu().numpy(), o_w)
+    ref_i, ref_w, g_i, g_w = _route_both(moe, cfg, inp)
+    assert np.array_equal(g_i, ref_i) and np.array_equal(g_w, ref_w)
 
 
 def test_noalloc_router_rejects_batches_beyond_its_scratch(moe):
