@@ -44,9 +44,11 @@ def kernels_per_step(cfg, mode="layer"):
     with the shared expert on a side stream, its two GEMMs as launches of their own."""
     gather = "gather" in mode
     side = "side" in mode and cfg.d_ff_shared > 0
+    fused = "fused" in mode
     sched = 1 if cfg.T * cfg.k <= 1024 else 2
     quant = 1 if cfg.act == "fp8" and (cfg.d_ff_shared or gather) else 0
-    return 7 + sched + quant - (1 if gather else 0) + (2 if side else 0)
+    return (7 + sched + quant - (1 if gather else 0) + (2 if side else 0)
+            - (2 if fused else 0))
 L2_BYTES = 129 * 2 ** 20
 CPU_SAMPLE_SECONDS = 12.0   # target CPU time of the oracle sample behind cpu_baseline
 
@@ -255,7 +257,8 @@ def weight_dict(W):
 MODES = {"layer": {}, "gather": {"gather": True}, "side": {"side_stream": True},
          "gather+side": {"gather": True, "side_stream": True},
          "side32": {"side_stream": True, "side_ctas": 32},
-         "side64": {"side_stream": True, "side_ctas": 64}}
+         "side64": {"side_stream": True, "side_ctas": 64},
+         "fused": {"fused": True}, "gather+fused": {"gather": True, "fused": True}}
 
 
 def setup(cfg, dev, rank=0, world=1, W=None, mode="layer"):
@@ -446,7 +449,11 @@ def run_extras(args, dev, W_decode, pk):
     dec = synth.CONFIGS["dsv3_decode"]
     out["variants"] = {dec.name: time_modes(dec, dev, W_decode, steps, warm,
                                             ("gather", "side", "side32", "side64",
-                                             "gather+side"))}
+                                             "gather+side", "fused", "gather+fused"))}
+    for T in (8, 256, 1024):   # the fused stage across the sweep
+        out["variants"][dec.with_T(T).name] = time_modes(dec.with_T(T), dev, W_decode, steps, warm,
+                                                         ("layer", "gather", "fused",
+                                                          "gather+fused"))
     out["placed"] = {dec.name: time_placed(dec, dev, W_decode, steps, warm)}
     for T in synth.SWEEP_T:
         cfg = dec.with_T(T)
@@ -465,7 +472,10 @@ def run_extras(args, dev, W_decode, pk):
         r = time_layer(cfg, inp, lay, steps, warm, dev)
         out[key] = summarise(cfg, r, pk)
         del lay, inp
-        out["variants"][cfg.name] = time_modes(cfg, dev, W, steps, warm)
+        out["variants"][cfg.name] = time_modes(
+            cfg, dev, W, steps, warm,
+            ("gather", "side", "gather+side") + (("fused", "gather+fused") if cfg.act == "bf16"
+                                                 else ()))
         out["placed"][cfg.name] = time_placed(cfg, dev, W, steps, warm)
         del W
         torch.cuda.empty_cache()

@@ -44,7 +44,7 @@ class Sizes(ctypes.Structure):
                 ("ebuf_bytes", ctypes.c_size_t), ("ws_bytes", ctypes.c_size_t)]
 
 
-MOE_OPT_GATHER_X, MOE_OPT_SHARED_SIDE_STREAM = 1, 2
+MOE_OPT_GATHER_X, MOE_OPT_SHARED_SIDE_STREAM, MOE_OPT_FUSED_FFN = 1, 2, 4
 
 
 class PlacementC(ctypes.Structure):
@@ -345,10 +345,12 @@ class MoELayer:
     gather: the expert GEMMs read routed rows from x by token (no receive-buffer copy; the
     receive buffers are not allocated). side_stream: the shared expert runs on a second stream
     of its own, limited to side_ctas CTAs per GEMM. placement: redundant experts on slots
-    (Placement); the dispatch splits each expert's rows over its copies."""
+    (Placement); the dispatch splits each expert's rows over its copies. fused: both expert
+    GEMMs and the combine in one persistent launch (bf16)."""
 
     def __init__(self, cfg, w_gate, bias, weights: dict, device="cuda", gather=False,
-                 side_stream=False, side_ctas=0, placement: Placement | None = None):
+                 side_stream=False, side_ctas=0, placement: Placement | None = None,
+                 fused=False):
         self.cfg = cfg
         self.w_gate = w_gate
         self.bias = bias
@@ -357,9 +359,10 @@ class MoELayer:
         self.bufs = Buffers(cfg, device, with_recv=not gather,
                             slots_per_rank=placement.slots_per_rank if placement else 0)
         self.opts = None
-        if gather or side_stream or placement is not None:
+        if gather or side_stream or fused or placement is not None:
             self.opts = LayerOpts(flags=(MOE_OPT_GATHER_X if gather else 0)
-                                  | (MOE_OPT_SHARED_SIDE_STREAM if side_stream else 0),
+                                  | (MOE_OPT_SHARED_SIDE_STREAM if side_stream else 0)
+                                  | (MOE_OPT_FUSED_FFN if fused else 0),
                                   side_ctas=int(side_ctas))
             if placement is not None:
                 self.opts.placement = ctypes.pointer(placement.c)

@@ -103,6 +103,10 @@ WsLayout ws_layout(const moe_cfg& c) {
   L.run_pre = o;    o = up256(o + sizeof(int32_t) * (size_t)c.R * c.E);
   L.src_tok = o;    o = up256(o + sizeof(int32_t) * (size_t)c.R * c.R * cap_of(c));
   L.tok_list = o;   o = up256(o + sizeof(int32_t) * tk);
+  L.grp_order = o;  o = up256(o + sizeof(int32_t) * c.E);
+  L.shared_tiles = c.d_ff_shared ? (c.T + L.bn - 1) / L.bn : 0;
+  L.fused_done_n = L.max_tiles + L.shared_tiles + 1;
+  L.fused_done = o; o = up256(o + sizeof(int32_t) * (size_t)L.fused_done_n);
   L.total = o;
   return L;
 }
@@ -357,6 +361,7 @@ int layer_impl(const moe_cfg& c0, const moe_layer_opts& o, const void* x, const 
   const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
   const bool gather = (o.flags & MOE_OPT_GATHER_X) != 0;
   const bool side = (o.flags & MOE_OPT_SHARED_SIDE_STREAM) != 0 && c.d_ff_shared > 0;
+  const bool fused = (o.flags & MOE_OPT_FUSED_FFN) != 0;
   int32_t* src_tok = gather ? reinterpret_cast<int32_t*>(wsp + L.src_tok) : nullptr;
   auto rec = [&](int i) -> cudaError_t {
     return events ? cudaEventRecord(events[i], stream) : cudaSuccess;
@@ -406,7 +411,8 @@ int layer_impl(const moe_cfg& c0, const moe_layer_opts& o, const void* x, const 
   if (e == cudaSuccess) e = rec(2);
   if (e == cudaSuccess) {
     const StageRange r("ffn_setup");
-    e = launch_ffn_setup(c, L, counts, x, wsp, stream, pdl, src_tok, !quantised);
+    e = launch_ffn_setup(c, L, counts, x, wsp, stream, pdl, src_tok, !quantised,
+                         o.placement ? o.placement->slot_expert : nullptr);
   }
   if (e == cudaSuccess) e = rec(3);
   FfnPart mp;
@@ -414,6 +420,15 @@ int layer_impl(const moe_cfg& c0, const moe_layer_opts& o, const void* x, const 
   mp.src_tok = src_tok;
   mp.group_expert = o.placement ? o.placement->slot_expert : nullptr;
   mp.weight_experts = c0.E;
+  if (fused) {
+    // both GEMMs and the combine in one launch; the stage events after it all mark its end
+    const StageRange r("ffn_fused");
+    if (e == cudaSuccess)
+      e = launch_ffn_fused(c, L, recv, x, *w, ebuf, shared_out, row_of, topk_w, y, wsp, stream,
+                           mp);
+    for (int i = 4; i <= 6 && e == cudaSuccess; ++i) e = rec(i);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+  }
   if (e == cudaSuccess) {
     const StageRange r("ffn_gate_up");
     e = launch_ffn_gemm(c, L, 0, recv, recv_scales, x, *w, ebuf, shared_out, wsp, stream, pdl,
@@ -488,8 +503,14 @@ int moe_layer_ex(const moe_cfg* cfg, const moe_layer_opts* opts, const void* x,
                  void* ebuf, void* shared_out, void* y, void* ws, cudaStream_t stream,
                  const cudaEvent_t* events) {
   const moe_layer_opts o = opts ? *opts : moe_layer_opts{};
-  if (o.flags & ~(MOE_OPT_GATHER_X | MOE_OPT_SHARED_SIDE_STREAM)) return MOE_ERR_INVALID_ARG;
+  if (o.flags & ~(MOE_OPT_GATHER_X | MOE_OPT_SHARED_SIDE_STREAM | MOE_OPT_FUSED_FFN))
+    return MOE_ERR_INVALID_ARG;
   MOE_LAYER_CHECKS((o.flags & MOE_OPT_GATHER_X) != 0);
+  if (o.flags & MOE_OPT_FUSED_FFN) {
+    if (c.act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    // the combine runs inside the launch, so the shared expert cannot be on another stream
+    if ((o.flags & MOE_OPT_SHARED_SIDE_STREAM) && c.d_ff_shared) return MOE_ERR_INVALID_ARG;
+  }
   if (o.placement) {
     const moe_placement& p = *o.placement;
     if (p.slots_per_rank < 1 || (long long)p.slots_per_rank * c.R < c.E || p.max_copies < 1)

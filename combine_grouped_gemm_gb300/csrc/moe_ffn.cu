@@ -30,7 +30,7 @@
 // unit overlaps the main loop of the next. Every wait is bounded (see moe_device.cuh).
 #include <mutex>
 
-#include "moe_device.cuh"
+#include "moe_gemm.cuh"
 
 namespace moe {
 namespace {
@@ -40,8 +40,9 @@ namespace {
 // ---------------------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;             // upper bound; launched with E rounded up to 32
 // counts table staged in shared memory up to this: the 48 KB a kernel gets without an opt-in,
-// less 1 KB for the kernel's static shared memory (warp sums and rank bases, 388 bytes)
-constexpr size_t kPlanStageBytes = 47 * 1024;
+// less the kernel's static shared memory (warp sums and rank bases, 388 bytes; the schedule
+// order by position, 8 KB)
+constexpr size_t kPlanStageBytes = 39 * 1024;
 constexpr int kPlanFusedRows = 1024;            // fill the row list in the plan CTA up to this T*k
 
 // Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, <= 1024).
@@ -77,22 +78,30 @@ __device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
 // row_list[c] for every compact row c: its expert by binary search on the compact offsets,
 // its source run by a scan of the run prefixes, then the run's receive row plus the position.
 // In gather mode (src_tok != nullptr) tok_list[c] also receives the compact row's token.
+// grp_order (nullable): the group at each position of the schedule order (compact offsets
+// ascend along it); nullptr: the groups in index order.
 __device__ __forceinline__ void fill_rows(const int32_t* grp_n, const int32_t* grp_off,
                                           const int32_t* run_start, const int32_t* run_pre,
                                           int32_t* row_list, uint32_t* status, int E, int R,
                                           int tk, int first, int stride,
                                           const int32_t* src_tok, int32_t* tok_list,
-                                          long long recv_rows, int T) {
+                                          long long recv_rows, int T,
+                                          const int32_t* grp_order) {
+  auto at = [&](int i) -> int {
+    const int g = grp_order ? grp_order[i] : i;
+    return g >= 0 && g < E ? g : 0;
+  };
   for (int c = first; c < tk; c += stride) {
-    int lo = 0, hi = E - 1;  // last expert whose compact offset is <= c
+    int lo = 0, hi = E - 1;  // last position whose compact offset is <= c
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (grp_off[mid] <= c) lo = mid;
+      if (grp_off[at(mid)] <= c) lo = mid;
       else hi = mid - 1;
     }
-    int e = lo;
-    while (e > 0 && grp_n[e] == 0) --e;  // an empty expert shares its offset with the next
-    while (e < E - 1 && c >= grp_off[e] + grp_n[e]) ++e;
+    int i = lo;
+    while (i > 0 && grp_n[at(i)] == 0) --i;  // an empty group shares its offset with the next
+    while (i < E - 1 && c >= grp_off[at(i)] + grp_n[at(i)]) ++i;
+    const int e = at(i);
     const int p = c - grp_off[e];
     if (p < 0 || p >= grp_n[e]) {
       raise_status(status, MOE_DEV_BOUNDS);
@@ -125,9 +134,12 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     int32_t* __restrict__ n_tiles, Tile* __restrict__ tiles, int32_t* __restrict__ run_start,
     int32_t* __restrict__ run_pre, int32_t* __restrict__ row_list, uint32_t* status, int E, int R,
     int cap, int bn, int max_tiles, int tk, const int32_t* __restrict__ src_tok,
-    int32_t* __restrict__ tok_list, int T) {
+    int32_t* __restrict__ tok_list, int T, const int32_t* __restrict__ group_expert,
+    int32_t* __restrict__ grp_order) {
   __shared__ int warp_sums[33];
   __shared__ int rank_base[64];
+  __shared__ int ord_g[kPlanThreads];   // group at each schedule position
+  __shared__ int ord_n[kPlanThreads];   // its rows
   extern __shared__ int32_t cnt_s[];   // counts staged once: [R][E] when it fits, else unused
   pdl_wait();
   pdl_trigger();
@@ -145,18 +157,39 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
   int n = 0;
   if (act)
     for (int s = 0; s < R; ++s) n += cnt(s);
+  // Schedule order of the groups (compact rows and tiles): by index, or, when the groups are
+  // slots holding copies of experts, by (expert, slot), so the copies of one expert run on
+  // adjacent units and read its weight tiles at about the same time (from L2 after the
+  // first). Thread i then handles the group at position i.
+  int g_i = e, n_i = n;
+  if (group_expert) {
+    if (act) {
+      const int eg = group_expert[e];
+      int pos = 0;
+      for (int h = 0; h < E; ++h) {
+        const int eh = group_expert[h];
+        pos += (eh < eg || (eh == eg && h < e)) ? 1 : 0;
+      }
+      ord_g[pos] = e;
+      ord_n[pos] = n;
+      grp_order[pos] = e;
+    }
+    __syncthreads();
+    g_i = act ? ord_g[threadIdx.x] : 0;
+    n_i = act ? ord_n[threadIdx.x] : 0;
+  }
   int total;
-  const int off = block_exclusive_scan(act ? n : 0, &total, warp_sums);
+  const int off = block_exclusive_scan(act ? n_i : 0, &total, warp_sums);
   if (threadIdx.x == 0 && total != tk) raise_status(status, MOE_DEV_BOUNDS);
-  const int nt = act ? (n + bn - 1) / bn : 0;
+  const int nt = act ? (n_i + bn - 1) / bn : 0;
   int tiles_total;
   const int toff = block_exclusive_scan(nt, &tiles_total, warp_sums);
   if (act) {
-    grp_n[e] = n;
-    grp_off[e] = off;
+    grp_n[g_i] = n_i;
+    grp_off[g_i] = off;
     for (int j = 0; j < nt; ++j) {
       const int ti = toff + j;
-      if (ti < max_tiles) tiles[ti] = Tile{e, j * bn, min(bn, n - j * bn), nt};
+      if (ti < max_tiles) tiles[ti] = Tile{g_i, j * bn, min(bn, n_i - j * bn), nt};
     }
   }
   if (threadIdx.x == 0) {
@@ -207,7 +240,8 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
   if (tk <= kPlanFusedRows) {
     __syncthreads();
     fill_rows(grp_n, grp_off, run_start, run_pre, row_list, status, E, R, tk, threadIdx.x,
-              blockDim.x, src_tok, tok_list, (long long)R * R * cap, T);
+              blockDim.x, src_tok, tok_list, (long long)R * R * cap, T,
+              group_expert ? grp_order : nullptr);
   }
 }
 
@@ -220,125 +254,14 @@ __global__ void __launch_bounds__(256) ffn_rows_kernel(const int32_t* __restrict
                                                        uint32_t* status, int E, int R, int tk,
                                                        const int32_t* __restrict__ src_tok,
                                                        int32_t* __restrict__ tok_list,
-                                                       long long recv_rows, int T) {
+                                                       long long recv_rows, int T,
+                                                       const int32_t* __restrict__ grp_order) {
   pdl_wait();
   pdl_trigger();
   fill_rows(grp_n, grp_off, run_start, run_pre, row_list, status, E, R, tk,
             blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x, src_tok, tok_list,
-            recv_rows, T);
+            recv_rows, T, grp_order);
 }
-
-// ---------------------------------------------------------------------------------------
-// Grouped GEMM
-// ---------------------------------------------------------------------------------------
-struct GemmArgs {
-  const Tile* tiles;
-  const int32_t* n_tiles;
-  const int32_t* grp_off;
-  const int32_t* row_list;
-  int tk;                 // compact rows (T*k)
-  long long recv_rows;    // receive rows (bound of gathered / scattered row indices)
-  int T;                  // shared-expert rows
-  int mt_routed;          // 128-row weight tiles per routed expert
-  int mt_shared;          // 128-row weight tiles of the shared expert (0: none)
-  int n_shared_tiles;     // token tiles of the shared expert
-  int k_steps;            // K / 64
-  int a_rows_routed;      // weight rows per routed expert
-  int a_up_routed;        // offset of the up rows (gate/up stage)
-  int a_up_shared;
-  void* out_routed;       // gate/up: h [tk][F] (compact rows); down: ebuf [recv_rows][d]
-  void* out_shared;       // gate/up: hs [T][Fs]; down: shared_out [T][d]
-  int ld_routed;          // output row length (elements)
-  int ld_shared;
-  int box_routed;         // rows per box of the contiguous token-row maps (routed / shared)
-  int box_shared;
-  const uint8_t* gather_base;  // gate/up: receive buffer (routed token rows are gathered)
-  long long gather_ld;         // bytes per receive row
-  uint32_t* status;
-  const int32_t* group_expert; // expert whose weights group g uses (nullptr: expert g)
-  int n_experts;               // experts in the weight tensors
-};
-
-// The expert whose weight rows a routed group reads: itself, or the expert its slot holds
-// (redundant experts). An entry outside [0, n_experts) is reported and replaced by expert 0, so
-// no weight read leaves the tensors.
-__device__ __forceinline__ int weight_expert(const int32_t* group_expert, int g, int n_experts,
-                                             uint32_t* status) {
-  if (!group_expert) return g;
-  const int e = group_expert[g];
-  if (e >= 0 && e < n_experts) return e;
-  raise_status(status, MOE_DEV_BOUNDS);
-  return 0;
-}
-
-struct Unit {
-  int g;       // routed expert, or -1 for the shared expert
-  int n0, nlen, m;
-};
-
-// Unit u -> (group, token tile, weight tile). Shared-expert units come first, token-tile-major.
-// A routed expert with nt token tiles owns units [mt*b, mt*(b+nt)), b = its first tile. The
-// gate/up stage takes them token-tile-major (unit mt*b + j*mt + m), so a token tile's rows are
-// reused by consecutive units. The down stage takes them weight-tile-major (unit
-// mt*b + m*nt + j): the nt units that read weight tile m run on adjacent CTAs at about the same
-// time, and on the skew workload this cut the down GEMM's DRAM reads from 10.56 to 8.50 GB
-// (the gate/up stage's traffic did not move with it). n_tiles: entries in the tile list.
-template <int BN, bool kWeightMajor>
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u, int n_tiles) {
-  Unit r;
-  const int us = a.n_shared_tiles * a.mt_shared;
-  if (u < us) {
-    const int tt = u / a.mt_shared;
-    r.g = -1;
-    r.m = u - tt * a.mt_shared;
-    r.n0 = tt * BN;
-    r.nlen = min(BN, a.T - r.n0);
-  } else {
-    const int v = u - us;
-    const int tt0 = v / a.mt_routed;   // a tile of the unit's expert (the ranges coincide)
-    const Tile t0 = a.tiles[tt0];
-    Tile t = t0;
-    if (!kWeightMajor) {
-      r.m = v - tt0 * a.mt_routed;
-    } else {
-      const int base = tt0 - t0.n0 / BN;
-      // (a list cut short at its bound, already reported, keeps every index inside it)
-      const int nt = max(1, min(t0.ntiles, n_tiles - base));
-      const int local = v - base * a.mt_routed;
-      r.m = local / nt;
-      const int j = local - r.m * nt;
-      if (base + j != tt0) t = a.tiles[base + j];
-    }
-    r.g = t.group;
-    r.n0 = t.n0;
-    r.nlen = t.nlen;
-  }
-  return r;
-}
-
-// Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies (tiles of
-// more than kSmallTile rows; smaller ones are four-row TMA gathers).
-constexpr int kGatherWarps = 2;
-constexpr int kSmallTile = 32;
-constexpr int kGatherThreads = kGatherWarps * 32;
-template <int STAGE>
-struct GemmThreads {
-  static constexpr int kGather = STAGE == 0 ? kGatherThreads : 0;
-  static constexpr int kAll = 192 + kGather;
-};
-
-template <int STAGE, int BN, int STAGES>
-struct GemmShape {
-  static constexpr int NA = STAGE == 0 ? 2 : 1;    // weight tiles per stage (gate, up)
-  static constexpr int A_BYTES = 128 * 128;        // 128 rows x 64 bf16
-  static constexpr int B_BYTES = BN * 128;         // BN rows x 64 bf16
-  static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
-  static constexpr int ACC_COLS = NA * BN;         // fp32 accumulator columns per buffer
-  static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : 2 * ACC_COLS;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
-  static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
-  static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "tensor memory");
-};
 
 template <int STAGE, int BN, int STAGES>
 __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
@@ -743,7 +666,8 @@ cudaError_t launch_quant_x(const moe_cfg& c, const WsLayout& L, const void* x, c
 
 cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
                              const void* x, char* ws, cudaStream_t st, bool pdl,
-                             const int32_t* src_tok, bool quantise) {
+                             const int32_t* src_tok, bool quantise,
+                             const int32_t* group_expert) {
   if (quantise && c.act_dtype == MOE_FP8_E4M3 && (c.d_ff_shared || src_tok)) {
     const cudaError_t err = launch_quant_x(c, L, x, ws, st, pdl);
     if (err != cudaSuccess) return err;
@@ -761,7 +685,7 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
       reinterpret_cast<int32_t*>(ws + L.run_start), reinterpret_cast<int32_t*>(ws + L.run_pre),
       reinterpret_cast<int32_t*>(ws + L.row_list), status, c.E, c.R, cap_of(c), L.bn,
       L.max_tiles, tk, src_tok, src_tok ? reinterpret_cast<int32_t*>(ws + L.tok_list) : nullptr,
-      c.T);
+      c.T, group_expert, reinterpret_cast<int32_t*>(ws + L.grp_order));
   if (err != cudaSuccess) return err;
   if (tk <= kPlanFusedRows) return cudaSuccess;   // the plan CTA filled the row list
   const int blocks = (tk + 255) / 256 < 4 * 152 ? (tk + 255) / 256 : 4 * 152;
@@ -771,16 +695,14 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
       reinterpret_cast<const int32_t*>(ws + L.run_pre), reinterpret_cast<int32_t*>(ws + L.row_list),
       status, c.E, c.R, tk, src_tok,
       src_tok ? reinterpret_cast<int32_t*>(ws + L.tok_list) : nullptr,
-      (long long)c.R * c.R * cap_of(c), c.T);
+      (long long)c.R * c.R * cap_of(c), c.T,
+      group_expert ? reinterpret_cast<const int32_t*>(ws + L.grp_order) : nullptr);
 }
 
-cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
-                            const float* recv_scales, const void* x, const moe_weights& w,
-                            void* ebuf, void* shared_out, char* ws, cudaStream_t st, bool pdl,
-                            const FfnPart& part) {
-  if (c.act_dtype == MOE_FP8_E4M3)
-    return launch_ffn_gemm_e4m3(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st, pdl,
-                                part);
+cudaError_t prepare_bf16_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
+                              const void* x, const moe_weights& w, void* ebuf, void* shared_out,
+                              char* ws, const FfnPart& part, GemmArgs* args,
+                              CUtensorMap maps[4]) {
   const int cap = cap_of(c);
   const long long recv_rows = (long long)c.R * c.R * cap;
   const int F = c.d_ff, Fs = c.d_ff_shared, d = c.d, tk = c.T * c.k;
@@ -803,7 +725,10 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
   const int n_w = part.weight_experts > 0 ? part.weight_experts : c.E;
   a.n_experts = n_w;
 
-  CUtensorMap mA, mAs, mB, mBs;
+  CUtensorMap& mA = maps[0];
+  CUtensorMap& mAs = maps[1];
+  CUtensorMap& mB = maps[2];
+  CUtensorMap& mBs = maps[3];
   bool ok = true;
   if (stage == 0) {
     a.mt_routed = F / 128;
@@ -863,13 +788,28 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
     a.mt_shared = 0;
     a.n_shared_tiles = 0;
   }
+  *args = a;
+  return cudaSuccess;
+}
 
+cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
+                            const float* recv_scales, const void* x, const moe_weights& w,
+                            void* ebuf, void* shared_out, char* ws, cudaStream_t st, bool pdl,
+                            const FfnPart& part) {
+  if (c.act_dtype == MOE_FP8_E4M3)
+    return launch_ffn_gemm_e4m3(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st, pdl,
+                                part);
+  GemmArgs a{};
+  CUtensorMap m[4];
+  const cudaError_t err =
+      prepare_bf16_gemm(c, L, stage, recv, x, w, ebuf, shared_out, ws, part, &a, m);
+  if (err != cudaSuccess) return err;
   if (L.bn == 64) {
-    if (stage == 0) return run_gemm<0, 64, 5>(a, mA, mAs, mB, mBs, st, pdl, part.ctas);
-    return run_gemm<1, 64, 8>(a, mA, mAs, mB, mBs, st, pdl, part.ctas);
+    if (stage == 0) return run_gemm<0, 64, 5>(a, m[0], m[1], m[2], m[3], st, pdl, part.ctas);
+    return run_gemm<1, 64, 8>(a, m[0], m[1], m[2], m[3], st, pdl, part.ctas);
   }
-  if (stage == 0) return run_gemm<0, 128, 4>(a, mA, mAs, mB, mBs, st, pdl, part.ctas);
-  return run_gemm<1, 128, 6>(a, mA, mAs, mB, mBs, st, pdl, part.ctas);
+  if (stage == 0) return run_gemm<0, 128, 4>(a, m[0], m[1], m[2], m[3], st, pdl, part.ctas);
+  return run_gemm<1, 128, 6>(a, m[0], m[1], m[2], m[3], st, pdl, part.ctas);
 }
 
 }  // namespace moe

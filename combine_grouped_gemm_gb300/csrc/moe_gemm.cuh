@@ -1,0 +1,132 @@
+// Definitions shared by the bf16 grouped-GEMM kernels (moe_ffn.cu: one launch per stage;
+// moe_fused.cu: both stages and the combine in one persistent launch): the launch arguments,
+// the unit list (shared-expert tiles first, then every (token tile, weight tile) of every
+// routed group), the warp roles and the shared-memory stage shapes. The GEMMs themselves are
+// described in moe_ffn.cu.
+#pragma once
+
+#include "moe_device.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------------------
+// Grouped GEMM
+// ---------------------------------------------------------------------------------------
+struct GemmArgs {
+  const Tile* tiles;
+  const int32_t* n_tiles;
+  const int32_t* grp_off;
+  const int32_t* row_list;
+  int tk;                 // compact rows (T*k)
+  long long recv_rows;    // receive rows (bound of gathered / scattered row indices)
+  int T;                  // shared-expert rows
+  int mt_routed;          // 128-row weight tiles per routed expert
+  int mt_shared;          // 128-row weight tiles of the shared expert (0: none)
+  int n_shared_tiles;     // token tiles of the shared expert
+  int k_steps;            // K / 64
+  int a_rows_routed;      // weight rows per routed expert
+  int a_up_routed;        // offset of the up rows (gate/up stage)
+  int a_up_shared;
+  void* out_routed;       // gate/up: h [tk][F] (compact rows); down: ebuf [recv_rows][d]
+  void* out_shared;       // gate/up: hs [T][Fs]; down: shared_out [T][d]
+  int ld_routed;          // output row length (elements)
+  int ld_shared;
+  int box_routed;         // rows per box of the contiguous token-row maps (routed / shared)
+  int box_shared;
+  const uint8_t* gather_base;  // gate/up: receive buffer (routed token rows are gathered)
+  long long gather_ld;         // bytes per receive row
+  uint32_t* status;
+  const int32_t* group_expert; // expert whose weights group g uses (nullptr: expert g)
+  int n_experts;               // experts in the weight tensors
+};
+
+// The expert whose weight rows a routed group reads: itself, or the expert its slot holds
+// (redundant experts). An entry outside [0, n_experts) is reported and replaced by expert 0, so
+// no weight read leaves the tensors.
+__device__ __forceinline__ int weight_expert(const int32_t* group_expert, int g, int n_experts,
+                                             uint32_t* status) {
+  if (!group_expert) return g;
+  const int e = group_expert[g];
+  if (e >= 0 && e < n_experts) return e;
+  raise_status(status, MOE_DEV_BOUNDS);
+  return 0;
+}
+
+struct Unit {
+  int g;       // routed expert, or -1 for the shared expert
+  int n0, nlen, m;
+};
+
+// Unit u -> (group, token tile, weight tile). Shared-expert units come first, token-tile-major.
+// A routed expert with nt token tiles owns units [mt*b, mt*(b+nt)), b = its first tile. The
+// gate/up stage takes them token-tile-major (unit mt*b + j*mt + m), so a token tile's rows are
+// reused by consecutive units. The down stage takes them weight-tile-major (unit
+// mt*b + m*nt + j): the nt units that read weight tile m run on adjacent CTAs at about the same
+// time, and on the skew workload this cut the down GEMM's DRAM reads from 10.56 to 8.50 GB
+// (the gate/up stage's traffic did not move with it). n_tiles: entries in the tile list.
+template <int BN, bool kWeightMajor>
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u, int n_tiles) {
+  Unit r;
+  const int us = a.n_shared_tiles * a.mt_shared;
+  if (u < us) {
+    const int tt = u / a.mt_shared;
+    r.g = -1;
+    r.m = u - tt * a.mt_shared;
+    r.n0 = tt * BN;
+    r.nlen = min(BN, a.T - r.n0);
+  } else {
+    const int v = u - us;
+    const int tt0 = v / a.mt_routed;   // a tile of the unit's expert (the ranges coincide)
+    const Tile t0 = a.tiles[tt0];
+    Tile t = t0;
+    if (!kWeightMajor) {
+      r.m = v - tt0 * a.mt_routed;
+    } else {
+      const int base = tt0 - t0.n0 / BN;
+      // (a list cut short at its bound, already reported, keeps every index inside it)
+      const int nt = max(1, min(t0.ntiles, n_tiles - base));
+      const int local = v - base * a.mt_routed;
+      r.m = local / nt;
+      const int j = local - r.m * nt;
+      if (base + j != tt0) t = a.tiles[base + j];
+    }
+    r.g = t.group;
+    r.n0 = t.n0;
+    r.nlen = t.nlen;
+  }
+  return r;
+}
+
+// Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies (tiles of
+// more than kSmallTile rows; smaller ones are four-row TMA gathers).
+constexpr int kGatherWarps = 2;
+constexpr int kSmallTile = 32;
+constexpr int kGatherThreads = kGatherWarps * 32;
+template <int STAGE>
+struct GemmThreads {
+  static constexpr int kGather = STAGE == 0 ? kGatherThreads : 0;
+  static constexpr int kAll = 192 + kGather;
+};
+
+template <int STAGE, int BN, int STAGES>
+struct GemmShape {
+  static constexpr int NA = STAGE == 0 ? 2 : 1;    // weight tiles per stage (gate, up)
+  static constexpr int A_BYTES = 128 * 128;        // 128 rows x 64 bf16
+  static constexpr int B_BYTES = BN * 128;         // BN rows x 64 bf16
+  static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = NA * BN;         // fp32 accumulator columns per buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : 2 * ACC_COLS;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+  static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "tensor memory");
+};
+
+
+// Host side: the arguments and TMA tensor maps of one bf16 GEMM stage (0 = gate/up with the
+// SwiGLU epilogue, 1 = down projection) for configuration c, as launch_ffn_gemm builds them.
+// maps: A (routed weights), A shared, B (routed token rows), B shared.
+cudaError_t prepare_bf16_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
+                              const void* x, const moe_weights& w, void* ebuf, void* shared_out,
+                              char* ws, const FfnPart& part, GemmArgs* args, CUtensorMap maps[4]);
+
+}  // namespace moe

@@ -42,6 +42,10 @@ struct WsLayout {
   size_t run_pre;     // int32 [R][E]: rows of expert e from sources before s
   size_t src_tok;     // int32 [R*R*cap]: token of each filled receive row (gather mode)
   size_t tok_list;    // int32 [T*k]: token of each compact row (gather mode)
+  size_t grp_order;   // int32 [E]: group at each schedule position (placed experts)
+  size_t fused_done;  // int32 [fused_done_n]: dependency counters of the fused expert launch
+  int shared_tiles;   // token tiles of the shared expert (0: none)
+  int fused_done_n;   // max_tiles + shared_tiles + 1
   size_t total;
   int bn;             // token-tile width of the expert GEMMs
   int max_tiles;      // bound on routed tiles: E + T*k/bn
@@ -117,9 +121,11 @@ struct FfnPart {
 // and, in gather mode, the routed rows). src_tok != nullptr: gather mode (the schedule also
 // lists each compact row's token).
 // quantise == false: the e4m3 quantisation of x was enqueued already (launch_quant_x).
+// group_expert: the slot->expert map of a placement (the schedule orders the groups by expert).
 cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
                              const void* x, char* ws, cudaStream_t st, bool pdl = false,
-                             const int32_t* src_tok = nullptr, bool quantise = true);
+                             const int32_t* src_tok = nullptr, bool quantise = true,
+                             const int32_t* group_expert = nullptr);
 
 // e4m3: x quantised once per token into the workspace (xq, xq_scales).
 cudaError_t launch_quant_x(const moe_cfg& c, const WsLayout& L, const void* x, char* ws,
@@ -130,6 +136,14 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
                             const float* recv_scales, const void* x, const moe_weights& w,
                             void* ebuf, void* shared_out, char* ws, cudaStream_t st,
                             bool pdl = false, const FfnPart& part = FfnPart());
+
+// bf16: both GEMMs and the combine in one persistent (cooperative) launch with device-side
+// dependency counters (csrc/moe_fused.cu). The combine's arguments are those of
+// launch_combine; part as for launch_ffn_gemm (the shared expert must be part of it).
+cudaError_t launch_ffn_fused(const moe_cfg& c, const WsLayout& L, const void* recv, const void* x,
+                             const moe_weights& w, void* ebuf, void* shared_out,
+                             const int32_t* row_of, const float* topk_w, void* y, char* ws,
+                             cudaStream_t st, const FfnPart& part);
 
 // e4m3 grouped GEMMs (non-swapped, per-128-K-block scale promotion), same stages.
 cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,

@@ -243,6 +243,15 @@ int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const floa
  * join_event (recorded on side_stream after them). On one GPU this partitions the SMs between
  * the two streams. The events are created by the caller (cudaEventDisableTiming is enough). */
 #define MOE_OPT_SHARED_SIDE_STREAM 2u
+/* Fused expert stage (bf16 only): the gate/up GEMM, the down GEMM and the combine run in one
+ * persistent cooperative launch ("DeepSeek MoE Serving: Where Expert-Parallel All-to-All Time
+ * Goes" (groundy), regimes table and the paragraph after it: a fused MoE kernel against
+ * separate kernels). A down unit starts as soon as the gate/up units of its own token tile
+ * have published their rows (device-side counters in ws, every wait bounded), so SMs that run
+ * out of gate/up units do not idle until the whole stage ends; the combine follows in the same
+ * launch. Not with MOE_OPT_SHARED_SIDE_STREAM (MOE_ERR_INVALID_ARG) or e4m3
+ * (MOE_ERR_UNSUPPORTED). Stage events 4..6 are all recorded after the launch. */
+#define MOE_OPT_FUSED_FFN 4u
 
 /* Redundant experts ("Serving Mixture-of-Experts", Hot-Expert Skew: place extra copies of the
  * busiest experts on under-loaded ranks and let the dispatch split their tokens across the

@@ -813,3 +813,93 @@ def test_placed_skew_prefill_lowers_the_imbalance_and_keeps_the_output():
     after = loads.max() / loads.mean()
     print("skew prefill rank IF: contiguous %.3f, placed %.3f" % (before, after))
     assert after < before and after < 1.1
+
+
+# ------------------------------------------------------------------------------------------
+# The fused expert stage: both GEMMs and the combine in one persistent launch (bf16)
+# ------------------------------------------------------------------------------------------
+FUSED_CFGS = [synth.CONFIGS["tiny"], SMALL, HOT, ER64, E192_R64,
+              synth.CONFIGS["dsv3_sweep"].with_T(8), synth.CONFIGS["dsv3_decode"],
+              synth.CONFIGS["dsv3_sweep"].with_T(256)]
+
+
+@pytest.mark.parametrize("cfg", FUSED_CFGS, ids=lambda c: c.name)
+def test_fused_expert_stage_equals_the_layer(cfg):
+    """The same rows through the same GEMM units and the combine's arithmetic: bit for bit the
+    output of moe_layer, alone and with gather mode, on three calls in a row (the dependency
+    counters are reset by every call)."""
+    inp, W = inputs(cfg)
+    m = moe()
+    y0 = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))(inp["x"]).clone()
+    torch.cuda.synchronize()
+    for v in (dict(fused=True), dict(fused=True, gather=True)):
+        lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), **v)
+        for _ in range(3):
+            y = lay(inp["x"])
+        torch.cuda.synchronize()
+        assert m.read_status(lay.bufs["ws"]) == 0, v
+        assert torch.equal(y, y0), v
+
+
+def test_fused_expert_stage_with_placed_experts_and_events():
+    cfg = synth.CONFIGS["dsv3_decode"]
+    inp, W = inputs(cfg)
+    m = moe()
+    y0 = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))(inp["x"]).clone()
+    pl, _ = _placement_for(cfg, inp, 4, 31)
+    lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), placement=pl, fused=True,
+                     gather=True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_LAYER_EVENTS)]
+    for e in evs:
+        e.record()
+    y = lay(inp["x"], events=evs)
+    torch.cuda.synchronize()
+    assert m.read_status(lay.bufs["ws"]) == 0
+    assert torch.equal(y, y0)
+    times = [evs[0].elapsed_time(e) for e in evs]
+    assert all(b >= a for a, b in zip(times, times[1:]))
+
+
+def test_fused_back_to_back_and_in_a_cuda_graph():
+    cfg = SMALL
+    inp, W = inputs(cfg)
+    m = moe()
+    lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), fused=True, gather=True)
+    ref = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    g = torch.Generator(device="cuda").manual_seed(5)
+    xs = [torch.randn(tuple(inp["x"].shape), generator=g, device="cuda").to(inp["x"].dtype)
+          for _ in range(3)]
+    outs = [lay(x).clone() for x in xs]          # queued back to back, no synchronisation
+    torch.cuda.synchronize()
+    for x, y in zip(xs, outs):
+        assert torch.equal(y, ref(x))
+    x_buf = xs[0].clone()
+    y_buf = torch.empty_like(outs[0])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        lay(x_buf, y_buf)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        lay(x_buf, y_buf)
+    for x in xs:
+        x_buf.copy_(x)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y_buf, ref(x))
+    assert m.read_status(lay.bufs["ws"]) == 0
+
+
+def test_fused_rejects_fp8_and_the_side_stream():
+    m = moe()
+    inp, W = inputs(FP8_SMALL)
+    with pytest.raises(m.MoEError) as e:
+        m.MoELayer(FP8_SMALL, inp["w_gate"], inp["bias"], weight_dict(W), fused=True)(inp["x"])
+    assert e.value.code == 2
+    inp, W = inputs(SMALL)
+    with pytest.raises(m.MoEError) as e:
+        m.MoELayer(SMALL, inp["w_gate"], inp["bias"], weight_dict(W), fused=True,
+                   side_stream=True)(inp["x"])
+    assert e.value.code == 1
