@@ -105,7 +105,7 @@ WsLayout ws_layout(const moe_cfg& c) {
   L.tok_list = o;   o = up256(o + sizeof(int32_t) * tk);
   L.grp_order = o;  o = up256(o + sizeof(int32_t) * c.E);
   L.shared_tiles = c.d_ff_shared ? (c.T + L.bn - 1) / L.bn : 0;
-  L.fused_done_n = L.max_tiles + L.shared_tiles + 1;
+  L.fused_done_n = L.max_tiles + L.shared_tiles + 2;
   L.fused_done = o; o = up256(o + sizeof(int32_t) * (size_t)L.fused_done_n);
   L.total = o;
   return L;

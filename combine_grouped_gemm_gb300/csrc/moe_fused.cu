@@ -49,6 +49,7 @@ struct FusedArgs {
   int32_t* done_tile;        // [max_tiles]: gate/up epilogue warps finished per routed tile
   int32_t* done_shared;      // [shared tiles]: the same for the shared expert's token tiles
   int32_t* done_down;        // [1]: down epilogue warps finished
+  int32_t* done_up;          // [1]: gate/up epilogue warps finished, all tiles together
   CombineArgs cb;
 };
 
@@ -111,7 +112,20 @@ __device__ __forceinline__ bool wait_count(const int32_t* p, int target, volatil
   }
 }
 
-template <int BN, int STAGES>
+// Shared memory: the gate/up stages (two weight tiles and a token tile each) and, over the same
+// bytes, the down stages (one weight tile and a token tile: more of them, so the down phase
+// keeps as many bytes in flight as the down kernel does). A CTA's producer moves to the down
+// ring once, after its last gate/up stage has been consumed.
+template <int BN, int STAGES, int STAGES2>
+struct FusedShape {
+  using G = GemmShape<0, BN, STAGES>;
+  static constexpr int STAGE2_BYTES = G::A_BYTES + G::B_BYTES;
+  static_assert(STAGE2_BYTES % 1024 == 0, "down stages stay 1024-byte aligned");
+  static_assert(STAGES2 * STAGE2_BYTES <= STAGES * G::STAGE_BYTES, "down ring inside the ring");
+  static_assert((2 * STAGES + 2 * STAGES2 + 4) * 8 + 8 <= 256, "barriers in the reserved bytes");
+};
+
+template <int BN, int STAGES, int STAGES2>
 __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
     ffn_fused_bf16_kernel(const __grid_constant__ FusedArgs f, const __grid_constant__ CUtensorMap gA,
                           const __grid_constant__ CUtensorMap gAs,
@@ -123,12 +137,15 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
                           const __grid_constant__ CUtensorMap dBs) {
   // stages laid out for gate/up (two weight tiles); a down unit uses the first weight slot
   using S = GemmShape<0, BN, STAGES>;
+  constexpr int S2B = FusedShape<BN, STAGES, STAGES2>::STAGE2_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint64_t* full2 = empty + STAGES;     // the down ring
+  uint64_t* empty2 = full2 + STAGES2;
+  uint64_t* tfull = empty2 + STAGES2;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -139,6 +156,10 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1 + GemmThreads<0>::kGather);
       mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < STAGES2; ++i) {
+      mbar_init(&full2[i], 1);   // the producer's arrival only: nothing is gathered for down
+      mbar_init(&empty2[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -178,12 +199,24 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
     // ------------------------------ TMA producer ------------------------------
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_x = l2_policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
+    int stage = 0, stage2 = 0;
+    uint32_t phase = 0, phase2 = 0;
+    bool ok = true, on_ring2 = false;
+    bool all_up = false;   // seen every gate/up unit finish: no more waits or fences needed
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const FUnit fu = decode_fused<BN>(f, u, n_tiles, U0);
       const bool up = fu.stage == 0;
+      if (!up && !on_ring2) {
+        // the down ring overlays the gate/up stages: wait until every one of them has been
+        // consumed (the waits this warp would make before refilling each)
+        for (int i = 0; i < STAGES && ok; ++i) {
+          const int sl = (stage + i) % STAGES;
+          const uint32_t ph = stage + i >= STAGES ? phase ^ 1u : phase;
+          ok = mbar_wait(&empty[sl], ph ^ 1u, abort_flag, status);
+        }
+        on_ring2 = true;
+        if (!ok) break;
+      }
       const GemmArgs& a = up ? f.gu : f.dn;
       const Unit& t = fu.t;
       const bool sh = t.g < 0;
@@ -230,18 +263,25 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
         box_row = in ? row0 : -1;
         b_bytes = in ? 128u * static_cast<uint32_t>(sh ? a.box_shared : a.box_routed) : 0u;
       }
-      if (!up) {
+      if (!up && !all_up) {
         // this token tile's intermediate h must be complete: every gate/up unit of the tile
-        // (mt of them, four epilogue warps each) has published its rows
+        // (mt of them, four epilogue warps each) has published its rows. Once every gate/up
+        // unit of the launch has (one counter), all of h is there and the remaining down units
+        // go without a check.
         int done = 1;
         if (lane == 0) {
-          const int32_t* cnt = sh ? f.done_shared + fu.tile : f.done_tile + fu.tile;
-          const int target = 4 * (sh ? f.gu.mt_shared : f.gu.mt_routed);
-          done = wait_count(cnt, target, abort_flag, status) ? 1 : 0;
+          if (ld_acquire(f.done_up) >= 4 * U0) {
+            all_up = true;
+          } else {
+            const int32_t* cnt = sh ? f.done_shared + fu.tile : f.done_tile + fu.tile;
+            const int target = 4 * (sh ? f.gu.mt_shared : f.gu.mt_routed);
+            done = wait_count(cnt, target, abort_flag, status) ? 1 : 0;
+          }
           // the rows were written through the generic proxy; the TMA reads them through the
           // async proxy
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
+        all_up = __shfl_sync(0xffffffffu, all_up ? 1 : 0, 0) != 0;
         if (!__shfl_sync(0xffffffffu, done, 0)) {
           ok = false;
           break;
@@ -249,33 +289,39 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
       }
       const uint32_t tx = (up ? 2 : 1) * S::A_BYTES + b_bytes;
       for (int ks = 0; ks < a.k_steps; ++ks) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) {
+        uint64_t* fb = up ? &full[stage] : &full2[stage2];
+        if (!mbar_wait(up ? &empty[stage] : &empty2[stage2], (up ? phase : phase2) ^ 1u,
+                       abort_flag, status)) {
           ok = false;
           break;
         }
-        uint8_t* sa = smem + stage * S::STAGE_BYTES;
-        uint8_t* sb = sa + 2 * S::A_BYTES;
+        uint8_t* sa = up ? smem + stage * S::STAGE_BYTES : smem + stage2 * S2B;
+        uint8_t* sb = sa + (up ? 2 : 1) * S::A_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d(sa, amap, &full[stage], ks * 64, arow0, pol_w);
-          if (up) tma_load_2d(sa + S::A_BYTES, amap, &full[stage], ks * 64, arow1, pol_w);
-          if (box_row >= 0) tma_load_2d(sb, bmap, &full[stage], ks * 64, box_row, pol_x);
+          mbar_arrive_expect_tx(fb, tx);
+          tma_load_2d(sa, amap, fb, ks * 64, arow0, pol_w);
+          if (up) tma_load_2d(sa + S::A_BYTES, amap, fb, ks * 64, arow1, pol_w);
+          if (box_row >= 0) tma_load_2d(sb, bmap, fb, ks * 64, box_row, pol_x);
         }
         __syncwarp();
         if (g4_on)
-          tma_gather4(sb + lane * 512, bmap, &full[stage], ks * 64, g4[0], g4[1], g4[2], g4[3],
-                      pol_x);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+          tma_gather4(sb + lane * 512, bmap, fb, ks * 64, g4[0], g4[1], g4[2], g4[3], pol_x);
+        if (up) {
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        } else if (++stage2 == STAGES2) {
+          stage2 = 0;
+          phase2 ^= 1u;
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, stage2 = 0;
+      uint32_t phase = 0, phase2 = 0;
       bool ok = true;
       int it = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
@@ -290,14 +336,15 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
         const uint32_t d0 = tmem + b * S::ACC_COLS;
         const uint32_t d1 = d0 + BN;
         for (int ks = 0; ks < k_steps; ++ks) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, status)) {
+          if (!mbar_wait(up ? &full[stage] : &full2[stage2], up ? phase : phase2, abort_flag,
+                         status)) {
             ok = false;
             break;
           }
           fence_proxy_async_smem();   // gathered rows written by cp.async (gate/up)
           tc_fence_after();
-          const uint32_t sa = smem_addr(smem + stage * S::STAGE_BYTES);
-          const uint32_t sb = sa + 2 * S::A_BYTES;
+          const uint32_t sa = smem_addr(up ? smem + stage * S::STAGE_BYTES : smem + stage2 * S2B);
+          const uint32_t sb = sa + (up ? 2 : 1) * S::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t db = smem_desc_sw128(sb + kk * 32);
@@ -305,10 +352,18 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
             mma_f16(d0, smem_desc_sw128(sa + kk * 32), db, idesc, acc);
             if (up) mma_f16(d1, smem_desc_sw128(sa + S::A_BYTES + kk * 32), db, idesc, acc);
           }
-          mma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if (up) {
+            mma_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          } else {
+            mma_commit(&empty2[stage2]);
+            if (++stage2 == STAGES2) {
+              stage2 = 0;
+              phase2 ^= 1u;
+            }
           }
         }
         if (ok) mma_commit(&tfull[b]);
@@ -317,7 +372,8 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
     __syncwarp();
   } else if (warp >= 6) {
     // ------------------------------ token-row gather (gate/up) ------------------------------
-    // as in the gate/up kernel; on every other unit these threads only arrive once per k-step
+    // as in the gate/up kernel; on the gate/up units with nothing to gather these threads only
+    // arrive once per k-step
     constexpr int kRowsPer = BN / 8;
     const int gt = threadIdx.x - 192;
     const int j = gt & 7, rg = gt >> 3;
@@ -325,12 +381,14 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    // gate/up units only: every down unit comes after them, and the down ring's barriers
+    // expect no arrival from these warps
+    for (int u = blockIdx.x; u < U0 && ok; u += gridDim.x) {
       const FUnit fu = decode_fused<BN>(f, u, n_tiles, U0);
-      const bool up = fu.stage == 0;
-      const GemmArgs& a = up ? f.gu : f.dn;
+      const bool up = true;
+      const GemmArgs& a = f.gu;
       const Unit& t = fu.t;
-      const bool gather = up && t.g >= 0 && t.nlen > kSmallTile;
+      const bool gather = t.g >= 0 && t.nlen > kSmallTile;
       const uint8_t* src[kRowsPer];
 #pragma unroll
       for (int i = 0; i < kRowsPer; ++i) {
@@ -343,18 +401,21 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
           else raise_status(a.status, MOE_DEV_BOUNDS);
         }
       }
+      (void)up;
       for (int ks = 0; ks < a.k_steps; ++ks) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) {
           ok = false;
           break;
         }
         const uint32_t sb = smem_addr(smem + stage * S::STAGE_BYTES + 2 * S::A_BYTES) + dst_off;
+        if (gather) {
 #pragma unroll
-        for (int i = 0; i < kRowsPer; ++i)
-          if (src[i])
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sb + i * 1024),
-                         "l"(src[i] + ks * 128)
-                         : "memory");
+          for (int i = 0; i < kRowsPer; ++i)
+            if (src[i])
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sb + i * 1024),
+                           "l"(src[i] + ks * 128)
+                           : "memory");
+        }
         asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
                          smem_addr(&full[stage]))
                      : "memory");
@@ -425,6 +486,7 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
         // publish this warp's rows: the token tile's h (gate/up) or the output rows (down)
         int32_t* cnt = !up ? f.done_down : (sh ? f.done_shared + fu.tile : f.done_tile + fu.tile);
         red_release_add(cnt, 1);
+        if (up) red_release_add(f.done_up, 1);
       }
     }
   }
@@ -509,11 +571,11 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
   }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int STAGES2>
 cudaError_t run_fused(const FusedArgs& f, const CUtensorMap* g, const CUtensorMap* dm,
                       cudaStream_t st) {
   using S = GemmShape<0, BN, STAGES>;
-  auto kern = ffn_fused_bf16_kernel<BN, STAGES>;
+  auto kern = ffn_fused_bf16_kernel<BN, STAGES, STAGES2>;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), S::SMEM);
   if (err != cudaSuccess) return err;
   // cooperative: every CTA is resident at once, so a unit that waits for another CTA's units
@@ -549,6 +611,7 @@ cudaError_t launch_ffn_fused(const moe_cfg& c, const WsLayout& L, const void* re
   f.done_tile = reinterpret_cast<int32_t*>(ws + L.fused_done);
   f.done_shared = f.done_tile + L.max_tiles;
   f.done_down = f.done_shared + L.shared_tiles;
+  f.done_up = f.done_down + 1;
   err = cudaMemsetAsync(f.done_tile, 0, sizeof(int32_t) * (size_t)L.fused_done_n, st);
   if (err != cudaSuccess) return err;
   CombineArgs& cb = f.cb;
@@ -567,8 +630,10 @@ cudaError_t launch_ffn_fused(const moe_cfg& c, const WsLayout& L, const void* re
   while (c.T * nslice < 2 * 152 && vpr / (nslice * 2) >= 128) nslice *= 2;
   cb.slice_vecs = (vpr + nslice - 1) / nslice;
   cb.nslice = (vpr + cb.slice_vecs - 1) / cb.slice_vecs;
-  if (L.bn == 64) return run_fused<64, 5>(f, g, dm, st);
-  return run_fused<128, 4>(f, g, dm, st);
+  // the stage counts of the separate kernels: gate/up 5 x 40 KB and down 8 x 24 KB (64-token
+  // tiles), 4 x 48 KB and 6 x 32 KB (128-token tiles)
+  if (L.bn == 64) return run_fused<64, 5, 8>(f, g, dm, st);
+  return run_fused<128, 4, 6>(f, g, dm, st);
 }
 
 }  // namespace moe

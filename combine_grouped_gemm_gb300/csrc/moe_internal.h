@@ -45,7 +45,7 @@ struct WsLayout {
   size_t grp_order;   // int32 [E]: group at each schedule position (placed experts)
   size_t fused_done;  // int32 [fused_done_n]: dependency counters of the fused expert launch
   int shared_tiles;   // token tiles of the shared expert (0: none)
-  int fused_done_n;   // max_tiles + shared_tiles + 1
+  int fused_done_n;   // max_tiles + shared_tiles + 2
   size_t total;
   int bn;             // token-tile width of the expert GEMMs
   int max_tiles;      // bound on routed tiles: E + T*k/bn

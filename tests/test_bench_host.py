@@ -72,17 +72,26 @@ def test_binding_roof_per_stage():
 
 def test_traffic_lookup_goes_stale_with_its_kernel_source(tmp_path, monkeypatch):
     src = tmp_path / "kernel.cu"
+    hdr = tmp_path / "kernel.cuh"
     src.write_text("first version\n")
-    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    hdr.write_text("header\n")
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
-        {"ffn_gate_up@w": {"source": "kernel.cu", "source_sha256_16": h,
-                           "dram_bytes_per_launch": 123}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.measured_traffic("ffn_gate_up", "w") == 123
-    assert bench.measured_traffic("ffn_down", "w") is None
-    src.write_text("second version\n")
-    assert bench.measured_traffic("ffn_gate_up", "w") is None
+    h = bench.sources_hash(["kernel.cu", "kernel.cuh"])
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"ffn_gate_up@w": {"sources": ["kernel.cu", "kernel.cuh"], "sources_sha256_16": h,
+                           "dram_bytes_per_launch": 123},
+         "ffn_down@dsv3_decode_e32": {"sources": ["kernel.cu", "kernel.cuh"],
+                                      "sources_sha256_16": h, "dram_bytes_per_launch": 1100,
+                                      "algorithmic_bytes_per_launch": 1000}}))
+    assert bench.measured_traffic("ffn_gate_up", "w", 999)[0] == 123      # its own capture
+    assert bench.measured_traffic("ffn_down", "w", 999)[0] is None        # none at all
+    # the full decode launch scaled from its stand-in: 1.1 x its own algorithmic bytes
+    t, note = bench.measured_traffic("ffn_down", "dsv3_decode", 50000)
+    assert t == 55000 and "dsv3_decode_e32" in note
+    hdr.write_text("second version\n")                                   # any source changes
+    assert bench.measured_traffic("ffn_gate_up", "w", 999)[0] is None
+    assert bench.measured_traffic("ffn_down", "dsv3_decode", 50000)[0] is None
 
 
 @pytest.mark.parametrize("rank", [0, 1])
