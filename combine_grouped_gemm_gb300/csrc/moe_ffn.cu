@@ -319,7 +319,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
-    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_w1 = l2_policy_evict_first();   // weights read once
+    const uint64_t pol_wk = l2_policy_evict_last();    // weights read again (weight_policy)
     const uint64_t pol_x = l2_policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
@@ -327,6 +328,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
       const bool sh = t.g < 0;
+      const uint64_t pol_w = weight_policy(t, pol_w1, pol_wk);
       const CUtensorMap* amap = sh ? &mapAs : &mapA;
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
       const int we = sh ? 0 : weight_expert(a.group_expert, t.g, a.n_experts,

@@ -197,7 +197,8 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
-    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_w1 = l2_policy_evict_first();
+    const uint64_t pol_wk = l2_policy_evict_last();
     const uint64_t pol_x = l2_policy_evict_last();
     int stage = 0, stage2 = 0;
     uint32_t phase = 0, phase2 = 0;
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(GemmThreads<0>::kAll, 1)
       const GemmArgs& a = up ? f.gu : f.dn;
       const Unit& t = fu.t;
       const bool sh = t.g < 0;
+      const uint64_t pol_w = weight_policy(t, pol_w1, pol_wk);
       const CUtensorMap* amap = up ? (sh ? &gAs : &gA) : (sh ? &dAs : &dA);
       const CUtensorMap* bmap = up ? (sh ? &gBs : &gB) : (sh ? &dBs : &dB);
       const int we = sh ? 0 : weight_expert(a.group_expert, t.g, a.n_experts,

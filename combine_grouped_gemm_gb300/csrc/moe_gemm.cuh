@@ -55,6 +55,7 @@ __device__ __forceinline__ int weight_expert(const int32_t* group_expert, int g,
 struct Unit {
   int g;       // routed expert, or -1 for the shared expert
   int n0, nlen, m;
+  int nt;      // token tiles of the group (units of one weight tile that read it again)
 };
 
 // Unit u -> (group, token tile, weight tile). Shared-expert units come first, token-tile-major.
@@ -74,6 +75,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u, int n_tile
     r.m = u - tt * a.mt_shared;
     r.n0 = tt * BN;
     r.nlen = min(BN, a.T - r.n0);
+    r.nt = a.n_shared_tiles;
   } else {
     const int v = u - us;
     const int tt0 = v / a.mt_routed;   // a tile of the unit's expert (the ranges coincide)
@@ -93,8 +95,20 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u, int n_tile
     r.g = t.group;
     r.n0 = t.n0;
     r.nlen = t.nlen;
+    r.nt = t.ntiles;
   }
   return r;
+}
+
+// L2 policy of a unit's weight tiles. A group with one token tile reads each weight tile once:
+// evict-first, so the stream does not push out what is reused. A group with several token
+// tiles (a hot expert, or the shared expert at prefill) reads each weight tile once per token
+// tile, in units that run close together: evict-last keeps the tile for the next one. On the
+// skewed prefill (hottest expert about 10x the mean load) this took the gate/up GEMM from 3358
+// to 2858 us and the down GEMM from 1822 to 1761 us; the decode layer, one tile per expert,
+// is unchanged.
+__device__ __forceinline__ uint64_t weight_policy(const Unit& t, uint64_t once, uint64_t reused) {
+  return t.nt > 1 ? reused : once;
 }
 
 // Gate/up only: warps that gather the routed token rows with 16-byte cp.async copies (tiles of

@@ -25,6 +25,25 @@ def test_kernels_per_step_follows_the_launch_structure():
     assert bench.kernels_per_step(C["dsv3_fp8_prefill"]) == 10
 
 
+def test_kernels_per_step_of_the_layer_variants():
+    dec, f8 = C["dsv3_decode"], C["dsv3_fp8_prefill"]
+    assert bench.kernels_per_step(dec, "gather") == 7          # no copy kernel
+    assert bench.kernels_per_step(dec, "side") == 10           # + the shared expert's 2 GEMMs
+    assert bench.kernels_per_step(dec, "fused") == 6           # GEMMs and combine in one launch
+    assert bench.kernels_per_step(dec, "gather+fused") == 5
+    assert bench.kernels_per_step(C["tiny"], "side") == 8      # no shared expert: nothing moves
+    # e4m3: the quantisation of x runs for the shared expert and for gather mode alike
+    assert bench.kernels_per_step(f8, "gather") == 9
+    # without a shared expert gather mode swaps the dispatch's e4m3 copy for the quantisation
+    assert bench.kernels_per_step(dataclasses_replace(f8, d_ff_shared=0), "gather") == 9
+    assert bench.kernels_per_step(dataclasses_replace(f8, d_ff_shared=0), "layer") == 9
+
+
+def dataclasses_replace(cfg, **kw):
+    import dataclasses
+    return dataclasses.replace(cfg, **kw)
+
+
 def _counts(cfg, touched):
     c = np.zeros((cfg.R, cfg.E), dtype=np.int64)
     c[0, :touched] = 1
