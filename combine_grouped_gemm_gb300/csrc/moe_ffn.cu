@@ -40,8 +40,8 @@ namespace {
 // ---------------------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;             // upper bound; launched with E rounded up to 32
 // counts table staged in shared memory up to this: the 48 KB a kernel gets without an opt-in,
-// less the kernel's static shared memory (warp sums and rank bases, 388 bytes; the schedule
-// order by position, 8 KB)
+// less the kernel's static shared memory (warp sums and rank bases, 388 bytes; two tables by
+// schedule position, 8 KB)
 constexpr size_t kPlanStageBytes = 39 * 1024;
 constexpr int kPlanFusedRows = 1024;            // fill the row list in the plan CTA up to this T*k
 
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     int32_t* __restrict__ grp_order) {
   __shared__ int warp_sums[33];
   __shared__ int rank_base[64];
-  __shared__ int ord_g[kPlanThreads];   // group at each schedule position
+  __shared__ int ord_g[kPlanThreads];   // group at each schedule position (then its expert)
   __shared__ int ord_n[kPlanThreads];   // its rows
   extern __shared__ int32_t cnt_s[];   // counts staged once: [R][E] when it fits, else unused
   pdl_wait();
@@ -157,10 +157,9 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
   int n = 0;
   if (act)
     for (int s = 0; s < R; ++s) n += cnt(s);
-  // Schedule order of the groups (compact rows and tiles): by index, or, when the groups are
-  // slots holding copies of experts, by (expert, slot), so the copies of one expert run on
-  // adjacent units and read its weight tiles at about the same time (from L2 after the
-  // first). Thread i then handles the group at position i.
+  // Schedule order of the groups (compact rows): by index, or, when the groups are slots
+  // holding copies of experts, by (expert, slot), so the compact rows of an expert's copies are
+  // contiguous. Thread i then handles the group at position i.
   int g_i = e, n_i = n;
   if (group_expert) {
     if (act) {
@@ -181,7 +180,25 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
   int total;
   const int off = block_exclusive_scan(act ? n_i : 0, &total, warp_sums);
   if (threadIdx.x == 0 && total != tk) raise_status(status, MOE_DEV_BOUNDS);
-  const int nt = act ? (n_i + bn - 1) / bn : 0;
+  // GEMM tiles: over each group's rows, or, for the copies of a placed expert, over all of the
+  // expert's rows at once (contiguous in the order above), named by its first copy. The copies'
+  // rows then go through the expert's weights in the same units, as without a placement: on
+  // one GPU the copies share one set of weights, and reading it once per copy would only add
+  // weight traffic. The receive layout and the counts stay per slot.
+  int tile_rows = act ? n_i : 0;   // rows this position's tiles cover
+  if (group_expert) {
+    __syncthreads();   // (ord_g was read above)
+    if (act) ord_g[threadIdx.x] = group_expert[g_i];
+    __syncthreads();
+    if (act) {
+      const int eg = ord_g[threadIdx.x];
+      const bool head = threadIdx.x == 0 || ord_g[threadIdx.x - 1] != eg;
+      tile_rows = 0;
+      if (head)
+        for (int q = threadIdx.x; q < E && ord_g[q] == eg; ++q) tile_rows += ord_n[q];
+    }
+  }
+  const int nt = (tile_rows + bn - 1) / bn;
   int tiles_total;
   const int toff = block_exclusive_scan(nt, &tiles_total, warp_sums);
   if (act) {
@@ -189,7 +206,7 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     grp_off[g_i] = off;
     for (int j = 0; j < nt; ++j) {
       const int ti = toff + j;
-      if (ti < max_tiles) tiles[ti] = Tile{g_i, j * bn, min(bn, n_i - j * bn), nt};
+      if (ti < max_tiles) tiles[ti] = Tile{g_i, j * bn, min(bn, tile_rows - j * bn), nt};
     }
   }
   if (threadIdx.x == 0) {

@@ -63,24 +63,13 @@ template <int BN>
 __device__ __forceinline__ FUnit decode_fused(const FusedArgs& f, int u, int n_tiles, int U0) {
   FUnit r;
   if (u < U0) {
-    const GemmArgs& a = f.gu;
-    const int us = a.n_shared_tiles * a.mt_shared;
     r.stage = 0;
-    r.t = decode_unit<BN, false>(a, u, n_tiles);
-    r.tile = u < us ? u / a.mt_shared : (u - us) / a.mt_routed;
+    r.t = decode_unit<BN, false>(f.gu, u, n_tiles);
   } else {
-    const GemmArgs& a = f.dn;
-    const int v = u - U0;
-    const int us = a.n_shared_tiles * a.mt_shared;
     r.stage = 1;
-    r.t = decode_unit<BN, true>(a, v, n_tiles);
-    if (v < us) {
-      r.tile = v / a.mt_shared;
-    } else {   // the group's first tile plus this unit's token tile
-      const int tt0 = (v - us) / a.mt_routed;
-      r.tile = tt0 - a.tiles[tt0].n0 / BN + r.t.n0 / BN;
-    }
+    r.t = decode_unit<BN, true>(f.dn, u - U0, n_tiles);
   }
+  r.tile = r.t.ti;
   return r;
 }
 

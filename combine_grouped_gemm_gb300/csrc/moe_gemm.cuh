@@ -55,7 +55,8 @@ __device__ __forceinline__ int weight_expert(const int32_t* group_expert, int g,
 struct Unit {
   int g;       // routed expert, or -1 for the shared expert
   int n0, nlen, m;
-  int nt;      // token tiles of the group (units of one weight tile that read it again)
+  int nt;      // token tiles of the group (units that read this unit's weight tiles)
+  int ti;      // the unit's token tile: its index in the tile list, or the shared tile number
 };
 
 // Unit u -> (group, token tile, weight tile). Shared-expert units come first, token-tile-major.
@@ -76,11 +77,13 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u, int n_tile
     r.n0 = tt * BN;
     r.nlen = min(BN, a.T - r.n0);
     r.nt = a.n_shared_tiles;
+    r.ti = tt;
   } else {
     const int v = u - us;
     const int tt0 = v / a.mt_routed;   // a tile of the unit's expert (the ranges coincide)
     const Tile t0 = a.tiles[tt0];
     Tile t = t0;
+    int ti = tt0;
     if (!kWeightMajor) {
       r.m = v - tt0 * a.mt_routed;
     } else {
@@ -90,12 +93,14 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u, int n_tile
       const int local = v - base * a.mt_routed;
       r.m = local / nt;
       const int j = local - r.m * nt;
-      if (base + j != tt0) t = a.tiles[base + j];
+      ti = base + j;
+      if (ti != tt0) t = a.tiles[ti];
     }
+    r.nt = t0.ntiles;
     r.g = t.group;
     r.n0 = t.n0;
     r.nlen = t.nlen;
-    r.nt = t.ntiles;
+    r.ti = ti;
   }
   return r;
 }

@@ -14,7 +14,9 @@ namespace moe {
 constexpr int kRouteChunks = 16;
 
 // One entry of the expert-GEMM tile schedule: rows [n0, n0+nlen) of group g, which has ntiles
-// token tiles in all (its entries are consecutive, n0 = j * bn for the j-th).
+// token tiles in all (its entries are consecutive, n0 = j * bn for the j-th). With placed
+// experts a group's tiles cover the compact rows of all the expert's copies, and g is its first
+// copy.
 struct Tile {
   int32_t group;
   int32_t n0;

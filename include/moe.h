@@ -265,7 +265,9 @@ int moe_layer(const moe_cfg* cfg, const void* x, const float* w_gate, const floa
  *  slot_expert [G]: the expert each slot holds; n_copies [E]: copies of each expert (>= 1);
  *  copy_slot [E][max_copies]: the slots of each expert's copies in ascending order.
  * With a placement the receive layout and counts are over the G slots (counts [R][G],
- * cap = (T/R) * min(k, slots_per_rank); moe_query_sizes_placed gives the sizes). */
+ * cap = (T/R) * min(k, slots_per_rank); moe_query_sizes_placed gives the sizes). The expert
+ * GEMMs take the rows of all copies of an expert through its weights together (one GPU holds
+ * one set of weights per expert), so the output equals moe_layer's bit for bit. */
 typedef struct moe_placement {
   int32_t slots_per_rank;
   int32_t max_copies;
