@@ -5,18 +5,24 @@ no step of the MoE method (no routing, dispatch, expert or combine arithmetic): 
 counter-based random number generator, the value distributions of the workloads, and the
 workload shapes themselves.
 
-Generator definition (the same on every device, so a tensor made on the GPU equals the same
-tensor made on the CPU, bit for bit):
+Generator definition:
 
 * ``key(seed, tag)`` derives two 32-bit keys from the seed and a per-tensor tag.
 * 32-bit word number ``c`` (a 64-bit counter) of a stream is
   ``mix(mix(lo32(c) ^ k0) ^ mix(hi32(c) ^ k1))`` where ``mix`` is the "lowbias32" integer hash
   (C. Wellons, 2018: xor-shift 16, multiply 0x7feb352d, xor-shift 15, multiply 0x846ca68b,
-  xor-shift 16). All of it is integer arithmetic on int64 tensors kept below 2**63.
-* Element ``i`` of a tensor uses words ``2i`` and ``2i+1``. Their four 16-bit halves are summed
-  (an Irwin-Hall sum of four uniforms, a bounded bell-shaped stand-in for a normal draw, support
-  +-3.46 standard deviations); ``(2*sum - 262140)`` is an exact integer that is multiplied once,
-  in fp32, by ``std * sqrt(3) / 131072``. Uniform draws use the top 24 bits of word ``i``.
+  xor-shift 16). All of it is integer arithmetic on int64 tensors kept below 2**63, so the words
+  are the same on every device.
+* Element ``i`` of a normal tensor uses words ``2i`` and ``2i+1`` as two uniforms,
+  ``u1 = (w0 + 1) / 2**32`` in (0, 1] and ``u2 = w1 / 2**32`` in [0, 1), and takes the cosine
+  branch of the Box-Muller transform (G. Box and M. Muller, 1958),
+  ``z = sqrt(-2 ln u1) * cos(2 pi u2)``, a standard normal draw (|z| <= 6.66 at 32-bit
+  resolution). ``z * std`` is computed in fp64 and rounded once to fp32. The fp64 log, sqrt and
+  cos come from the device's math library, whose last bit can differ between devices; after
+  the rounding to fp32 such a difference survives only for the rare draws within a few fp64
+  ulps of an fp32 rounding boundary. Every check gives the oracle the host copy of the very
+  tensor the CUDA path reads, so none depends on it.
+* Uniform draws use the top 24 bits of word ``i`` (exact on every device).
 * bf16 values are the fp32 value rounded to nearest even (torch's conversion); e4m3 weights
   are block-quantised from fp32 draws (see ``fp8_block_weights``).
 """
@@ -174,25 +180,21 @@ def word_int(c: int, k0: int, k1: int) -> int:
     return _mix32_int(_mix32_int((c & M32) ^ k0) ^ _mix32_int(((c >> 32) & M32) ^ k1))
 
 
-def _irwin_hall4(idx: torch.Tensor, k0: int, k1: int) -> torch.Tensor:
-    s = torch.zeros_like(idx)
-    for j in range(2):
-        w = word(idx * 2 + j, k0, k1)
-        s += (w & 0xFFFF) + (w >> 16)
-    return s
+def _normal_f64(idx: torch.Tensor, k0: int, k1: int) -> torch.Tensor:
+    """Standard normal draws for element indices ``idx`` (Box-Muller, cosine branch, fp64)."""
+    u1 = (word(idx * 2, k0, k1) + 1).to(torch.float64) * 2.0 ** -32
+    u2 = word(idx * 2 + 1, k0, k1).to(torch.float64) * 2.0 ** -32
+    return torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
 
 
 def _normal_f32_range(seed, tag, start, n, std, device):
     k0, k1 = key(seed, tag)
     idx = torch.arange(start, start + n, dtype=torch.int64, device=device)
-    s = _irwin_hall4(idx, k0, k1)
-    c = torch.tensor(np.float32(std * math.sqrt(3.0) / 131072.0), dtype=torch.float32,
-                     device=device)
-    return (2 * s - 262140).to(torch.float32) * c
+    return (_normal_f64(idx, k0, k1) * float(std)).to(torch.float32)
 
 
 def normal_f32(seed: int, tag: int, shape, std: float, device="cpu", start: int = 0):
-    """fp32 tensor of bell-shaped draws with standard deviation ``std``.
+    """fp32 tensor of normal draws with mean 0 and standard deviation ``std``.
 
     ``start`` offsets the element counter, so a slice of a large tensor can be made alone."""
     n = int(np.prod(shape))

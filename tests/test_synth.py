@@ -1,5 +1,5 @@
 """The seeded generator: its tensor form equals its scalar definition, slices equal the whole,
-and the draws have the stated moments."""
+and the draws have the stated distributions."""
 import numpy as np
 import torch
 
@@ -14,13 +14,36 @@ def test_word_matches_scalar_definition():
     assert all(0 <= g < (1 << 32) for g in got)
 
 
-def test_normal_moments_and_bounds():
-    x = synth.normal_f32(5, synth.TAG_X, (1 << 20,), 1.0)
-    assert abs(x.mean().item()) < 0.01
-    assert abs(x.std().item() - 1.0) < 0.01
-    assert x.abs().max().item() <= 2 * 3 ** 0.5 + 1e-6
+def test_normal_draws_are_standard_normal():
+    """Moments, tails and the distribution function of N(0, 1): a bounded bell (such as a sum of
+    a few uniforms) fails the tail and kurtosis checks, a wrong branch or scale the moments."""
+    from scipy.special import ndtr
+    n = 1 << 20
+    x = synth.normal_f32(5, synth.TAG_X, (n,), 1.0).double().numpy()
+    assert abs(x.mean()) < 0.005
+    assert abs(x.std() - 1.0) < 0.005
+    kurt = np.mean((x - x.mean()) ** 4) / x.var() ** 2
+    assert abs(kurt - 3.0) < 0.05
+    # P(|z| > 3) = 0.0026998, P(|z| > 4) = 6.33e-5: about 2831 +- 53 and 66 +- 8 of 2**20
+    assert 2550 <= int((np.abs(x) > 3).sum()) <= 3110
+    assert 30 <= int((np.abs(x) > 4).sum()) <= 110
+    # 32-bit uniforms bound the draws at sqrt(2 * 32 ln 2)
+    assert np.abs(x).max() <= (64 * np.log(2)) ** 0.5 + 1e-6
+    # Kolmogorov-Smirnov distance to the normal CDF (the 1 % critical value is 1.63 / sqrt(n))
+    xs = np.sort(x)
+    cdf = ndtr(xs)
+    i = np.arange(1, n + 1)
+    ks = max(np.max(i / n - cdf), np.max(cdf - (i - 1) / n))
+    assert ks < 1.63 / n ** 0.5
+    # a known draw from the definition: z for element 0 of this stream
+    k0, k1 = synth.key(5, synth.TAG_X)
+    u1 = (synth.word_int(0, k0, k1) + 1) / 2.0 ** 32
+    u2 = synth.word_int(1, k0, k1) / 2.0 ** 32
+    import math
+    z0 = math.sqrt(-2.0 * math.log(u1)) * math.cos(2.0 * math.pi * u2)
+    assert abs(x[0] - z0) <= 2.0 ** -23 * max(1.0, abs(z0))
     w = synth.normal_bf16(5, synth.TAG_W2, (1 << 18,), 0.02).float()
-    assert abs(w.std().item() - 0.02) < 0.0005
+    assert abs(w.std().item() - 0.02) < 0.0002
 
 
 def test_uniform_range():
