@@ -53,9 +53,13 @@ _SIGS = {
     "oracle_select": (_I, [_I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "oracle_dispatch_index": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "oracle_dispatch_payload": (None, [_I, _I, _I, _P, _P, _P, _P]),
+    "oracle_dispatch_payload_ex": (None, [_I, _I, _I, _P, _P, _P, _P, _I]),
     "oracle_quant_row_e4m3": (None, [_P, _I, _P, _P]),
+    "oracle_quant_row_e4m3_ex": (None, [_P, _I, _P, _P, _I]),
+    "oracle_pow2_scale": (_F, [_F]),
     "oracle_swiglu_row_bf16": (None, [_I, _I, _P, _P, _P, _P, _P, _P]),
     "oracle_swiglu_row_fp8": (None, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "oracle_swiglu_row_fp8_ex": (None, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I]),
     "oracle_combine": (None, [_I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "oracle_place_experts": (_I, [_I, _I, _I, _P, _I, _P, _P, _P]),
     "oracle_dispatch_index_placed": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
@@ -136,15 +140,21 @@ def bf16_to_f32(h):
     return (h.astype(np.uint32) << 16).view(np.float32)
 
 
-def quant_rows_e4m3(v):
-    """1x128 block quantisation of each row of a float32 [n][m] array -> (codes, scales)."""
+def quant_rows_e4m3(v, pow2=False):
+    """1x128 block quantisation of each row of a float32 [n][m] array -> (codes, scales):
+    scale amax/448 (reading R-i) or, with pow2, its power of two (reading R-l)."""
     v = _c(v, np.float32)
     n, m = v.shape
     q = np.empty((n, m), dtype=np.uint8)
     s = np.empty((n, m // 128), dtype=np.float32)
     for i in range(n):
-        lib().oracle_quant_row_e4m3(_ptr(v[i]), m, _ptr(q[i]), _ptr(s[i]))
+        lib().oracle_quant_row_e4m3_ex(_ptr(v[i]), m, _ptr(q[i]), _ptr(s[i]), int(bool(pow2)))
     return q, s
+
+
+def pow2_scale(amax):
+    """Reading R-l's block scale for one amax (float32)."""
+    return np.float32(lib().oracle_pow2_scale(float(np.float32(amax))))
 
 
 # ------------------------------------------------------------------------------------------
@@ -209,9 +219,10 @@ def dispatch_index(topk_idx, E, R):
     return counts, offsets, row_of, src_tok
 
 
-def dispatch_payload(x_bits, row_of, n_rows, fp8=False):
+def dispatch_payload(x_bits, row_of, n_rows, fp8=False, pow2=False):
     """Receive buffer [n_rows][d] (uint16 bf16 bits, or uint8 e4m3 codes plus f32 scales
-    [n_rows][d/128]); rows that receive nothing stay zero."""
+    [n_rows][d/128], the scales of reading R-i or, with pow2, R-l); rows that receive nothing
+    stay zero."""
     x = _c(x_bits, np.uint16)
     ro = _c(row_of, np.int32)
     T, d = x.shape
@@ -222,7 +233,8 @@ def dispatch_payload(x_bits, row_of, n_rows, fp8=False):
     else:
         recv = np.zeros((n_rows, d), dtype=np.uint16)
         sc = None
-    lib().oracle_dispatch_payload(T, d, k, _ptr(x), _ptr(ro), _ptr(recv), _ptr(sc))
+    lib().oracle_dispatch_payload_ex(T, d, k, _ptr(x), _ptr(ro), _ptr(recv), _ptr(sc),
+                                     int(bool(pow2)))
     return recv, sc
 
 
@@ -285,9 +297,10 @@ def swiglu_row_bf16(x_row_bits, w13_bits, w2_bits, exact=False):
     return (out, h, ox) if exact else (out, h)
 
 
-def swiglu_row_fp8(xq, xs, w13q, w13s, w2q, w2s, exact=False):
+def swiglu_row_fp8(xq, xs, w13q, w13s, w2q, w2s, exact=False, pow2=False):
     """One e4m3 row (codes + 1x128 scales) through one e4m3 expert -> (out bf16 [d], h [F]);
-    with exact, also the fp64 output before its rounding to bf16 [d]."""
+    with exact, also the fp64 output before its rounding to bf16 [d]. pow2: h is re-quantised
+    with power-of-two scales (reading R-l)."""
     xq = _c(xq, np.uint8)
     xs = _c(xs, np.float32)
     w13q = _c(w13q, np.uint8)
@@ -299,8 +312,8 @@ def swiglu_row_fp8(xq, xs, w13q, w13s, w2q, w2s, exact=False):
     out = np.empty(d, dtype=np.uint16)
     h = np.empty(F, dtype=np.float32)
     ox = np.empty(d, dtype=np.float64) if exact else None
-    lib().oracle_swiglu_row_fp8(d, F, _ptr(xq), _ptr(xs), _ptr(w13q), _ptr(w13s), _ptr(w2q),
-                                _ptr(w2s), _ptr(out), _ptr(h), _ptr(ox))
+    lib().oracle_swiglu_row_fp8_ex(d, F, _ptr(xq), _ptr(xs), _ptr(w13q), _ptr(w13s), _ptr(w2q),
+                                   _ptr(w2s), _ptr(out), _ptr(h), _ptr(ox), int(bool(pow2)))
     return (out, h, ox) if exact else (out, h)
 
 
@@ -349,8 +362,9 @@ def layer_tokens(cfg, x_bits, w_gate, bias, expert_weights, shared_weights, toke
     idx, w = route(xs, w_gate, bias, cfg.k, cfg.n_group, cfg.topk_group, cfg.route_scale)
     n, d = xs.shape
     fp8 = cfg.act == "fp8"
+    p2 = getattr(cfg, "scales", "amax") == "pow2"
     if fp8:
-        xq, xsc = quant_rows_e4m3(bf16_to_f32(xs))
+        xq, xsc = quant_rows_e4m3(bf16_to_f32(xs), pow2=p2)
     cache = {}
     eo = np.empty((n, cfg.k, d), dtype=np.uint16)
     for j in range(n):
@@ -361,7 +375,8 @@ def layer_tokens(cfg, x_bits, w_gate, bias, expert_weights, shared_weights, toke
                 cache[e] = expert_weights(e)
             W = cache[e]
             if fp8:
-                eo[j, i], _ = swiglu_row_fp8(xq[j], xsc[j], W["w13"], W["w13_s"], W["w2"], W["w2_s"])
+                eo[j, i], _ = swiglu_row_fp8(xq[j], xsc[j], W["w13"], W["w13_s"], W["w2"], W["w2_s"],
+                                             pow2=p2)
             else:
                 eo[j, i], _ = swiglu_row_bf16(xs[j], W["w13"], W["w2"])
     sh = None
@@ -370,7 +385,8 @@ def layer_tokens(cfg, x_bits, w_gate, bias, expert_weights, shared_weights, toke
         for j in range(n):
             S = shared_weights
             if fp8:
-                sh[j], _ = swiglu_row_fp8(xq[j], xsc[j], S["ws13"], S["ws13_s"], S["ws2"], S["ws2_s"])
+                sh[j], _ = swiglu_row_fp8(xq[j], xsc[j], S["ws13"], S["ws13_s"], S["ws2"], S["ws2_s"],
+                                          pow2=p2)
             else:
                 sh[j], _ = swiglu_row_bf16(xs[j], S["ws13"], S["ws2"])
     rows = np.arange(n * cfg.k, dtype=np.int32).reshape(n, cfg.k)

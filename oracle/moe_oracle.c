@@ -43,6 +43,11 @@
  *  R-i  FP8: per-row 1x128 blocks, scale = amax/448 (1 when amax is 0), code = e4m3 with
  *       round-to-nearest-even and saturation of value/scale; weights e4m3 with one fp32 scale
  *       per 128x128 block.
+ *  R-l  FP8 with power-of-two scales (the second FP8 recipe): the same blocks as R-i, but each
+ *       block's fp32 scale is the smallest power of two 2^e with amax <= 448 * 2^e, e kept in
+ *       [-126, 127] (scale 1 when amax is 0), so value / scale is exact; weight block scales
+ *       are powers of two as well. The pages fix e4m3 payloads with fp32 block scales, not the
+ *       scale values; powers of two are the values the block-scaled tensor-core MMA applies.
  *  R-j  Combine: y = bf16(sum_i w_i * o_i + sh) with the sum taken in fp64 here.
  *  R-k  Redundant experts ([SMoE] "Hot-Expert Skew", redundant experts; exercise 5,
  *       imbalance_factor_replicated): a deployment has S expert slots on each of the R ranks
@@ -285,30 +290,45 @@ int oracle_dispatch_index(int T, int E, int k, int R, const int32_t* topk_idx,
     return 0;
 }
 
-/* 1x128 block quantisation of one row of n floats (n % 128 == 0), reading R-i:
- * amax per block, scale = amax / 448 (1 if amax == 0), code = e4m3(value / scale). */
-void oracle_quant_row_e4m3(const float* v, int n, uint8_t* q, float* scales) {
+/* Reading R-l: the smallest power of two 2^e, -126 <= e <= 127, with amax <= 448 * 2^e (1 when
+ * amax is 0). Found by stepping e, every comparison exact in double. */
+float oracle_pow2_scale(float amax) {
+    if (!(amax > 0.0f)) return 1.0f;
+    int e = 0;
+    while (e < 127 && ldexp(448.0, e) < (double)amax) ++e;
+    while (e > -126 && ldexp(448.0, e - 1) >= (double)amax) --e;
+    return (float)ldexp(1.0, e);
+}
+
+/* 1x128 block quantisation of one row of n floats (n % 128 == 0): amax per block, scale =
+ * amax / 448 (reading R-i; 1 if amax == 0) or its power of two (reading R-l, pow2 != 0),
+ * code = e4m3(value / scale). */
+void oracle_quant_row_e4m3_ex(const float* v, int n, uint8_t* q, float* scales, int pow2) {
     for (int b = 0; b < n / 128; ++b) {
         float amax = 0.0f;
         for (int c = b * 128; c < (b + 1) * 128; ++c) if (fabsf(v[c]) > amax) amax = fabsf(v[c]);
-        float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        float scale = pow2 ? oracle_pow2_scale(amax) : (amax > 0.0f ? amax / 448.0f : 1.0f);
         scales[b] = scale;
         for (int c = b * 128; c < (b + 1) * 128; ++c) q[c] = oracle_f32_to_e4m3(v[c] / scale);
     }
 }
 
+void oracle_quant_row_e4m3(const float* v, int n, uint8_t* q, float* scales) {
+    oracle_quant_row_e4m3_ex(v, n, q, scales, 0);
+}
+
 /* Copy payload rows. bf16 mode: recv[row] = x[t]. fp8 mode (recv_scales != NULL): recv holds
  * e4m3 codes of x[t] and recv_scales[row][d/128] its block scales; a token is quantised once
  * and its codes written to each of its k rows. Unfilled rows are left untouched. */
-void oracle_dispatch_payload(int T, int d, int k, const uint16_t* x, const int32_t* row_of,
-                             void* recv, float* recv_scales) {
+void oracle_dispatch_payload_ex(int T, int d, int k, const uint16_t* x, const int32_t* row_of,
+                                void* recv, float* recv_scales, int pow2) {
     float* xf = (float*)malloc(sizeof(float) * d);
     uint8_t* q = (uint8_t*)malloc(d);
     float* sc = (float*)malloc(sizeof(float) * (d / 128 + 1));
     for (int t = 0; t < T; ++t) {
         if (recv_scales) {
             for (int c = 0; c < d; ++c) xf[c] = oracle_bf16_to_f32(x[(size_t)t * d + c]);
-            oracle_quant_row_e4m3(xf, d, q, sc);
+            oracle_quant_row_e4m3_ex(xf, d, q, sc, pow2);
         }
         for (int i = 0; i < k; ++i) {
             long row = row_of[(size_t)t * k + i];
@@ -321,6 +341,11 @@ void oracle_dispatch_payload(int T, int d, int k, const uint16_t* x, const int32
         }
     }
     free(xf); free(q); free(sc);
+}
+
+void oracle_dispatch_payload(int T, int d, int k, const uint16_t* x, const int32_t* row_of,
+                             void* recv, float* recv_scales) {
+    oracle_dispatch_payload_ex(T, d, k, x, row_of, recv, recv_scales, 0);
 }
 
 /* ------------------------------------------------------------------------------------------
@@ -361,11 +386,12 @@ void oracle_swiglu_row_bf16(int d, int F, const uint16_t* x, const uint16_t* w13
 
 /* One row through one e4m3 SwiGLU expert. xq [d] codes with xs [d/128] scales; w13q [2F][d]
  * with w13s [2F/128][d/128]; w2q [d][F] with w2s [d/128][F/128]. h is re-quantised 1x128 before
- * the down projection (reading R-i). out: bf16 [d]. h_out (nullable): dequantised h [F].
+ * the down projection (reading R-i, or R-l when pow2 != 0). out: bf16 [d]. h_out (nullable): dequantised h [F].
  * out_exact (nullable): the down projection's fp64 sums before their rounding to bf16 [d]. */
-void oracle_swiglu_row_fp8(int d, int F, const uint8_t* xq, const float* xs,
-                           const uint8_t* w13q, const float* w13s, const uint8_t* w2q,
-                           const float* w2s, uint16_t* out, float* h_out, double* out_exact) {
+void oracle_swiglu_row_fp8_ex(int d, int F, const uint8_t* xq, const float* xs,
+                              const uint8_t* w13q, const float* w13s, const uint8_t* w2q,
+                              const float* w2s, uint16_t* out, float* h_out, double* out_exact,
+                              int pow2) {
     int db = d / 128, fb = F / 128;
     double* xv = (double*)malloc(sizeof(double) * d);
     float* hf = (float*)calloc((size_t)F, sizeof(float));
@@ -383,7 +409,7 @@ void oracle_swiglu_row_fp8(int d, int F, const uint8_t* xq, const float* xs,
         }
         hf[f] = (float)(silu(g) * u);
     }
-    oracle_quant_row_e4m3(hf, F, hq, hs);
+    oracle_quant_row_e4m3_ex(hf, F, hq, hs, pow2);
     for (int f = 0; f < F; ++f) {
         hf[f] = oracle_e4m3_to_f32(hq[f]) * hs[f / 128];
         if (h_out) h_out[f] = hf[f];
@@ -396,6 +422,12 @@ void oracle_swiglu_row_fp8(int d, int F, const uint8_t* xq, const float* xs,
         if (out_exact) out_exact[c] = o;
     }
     free(xv); free(hf); free(hq); free(hs);
+}
+
+void oracle_swiglu_row_fp8(int d, int F, const uint8_t* xq, const float* xs,
+                           const uint8_t* w13q, const float* w13s, const uint8_t* w2q,
+                           const float* w2s, uint16_t* out, float* h_out, double* out_exact) {
+    oracle_swiglu_row_fp8_ex(d, F, xq, xs, w13q, w13s, w2q, w2s, out, h_out, out_exact, 0);
 }
 
 /* ------------------------------------------------------------------------------------------

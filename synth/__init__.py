@@ -64,6 +64,7 @@ class MoEConfig:
     act: str = "bf16"     # dispatched activation format: "bf16" or "fp8"
     w: str = "bf16"       # expert weight format: "bf16" or "fp8"
     bias: str = "uniform" # "uniform": U(-0.1, 0.1); "zipf": skewed popularity
+    scales: str = "amax"  # e4m3 block scales: "amax" (amax/448) or "pow2" (its power of two)
     seed: int = 0
     x_std: float = 1.0
     w_std: float = 0.02
@@ -107,6 +108,9 @@ CONFIGS = {
     # (128x128 scales).
     "dsv3_fp8_prefill": MoEConfig("dsv3_fp8_prefill", T=16384, act="fp8", w="fp8", seed=4000,
                                   **_DSV3),
+    # The FP8 prefill layer with power-of-two block scales (the block-scaled MMA's recipe).
+    "dsv3_fp8_pow2_prefill": MoEConfig("dsv3_fp8_pow2_prefill", T=16384, act="fp8", w="fp8",
+                                       scales="pow2", seed=4000, **_DSV3),
     # Profiling stand-in for the decode layer: the same per-expert shapes, 32 experts (E/R = 4
     # per logical rank, groups of 4), so one capture holds about 3 GB on the device.
     "dsv3_decode_e32": MoEConfig("dsv3_decode_e32", T=64, d=7168, E=32, k=8, n_group=8,
@@ -122,6 +126,10 @@ CONFIGS = {
     "dsv3_fp8_e32": MoEConfig("dsv3_fp8_e32", T=2048, d=7168, E=32, k=8, n_group=8, topk_group=4,
                               d_ff=2048, d_ff_shared=2048, R=8, route_scale=2.5, act="fp8",
                               w="fp8", seed=4000),
+    "dsv3_fp8_pow2_e32": MoEConfig("dsv3_fp8_pow2_e32", T=2048, d=7168, E=32, k=8, n_group=8,
+                                   topk_group=4, d_ff=2048, d_ff_shared=2048, R=8,
+                                   route_scale=2.5, act="fp8", w="fp8", scales="pow2",
+                                   seed=4000),
 }
 SWEEP_T = [8 * m for m in (1, 2, 4, 8, 16, 32, 64, 128)]
 
@@ -233,14 +241,26 @@ def permutation(seed: int, tag: int, n: int) -> np.ndarray:
 # --------------------------------------------------------------------------------------------
 # Block-quantised e4m3 weights
 # --------------------------------------------------------------------------------------------
+def pow2_block_scale(amax: torch.Tensor) -> torch.Tensor:
+    """The smallest power of two 2^e (-126 <= e <= 127) with amax <= 448 * 2^e, 1 where amax is
+    0: a log2 estimate corrected by exact fp64 comparisons."""
+    a = amax.double()
+    e = torch.ceil(torch.log2(torch.where(a > 0, a, torch.ones_like(a)) / 448.0)).clamp(-126, 127)
+    e = torch.where(a > 448.0 * torch.exp2(e), e + 1, e)
+    e = torch.where((e > -126) & (a <= 448.0 * torch.exp2(e - 1)), e - 1, e).clamp(-126, 127)
+    return torch.where(a > 0, torch.exp2(e), torch.ones_like(a)).float()
+
+
 def fp8_block_weights(seed: int, tag: int, n_mat: int, rows: int, cols: int, std: float,
-                      device="cpu", mat_start: int = 0, mat_count: int | None = None):
+                      device="cpu", mat_start: int = 0, mat_count: int | None = None,
+                      pow2: bool = False):
     """e4m3 weights [n_mat][rows][cols] (as uint8 codes) and fp32 scales
     [n_mat][rows/128][cols/128].
 
-    Draws fp32 values, then per 128x128 block takes amax, scale = amax/448 (1 if amax is 0)
-    and codes = round-to-nearest-even e4m3 of value/scale (torch's float8_e4m3fn conversion).
-    Matrices ``mat_start .. mat_start+mat_count`` are made (a slice keeps the same values)."""
+    Draws fp32 values, then per 128x128 block takes amax, scale = amax/448 (1 if amax is 0), or
+    with pow2 the smallest power of two not below it, and codes = round-to-nearest-even e4m3
+    of value/scale (torch's float8_e4m3fn conversion). Matrices
+    ``mat_start .. mat_start+mat_count`` are made (a slice keeps the same values)."""
     if mat_count is None:
         mat_count = n_mat - mat_start
     assert rows % 128 == 0 and cols % 128 == 0
@@ -251,8 +271,11 @@ def fp8_block_weights(seed: int, tag: int, n_mat: int, rows: int, cols: int, std
         w = normal_f32(seed, tag, (rows, cols), std, device, start=(mat_start + m) * per)
         blk = w.view(rows // 128, 128, cols // 128, 128)
         amax = blk.abs().amax(dim=(1, 3))
-        scale = torch.where(amax > 0, amax / torch.tensor(448.0, device=device),
-                            torch.ones_like(amax))
+        if pow2:
+            scale = pow2_block_scale(amax)
+        else:
+            scale = torch.where(amax > 0, amax / torch.tensor(448.0, device=device),
+                                torch.ones_like(amax))
         qq = (blk / scale[:, None, :, None]).to(torch.float8_e4m3fn)
         q[m] = qq.view(torch.uint8).view(rows, cols)
         s[m] = scale
@@ -298,13 +321,15 @@ def make_expert_weights(cfg: MoEConfig, device="cpu"):
             out["ws2"] = normal_bf16(cfg.seed, TAG_WS2, (d, Fs), cfg.w_std, device)
         out["ws13_s"] = out["ws2_s"] = None
     else:
+        p2 = cfg.scales == "pow2"
         out["w13"], out["w13_s"] = fp8_block_weights(cfg.seed, TAG_W13, E, 2 * F, d, cfg.w_std,
-                                                     device)
-        out["w2"], out["w2_s"] = fp8_block_weights(cfg.seed, TAG_W2, E, d, F, cfg.w_std, device)
+                                                     device, pow2=p2)
+        out["w2"], out["w2_s"] = fp8_block_weights(cfg.seed, TAG_W2, E, d, F, cfg.w_std, device,
+                                                   pow2=p2)
         if Fs:
-            q, s = fp8_block_weights(cfg.seed, TAG_WS13, 1, 2 * Fs, d, cfg.w_std, device)
+            q, s = fp8_block_weights(cfg.seed, TAG_WS13, 1, 2 * Fs, d, cfg.w_std, device, pow2=p2)
             out["ws13"], out["ws13_s"] = q[0], s[0]
-            q, s = fp8_block_weights(cfg.seed, TAG_WS2, 1, d, Fs, cfg.w_std, device)
+            q, s = fp8_block_weights(cfg.seed, TAG_WS2, 1, d, Fs, cfg.w_std, device, pow2=p2)
             out["ws2"], out["ws2_s"] = q[0], s[0]
     if not Fs:
         out["ws13"] = out["ws2"] = out["ws13_s"] = out["ws2_s"] = None
@@ -318,10 +343,11 @@ def expert_weight_slice(cfg: MoEConfig, e: int, device="cpu"):
         w13 = normal_bf16(cfg.seed, TAG_W13, (2 * F, d), cfg.w_std, device, start=e * 2 * F * d)
         w2 = normal_bf16(cfg.seed, TAG_W2, (d, F), cfg.w_std, device, start=e * d * F)
         return dict(w13=w13, w2=w2, w13_s=None, w2_s=None)
+    p2 = cfg.scales == "pow2"
     q13, s13 = fp8_block_weights(cfg.seed, TAG_W13, cfg.E, 2 * F, d, cfg.w_std, device,
-                                 mat_start=e, mat_count=1)
+                                 mat_start=e, mat_count=1, pow2=p2)
     q2, s2 = fp8_block_weights(cfg.seed, TAG_W2, cfg.E, d, F, cfg.w_std, device,
-                               mat_start=e, mat_count=1)
+                               mat_start=e, mat_count=1, pow2=p2)
     return dict(w13=q13[0], w2=q2[0], w13_s=s13[0], w2_s=s2[0])
 
 

@@ -272,6 +272,75 @@ def test_dispatch_payload_bf16_and_fp8():
             assert np.array_equal(sc[row_of[t, i]], scale)
 
 
+def _is_pow2_scale_of(amax, scale):
+    """Reading R-l's defining properties: scale = 2^e, -126 <= e <= 127, amax <= 448 * 2^e, and
+    no smaller power of two would do (or e is at its floor); 1 for amax 0."""
+    amax, scale = float(amax), float(scale)
+    if amax == 0.0:
+        return scale == 1.0
+    m, e = math.frexp(scale)           # scale = m * 2^e, m in [0.5, 1)
+    if m != 0.5 or not (-126 <= e - 1 <= 127):
+        return False
+    return amax <= 448.0 * scale and (e - 1 == -126 or amax > 224.0 * scale)
+
+
+def test_pow2_scale_definition_at_block_boundaries():
+    """The power-of-two scale at and around the edges of each binade of 448 * 2^e, at zero, for
+    fp32 subnormals and near the top of the range; the generator's independent torch form
+    (log2 estimate + exact corrections) gives the same scales."""
+    vals = [0.0, 1e-45, 1e-40, 1.17e-38, 1e-20, 0.001, 1.0, 3.0, 447.99, 448.0, 448.00003, 500.0,
+            896.0, 1e6, 3e38]
+    for k in range(-130, 120, 7):
+        b = np.float32(448.0 * 2.0 ** k) if 448.0 * 2.0 ** k < 3.4e38 else None
+        if b is None or b == 0:
+            continue
+        vals += [float(b), float(np.nextafter(b, np.float32(np.inf))),
+                 float(np.nextafter(b, np.float32(0)))]
+    amax = np.asarray(vals, dtype=np.float32)
+    got = np.array([oracle.pow2_scale(a) for a in amax], dtype=np.float32)
+    for a, sc in zip(amax, got):
+        assert _is_pow2_scale_of(a, sc), (a, sc)
+    ref = synth.pow2_block_scale(torch.from_numpy(amax)).numpy()
+    assert np.array_equal(got, ref)
+    # 448 * 2^k itself takes 2^k; one step above it takes 2^(k+1)
+    assert oracle.pow2_scale(np.float32(448.0)) == 1.0
+    assert oracle.pow2_scale(np.nextafter(np.float32(448.0), np.float32(1e9))) == 2.0
+
+
+def test_quant_pow2_rows_and_payload():
+    """Reading R-l on rows: every block's scale has the defining properties, the codes are
+    torch's e4m3 conversion of value / scale (exact division), nothing saturates, and the
+    dispatch payload carries the same codes and scales."""
+    T, d, E, k, R = 16, 512, 16, 2, 2
+    x = synth.bf16_bits(synth.normal_bf16(5, synth.TAG_X, (T, d), 1.0))
+    xf = oracle.bf16_to_f32(x)
+    xf[3, :128] *= 1e-30          # a block with a tiny amax
+    xf[4, 128:256] = 0.0           # an all-zero block
+    q, sc = oracle.quant_rows_e4m3(xf, pow2=True)
+    for t in range(T):
+        blk = xf[t].reshape(d // 128, 128)
+        amax = np.abs(blk).max(1)
+        for b in range(d // 128):
+            assert _is_pow2_scale_of(amax[b], sc[t, b])
+        v = (blk / sc[t][:, None]).astype(np.float32)
+        assert np.all(np.abs(v) <= 448.0)
+        assert np.array_equal(v * sc[t][:, None], blk)   # the division by 2^e was exact
+        ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy().reshape(-1)
+        assert np.array_equal(q[t], ref)
+    # the amax/448 recipe differs from it on these rows
+    q0, sc0 = oracle.quant_rows_e4m3(xf)
+    assert not np.array_equal(sc0, sc)
+    ti = _random_topk(T, E, k, 9)
+    _, _, row_of, src_tok = oracle.dispatch_index(ti, E, R)
+    xb = oracle.f32_to_bf16(xf)
+    q2, s2 = oracle.quant_rows_e4m3(oracle.bf16_to_f32(xb), pow2=True)
+    recv, rsc = oracle.dispatch_payload(xb, row_of, src_tok.size, fp8=True, pow2=True)
+    for t in range(T):
+        for i in range(k):
+            assert np.array_equal(recv[row_of[t, i]], q2[t])
+            assert np.array_equal(rsc[row_of[t, i]], s2[t])
+
+
 # ------------------------------------------------------------------------------------------
 # Experts and combine
 # ------------------------------------------------------------------------------------------
@@ -366,6 +435,44 @@ def test_swiglu_fp8_matches_torch_dequantised_mlp():
                            rtol=1e-12, atol=1e-12)
         rounded = torch.from_numpy(ox).float().to(torch.bfloat16).view(torch.int16).numpy()
         assert np.array_equal(rounded.view(np.uint16), out)
+
+
+def test_swiglu_fp8_pow2_matches_torch_dequantised_mlp():
+    """Reading R-l through one expert: power-of-two weight block scales from the generator and
+    the intermediate re-quantised with power-of-two scales, against fp64 torch."""
+    cfg = synth.MoEConfig("t", T=4, d=256, E=2, k=1, n_group=1, topk_group=1, d_ff=256,
+                          d_ff_shared=0, R=1, route_scale=1.0, act="fp8", w="fp8",
+                          scales="pow2", seed=3)
+    W = synth.expert_weight_slice(cfg, 1)
+    for s_ in (W["w13_s"], W["w2_s"]):
+        m, _ = np.frexp(s_.numpy())
+        assert np.all(m == 0.5)
+    x = synth.normal_bf16(3, synth.TAG_X, (4, cfg.d), 1.0)
+    xq, xs = oracle.quant_rows_e4m3(oracle.bf16_to_f32(synth.bf16_bits(x)), pow2=True)
+    F = cfg.d_ff
+
+    def deq(q, s):
+        v = torch.from_numpy(q.numpy()).view(torch.float8_e4m3fn).double()
+        s = torch.as_tensor(s).double()
+        return v * s.repeat_interleave(128, 0).repeat_interleave(128, 1)
+
+    w13 = deq(W["w13"], W["w13_s"])
+    w2 = deq(W["w2"], W["w2_s"])
+    for t in range(4):
+        xv = torch.from_numpy(xq[t]).view(torch.float8_e4m3fn).double() * \
+            torch.from_numpy(xs[t]).double().repeat_interleave(128)
+        hf = (torch.nn.functional.silu(w13[:F] @ xv) * (w13[F:] @ xv)).float()
+        blk = hf.view(F // 128, 128)
+        sc = synth.pow2_block_scale(blk.abs().amax(1))
+        for b in range(F // 128):
+            assert _is_pow2_scale_of(blk[b].abs().max().item(), sc[b].item())
+        hq = (blk / sc[:, None]).to(torch.float8_e4m3fn).double() * sc[:, None].double()
+        ref = (w2 @ hq.reshape(-1)).float()
+        out, h = oracle.swiglu_row_fp8(xq[t], xs[t], W["w13"].numpy(), W["w13_s"].numpy(),
+                                       W["w2"].numpy(), W["w2_s"].numpy(), pow2=True)
+        assert np.abs(oracle.bf16_to_f32(out) - ref.numpy()).max() <= \
+            2 ** -7 * np.abs(ref.numpy()).max() + 1e-6
+        assert np.allclose(h, hq.reshape(-1).float().numpy(), rtol=0, atol=0)
 
 
 def test_combine_identity_experts_return_scaled_x():
