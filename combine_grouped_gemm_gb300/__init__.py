@@ -16,8 +16,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libmoe.so")
 
-MOE_BF16, MOE_FP8_E4M3 = 0, 1
-MOE_DEV_TIMEOUT, MOE_DEV_BOUNDS = 1, 2
+MOE_BF16, MOE_FP8_E4M3, MOE_FP8_E4M3_POW2 = 0, 1, 2
+MOE_DEV_TIMEOUT, MOE_DEV_BOUNDS, MOE_DEV_SCALE = 1, 2, 4
 MOE_LAYER_EVENTS = 7
 STAGE_NAMES = ["route", "dispatch", "ffn_setup", "ffn_gate_up", "ffn_down", "combine"]
 
@@ -121,11 +121,15 @@ def _dtype_code(v):
 
 
 def make_cfg(c) -> Cfg:
-    """Cfg from any object with the moe_cfg fields (act / w may be "bf16" / "fp8")."""
-    act = getattr(c, "act_dtype", getattr(c, "act", MOE_BF16))
-    w = getattr(c, "w_dtype", getattr(c, "w", act))
+    """Cfg from any object with the moe_cfg fields (act / w may be "bf16" / "fp8"; an e4m3
+    configuration with scales == "pow2" takes the power-of-two recipe)."""
+    act = _dtype_code(getattr(c, "act_dtype", getattr(c, "act", MOE_BF16)))
+    w = _dtype_code(getattr(c, "w_dtype", getattr(c, "w", act)))
+    if getattr(c, "scales", "amax") == "pow2":
+        act = MOE_FP8_E4M3_POW2 if act == MOE_FP8_E4M3 else act
+        w = MOE_FP8_E4M3_POW2 if w == MOE_FP8_E4M3 else w
     return Cfg(c.T, c.d, c.E, c.k, c.n_group, c.topk_group, c.d_ff, c.d_ff_shared, c.R,
-               float(c.route_scale), _dtype_code(act), _dtype_code(w))
+               float(c.route_scale), act, w)
 
 
 def _p(t):
@@ -321,7 +325,7 @@ class Buffers(dict):
         if slots_per_rank:
             E = R * slots_per_rank     # counts are over the slots
         self.sizes = s
-        fp8 = make_cfg(cfg).act_dtype == MOE_FP8_E4M3
+        fp8 = make_cfg(cfg).act_dtype != MOE_BF16
         self["topk_idx"] = torch.empty((T, k), dtype=torch.int32, device=device)
         self["topk_w"] = torch.empty((T, k), dtype=torch.float32, device=device)
         self["recv"] = (torch.empty((s["recv_rows"], d),

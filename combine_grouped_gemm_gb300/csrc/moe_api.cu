@@ -61,8 +61,8 @@ int validate(const moe_cfg& c) {
   if (c.T % c.R || c.E % c.R || c.E % c.n_group) return MOE_ERR_INVALID_ARG;
   if (c.topk_group > c.n_group || c.k > c.topk_group * (c.E / c.n_group))
     return MOE_ERR_INVALID_ARG;
-  if ((c.act_dtype != MOE_BF16 && c.act_dtype != MOE_FP8_E4M3) ||
-      (c.w_dtype != MOE_BF16 && c.w_dtype != MOE_FP8_E4M3))
+  if (c.act_dtype < MOE_BF16 || c.act_dtype > MOE_FP8_E4M3_POW2 || c.w_dtype < MOE_BF16 ||
+      c.w_dtype > MOE_FP8_E4M3_POW2)
     return MOE_ERR_INVALID_ARG;
   if (!isfinite(c.route_scale)) return MOE_ERR_INVALID_ARG;
   // limits of these kernels
@@ -70,6 +70,8 @@ int validate(const moe_cfg& c) {
   if (c.E > 1024 || c.k > 32 || c.n_group > 64 || c.R > 64) return MOE_ERR_UNSUPPORTED;
   if (c.act_dtype != c.w_dtype) return MOE_ERR_UNSUPPORTED;
   if (c.d_ff_shared != 0 && c.d_ff_shared != c.d_ff) return MOE_ERR_UNSUPPORTED;
+  // the block-scaled down GEMM computes two 128-column output tiles per unit
+  if (c.act_dtype == MOE_FP8_E4M3_POW2 && c.d % 256) return MOE_ERR_UNSUPPORTED;
   const long long rows = (long long)c.R * c.R * cap_of(c);
   if (rows >= (1ll << 31) || (long long)c.T * c.k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -79,7 +81,7 @@ WsLayout ws_layout(const moe_cfg& c) {
   WsLayout L{};
   const size_t tk = (size_t)c.T * c.k;
   const size_t ab = act_bytes(c);
-  const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(c);
   // token tile: 128 rows for e4m3 (the token rows are the M operand there) and for bf16 when
   // experts average 16 rows or more; 64 otherwise (DSV3 layer: 128 is 2-17 % faster from 512
   // tokens, 64 is 1.5 % faster at 256)
@@ -162,7 +164,7 @@ void fill_sizes(const moe_cfg& c, moe_sizes* out) {
   out->recv_rows = (int64_t)c.R * c.R * cap;
   out->recv_bytes = (size_t)out->recv_rows * c.d * act_bytes(c);
   out->recv_scale_bytes =
-      c.act_dtype == MOE_FP8_E4M3 ? (size_t)out->recv_rows * (c.d / 128) * sizeof(float) : 0;
+      is_fp8(c) ? (size_t)out->recv_rows * (c.d / 128) * sizeof(float) : 0;
   out->ebuf_bytes = (size_t)out->recv_rows * c.d * 2;
   out->ws_bytes = ws_layout(c).total;
 }
@@ -284,7 +286,7 @@ int moe_dispatch(const moe_cfg* cfg, const void* x, const int32_t* topk_idx, voi
   MOE_NEED(counts);
   MOE_NEED(row_of);
   MOE_OPT(src_tok);
-  if (cfg->act_dtype == MOE_FP8_E4M3) MOE_NEED(recv_scales);
+  if (is_fp8(*cfg)) MOE_NEED(recv_scales);
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_MISALIGNED;
   cudaError_t e = launch_dispatch(*cfg, x, topk_idx, recv, recv_scales, counts, row_of, src_tok,
                                   status, stream);
@@ -303,7 +305,7 @@ int moe_expert_ffn(const moe_cfg* cfg, const void* recv, const float* recv_scale
   if (!w) return MOE_ERR_INVALID_ARG;
   MOE_NEED(w->w13);
   MOE_NEED(w->w2);
-  const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(c);
   if (fp8) {
     MOE_NEED(recv_scales);
     MOE_NEED(w->w13_scales);
@@ -358,7 +360,7 @@ int layer_impl(const moe_cfg& c0, const moe_layer_opts& o, const void* x, const 
   const moe_cfg c = slot_cfg(c0, o.placement);
   const WsLayout L = ws_layout(c);
   char* wsp = static_cast<char*>(ws);
-  const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(c);
   const bool gather = (o.flags & MOE_OPT_GATHER_X) != 0;
   const bool side = (o.flags & MOE_OPT_SHARED_SIDE_STREAM) != 0 && c.d_ff_shared > 0;
   const bool fused = (o.flags & MOE_OPT_FUSED_FFN) != 0;
@@ -470,7 +472,7 @@ int layer_impl(const moe_cfg& c0, const moe_layer_opts& o, const void* x, const 
   if (!w) return MOE_ERR_INVALID_ARG;         \
   MOE_NEED(w->w13);                           \
   MOE_NEED(w->w2);                            \
-  const bool fp8 = c.act_dtype == MOE_FP8_E4M3; \
+  const bool fp8 = is_fp8(c); \
   if (fp8) {                                  \
     if (!(gather)) MOE_NEED(recv_scales);     \
     MOE_NEED(w->w13_scales);                  \
@@ -558,7 +560,7 @@ int moe_expert_ffn_gather(const moe_cfg* cfg, const void* x, const int32_t* coun
   if (!w) return MOE_ERR_INVALID_ARG;
   MOE_NEED(w->w13);
   MOE_NEED(w->w2);
-  const bool fp8 = c.act_dtype == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(c);
   if (fp8) {
     MOE_NEED(w->w13_scales);
     MOE_NEED(w->w2_scales);

@@ -12,6 +12,7 @@
 // a segment, rows are grouped by local expert (ascending) and by token index inside an expert.
 // Each source computes its own offsets, so no rank needs another rank's counts.
 #include "moe_device.cuh"
+#include "moe_scale.cuh"
 
 namespace moe {
 namespace {
@@ -232,12 +233,13 @@ __global__ void __launch_bounds__(128) dispatch_copy_bf16_kernel(
 }
 
 // e4m3 payload: 16 threads per 128-column block, 8 columns per thread. amax over the block,
-// scale = amax/448 (1 if amax is 0), code = e4m3(x / scale) with IEEE division, nearest even,
-// saturating. The codes and the scale are written to each of the token's rows; the scales are
-// block-major, recv_scales[block][row] with sc_ld rows per block.
+// scale = amax/448 (1 if amax is 0), or with pow2 the smallest power of two not below it,
+// code = e4m3(x / scale) with IEEE division, nearest even, saturating. The codes and the scale
+// are written to each of the token's rows; the scales are block-major, recv_scales[block][row]
+// with sc_ld rows per block.
 __global__ void __launch_bounds__(128) dispatch_copy_e4m3_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ row_of, uint2* __restrict__ recv,
-    float* __restrict__ recv_scales, long long sc_ld, int d, int k, int slice_vecs) {
+    float* __restrict__ recv_scales, long long sc_ld, int d, int k, int slice_vecs, int pow2) {
   __shared__ int32_t rows[32];
   const int t = blockIdx.x;
   pdl_wait();
@@ -259,7 +261,8 @@ __global__ void __launch_bounds__(128) dispatch_copy_e4m3_kernel(
     for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const float scale =
+        pow2 ? pow2_block_scale(amax) : (amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f);
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int j = 0; j < 4; j += 2) {
@@ -302,12 +305,13 @@ void copy_grid(int T, int d, int* nslice_out, int* slice_vecs_out) {
 }  // namespace
 
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int d, void* out, float* scales,
-                                   cudaStream_t st, bool pdl) {
+                                   cudaStream_t st, bool pdl, bool pow2) {
   int nslice, slice_vecs;
   copy_grid(T, d, &nslice, &slice_vecs);
   return launch_kernel(dispatch_copy_e4m3_kernel, dim3(T, nslice), dim3(128), 0, st, pdl,
                        static_cast<const uint4*>(x), static_cast<const int32_t*>(nullptr),
-                       static_cast<uint2*>(out), scales, (long long)T, d, 1, slice_vecs);
+                       static_cast<uint2*>(out), scales, (long long)T, d, 1, slice_vecs,
+                       pow2 ? 1 : 0);
 }
 
 cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk_idx, void* recv,
@@ -342,11 +346,11 @@ cudaError_t launch_dispatch(const moe_cfg& c, const void* x, const int32_t* topk
   int nslice, slice_vecs;
   copy_grid(c.T, c.d, &nslice, &slice_vecs);
   dim3 grid(c.T, nslice);
-  if (c.act_dtype == MOE_FP8_E4M3) {
+  if (is_fp8(c)) {
     return launch_kernel(dispatch_copy_e4m3_kernel, grid, dim3(128), 0, st, pdl,
                          static_cast<const uint4*>(x), static_cast<const int32_t*>(row_of),
                          static_cast<uint2*>(recv), recv_scales, (long long)c.R * c.R * cap, c.d,
-                         c.k, slice_vecs);
+                         c.k, slice_vecs, pow2_scales(c) ? 1 : 0);
   }
   return launch_kernel(dispatch_copy_bf16_kernel, grid, dim3(128), 0, st, pdl,
                        static_cast<const uint4*>(x), static_cast<const int32_t*>(row_of),

@@ -680,14 +680,14 @@ int sm_count() {
 cudaError_t launch_quant_x(const moe_cfg& c, const WsLayout& L, const void* x, char* ws,
                            cudaStream_t st, bool pdl) {
   return launch_quant_rows_e4m3(x, c.T, c.d, ws + L.xq, reinterpret_cast<float*>(ws + L.xq_scales),
-                                st, pdl);
+                                st, pdl, pow2_scales(c));
 }
 
 cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t* counts,
                              const void* x, char* ws, cudaStream_t st, bool pdl,
                              const int32_t* src_tok, bool quantise,
                              const int32_t* group_expert) {
-  if (quantise && c.act_dtype == MOE_FP8_E4M3 && (c.d_ff_shared || src_tok)) {
+  if (quantise && is_fp8(c) && (c.d_ff_shared || src_tok)) {
     const cudaError_t err = launch_quant_x(c, L, x, ws, st, pdl);
     if (err != cudaSuccess) return err;
   }
@@ -815,7 +815,10 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
                             const float* recv_scales, const void* x, const moe_weights& w,
                             void* ebuf, void* shared_out, char* ws, cudaStream_t st, bool pdl,
                             const FfnPart& part) {
-  if (c.act_dtype == MOE_FP8_E4M3)
+  if (pow2_scales(c))
+    return launch_ffn_gemm_mx8(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st, pdl,
+                               part);
+  if (is_fp8(c))
     return launch_ffn_gemm_e4m3(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st, pdl,
                                 part);
   GemmArgs a{};

@@ -62,7 +62,10 @@ inline int cap_of(const moe_cfg& c) {
   int Er = c.E / c.R, Ts = c.T / c.R;
   return Ts * (c.k < Er ? c.k : Er);
 }
-inline size_t act_bytes(const moe_cfg& c) { return c.act_dtype == MOE_FP8_E4M3 ? 1 : 2; }
+inline bool is_fp8(const moe_cfg& c) { return c.act_dtype != MOE_BF16; }
+// e4m3 with power-of-two block scales (the block-scaled MMA's recipe)
+inline bool pow2_scales(const moe_cfg& c) { return c.act_dtype == MOE_FP8_E4M3_POW2; }
+inline size_t act_bytes(const moe_cfg& c) { return is_fp8(c) ? 1 : 2; }
 
 // The configuration seen by the stages after the router when the experts are placed on slots:
 // E becomes the slot count R * slots_per_rank (one group of the grouped GEMMs per slot). The
@@ -153,9 +156,17 @@ cudaError_t launch_ffn_gemm_e4m3(const moe_cfg& c, const WsLayout& L, int stage,
                                  void* shared_out, char* ws, cudaStream_t st, bool pdl,
                                  const FfnPart& part);
 
-// 1x128 e4m3 quantisation of T rows of width d (the dispatch's rule), row t -> row t.
+// e4m3 grouped GEMMs with power-of-two block scales applied by the tensor core (block-scaled
+// MMA, csrc/moe_ffn_mx8.cu), same stages.
+cudaError_t launch_ffn_gemm_mx8(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
+                                const float* recv_scales, const moe_weights& w, void* ebuf,
+                                void* shared_out, char* ws, cudaStream_t st, bool pdl,
+                                const FfnPart& part);
+
+// 1x128 e4m3 quantisation of T rows of width d (the dispatch's rule), row t -> row t; pow2:
+// power-of-two scales.
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int d, void* out, float* scales,
-                                   cudaStream_t st, bool pdl = false);
+                                   cudaStream_t st, bool pdl = false, bool pow2 = false);
 
 // 2-D row-major tensor map [rows][cols] with a box of box_rows x 128 bytes, 128-byte swizzle.
 bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t cols,

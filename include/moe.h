@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 /* Return codes */
 #define MOE_OK 0
@@ -49,10 +49,20 @@ extern "C" {
 /* Device status bits (moe_read_status) */
 #define MOE_DEV_TIMEOUT 1u     /* a bounded wait inside a kernel gave up; outputs invalid */
 #define MOE_DEV_BOUNDS 2u      /* an index read from device memory was out of range */
+#define MOE_DEV_SCALE 4u       /* MOE_FP8_E4M3_POW2: a weight block scale is not a power of two
+                                  (not positive, not finite, or with mantissa bits); the GEMM
+                                  applied 2^(its exponent field - 127) in its place */
 
 /* Element formats */
 #define MOE_BF16 0
-#define MOE_FP8_E4M3 1
+#define MOE_FP8_E4M3 1       /* e4m3 with fp32 block scales: 1x128 for activations (scale =
+                                amax / 448), 128x128 for weights (any positive scales) */
+#define MOE_FP8_E4M3_POW2 2  /* e4m3 with power-of-two fp32 block scales: the same blocks, each
+                                activation scale the smallest power of two 2^e with
+                                amax <= 448 * 2^e (e in [-126, 127], 1 for an all-zero block);
+                                the weight scales must be powers of two too. The grouped GEMMs
+                                apply the scales in the tensor core (block-scaled MMA) instead
+                                of promoting each 128-K block's partial sums. */
 
 /* Number of events moe_layer records when given an event array (see moe_layer). */
 #define MOE_LAYER_EVENTS 7
@@ -72,7 +82,7 @@ typedef struct moe_cfg {
   int32_t R;            /* logical ranks; expert e lives on rank e / (E/R), token t is sent by
                            rank t / (T/R); R <= 64 */
   float route_scale;    /* factor applied to the renormalised gate weights */
-  int32_t act_dtype;    /* dispatched activations: MOE_BF16 or MOE_FP8_E4M3 */
+  int32_t act_dtype;    /* dispatched activations: MOE_BF16, MOE_FP8_E4M3 or MOE_FP8_E4M3_POW2 */
   int32_t w_dtype;      /* expert weights: must equal act_dtype */
 } moe_cfg;
 

@@ -40,6 +40,7 @@ def _rows_of(t_dev, rows):
 def check_layer(cfg, inp, W, bufs, y, tokens, extra_pairs=(), tol=2e-2):
     """Returns a dict of the worst errors; asserts every rule on the way."""
     fp8 = cfg.w == "fp8"
+    p2 = getattr(cfg, "scales", "amax") == "pow2"   # e4m3 with power-of-two block scales
     k = cfg.k
     tokens = np.asarray(sorted(set(int(t) for t in tokens)), dtype=np.int64)
     x = host_bits(inp["x"])
@@ -59,7 +60,7 @@ def check_layer(cfg, inp, W, bufs, y, tokens, extra_pairs=(), tol=2e-2):
     # oracle inputs per token (e4m3: the dispatch's 1x128 quantisation of x)
     pos = {int(t): j for j, t in enumerate(toks_all)}
     if fp8:
-        xq, xsc = oracle.quant_rows_e4m3(oracle.bf16_to_f32(x[toks_all]))
+        xq, xsc = oracle.quant_rows_e4m3(oracle.bf16_to_f32(x[toks_all]), pow2=p2)
 
     by_e = collections.defaultdict(list)
     for t, i in sorted(pairs):
@@ -72,7 +73,7 @@ def check_layer(cfg, inp, W, bufs, y, tokens, extra_pairs=(), tol=2e-2):
             j = pos[t]
             if fp8:
                 o, _, ox = oracle.swiglu_row_fp8(xq[j], xsc[j], Wt["w13"], Wt["w13_s"], Wt["w2"],
-                                                 Wt["w2_s"], exact=True)
+                                                 Wt["w2_s"], exact=True, pow2=p2)
             else:
                 o, _, ox = oracle.swiglu_row_bf16(x[t], Wt["w13"], Wt["w2"], exact=True)
             out[(t, i)] = (o, ox)
@@ -84,7 +85,7 @@ def check_layer(cfg, inp, W, bufs, y, tokens, extra_pairs=(), tol=2e-2):
             j = pos[t]
             if fp8:
                 o, _, ox = oracle.swiglu_row_fp8(xq[j], xsc[j], S["ws13"], S["ws13_s"], S["ws2"],
-                                                 S["ws2_s"], exact=True)
+                                                 S["ws2_s"], exact=True, pow2=p2)
             else:
                 o, _, ox = oracle.swiglu_row_bf16(x[t], S["ws13"], S["ws2"], exact=True)
             out[t] = (o, ox)

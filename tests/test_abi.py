@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(moe):
 
 
 def test_abi_version_and_strerror(moe):
-    assert moe.abi_version() == 2
+    assert moe.abi_version() == 3
     for code in range(5):
         assert moe._lib.moe_strerror(code)
     assert b"unknown" in moe._lib.moe_strerror(99)
@@ -58,12 +58,29 @@ def test_workload_configs_validate(moe):
     (dict(k=33, E=64, n_group=1), 2),     # k > 32
     (dict(d_ff_shared=256), 2),           # shared width != routed width
     (dict(act="fp8"), 2),                 # mixed activation / weight formats
+    (dict(act="fp8", w="fp8", scales="pow2", d=384), 2),   # power-of-two recipe: d % 256
 ])
 def test_invalid_configs_are_rejected(moe, change, code):
     import dataclasses
     base = dataclasses.replace(synth.CONFIGS["tiny"], n_group=2, topk_group=1)
     c = dataclasses.replace(base, **change)
     assert moe.validate(c) == code
+
+
+def test_pow2_recipe_maps_to_its_own_format(moe):
+    """An e4m3 configuration with power-of-two scales is its own element format; out-of-range
+    format codes are rejected."""
+    import dataclasses
+    c = synth.CONFIGS["dsv3_fp8_pow2_prefill"]
+    mc = moe.make_cfg(c)
+    assert mc.act_dtype == mc.w_dtype == moe.MOE_FP8_E4M3_POW2
+    assert moe.make_cfg(synth.CONFIGS["dsv3_fp8_prefill"]).act_dtype == moe.MOE_FP8_E4M3
+    assert moe.query_sizes(c) == moe.query_sizes(synth.CONFIGS["dsv3_fp8_prefill"])
+    L = moe._lib
+    for bad in (-1, 3):
+        b = moe.make_cfg(dataclasses.replace(synth.CONFIGS["tiny"], n_group=2, topk_group=1))
+        b.act_dtype = b.w_dtype = bad
+        assert L.moe_validate(ctypes.byref(b)) == 1
 
 
 def test_sizes_follow_the_layout(moe):

@@ -53,7 +53,7 @@ BIG_KEEP = 4      # DeepSeek-V3-sized weight sets kept at once (<= 23 GB each)
 def inputs(cfg):
     """Device inputs for cfg. Weight sets are shared by workloads that differ only in T; at most
     BIG_KEEP large ones stay alive."""
-    wkey = (cfg.seed, cfg.E, cfg.d, cfg.d_ff, cfg.d_ff_shared, cfg.w)
+    wkey = (cfg.seed, cfg.E, cfg.d, cfg.d_ff, cfg.d_ff_shared, cfg.w, cfg.scales)
     if wkey not in _wcache:
         big = cfg.d * cfg.d_ff * cfg.E > 10 ** 8
         if big:
@@ -653,6 +653,131 @@ def test_fp8_prefill_rows_and_tokens():
     of a <=32-row and a 33..64-row expert where they exist, and of two experts past the first
     1024 compact rows, plus 256 tokens' whole layer output; >= 1024 rows."""
     cfg = synth.CONFIGS["dsv3_fp8_prefill"]
+    inp, W, lay, y = _run_layer(cfg)
+    rng = np.random.default_rng(cfg.seed)
+    extra, hot, n = _prefill_pairs(cfg, lay.bufs, rng)
+    tokens = np.sort(np.concatenate([[0, cfg.T - 1],
+                                     rng.choice(np.arange(1, cfg.T - 1), 254, replace=False)]))
+    res = check_layer(cfg, inp, W, lay.bufs, y, tokens, extra, tol=TOL_FP8)
+    print(cfg.name, res)
+    assert res["rows"] >= 1024
+
+
+# ------------------------------------------------------------------------------------------
+# e4m3 with power-of-two block scales (the block-scaled MMA's recipe)
+# ------------------------------------------------------------------------------------------
+P2_SMALL = dataclasses.replace(FP8_SMALL, name="small_fp8p2", scales="pow2")
+P2_HOT = dataclasses.replace(FP8_HOT, name="hot_fp8p2", scales="pow2")
+# several k-steps in both GEMMs (d = 4 x 128, d_ff = 3 x 128), ragged token tiles, 4 ranks
+P2_WIDE = dataclasses.replace(SMALL, name="wide_fp8p2", act="fp8", w="fp8", scales="pow2",
+                              T=200, d=512, d_ff=384, d_ff_shared=384, E=16, k=4, n_group=4,
+                              topk_group=2, R=4, seed=91)
+
+
+def test_dispatch_pow2_codes_and_scales_bit_exact():
+    cfg = P2_SMALL
+    inp = synth.make_router_inputs(cfg, "cuda")
+    m = moe()
+    b = m.Buffers(cfg)
+    m.route(cfg, inp["x"], inp["w_gate"], inp["bias"], b["topk_idx"], b["topk_w"], b["ws"])
+    m.dispatch(cfg, inp["x"], b["topk_idx"], b["recv"], b["recv_scales"], b["counts"],
+               b["row_of"], None)
+    idx, _ = oracle_route(cfg, inp)
+    _, _, row_of, src_tok = oracle.dispatch_index(idx, cfg.E, cfg.R)
+    q, sc = oracle.dispatch_payload(host_bits(inp["x"]), row_of, src_tok.size, fp8=True,
+                                    pow2=True)
+    filled = src_tok >= 0
+    assert np.array_equal(b["recv"].cpu().numpy()[filled], q[filled])
+    assert np.array_equal(b["recv_scales"].cpu().numpy().T[filled], sc[filled])
+    m_, _ = np.frexp(sc[filled])
+    assert np.all(m_ == 0.5)
+
+
+@pytest.mark.parametrize("cfg", [P2_SMALL, P2_HOT, P2_WIDE], ids=lambda c: c.name)
+def test_fp8_pow2_expert_rows_and_layer(cfg):
+    """Every routed row and every 3rd shared row against the oracle's reading R-l, the whole
+    layer output of every token, the gate/up intermediate's codes and scales close to the
+    oracle's and its scales powers of two."""
+    inp, W = inputs(cfg)
+    m = moe()
+    lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    y = lay(inp["x"])
+    assert m.read_status(lay.bufs["ws"]) == 0
+    b = lay.bufs
+    ti = b["topk_idx"].cpu().numpy()
+    ro = b["row_of"].cpu().numpy()
+    idx, _ = oracle_route(cfg, inp)
+    assert np.array_equal(ti, idx)
+    xq, xs = oracle.quant_rows_e4m3(oracle.bf16_to_f32(host_bits(inp["x"])), pow2=True)
+    get = expert_getter(W, True)
+    eb = host_bits(b["ebuf"])
+    worst = 0.0
+    n = 0
+    for e in np.unique(ti):
+        Wt = get(int(e))
+        for t, i in zip(*np.nonzero(ti == e)):
+            ref, _ = oracle.swiglu_row_fp8(xq[t], xs[t], Wt["w13"], Wt["w13_s"], Wt["w2"],
+                                           Wt["w2_s"], pow2=True)
+            worst = max(worst, rel_max_err(bf16_to_f64(eb[ro[t, i]]), bf16_to_f64(ref)))
+            n += 1
+    assert n == cfg.T * cfg.k
+    assert worst <= TOL_FP8, worst
+    S = shared_host(W, True)
+    sh = host_bits(b["shared_out"])
+    for t in range(0, cfg.T, 3):
+        ref, _ = oracle.swiglu_row_fp8(xq[t], xs[t], S["ws13"], S["ws13_s"], S["ws2"], S["ws2_s"],
+                                       pow2=True)
+        assert rel_max_err(bf16_to_f64(sh[t]), bf16_to_f64(ref)) <= TOL_FP8
+    assert _layer_tokens_check(cfg, np.arange(cfg.T), inp, W, y) <= TOL_FP8
+
+
+@pytest.mark.parametrize("cfg", [P2_SMALL, P2_WIDE], ids=lambda c: c.name)
+def test_fp8_pow2_variants_equal_the_layer(cfg):
+    """Gather mode, the shared expert on a side stream, a placement and back-to-back calls give
+    the pow2 layer's output bit for bit; the amax/448 recipe gives a different one."""
+    inp, W = inputs(cfg)
+    m = moe()
+    y0 = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))(inp["x"]).clone()
+    for v in (dict(gather=True), dict(side_stream=True), dict(gather=True, side_stream=True)):
+        y = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), **v)(inp["x"])
+        torch.cuda.synchronize()
+        assert torch.equal(y, y0), v
+    pl, _ = _placement_for(cfg, inp, 2, 31)
+    lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W), placement=pl)
+    assert torch.equal(lay(inp["x"]), y0)
+    assert torch.equal(lay(inp["x"]), y0)
+    assert m.read_status(lay.bufs["ws"]) == 0
+    amax_cfg = dataclasses.replace(cfg, scales="amax")
+    W8 = synth.make_expert_weights(amax_cfg, "cuda")
+    y8 = m.MoELayer(amax_cfg, inp["w_gate"], inp["bias"], weight_dict(W8))(inp["x"])
+    assert not torch.equal(y8, y0)
+
+
+def test_fp8_pow2_reports_a_weight_scale_that_is_not_a_power_of_two():
+    """Weights with one block scale off the power-of-two grid: the GEMM reports MOE_DEV_SCALE
+    in the status word and keeps running; the context stays usable."""
+    cfg = P2_SMALL
+    inp, W = inputs(cfg)
+    m = moe()
+    Wbad = dict(weight_dict(W))
+    Wbad["w13_s"] = W["w13_s"].clone()
+    Wbad["w13_s"][:, 0, 0] *= 1.5   # every routed expert's first gate block
+    lay = m.MoELayer(cfg, inp["w_gate"], inp["bias"], Wbad)
+    lay(inp["x"])
+    torch.cuda.synchronize()
+    st = m.read_status(lay.bufs["ws"])
+    assert st & m.MOE_DEV_SCALE and not st & m.MOE_DEV_TIMEOUT
+    ok = m.MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
+    ok(inp["x"])
+    assert m.read_status(ok.bufs["ws"]) == 0
+
+
+@pytest.mark.slow
+def test_fp8_pow2_prefill_rows_and_tokens():
+    """The FP8 prefill with power-of-two scales (T=16384): every row of the hottest expert, of a
+    <=32-row and a 33..64-row expert where they exist, of two experts past the first 1024
+    compact rows, and 256 tokens' whole layer output; >= 1024 rows."""
+    cfg = synth.CONFIGS["dsv3_fp8_pow2_prefill"]
     inp, W, lay, y = _run_layer(cfg)
     rng = np.random.default_rng(cfg.seed)
     extra, hot, n = _prefill_pairs(cfg, lay.bufs, rng)
