@@ -41,13 +41,15 @@ def kernels_per_step(cfg, mode="layer"):
     """Library kernels one layer step launches: route 2, dispatch 2 (1 in gather mode: no copy),
     schedule 2 (1 when the plan kernel fills the row list itself, up to 1024 rows), gate/up,
     down, combine; for e4m3 the quantisation of x when a shared expert or gather mode needs it;
+    with power-of-two e4m3 scales the gate/up GEMM's scale-byte pass (one per gate/up launch);
     with the shared expert on a side stream, its two GEMMs as launches of their own."""
     gather = "gather" in mode
     side = "side" in mode and cfg.d_ff_shared > 0
     fused = "fused" in mode
     sched = 1 if cfg.T * cfg.k <= 1024 else 2
     quant = 1 if cfg.act == "fp8" and (cfg.d_ff_shared or gather) else 0
-    return (7 + sched + quant - (1 if gather else 0) + (2 if side else 0)
+    sfpass = (2 if side else 1) if cfg.act == "fp8" and cfg.scales == "pow2" else 0
+    return (7 + sched + quant + sfpass - (1 if gather else 0) + (2 if side else 0)
             - (2 if fused else 0))
 L2_BYTES = 129 * 2 ** 20
 CPU_SAMPLE_SECONDS = 12.0   # target CPU time of the oracle sample behind cpu_baseline
@@ -152,7 +154,8 @@ def roofline(cfg, stage, ms, bytes_, flops, pk):
     t_hbm = bytes_[stage] / (pk["hbm"] * 1e9)
     t_tc = flops.get(stage, 0) / (tc_peak * 1e12) if stage in ("ffn_gate_up", "ffn_down") else 0.0
     t_alu = flops.get(stage, 0) / (ALU_FP32_TFLOPS * 1e12) if stage == "route" else 0.0
-    name = KERNEL_NAMES[stage].format("e4m3" if cfg.w == "fp8" else "bf16")
+    kind = "bf16" if cfg.w != "fp8" else ("mx8" if cfg.scales == "pow2" else "e4m3")
+    name = KERNEL_NAMES[stage].format(kind)
     traffic, note = measured_traffic(stage, cfg.name, bytes_[stage])
     base = {"kernel": name, "launch_ms": round(ms, 4), "traffic": traffic,
             "algorithmic_bytes_per_launch": bytes_[stage],
@@ -179,7 +182,8 @@ def roofline(cfg, stage, ms, bytes_, flops, pk):
 # shapes and kernels, a few GB on the device (ncu captures of full-size launches are avoided).
 # (The skewed prefill has none: 32 experts cannot hold its 10x hot expert, whose token tiles
 # are what its excess traffic comes from.)
-TRAFFIC_STANDIN = {"dsv3_decode": "dsv3_decode_e32", "dsv3_fp8_prefill": "dsv3_fp8_e32"}
+TRAFFIC_STANDIN = {"dsv3_decode": "dsv3_decode_e32", "dsv3_fp8_prefill": "dsv3_fp8_e32",
+                   "dsv3_fp8_pow2_prefill": "dsv3_fp8_pow2_e32"}
 
 
 def sources_hash(paths):
@@ -471,7 +475,8 @@ def time_placed(cfg, dev, W, steps, warm, spare_per_rank=4, seed=17):
 def run_extras(args, dev, W_decode, pk):
     """The rest of the metric's token range in the same process: the decode sweep (the decode
     layer's weights at T = 8 .. 1024), the Zipf-skewed bf16 prefill (T = 4096) and the FP8
-    prefill (T = 16384). Each prefill's weights are made, timed and freed before the next."""
+    prefill (T = 16384) with amax/448 and with power-of-two block scales. Each prefill's
+    weights are made, timed and freed before the next."""
     steps = max(3, args.extra_steps)
     warm = max(3, args.warmup)
     out = {"sweep": []}
@@ -494,7 +499,8 @@ def run_extras(args, dev, W_decode, pk):
                                                "gpu_launches")}
                             | {"sm_mhz": (r["clocks"] or {}).get("sm_mhz")})
         del lay, inp
-    for key, name in (("skew_prefill", "dsv3_skew_prefill"), ("fp8_prefill", "dsv3_fp8_prefill")):
+    for key, name in (("skew_prefill", "dsv3_skew_prefill"), ("fp8_prefill", "dsv3_fp8_prefill"),
+                      ("fp8_pow2_prefill", "dsv3_fp8_pow2_prefill")):
         cfg = synth.CONFIGS[name]
         torch.cuda.empty_cache()
         inp, W, lay = setup(cfg, dev)

@@ -72,6 +72,9 @@ int validate(const moe_cfg& c) {
   if (c.d_ff_shared != 0 && c.d_ff_shared != c.d_ff) return MOE_ERR_UNSUPPORTED;
   // the block-scaled down GEMM computes two 128-column output tiles per unit
   if (c.act_dtype == MOE_FP8_E4M3_POW2 && c.d % 256) return MOE_ERR_UNSUPPORTED;
+  // ... and keeps a row's scale bytes (one per 128-column block) in 64 bytes
+  if (c.act_dtype == MOE_FP8_E4M3_POW2 && (c.d > 128 * kSfRowBytes || c.d_ff > 128 * kSfRowBytes))
+    return MOE_ERR_UNSUPPORTED;
   const long long rows = (long long)c.R * c.R * cap_of(c);
   if (rows >= (1ll << 31) || (long long)c.T * c.k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -109,6 +112,11 @@ WsLayout ws_layout(const moe_cfg& c) {
   L.shared_tiles = c.d_ff_shared ? (c.T + L.bn - 1) / L.bn : 0;
   L.fused_done_n = L.max_tiles + L.shared_tiles + 2;
   L.fused_done = o; o = up256(o + sizeof(int32_t) * (size_t)L.fused_done_n);
+  const bool p2 = pow2_scales(c);
+  L.sf_gu = o;      o = up256(o + (p2 ? (size_t)kSfRowBytes * tk : 0));
+  L.sf_x = o;       o = up256(o + (p2 ? (size_t)kSfRowBytes * c.T : 0));
+  L.sf_h = o;       o = up256(o + (p2 ? (size_t)kSfRowBytes * tk : 0));
+  L.sf_hs = o;      o = up256(o + (p2 ? (size_t)kSfRowBytes * c.T : 0));
   L.total = o;
   return L;
 }

@@ -17,6 +17,12 @@
 // the B scales of column n in lanes 32q + n % 32 of every lane quarter q, column base + n / 32.
 // Here one 128-K block has one scale, so a cell holds the same byte four times.
 //
+// The input rows' scale bytes come from row-major byte tables in the workspace (64 bytes a
+// row, byte b for the row's 128-column block b): a scale warp loads its row's bytes once per
+// unit, as four 16-byte vectors, one unit ahead, instead of one scattered fp32 scale per
+// k-step. mx8_scale_bytes_kernel fills the gate/up tables from the dispatch's fp32 scales;
+// the gate/up epilogue writes h's bytes itself.
+//
 // Roles (768 threads, one CTA per SM, persistent over the unit list):
 //   warps 0..3    scale warps: warp q writes its lane quarter's A scale cell and B scale cells
 //                 of each k-step into the stage's tensor-memory scale slot (tcgen05.st)
@@ -30,7 +36,8 @@
 //                 into the 128-byte-swizzled tile (a TMA tile::gather4 per four rows measured
 //                 about four times slower on 128-row tiles)
 // Units are weight-tile-major (the token tiles that read one weight tile run on adjacent CTAs
-// and fetch each 32 KB weight tile of a k-step together).
+// and fetch each 32 KB weight tile of a k-step together). Each CTA decodes its units once,
+// into a table in shared memory, before the roles start.
 #include "moe_device.cuh"
 #include "moe_scale.cuh"
 
@@ -51,15 +58,14 @@ struct Mx8Args {
   int b_rows_routed;            // weight rows per routed expert (2F or d)
   int b_up_routed, b_up_shared; // offset of a unit's second weight tile (up rows, or the next
                                 // 128 output columns)
-  const float* a_sc_routed;     // token scales of routed A rows, block-major [K/128][ld]
-  const float* a_sc_shared;     // token scales of shared A rows [K/128][T]
-  int a_sc_ld_routed;
+  const uint8_t* sf_routed;     // scale bytes of the routed input rows, by compact row
+  const uint8_t* sf_shared;     // scale bytes of the shared expert's input rows, by token
   const float* w_sc_routed;     // [E][b_rows_routed/128][K/128]
   const float* w_sc_shared;     // [b_rows_shared/128][K/128]
   void* out_routed;             // gate/up: e4m3 h [tk][F]; down: bf16 ebuf [recv rows][d]
-  float* out_sc_routed;         // gate/up: h scales, block-major [F/128][tk]
+  uint8_t* out_sf_routed;       // gate/up: h's scale bytes, by compact row
   void* out_shared;             // gate/up: e4m3 hs [T][Fs]; down: bf16 shared_out [T][d]
-  float* out_sc_shared;         // gate/up: hs scales [Fs/128][T]
+  uint8_t* out_sf_shared;       // gate/up: hs's scale bytes, by token
   int ld_routed, ld_shared;     // output row length (elements)
   long long out_rows_routed;    // bound of routed output row indices
   int box_routed, box_shared;   // rows per box of the contiguous token-row maps
@@ -70,19 +76,34 @@ struct Mx8Args {
   int n_experts;
 };
 
-struct UnitX {
-  int g, n0, nlen, m;
+// One unit of a CTA: group g (-1: the shared expert), token tile [n0, n0 + nlen), weight tile
+// m, the group's first compact row goff and the expert whose weights it reads.
+struct UnitInfo {
+  int g, n0, nlen, m, goff, we;
 };
 
-// Unit u -> (group, token tile, weight tile), weight-tile-major; shared-expert units first.
-__device__ __forceinline__ UnitX decode_unit_mx(const Mx8Args& a, int u, int n_tiles) {
-  UnitX r;
+__device__ __forceinline__ int weight_expert_mx(const int32_t* group_expert, int g, int n_experts,
+                                                uint32_t* status) {
+  if (!group_expert) return g;
+  const int e = group_expert[g];
+  if (e >= 0 && e < n_experts) return e;
+  if (status) raise_status(status, MOE_DEV_BOUNDS);
+  return 0;
+}
+
+// Unit u -> its UnitInfo, weight-tile-major; shared-expert units first. n_tiles: entries in
+// the tile list. status (nullable) receives MOE_DEV_BOUNDS for a slot outside the weights.
+__device__ __forceinline__ UnitInfo decode_unit_mx(const Mx8Args& a, int u, int n_tiles,
+                                                   uint32_t* status) {
+  UnitInfo r;
   const int us = a.n_shared_tiles * a.mt_shared;
   if (u < us) {
     r.g = -1;
     r.m = u / a.n_shared_tiles;
     r.n0 = (u - r.m * a.n_shared_tiles) * 128;
     r.nlen = min(128, a.T - r.n0);
+    r.goff = 0;
+    r.we = 0;
   } else {
     const int v = u - us;
     const int tt0 = v / a.mt_routed;   // a tile of the unit's expert (the ranges coincide)
@@ -97,17 +118,10 @@ __device__ __forceinline__ UnitX decode_unit_mx(const Mx8Args& a, int u, int n_t
     r.g = t.group;
     r.n0 = t.n0;
     r.nlen = t.nlen;
+    r.goff = a.grp_off[t.group];
+    r.we = weight_expert_mx(a.group_expert, t.group, a.n_experts, status);
   }
   return r;
-}
-
-__device__ __forceinline__ int weight_expert_mx(const int32_t* group_expert, int g, int n_experts,
-                                                uint32_t* status) {
-  if (!group_expert) return g;
-  const int e = group_expert[g];
-  if (e >= 0 && e < n_experts) return e;
-  if (status) raise_status(status, MOE_DEV_BOUNDS);
-  return 0;
 }
 
 constexpr int kStages = 4;
@@ -124,13 +138,12 @@ constexpr int kStageBytes = kABytes + 2 * kBBytes;
 constexpr int kTmemCols = 512;
 constexpr int kSfCol0 = 256;        // scale slots after the 256-column accumulator
 constexpr int kSfSlotCols = 32;     // per stage: A scales at +0..3, B scales at +16..23
-constexpr int kScalePrefetch = 6;   // k-steps the scale copies run ahead
-constexpr int kScaleSlots = kScalePrefetch + 1;
-constexpr int kScaleSlotFloats = 36;   // 32 row scales, gate and up (or two tile) scales, pad
+constexpr int kMaxUnitTable = 256;  // units of a CTA decoded into shared memory (more: on the fly)
 constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kAmaxOff = kBarOff + 512;               // [2][4][32][4] floats
-constexpr int kRingOff = kAmaxOff + 2 * 4 * 32 * 4 * 4;   // [4 warps][slots][36] floats
-constexpr int kSmem = kRingOff + kSfWarps * kScaleSlots * kScaleSlotFloats * 4 + 1024;
+constexpr int kAmaxOff = kBarOff + 512;                          // [2][4][32][4] floats
+constexpr int kUnitOff = kAmaxOff + 2 * 4 * 32 * 4 * 4;          // UnitInfo [kMaxUnitTable]
+constexpr int kWsfOff = kUnitOff + kMaxUnitTable * (int)sizeof(UnitInfo);   // [4 warps][128] B
+constexpr int kSmem = kWsfOff + kSfWarps * 2 * kSfRowBytes + 1024;
 
 // Instruction descriptor of the block-scaled e4m3 MMA, M = 128, N = 256, K-major operands:
 // B scale-factor id in bits 4-5, formats e4m3 (0) in bits 7-9 and 10-12, N >> 3 in bits 17-22,
@@ -169,73 +182,12 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 __device__ __forceinline__ uint32_t rep4(uint32_t byte) { return byte * 0x01010101u; }
 
-__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
 // The hardware arrives on bar once every cp.async this thread has issued so far has landed;
 // the arrival counts as one of the barrier's expected arrivals.
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Where the scales of one k-step of one unit come from, for tile row r: the row's A scale at
-// xs[ks * xs_ld + srow] (srow -1: past the tile's rows), the unit's two weight-block scales
-// at wsc[ks] and wsc[w_up + ks]. Walks the CTA's units in order, one k-step per next().
-template <int STAGE>
-struct ScaleCursor {
-  static constexpr int kStep = STAGE == 0 ? 128 : 256;
-  int u = 0, ks = 0;
-  long long srow = -1, xs_ld = 0;
-  const float* xs = nullptr;
-  const float* wsc = nullptr;
-  int w_up = 0;
-
-  __device__ void load(const Mx8Args& a, int n_tiles, int r) {
-    const UnitX t = decode_unit_mx(a, u, n_tiles);
-    const bool sh = t.g < 0;
-    srow = -1;
-    if (r < t.nlen) {
-      long long row;
-      if (sh) {
-        row = t.n0 + r;
-      } else {
-        const int ci = a.grp_off[t.g] + t.n0 + r;
-        row = ci;   // down: compact row of h
-        if (STAGE == 0) row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
-      }
-      const long long bound = sh ? a.T : (STAGE == 0 ? a.a_rows_routed : a.tk);
-      if (row >= 0 && row < bound) srow = row;
-      else raise_status(a.status, MOE_DEV_BOUNDS);
-    }
-    xs = sh ? a.a_sc_shared : a.a_sc_routed;
-    xs_ld = sh ? a.T : a.a_sc_ld_routed;
-    const int we = sh ? 0 : weight_expert_mx(a.group_expert, t.g, a.n_experts, nullptr);
-    const int kb_n = a.k_steps;
-    wsc = (sh ? a.w_sc_shared : a.w_sc_routed + (size_t)we * (a.b_rows_routed / 128) * kb_n) +
-          (size_t)t.m * (kStep / 128) * kb_n;
-    w_up = (sh ? a.b_up_shared : a.b_up_routed) / 128 * kb_n;
-  }
-  __device__ void start(const Mx8Args& a, int u0, int n_tiles, int r) {
-    u = u0;
-    ks = 0;
-    load(a, n_tiles, r);
-  }
-  __device__ void next(const Mx8Args& a, int units, int n_tiles, int r) {
-    if (++ks < a.k_steps) return;
-    ks = 0;
-    u += gridDim.x;
-    if (u < units) load(a, n_tiles, r);
-  }
-};
 
 template <int STAGE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -257,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* amax_x = reinterpret_cast<float*>(smem + kAmaxOff);
+  UnitInfo* unit_tab = reinterpret_cast<UnitInfo*>(smem + kUnitOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -281,6 +234,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // the previous kernel's outputs (schedule, activations) and its tensor memory are free from here
   pdl_wait();
+  const int n_tiles = *a.n_tiles;
+  const int units = a.n_shared_tiles * a.mt_shared + n_tiles * a.mt_routed;
+  // units of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int n_my = blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  for (int i = threadIdx.x; i < min(n_my, kMaxUnitTable); i += blockDim.x)
+    unit_tab[i] = decode_unit_mx(a, blockIdx.x + i * gridDim.x, n_tiles, a.status);
+  auto unit_at = [&](int i) -> UnitInfo {
+    return i < kMaxUnitTable ? unit_tab[i]
+                             : decode_unit_mx(a, blockIdx.x + i * gridDim.x, n_tiles, nullptr);
+  };
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -289,8 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_tiles = *a.n_tiles;
-  const int units = a.n_shared_tiles * a.mt_shared + n_tiles * a.mt_routed;
 
   if (warp == kProducerWarp) {
     // ------------------------------ TMA producer ------------------------------
@@ -299,21 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const UnitX t = decode_unit_mx(a, u, n_tiles);
+    for (int i = 0; i < n_my && ok; ++i) {
+      const UnitInfo t = unit_at(i);
       const bool sh = t.g < 0;
       const CUtensorMap* amap = sh ? &mapAs : &mapA;
       const CUtensorMap* bmap = sh ? &mapBs : &mapB;
-      const int we = sh ? 0 : weight_expert_mx(a.group_expert, t.g, a.n_experts,
-                                                lane == 0 ? a.status : nullptr);
-      const int brow0 = (sh ? 0 : we * a.b_rows_routed) + t.m * kStep;
+      const int brow0 = (sh ? 0 : t.we * a.b_rows_routed) + t.m * kStep;
       const int brow1 = brow0 + (sh ? a.b_up_shared : a.b_up_routed);
       // Token rows: the shared expert's rows (x) and the down projection's rows (h) are one box
       // per k-step; routed gate/up rows are gathered by the copy warps.
       int box_row = -1;
       uint32_t a_bytes = 0;
       if (STAGE == 1 || sh) {
-        const int row0 = sh ? t.n0 : a.grp_off[t.g] + t.n0;
+        const int row0 = sh ? t.n0 : t.goff + t.n0;
         const bool in = row0 >= 0 && row0 < (sh ? a.T : a.tk);
         if (!in && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
         box_row = in ? row0 : -1;
@@ -347,11 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+      for (int i = 0; i < n_my && ok; ++i) {
         // the epilogue has drained the previous unit's accumulator
-        if (!mbar_wait(acc_empty, (it & 1u) ^ 1u, abort_flag, a.status)) break;
+        if (!mbar_wait(acc_empty, (static_cast<uint32_t>(i) & 1u) ^ 1u, abort_flag, a.status))
+          break;
         tc_fence_after();
         for (int ks = 0; ks < a.k_steps; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort_flag, a.status)) {
@@ -394,18 +353,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const UnitX t = decode_unit_mx(a, u, n_tiles);
+      for (int i = 0; i < n_my && ok; ++i) {
+        const UnitInfo t = unit_at(i);
         const bool gather = t.g >= 0;
         int src[16];   // row of each of the thread's 16 tile rows (-1: none)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int p = rg + 8 * i;
-          src[i] = -1;
+        for (int i2 = 0; i2 < 16; ++i2) {
+          const int p = rg + 8 * i2;
+          src[i2] = -1;
           if (gather && p < t.nlen) {
-            const int ci = a.grp_off[t.g] + t.n0 + p;
+            const int ci = t.goff + t.n0 + p;
             const long long row = (ci >= 0 && ci < a.tk) ? a.row_list[ci] : -1;
-            if (row >= 0 && row < a.a_rows_routed) src[i] = static_cast<int>(row);
+            if (row >= 0 && row < a.a_rows_routed) src[i2] = static_cast<int>(row);
             else raise_status(a.status, MOE_DEV_BOUNDS);
           }
         }
@@ -418,10 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sa = smem_addr(smem + stage * kStageBytes) + dst_off;
             const uint8_t* gk = gbase + ks * 128;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (src[i] >= 0)
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa + i * 1024),
-                             "l"(gk + (long long)src[i] * a.gather_ld)
+            for (int i2 = 0; i2 < 16; ++i2)
+              if (src[i2] >= 0)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa + i2 * 1024),
+                             "l"(gk + (long long)src[i2] * a.gather_ld)
                              : "memory");
           }
           cp_async_arrive(&full[stage]);
@@ -436,70 +395,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kSfWarps) {
     // ------------------------------ scale warps ------------------------------
-    // Warp q, lane l: the A scale of tile row r = 32q + l into (lane r, column q of the slot),
-    // and the B scales (the unit's two weight blocks of the k-step) into columns 16..23 of the
-    // slot for its 32 lanes. A slot is rewritten once the MMAs that read it have completed
-    // (the stage's empty barrier); the stage's full barrier then counts this warp's arrival.
-    // The fp32 scales come through a shared-memory ring filled with cp.async kScalePrefetch
-    // k-steps ahead (across unit boundaries): a token's scales are scattered rows of a table
-    // far larger than L2, so a load issued at its own k-step would put a DRAM round trip on
-    // every k-step.
+    // Warp q, lane l: tile row r = 32q + l. Per unit: the row's scale bytes (four 16-byte loads
+    // of its table row) and the unit's two weight-block scales of every k-step (lane l loads
+    // k-steps l and l + 32, converted to bytes in the warp's shared-memory rows), both issued
+    // one unit ahead. Per k-step: the A cell (lane r, column q of the stage's slot) and the B
+    // cells (columns 16..23, gate bytes then up bytes) once the MMAs that read the slot's
+    // previous k-step have completed (the stage's empty barrier); the stage's full barrier
+    // then counts this warp's arrival.
     const int q = warp;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    float* ring = reinterpret_cast<float*>(smem + kRingOff) + q * kScaleSlots * kScaleSlotFloats;
+    const int r = q * 32 + lane;
+    uint8_t* wsf = smem + kWsfOff + q * 2 * kSfRowBytes;   // [gate 64][up 64] bytes
+    const int kb_n = a.k_steps;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     bool scale_ok = true;
-    // k-steps of this CTA: its units times K / 128
-    const long long steps =
-        blockIdx.x < units
-            ? (long long)((units - blockIdx.x + gridDim.x - 1) / gridDim.x) * a.k_steps
-            : 0;
-    ScaleCursor<STAGE> pf;   // the prefetch cursor, kScalePrefetch k-steps ahead
-    if (steps > 0) pf.start(a, blockIdx.x, n_tiles, q * 32 + lane);
-    auto prefetch = [&](long long c) {
-      if (c < steps) {
-        float* sl = ring + (c % kScaleSlots) * kScaleSlotFloats;
-        if (pf.srow >= 0) cp_async4(sl + lane, pf.xs + pf.ks * pf.xs_ld + pf.srow);
-        else sl[lane] = 1.0f;
-        if (lane == 0) cp_async4(sl + 32, pf.wsc + pf.ks);
-        if (lane == 1) cp_async4(sl + 33, pf.wsc + pf.w_up + pf.ks);
-        pf.next(a, units, n_tiles, q * 32 + lane);
-      }
-      cp_async_commit();
+    uint4 na[4];
+    float nw[4];   // weight scales of k-steps l, l + 32 (gate), l, l + 32 (up)
+    auto issue = [&](int i) {
+      const UnitInfo t = unit_at(i);
+      const bool sh = t.g < 0;
+      const long long row = sh ? (long long)t.n0 + r : (long long)t.goff + t.n0 + r;
+      const bool in = r < t.nlen && row >= 0 && row < (sh ? a.T : a.tk);
+      const uint4* src = reinterpret_cast<const uint4*>((sh ? a.sf_shared : a.sf_routed) +
+                                                        (in ? row : 0) * kSfRowBytes);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        na[j] = in ? __ldg(src + j) : make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+      const float* wsc = (sh ? a.w_sc_shared
+                             : a.w_sc_routed + (size_t)t.we * (a.b_rows_routed / 128) * kb_n) +
+                         (size_t)t.m * (kStep / 128) * kb_n;
+      const int w_up = (sh ? a.b_up_shared : a.b_up_routed) / 128 * kb_n;
+      nw[0] = lane < kb_n ? __ldg(wsc + lane) : 1.0f;
+      nw[1] = lane + 32 < kb_n ? __ldg(wsc + lane + 32) : 1.0f;
+      nw[2] = lane < kb_n ? __ldg(wsc + w_up + lane) : 1.0f;
+      nw[3] = lane + 32 < kb_n ? __ldg(wsc + w_up + lane + 32) : 1.0f;
     };
-    for (int c = 0; c < kScalePrefetch; ++c) prefetch(c);
-    for (long long c = 0; c < steps; ++c) {
-      prefetch(c + kScalePrefetch);
-      cp_async_wait<kScalePrefetch>();   // step c's copies have landed
+    if (n_my > 0) issue(0);
+    for (int i = 0; i < n_my && ok; ++i) {
+      uint32_t aw[16] = {na[0].x, na[0].y, na[0].z, na[0].w, na[1].x, na[1].y, na[1].z, na[1].w,
+                         na[2].x, na[2].y, na[2].z, na[2].w, na[3].x, na[3].y, na[3].z, na[3].w};
+      __syncwarp();   // every lane is done with the previous unit's weight bytes
+      wsf[lane] = static_cast<uint8_t>(ue8m0_of(nw[0], scale_ok));
+      wsf[lane + 32] = static_cast<uint8_t>(ue8m0_of(nw[1], scale_ok));
+      wsf[64 + lane] = static_cast<uint8_t>(ue8m0_of(nw[2], scale_ok));
+      wsf[96 + lane] = static_cast<uint8_t>(ue8m0_of(nw[3], scale_ok));
       __syncwarp();
-      const float* sl = ring + (c % kScaleSlots) * kScaleSlotFloats;
-      const float xsv = sl[lane], wg = sl[32], wu = sl[33];
-      if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      bool unused = true;
-      const uint32_t sfa = rep4(ue8m0_of(xsv, unused));
-      const uint32_t sfg = rep4(ue8m0_of(wg, scale_ok));
-      const uint32_t sfu = rep4(ue8m0_of(wu, scale_ok));
-      const uint32_t slot = tmem + lane_base + kSfCol0 + stage * kSfSlotCols;
-      tmem_st1(slot + q, sfa);
-      tmem_st8(slot + 16, sfg, sfu);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();   // (also: every lane has read ring slot c before it is refilled)
-      if (lane == 0) mbar_arrive(&full[stage]);
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
+      if (i + 1 < n_my) issue(i + 1);
+      uint32_t cur = aw[0];
+      for (int ks = 0; ks < kb_n; ++ks) {
+        const uint32_t ab = cur & 0xFFu;
+        cur >>= 8;
+        if ((ks & 3) == 3) {   // the next four k-steps' bytes
+#pragma unroll
+          for (int j = 0; j < 15; ++j) aw[j] = aw[j + 1];
+          cur = aw[0];
+        }
+        const uint32_t gb = wsf[ks], ub = wsf[64 + ks];
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t slot = tmem + lane_base + kSfCol0 + stage * kSfSlotCols;
+        tmem_st1(slot + q, rep4(ab));
+        tmem_st8(slot + 16, rep4(gb), rep4(ub));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
-    // after an abort: copies still in flight land before the CTA exits
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    (void)ok;
     if (!__all_sync(0xffffffffu, scale_ok) && lane == 0) raise_status(a.status, MOE_DEV_SCALE);
   } else {
     // ------------------------------ epilogue ------------------------------
@@ -507,12 +478,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = (warp - kSfWarps) >> 2;   // columns 32*part .. 32*part+31 of each tile
     const int r = quarter * 32 + lane;         // token row of the tile (tensor-memory lane)
     const uint32_t tb = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + part * 32;
-    uint32_t it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
-      const UnitX t = decode_unit_mx(a, u, n_tiles);
+    for (int i = 0; i < n_my; ++i) {
+      const uint32_t it = static_cast<uint32_t>(i);
+      const UnitInfo t = unit_at(i);
       const bool sh = t.g < 0;
       const bool live = r < t.nlen;
-      const int goff = sh ? 0 : a.grp_off[t.g];
+      const int goff = t.goff;
       // down: this lane's output row (the receive row), looked up before the accumulator wait
       long long orow_down = -1;
       if (STAGE == 1 && live) {
@@ -576,9 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               reinterpret_cast<uint4*>(out)[qq] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            if (part == 0) {   // block-major: consecutive lanes write consecutive rows
-              float* osc = sh ? a.out_sc_shared : a.out_sc_routed;
-              osc[(long long)t.m * (sh ? a.T : a.tk) + orow] = scale;
+            if (part == 0) {   // the row's scale byte for block m (its exponent field)
+              uint8_t* osf = sh ? a.out_sf_shared : a.out_sf_routed;
+              osf[orow * kSfRowBytes + t.m] =
+                  static_cast<uint8_t>((__float_as_uint(scale) >> 23) & 0xFFu);
             }
           }
         }
@@ -631,6 +603,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+namespace {
+
+// The gate/up GEMM's input scale bytes. Compact row c < n_routed takes the scales of its
+// source row row_list[c] (a receive row, or a token in gather mode; -1 or out of range: none)
+// from the block-major fp32 table xs [K/128][xs_ld]; token t < n_shared (the shared expert's
+// input) those of x quantised, xq_sc [K/128][T]. A byte is the scale's exponent field; a scale
+// that is not a positive normal power of two is reported (MOE_DEV_SCALE). Bytes past K/128,
+// and the bytes of a row without a source, are 127 (scale 1).
+__global__ void __launch_bounds__(256) mx8_scale_bytes_kernel(
+    const int32_t* __restrict__ row_list, long long row_bound, const float* __restrict__ xs,
+    long long xs_ld, const float* __restrict__ xq_sc, int T, int n_routed, int n_shared, int kb_n,
+    uint8_t* __restrict__ sf_gu, uint8_t* __restrict__ sf_x, uint32_t* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)n_routed + n_shared) return;
+  const float* src;
+  long long ld, row;
+  uint8_t* dst;
+  if (i < n_routed) {
+    const long long r = row_list[i];
+    row = (r >= 0 && r < row_bound) ? r : -1;
+    src = xs;
+    ld = xs_ld;
+    dst = sf_gu + i * kSfRowBytes;
+  } else {
+    row = i - n_routed;
+    src = xq_sc;
+    ld = T;
+    dst = sf_x + row * kSfRowBytes;
+  }
+  bool ok = true;
+  uint32_t w[kSfRowBytes / 4];
+#pragma unroll
+  for (int j = 0; j < kSfRowBytes / 4; ++j) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int kb = 4 * j + b;
+      const uint32_t byte = (row >= 0 && kb < kb_n) ? ue8m0_of(src[kb * ld + row], ok) : 127u;
+      v |= byte << (8 * b);
+    }
+    w[j] = v;
+  }
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < kSfRowBytes / 16; ++j)
+    d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  if (!ok) raise_status(status, MOE_DEV_SCALE);
+}
+
+}  // namespace
+
 cudaError_t launch_ffn_gemm_mx8(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                                 const float* recv_scales, const moe_weights& w, void* ebuf,
                                 void* shared_out, char* ws, cudaStream_t st, bool pdl,
@@ -667,15 +692,14 @@ cudaError_t launch_ffn_gemm_mx8(const moe_cfg& c, const WsLayout& L, int stage, 
     a.b_rows_routed = 2 * F;
     a.b_up_routed = F;
     a.b_up_shared = Fs;
-    a.a_sc_routed = recv_scales;
-    a.a_sc_ld_routed = static_cast<int>(recv_rows);
-    a.a_sc_shared = reinterpret_cast<const float*>(ws + L.xq_scales);
+    a.sf_routed = reinterpret_cast<const uint8_t*>(ws + L.sf_gu);
+    a.sf_shared = reinterpret_cast<const uint8_t*>(ws + L.sf_x);
     a.w_sc_routed = w.w13_scales;
     a.w_sc_shared = w.ws13_scales;
     a.out_routed = ws + L.h;
-    a.out_sc_routed = reinterpret_cast<float*>(ws + L.h_scales);
+    a.out_sf_routed = reinterpret_cast<uint8_t*>(ws + L.sf_h);
     a.out_shared = ws + L.hs;
-    a.out_sc_shared = reinterpret_cast<float*>(ws + L.hs_scales);
+    a.out_sf_shared = reinterpret_cast<uint8_t*>(ws + L.sf_hs);
     a.ld_routed = F;
     a.ld_shared = Fs;
     a.box_routed = 1;
@@ -685,8 +709,6 @@ cudaError_t launch_ffn_gemm_mx8(const moe_cfg& c, const WsLayout& L, int stage, 
     if (gather) {
       a.row_list = reinterpret_cast<const int32_t*>(ws + L.tok_list);
       a.a_rows_routed = c.T;
-      a.a_sc_routed = reinterpret_cast<const float*>(ws + L.xq_scales);
-      a.a_sc_ld_routed = c.T;
       a.gather_base = ws + L.xq;
     }
     // (routed gate/up rows are gathered with cp.async; the map is a placeholder)
@@ -705,9 +727,8 @@ cudaError_t launch_ffn_gemm_mx8(const moe_cfg& c, const WsLayout& L, int stage, 
     a.b_rows_routed = d;
     a.b_up_routed = 128;
     a.b_up_shared = 128;
-    a.a_sc_routed = reinterpret_cast<const float*>(ws + L.h_scales);
-    a.a_sc_ld_routed = tk;
-    a.a_sc_shared = reinterpret_cast<const float*>(ws + L.hs_scales);
+    a.sf_routed = reinterpret_cast<const uint8_t*>(ws + L.sf_h);
+    a.sf_shared = reinterpret_cast<const uint8_t*>(ws + L.sf_hs);
     a.w_sc_routed = w.w2_scales;
     a.w_sc_shared = w.ws2_scales;
     a.out_routed = ebuf;
@@ -735,6 +756,21 @@ cudaError_t launch_ffn_gemm_mx8(const moe_cfg& c, const WsLayout& L, int stage, 
   }
   const dim3 grid(part.ctas > 0 ? part.ctas : sm_count());
   if (stage == 0) {
+    // the input rows' scale bytes first (routed rows of this launch, and the shared expert's)
+    const int n_routed = a.mt_routed ? tk : 0;
+    const int n_shared = a.mt_shared ? c.T : 0;
+    if (n_routed + n_shared > 0) {
+      const cudaError_t e = launch_kernel(
+          mx8_scale_bytes_kernel, dim3((n_routed + n_shared + 255) / 256), dim3(256), 0, st, pdl,
+          a.row_list, a.a_rows_routed, gather ? reinterpret_cast<const float*>(ws + L.xq_scales)
+                                              : recv_scales,
+          gather ? (long long)c.T : recv_rows,
+          reinterpret_cast<const float*>(ws + L.xq_scales), c.T, n_routed, n_shared, d / 128,
+          reinterpret_cast<uint8_t*>(ws + L.sf_gu), reinterpret_cast<uint8_t*>(ws + L.sf_x),
+          a.status);
+      if (e != cudaSuccess) return e;
+      pdl = true;   // the GEMM follows the pre-pass
+    }
     auto kern = ffn_gemm_mx8_kernel<0>;
     const cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), kSmem);
     if (err != cudaSuccess) return err;

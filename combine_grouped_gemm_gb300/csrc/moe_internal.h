@@ -46,6 +46,12 @@ struct WsLayout {
   size_t tok_list;    // int32 [T*k]: token of each compact row (gather mode)
   size_t grp_order;   // int32 [E]: group at each schedule position (placed experts)
   size_t fused_done;  // int32 [fused_done_n]: dependency counters of the fused expert launch
+  // power-of-two e4m3 only: the UE8M0 scale bytes of each GEMM input row, row-major with
+  // kSfRowBytes bytes a row (byte b: the row's 128-column block b), for the block-scaled MMA
+  size_t sf_gu;       // [T*k]: routed gate/up input rows (compact order)
+  size_t sf_x;        // [T]: the shared expert's gate/up input rows (x quantised)
+  size_t sf_h;        // [T*k]: routed down input rows (h)
+  size_t sf_hs;       // [T]: the shared expert's down input rows (hs)
   int shared_tiles;   // token tiles of the shared expert (0: none)
   int fused_done_n;   // max_tiles + shared_tiles + 2
   size_t total;
@@ -63,6 +69,9 @@ inline int cap_of(const moe_cfg& c) {
   return Ts * (c.k < Er ? c.k : Er);
 }
 inline bool is_fp8(const moe_cfg& c) { return c.act_dtype != MOE_BF16; }
+// Scale bytes per row of the power-of-two recipe's byte tables: one per 128-column block of
+// K <= 8192.
+constexpr int kSfRowBytes = 64;
 // e4m3 with power-of-two block scales (the block-scaled MMA's recipe)
 inline bool pow2_scales(const moe_cfg& c) { return c.act_dtype == MOE_FP8_E4M3_POW2; }
 inline size_t act_bytes(const moe_cfg& c) { return is_fp8(c) ? 1 : 2; }

@@ -62,7 +62,9 @@ extern "C" {
                                 amax <= 448 * 2^e (e in [-126, 127], 1 for an all-zero block);
                                 the weight scales must be powers of two too. The grouped GEMMs
                                 apply the scales in the tensor core (block-scaled MMA) instead
-                                of promoting each 128-K block's partial sums. */
+                                of promoting each 128-K block's partial sums. These kernels
+                                take d % 256 == 0, d <= 8192 and d_ff <= 8192 in this format
+                                (MOE_ERR_UNSUPPORTED otherwise). */
 
 /* Number of events moe_layer records when given an event array (see moe_layer). */
 #define MOE_LAYER_EVENTS 7

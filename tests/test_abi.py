@@ -75,7 +75,11 @@ def test_pow2_recipe_maps_to_its_own_format(moe):
     mc = moe.make_cfg(c)
     assert mc.act_dtype == mc.w_dtype == moe.MOE_FP8_E4M3_POW2
     assert moe.make_cfg(synth.CONFIGS["dsv3_fp8_prefill"]).act_dtype == moe.MOE_FP8_E4M3
-    assert moe.query_sizes(c) == moe.query_sizes(synth.CONFIGS["dsv3_fp8_prefill"])
+    s2, s8 = moe.query_sizes(c), moe.query_sizes(synth.CONFIGS["dsv3_fp8_prefill"])
+    assert {k: v for k, v in s2.items() if k != "ws_bytes"} == \
+        {k: v for k, v in s8.items() if k != "ws_bytes"}
+    # the workspace adds the 64-byte scale rows of the GEMM inputs: 2 x T*k + 2 x T of them
+    assert s2["ws_bytes"] - s8["ws_bytes"] >= 64 * (2 * c.T * c.k + 2 * c.T)
     L = moe._lib
     for bad in (-1, 3):
         b = moe.make_cfg(dataclasses.replace(synth.CONFIGS["tiny"], n_group=2, topk_group=1))

@@ -23,6 +23,9 @@ def test_kernels_per_step_follows_the_launch_structure():
     assert bench.kernels_per_step(C["dsv3_skew_prefill"]) == 9
     # + the e4m3 quantisation of the shared expert's input
     assert bench.kernels_per_step(C["dsv3_fp8_prefill"]) == 10
+    # the power-of-two recipe adds the scale-byte pass before each gate/up launch
+    assert bench.kernels_per_step(C["dsv3_fp8_pow2_prefill"]) == 11
+    assert bench.kernels_per_step(C["dsv3_fp8_pow2_prefill"], "side") == 14
 
 
 def test_kernels_per_step_of_the_layer_variants():
