@@ -555,11 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // the unit's two 128-column output tiles: columns 32*part.. of each, as bf16
-        __nv_bfloat16* orow_p = nullptr;
-        if (live && orow_down >= 0)
-          orow_p = static_cast<__nv_bfloat16*>(sh ? a.out_shared : a.out_routed) +
-                   orow_down * (sh ? a.ld_shared : a.ld_routed) + t.m * 256 + part * 32;
+        // the unit's two 128-column output tiles: columns 32*part.. of each, packed to bf16 as
+        // they are drained; the accumulator is released before any store is issued
+        uint32_t pk[2][16];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           uint32_t v0[16], v1[16];
@@ -571,22 +569,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
           }
-          if (orow_p) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            pk[h2][j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+            pk[h2][8 + j] =
+                pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
+          }
+        }
+        if (live && orow_down >= 0) {
+          __nv_bfloat16* orow_p = static_cast<__nv_bfloat16*>(sh ? a.out_shared : a.out_routed) +
+                                  orow_down * (sh ? a.ld_shared : a.ld_routed) + t.m * 256 +
+                                  part * 32;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
             uint4* out = reinterpret_cast<uint4*>(orow_p + h2 * 128);
 #pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-              const uint32_t* s0 = qq ? v1 : v0;
-              out[2 * qq] = make_uint4(
-                  pack_bf16x2(__uint_as_float(s0[0]), __uint_as_float(s0[1])),
-                  pack_bf16x2(__uint_as_float(s0[2]), __uint_as_float(s0[3])),
-                  pack_bf16x2(__uint_as_float(s0[4]), __uint_as_float(s0[5])),
-                  pack_bf16x2(__uint_as_float(s0[6]), __uint_as_float(s0[7])));
-              out[2 * qq + 1] = make_uint4(
-                  pack_bf16x2(__uint_as_float(s0[8]), __uint_as_float(s0[9])),
-                  pack_bf16x2(__uint_as_float(s0[10]), __uint_as_float(s0[11])),
-                  pack_bf16x2(__uint_as_float(s0[12]), __uint_as_float(s0[13])),
-                  pack_bf16x2(__uint_as_float(s0[14]), __uint_as_float(s0[15])));
-            }
+            for (int qq = 0; qq < 4; ++qq)
+              out[qq] = make_uint4(pk[h2][4 * qq], pk[h2][4 * qq + 1], pk[h2][4 * qq + 2],
+                                   pk[h2][4 * qq + 3]);
           }
         }
       }
