@@ -72,7 +72,24 @@ def ws_offsets(cfg):
                        ("row_list", 4 * tk), ("h", ab * tk * cfg.d_ff)]:
         o[name] = cur
         cur = up(cur + size)
-    o["hs"] = up(cur + (4 * tk * (cfg.d_ff // 128) if cfg.act == "fp8" else 0))
+    fp8 = cfg.act == "fp8"
+    p2 = fp8 and getattr(cfg, "scales", "amax") == "pow2"
+    cur = up(cur + (4 * tk * (cfg.d_ff // 128) if fp8 else 0))          # h_scales
+    cap = (cfg.T // cfg.R) * min(cfg.k, cfg.E // cfg.R)
+    shared_tiles = (cfg.T + bn - 1) // bn if cfg.d_ff_shared else 0
+    for name, size in [("hs", ab * cfg.T * cfg.d_ff_shared),
+                       ("hs_scales", 4 * cfg.T * (cfg.d_ff_shared // 128) if fp8 else 0),
+                       ("xq", cfg.T * cfg.d if fp8 else 0),
+                       ("xq_scales", 4 * cfg.T * (cfg.d // 128) if fp8 else 0),
+                       ("run_start", 4 * cfg.R * cfg.E), ("run_pre", 4 * cfg.R * cfg.E),
+                       ("src_tok", 4 * cfg.R * cfg.R * cap), ("tok_list", 4 * tk),
+                       ("grp_order", 4 * cfg.E),
+                       ("fused_done", 4 * (max_tiles + shared_tiles + 2)),
+                       ("sf_gu", 64 * tk if p2 else 0), ("sf_x", 64 * cfg.T if p2 else 0),
+                       ("sf_h", 64 * tk if p2 else 0), ("sf_hs", 64 * cfg.T if p2 else 0)]:
+        o[name] = cur
+        cur = up(cur + size)
+    o["total"] = cur
     o["bn"] = bn
     return o
 

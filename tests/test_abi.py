@@ -87,6 +87,16 @@ def test_pow2_recipe_maps_to_its_own_format(moe):
         assert L.moe_validate(ctypes.byref(b)) == 1
 
 
+def test_workspace_mirror_matches_the_library(moe):
+    """The tests' copy of the workspace layout (used to read intermediates) ends where the
+    library's does, for every format."""
+    import dataclasses
+    from gpu_util import ws_offsets
+    for c in list(synth.CONFIGS.values()) + [
+            dataclasses.replace(synth.CONFIGS["dsv3_fp8_pow2_e32"], T=200, R=8, E=32)]:
+        assert ws_offsets(c)["total"] == moe.query_sizes(c)["ws_bytes"], c.name
+
+
 def test_sizes_follow_the_layout(moe):
     c = synth.CONFIGS["dsv3_decode"]
     s = moe.query_sizes(c)
