@@ -420,17 +420,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool in = r < t.nlen && row >= 0 && row < (sh ? a.T : a.tk);
       const uint4* src = reinterpret_cast<const uint4*>((sh ? a.sf_shared : a.sf_routed) +
                                                         (in ? row : 0) * kSfRowBytes);
+      // (defaults first, then loads under a predicate, so nothing waits for them before their
+      // use one unit later)
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        na[j] = in ? __ldg(src + j) : make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+      for (int j = 0; j < 4; ++j) na[j] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+      if (in) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) na[j] = __ldg(src + j);
+      }
       const float* wsc = (sh ? a.w_sc_shared
                              : a.w_sc_routed + (size_t)t.we * (a.b_rows_routed / 128) * kb_n) +
                          (size_t)t.m * (kStep / 128) * kb_n;
       const int w_up = (sh ? a.b_up_shared : a.b_up_routed) / 128 * kb_n;
-      nw[0] = lane < kb_n ? __ldg(wsc + lane) : 1.0f;
-      nw[1] = lane + 32 < kb_n ? __ldg(wsc + lane + 32) : 1.0f;
-      nw[2] = lane < kb_n ? __ldg(wsc + w_up + lane) : 1.0f;
-      nw[3] = lane + 32 < kb_n ? __ldg(wsc + w_up + lane + 32) : 1.0f;
+      nw[0] = nw[1] = nw[2] = nw[3] = 1.0f;
+      if (lane < kb_n) {
+        nw[0] = __ldg(wsc + lane);
+        nw[2] = __ldg(wsc + w_up + lane);
+      }
+      if (lane + 32 < kb_n) {
+        nw[1] = __ldg(wsc + lane + 32);
+        nw[3] = __ldg(wsc + w_up + lane + 32);
+      }
     };
     if (n_my > 0) issue(0);
     for (int i = 0; i < n_my && ok; ++i) {
