@@ -174,6 +174,8 @@ def test_dispatch_given_topk_matches_oracle():
 
 FP8_SMALL = dataclasses.replace(SMALL, name="small_fp8", act="fp8", w="fp8", d=512, d_ff=256,
                                 d_ff_shared=256)
+# the same with power-of-two block scales (block-scaled MMA)
+P2_SMALL = dataclasses.replace(FP8_SMALL, name="small_fp8p2", scales="pow2")
 
 
 def test_dispatch_e4m3_codes_and_scales_bit_exact():
@@ -453,7 +455,7 @@ def test_layer_equals_stage_calls_and_is_deterministic():
     assert torch.equal(y1, y3)
 
 
-@pytest.mark.parametrize("cfg", [SMALL, FP8_SMALL, synth.CONFIGS["dsv3_decode"]],
+@pytest.mark.parametrize("cfg", [SMALL, FP8_SMALL, P2_SMALL, synth.CONFIGS["dsv3_decode"]],
                          ids=lambda c: c.name)
 def test_back_to_back_layers_match_single_calls(cfg):
     # Layer calls queued one after another on the stream with no synchronisation: within a call
@@ -479,7 +481,7 @@ def test_back_to_back_layers_match_single_calls(cfg):
     assert not torch.equal(ref[0], ref[1])
 
 
-@pytest.mark.parametrize("cfg", [SMALL, FP8_SMALL, synth.CONFIGS["dsv3_decode"]],
+@pytest.mark.parametrize("cfg", [SMALL, FP8_SMALL, P2_SMALL, synth.CONFIGS["dsv3_decode"]],
                          ids=lambda c: c.name)
 def test_layer_captured_in_a_cuda_graph_replays_like_eager_calls(cfg):
     # The layer enqueues kernel launches only (no allocation, no host sync), so it can be
@@ -523,7 +525,8 @@ def _guarded(shape, dtype, store):
     return raw[GUARD:GUARD + n].view(dtype).view(shape)
 
 
-@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, FP8_SMALL], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, FP8_SMALL, P2_SMALL],
+                         ids=lambda c: c.name)
 def test_layer_writes_stay_inside_every_buffer(cfg):
     # Every buffer the layer writes (outputs, receive buffers, metadata, workspace) lies between
     # two guard bands of a canary byte; two layer calls later the bands are untouched.
@@ -666,7 +669,6 @@ def test_fp8_prefill_rows_and_tokens():
 # ------------------------------------------------------------------------------------------
 # e4m3 with power-of-two block scales (the block-scaled MMA's recipe)
 # ------------------------------------------------------------------------------------------
-P2_SMALL = dataclasses.replace(FP8_SMALL, name="small_fp8p2", scales="pow2")
 P2_HOT = dataclasses.replace(FP8_HOT, name="hot_fp8p2", scales="pow2")
 # several k-steps in both GEMMs (d = 4 x 128, d_ff = 3 x 128), ragged token tiles, 4 ranks
 P2_WIDE = dataclasses.replace(SMALL, name="wide_fp8p2", act="fp8", w="fp8", scales="pow2",
