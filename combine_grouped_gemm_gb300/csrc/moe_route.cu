@@ -211,6 +211,188 @@ cudaError_t launch_partials(const __nv_bfloat16* x, const float* wg, float* part
   return launch_partials_bk<BT, BE, TM, TN, 8>(x, wg, partials, T, d, E, st, pdl);
 }
 
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// wait until at most n of this thread's newest commit groups are still pending (n <= 3)
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else if (n == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+  else asm volatile("cp.async.wait_group 3;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------
+// Partial logits for large batches through a cp.async ring. The staged kernel above holds the
+// next k-step in registers; here every thread copies its share of the next kRingStages - 1
+// k-steps straight into shared memory (16-byte cp.async, nothing held in registers), so no
+// warp waits on a global load before the step that needs it.
+//  * Copies are coalesced: two threads per 32-byte x row slice, four per 64-byte w row slice.
+//    Each thread copies into slots of its own in the ring, so it can convert and transpose what
+//    it copied as soon as its own copies have landed, with no barrier in between.
+//  * The compute tiles are k-major fp32 as in the staged kernel ([BK][128]), with the column
+//    index XOR-swizzled per k row (x: bit 4 by k/8; w: bits 3-4 by (k/4)%4) so the transposing
+//    stores are free of bank conflicts; the swizzle moves 16-column groups, so a thread's
+//    4-row (4-column) float4 stays contiguous.
+//  * Lanes: each half-warp covers 4 thread rows x 4 thread columns, so each 16-byte operand
+//    load of a half-warp touches 64 contiguous bytes.
+// CTA 128 tokens x 128 experts of one chunk, 256 threads of 8 x 8 outputs, BK = 16. Every
+// output is the same sequential fused multiply-add chain over its chunk as in the other
+// kernels.
+// ---------------------------------------------------------------------------------------
+constexpr int kRingStages = 4;
+constexpr int kRingBK = 16;
+constexpr size_t ring_smem_bytes() {
+  return (size_t)kRingStages * (256 + 512) * 16 + (size_t)2 * 2 * kRingBK * 128 * 4;
+}
+
+__global__ void __launch_bounds__(256, 2)
+    route_partials_ring_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wg,
+                               float* __restrict__ partials, int T, int d, int E) {
+  constexpr int BT = 128, BE = 128, BK = kRingBK, S = kRingStages;
+  extern __shared__ __align__(16) unsigned char rring[];
+  uint4* xr = reinterpret_cast<uint4*>(rring);                    // [S][256] raw x pieces
+  uint4* wr = xr + S * 256;                                       // [S][512] raw w pieces
+  float (*xs)[BK][BT] = reinterpret_cast<float (*)[BK][BT]>(wr + S * 512);
+  float (*ws)[BK][BE] = reinterpret_cast<float (*)[BK][BE]>(&xs[2][0][0]);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ty = (warp >> 1) * 4 + ((lane & 15) >> 2);
+  const int tx = (warp & 1) * 8 + (lane >> 4) * 4 + (lane & 3);
+  const int e0 = blockIdx.x * BE, t0 = blockIdx.y * BT, c = blockIdx.z;
+  const int L = d / kRouteChunks, kbeg = c * L, nsteps = L / BK;
+
+  // this thread's copy pieces: x row t0 + tid/2, columns 8*(tid%2)..+7 of the step;
+  // w rows e0 + p/4, columns 4*(p%4)..+3 for p = tid and tid + 256
+  const int xrow = tid >> 1, xhalf = tid & 1;
+  const bool xok = t0 + xrow < T;
+  const __nv_bfloat16* xsrc = x + (size_t)(xok ? t0 + xrow : 0) * d + kbeg + xhalf * 8;
+  int wrow[2], wq[2];
+  const float* wsrc[2];
+  bool wok[2];
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    const int p = tid + n * 256;
+    wrow[n] = p >> 2;
+    wq[n] = p & 3;
+    wok[n] = e0 + wrow[n] < E;
+    wsrc[n] = wg + (size_t)(wok[n] ? e0 + wrow[n] : 0) * d + kbeg + wq[n] * 4;
+  }
+  pdl_wait();
+  pdl_trigger();
+
+  auto issue = [&](int step) {
+    const int slot = step % S, k0 = step * BK;
+    cp_async16_zfill(xr + slot * 256 + tid, xsrc + k0, xok ? 16 : 0);
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+      cp_async16_zfill(wr + slot * 512 + tid + n * 256, wsrc[n] + k0, wok[n] ? 16 : 0);
+  };
+  // convert / transpose this thread's landed pieces of a step into compute buffer buf
+  auto stash = [&](int step, int buf) {
+    const int slot = step % S;
+    const uint4 v = xr[slot * 256 + tid];
+    const int xk = xhalf * 8, xcol = xrow ^ (xhalf << 4);
+    xs[buf][xk + 0][xcol] = bf16_lo(v.x);
+    xs[buf][xk + 1][xcol] = bf16_hi(v.x);
+    xs[buf][xk + 2][xcol] = bf16_lo(v.y);
+    xs[buf][xk + 3][xcol] = bf16_hi(v.y);
+    xs[buf][xk + 4][xcol] = bf16_lo(v.z);
+    xs[buf][xk + 5][xcol] = bf16_hi(v.z);
+    xs[buf][xk + 6][xcol] = bf16_lo(v.w);
+    xs[buf][xk + 7][xcol] = bf16_hi(v.w);
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+      const float4 w = *reinterpret_cast<const float4*>(wr + slot * 512 + tid + n * 256);
+      const int wk = wq[n] * 4, wcol = wrow[n] ^ (wq[n] << 3);
+      ws[buf][wk + 0][wcol] = w.x;
+      ws[buf][wk + 1][wcol] = w.y;
+      ws[buf][wk + 2][wcol] = w.z;
+      ws[buf][wk + 3][wcol] = w.w;
+    }
+  };
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    if (s < nsteps) issue(s);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");
+  stash(0, 0);
+  __syncthreads();
+  for (int step = 0; step < nsteps; ++step) {
+    const int buf = step & 1;
+    if (step + S - 1 < nsteps) issue(step + S - 1);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      const int sx = (kk >> 3) << 4, sw = ((kk >> 2) & 3) << 3;
+      const float4 a0 = *reinterpret_cast<const float4*>(&xs[buf][kk][(ty * 4) ^ sx]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&xs[buf][kk][(64 + ty * 4) ^ sx]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&ws[buf][kk][(tx * 4) ^ sw]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&ws[buf][kk][(64 + tx * 4) ^ sw]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) fma2_bcast(acc[i][j], acc[i][j + 1], b[j], b[j + 1], a[i]);
+    }
+    if (step + 1 < nsteps) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");
+      stash(step + 1, buf ^ 1);
+    }
+    __syncthreads();
+  }
+
+  // rows ty*4 + (i%4) (+64 for i >= 4), columns tx*4 + (j%4) (+64 for j >= 4)
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + (i >> 2) * 64 + ty * 4 + (i & 3);
+    if (t >= T) continue;
+    float* prow = partials + ((size_t)c * T + t) * E;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = e0 + h * 64 + tx * 4;
+      if (e + 3 < E && (E & 3) == 0) {
+        *reinterpret_cast<float4*>(prow + e) =
+            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (e + j < E) prow[e + j] = acc[i][4 * h + j];
+      }
+    }
+  }
+}
+
+// Whether the ring kernel takes this shape: 16-byte aligned rows and k-steps.
+bool ring_fits(const void* x, const void* wg, int d) {
+  const int L = d / kRouteChunks;
+  return L % kRingBK == 0 && L > 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(wg) & 15) == 0;
+}
+
+cudaError_t launch_partials_ring(const __nv_bfloat16* x, const float* wg, float* partials, int T,
+                                 int d, int E, cudaStream_t st, bool pdl) {
+  const size_t smem = ring_smem_bytes();
+  const cudaError_t err =
+      ensure_smem_limit(reinterpret_cast<const void*>(route_partials_ring_kernel), smem);
+  if (err != cudaSuccess) return err;
+  dim3 grid((E + 127) / 128, (T + 127) / 128, kRouteChunks);
+  return launch_kernel(route_partials_ring_kernel, grid, dim3(256), smem, st, pdl, x, wg,
+                       partials, T, d, E);
+}
+
 // ---------------------------------------------------------------------------------------
 // Partial logits for small batches, the CTA's whole slice resident. With few tokens the grid
 // is only E/BE x 16 CTAs, and a kernel that stages one k-step at a time keeps a few KB in
@@ -228,20 +410,6 @@ cudaError_t launch_partials(const __nv_bfloat16* x, const float* wg, float* part
 // ---------------------------------------------------------------------------------------
 __host__ __device__ constexpr size_t resident_smem_bytes(int BT, int BE, int L) {
   return (size_t)BT * (L + 8) * 2 + (size_t)BE * (L + 4) * 4;
-}
-
-__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-
-// wait until at most n of this thread's newest commit groups are still pending (n <= 3)
-__device__ __forceinline__ void cp_async_wait_pending(int n) {
-  if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
-  else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
-  else if (n == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
-  else asm volatile("cp.async.wait_group 3;" ::: "memory");
 }
 
 template <int BT, int BE, int TM, int TN>
@@ -613,6 +781,165 @@ __global__ void __launch_bounds__(256) route_select_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Selection for large batches of the DeepSeek-V3 router shape (256 experts in 8 groups of
+// 32): 8 lanes per token, 4 tokens per warp. Lane q of a token's segment holds experts
+// 32g + 4q + m (g = 0..7, m = 0..3) as key slots j = 4g + m: 4 experts of every group, so the
+// segment's 16-byte loads of one chunk partial row are 128 contiguous bytes. The operations
+// and their order are those of the file comment:
+//  1. per expert: the 16 chunk partials, pairwise tree, sigmoid, selection key v = s + bias
+//     (v kept in registers, s in shared memory);
+//  2. per group: the two largest keys (values only), each lane's own 4 then a 3-step butterfly
+//     over the segment (equal keys give equal scores whichever lane holds them);
+//  3. lane q: rank of group q among the 8 groups -> kept or not (a segment ballot);
+//  4. k <= 8 rounds of a segment-wide argmax over the eligible experts (key desc, index asc);
+//     each lane keeps its best eligible candidate between rounds and only the owner of the
+//     chosen expert rescans; lane i of the segment records the i-th choice;
+//  5. weights from the raw sigmoid scores in selection order (every lane of the segment forms
+//     the same sequential sum).
+// ---------------------------------------------------------------------------------------
+constexpr int kSegThreads = 128;   // 4 warps, 16 tokens a CTA
+constexpr int kSegE = 256, kSegGroups = 8;
+
+__global__ void __launch_bounds__(kSegThreads) route_select_seg_kernel(
+    const float* __restrict__ partials, const float* __restrict__ bias,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int k, int topk_group,
+    float route_scale, const void* warm, size_t warm_bytes, int warm_ctas) {
+  constexpr int E = kSegE;
+  extern __shared__ float s_all[];   // [16 tokens][E] sigmoid scores
+  pdl_wait();
+  pdl_trigger();
+  if ((int)blockIdx.x < warm_ctas) {   // the first CTAs only start the L2 warm-up
+    l2_warm(warm, warm_bytes, blockIdx.x, warm_ctas);
+    return;
+  }
+  const int lane = threadIdx.x & 31, q = lane & 7, seg0 = lane & ~7;
+  const int tl = (threadIdx.x >> 5) * 4 + (lane >> 3);   // token within the CTA
+  const int t = (blockIdx.x - warm_ctas) * (kSegThreads / 8) + tl;
+  const bool tok = t < T;
+  const int tt = tok ? t : 0;   // rows past T compute on token 0 and write nothing
+  float* s_row = s_all + tl * E;
+
+  // 1. selection keys of experts 32g + 4q + m
+  float v[32];
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int col = 32 * g + 4 * q;
+    float4 p[kRouteChunks];
+#pragma unroll
+    for (int c = 0; c < kRouteChunks; ++c)
+      p[c] = *reinterpret_cast<const float4*>(partials + ((size_t)c * T + tt) * E + col);
+#pragma unroll
+    for (int w = kRouteChunks; w > 1; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w / 2; ++j) {
+        p[j].x = __fadd_rn(p[2 * j].x, p[2 * j + 1].x);
+        p[j].y = __fadd_rn(p[2 * j].y, p[2 * j + 1].y);
+        p[j].z = __fadd_rn(p[2 * j].z, p[2 * j + 1].z);
+        p[j].w = __fadd_rn(p[2 * j].w, p[2 * j + 1].w);
+      }
+    const float4 z = p[0];
+    const float4 bb = *reinterpret_cast<const float4*>(bias + col);
+    float4 sv;
+    sv.x = __fdiv_rn(1.0f, __fadd_rn(1.0f, route_exp(-z.x)));
+    sv.y = __fdiv_rn(1.0f, __fadd_rn(1.0f, route_exp(-z.y)));
+    sv.z = __fdiv_rn(1.0f, __fadd_rn(1.0f, route_exp(-z.z)));
+    sv.w = __fdiv_rn(1.0f, __fadd_rn(1.0f, route_exp(-z.w)));
+    v[4 * g + 0] = __fadd_rn(sv.x, bb.x);
+    v[4 * g + 1] = __fadd_rn(sv.y, bb.y);
+    v[4 * g + 2] = __fadd_rn(sv.z, bb.z);
+    v[4 * g + 3] = __fadd_rn(sv.w, bb.w);
+    *reinterpret_cast<float4*>(s_row + col) = sv;
+  }
+  auto expert_of = [&](int j) { return 32 * (j >> 2) + 4 * q + (j & 3); };
+
+  // 2. group scores: the two largest keys of each group, own 4 then the segment butterfly
+  float gscore = 0.0f;   // lane q ends with group q's score
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    float a = -INFINITY, b = -INFINITY;
+#pragma unroll
+    for (int j = 4 * g; j < 4 * g + 4; ++j) {
+      const float x = v[j];
+      if (x > a) {
+        b = a;
+        a = x;
+      } else if (x > b) {
+        b = x;
+      }
+    }
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) {
+      const float c = __shfl_xor_sync(0xffffffffu, a, off);
+      const float d = __shfl_xor_sync(0xffffffffu, b, off);
+      const float hi = fmaxf(a, c);
+      b = fmaxf(fminf(a, c), fmaxf(b, d));
+      a = hi;
+    }
+    if (q == g) gscore = __fadd_rn(a, b);
+  }
+
+  // 3. group q is kept when fewer than topk_group groups rank before it
+  int rank = 0;
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const float gh = __shfl_sync(0xffffffffu, gscore, seg0 + h);
+    rank += ranks_before(gh, h, gscore, q) ? 1 : 0;
+  }
+  const uint32_t kept = (__ballot_sync(0xffffffffu, rank < topk_group) >> seg0) & 0xFFu;
+
+  // 4. k rounds of the segment argmax (key desc, index asc)
+  uint32_t elig = 0;   // bit j: key slot j is in a kept group and not yet chosen
+#pragma unroll
+  for (int g = 0; g < 8; ++g)
+    if ((kept >> g) & 1u) elig |= 0xFu << (4 * g);
+  float lv = -INFINITY;
+  int le = 0x7fffffff;
+  auto lane_best = [&]() {
+    lv = -INFINITY;
+    le = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (!((elig >> j) & 1u)) continue;
+      const int e = expert_of(j);
+      if (le == 0x7fffffff || ranks_before(v[j], e, lv, le)) {
+        lv = v[j];
+        le = e;
+      }
+    }
+  };
+  lane_best();
+  int sel_e = 0;
+  for (int i = 0; i < k; ++i) {
+    float bv = lv;
+    int be = le;
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (oe != 0x7fffffff && (be == 0x7fffffff || ranks_before(ov, oe, bv, be))) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (be == le) {   // this lane held the chosen expert: slot 4 * (be / 32) + be % 4
+      elig &= ~(1u << (4 * (be >> 5) + (be & 3)));
+      lane_best();
+    }
+    if (q == i) sel_e = be;
+  }
+
+  // 5. weights in selection order
+  __syncwarp();
+  const float si = (q < k) ? s_row[sel_e & (E - 1)] : 0.0f;
+  float sum = 0.0f;
+  for (int i = 0; i < k; ++i) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, si, seg0 + i));
+  if (tok && q < k) {
+    topk_idx[(size_t)t * k + q] = sel_e;
+    topk_w[(size_t)t * k + q] = __fmul_rn(__fdiv_rn(si, sum), route_scale);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, const float* bias,
@@ -641,6 +968,8 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
     err = launch_partials_resident<64, 32, 2, 4>(xb, w_gate, partials, T, d, E, st, false);
   else if (T <= 128 && resident_fits<128, 32>(xb, w_gate, d))
     err = launch_partials_resident<128, 32, 4, 4>(xb, w_gate, partials, T, d, E, st, false);
+  else if (T >= 512 && ring_fits(xb, w_gate, d))
+    err = launch_partials_ring(xb, w_gate, partials, T, d, E, st, false);
   else if (T >= 512)
     err = launch_partials<128, 128, 8, 8, 16>(xb, w_gate, partials, T, d, E, st, false);
   else if (T >= 128)
@@ -655,6 +984,17 @@ cudaError_t launch_route(const moe_cfg& c, const void* x, const float* w_gate, c
     return launch_kernel(route_select_cta_kernel, dim3(warm_ctas + c.T), dim3(kSelThreads), smem1,
                          st, pdl, partials, bias, topk_idx, topk_w, c.T, c.E, c.k, c.n_group,
                          c.topk_group, c.route_scale, warm, warm_bytes, warm_ctas);
+  }
+  // the DeepSeek-V3 router shape from 2048 tokens: 8 lanes per token (1024 tokens: 106 us
+  // against 99 us with a warp per token, whose CTAs spread over more SMs; 4096 / 16384 tokens:
+  // 295 / 1080 us against 304 / 1109 us, router stage with the partial-dot kernel)
+  if (c.T >= 2048 && c.E == kSegE && c.n_group == kSegGroups && c.k <= 8 &&
+      (reinterpret_cast<uintptr_t>(bias) & 15) == 0 && (reinterpret_cast<uintptr_t>(partials) & 15) == 0) {
+    const int per_cta = kSegThreads / 8;
+    return launch_kernel(route_select_seg_kernel, dim3(warm_ctas + (c.T + per_cta - 1) / per_cta),
+                         dim3(kSegThreads), (size_t)per_cta * kSegE * sizeof(float), st, pdl,
+                         partials, bias, topk_idx, topk_w, c.T, c.k, c.topk_group, c.route_scale,
+                         warm, warm_bytes, warm_ctas);
   }
   // one warp per token; CTAs of up to 8 warps, fewer when T is small so the tokens still spread
   // over the SMs

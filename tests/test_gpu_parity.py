@@ -98,13 +98,15 @@ def oracle_route(cfg, inp, tokens=None):
 # Router
 # ------------------------------------------------------------------------------------------
 # T spans the partial-dot kernels (the resident slice with 32 / 64 / 128-token tiles up to 128
-# tokens, ragged at 40 and 104; staged 64x64 tiles below 512, 128x128 from there) and both
-# selection kernels (a CTA per token below 1024 tokens, a warp per token from there, 2 / 4 / 8
-# warps per CTA at 1024 / 1536 / 4096+ tokens)
+# tokens, ragged at 40 and 104; staged 64x64 tiles below 512, the cp.async ring's 128x128 tiles
+# from there) and the selection kernels (a CTA per token below 1024 tokens, a warp per token
+# from there, 2 / 4 warps per CTA at 1024 and 1152 / 1536 tokens; 8 lanes per token for 256
+# experts in 8 groups from 2048 tokens: the direct tests below)
 ROUTE_FULL = [synth.CONFIGS["tiny"], SMALL, HOT, synth.CONFIGS["dsv3_decode"],
               synth.CONFIGS["dsv3_sweep"].with_T(8), synth.CONFIGS["dsv3_sweep"].with_T(40),
               synth.CONFIGS["dsv3_sweep"].with_T(104), synth.CONFIGS["dsv3_sweep"].with_T(256),
-              synth.CONFIGS["dsv3_sweep"].with_T(1024), synth.CONFIGS["dsv3_sweep"].with_T(1536)]
+              synth.CONFIGS["dsv3_sweep"].with_T(1024), synth.CONFIGS["dsv3_sweep"].with_T(1536),
+              dataclasses.replace(HOT, name="hot_T1152", T=1152)]
 
 
 @pytest.mark.parametrize("cfg", ROUTE_FULL, ids=lambda c: c.name)
@@ -134,6 +136,63 @@ def test_route_bit_exact_sampled_large(name):
     if cfg.bias == "zipf":   # the skew recipe: hottest expert about 10x the mean load
         c = np.bincount(idx_d.cpu().numpy().reshape(-1), minlength=cfg.E)
         assert 8.0 <= c.max() / c.mean() <= 12.0
+
+
+# From 512 tokens the partial dot products go through the cp.async ring kernel (128x128 tiles,
+# 16-column k-steps): token and expert counts that leave the last tiles part-filled, a chunk of
+# two k-steps (fewer than the ring's stages), expert counts that are not a multiple of 4 (the
+# scalar store path), and the full model width at ragged token counts, the second one past
+# 2048 tokens (8-lane-per-token selection, its last CTA part-filled). Every token is checked.
+RING_RAGGED = [
+    dataclasses.replace(SMALL, name="ring_small", T=702, d=512),
+    synth.MoEConfig("ring_e18", T=531, d=768, E=18, k=3, n_group=3, topk_group=2, d_ff=128,
+                    d_ff_shared=0, R=3, route_scale=1.5, seed=123),
+    synth.CONFIGS["dsv3_sweep"].with_T(600),
+    synth.CONFIGS["dsv3_sweep"].with_T(2056),
+]
+
+
+@pytest.mark.parametrize("cfg", RING_RAGGED, ids=lambda c: c.name)
+def test_route_bit_exact_ring_ragged(cfg):
+    inp = synth.make_router_inputs(cfg, "cuda")
+    m = moe()
+    ws = torch.zeros(m.query_sizes(cfg)["ws_bytes"], dtype=torch.uint8, device="cuda")
+    idx_d = torch.full((cfg.T, cfg.k), -1, dtype=torch.int32, device="cuda")
+    w_d = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device="cuda")
+    m.route(cfg, inp["x"], inp["w_gate"], inp["bias"], idx_d, w_d, ws)
+    idx, w = oracle_route(cfg, inp)
+    assert np.array_equal(idx_d.cpu().numpy(), idx)
+    assert np.array_equal(w_d.cpu().numpy(), w)   # same op sequence: exact
+
+
+@pytest.mark.parametrize("T", [64, 1024, 2048])
+def test_route_ties_go_to_the_lower_index(T):
+    # experts 2i and 2i+1 get the same gate row and bias, so every key comes in equal pairs
+    # (and a group's two largest keys can be a pair): the three selection kernels (a CTA per
+    # token, a warp per token, 8 lanes per token) must pick the lower index first, as the
+    # oracle does
+    cfg = synth.CONFIGS["dsv3_sweep"].with_T(T)
+    inp = synth.make_router_inputs(cfg, "cuda")
+    wg = inp["w_gate"].clone()
+    wg[1::2] = wg[0::2]
+    b = inp["bias"].clone()
+    b[1::2] = b[0::2]
+    inp = dict(x=inp["x"], w_gate=wg, bias=b)
+    m = moe()
+    ws = torch.zeros(m.query_sizes(cfg)["ws_bytes"], dtype=torch.uint8, device="cuda")
+    idx_d = torch.full((cfg.T, cfg.k), -1, dtype=torch.int32, device="cuda")
+    w_d = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device="cuda")
+    m.route(cfg, inp["x"], inp["w_gate"], inp["bias"], idx_d, w_d, ws)
+    idx, w = oracle_route(cfg, inp)
+    got = idx_d.cpu().numpy()
+    assert np.array_equal(got, idx)
+    assert np.array_equal(w_d.cpu().numpy(), w)
+    # both members of a pair chosen: the even one comes first
+    for row in got:
+        pos = {e: i for i, e in enumerate(row)}
+        for e, i in pos.items():
+            if e % 2 == 1 and e - 1 in pos:
+                assert pos[e - 1] < i
 
 
 # ------------------------------------------------------------------------------------------
