@@ -117,6 +117,9 @@ WsLayout ws_layout(const moe_cfg& c) {
   L.sf_x = o;       o = up256(o + (p2 ? (size_t)kSfRowBytes * c.T : 0));
   L.sf_h = o;       o = up256(o + (p2 ? (size_t)kSfRowBytes * tk : 0));
   L.sf_hs = o;      o = up256(o + (p2 ? (size_t)kSfRowBytes * c.T : 0));
+  L.max_tiles2 = c.E + (int)((tk + 2 * L.bn - 1) / (2 * L.bn));
+  L.n_tiles2 = o;   o = up256(o + sizeof(int32_t));
+  L.tiles2 = o;     o = up256(o + sizeof(Tile) * (size_t)L.max_tiles2);
   L.total = o;
   return L;
 }

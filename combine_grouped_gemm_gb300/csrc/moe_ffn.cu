@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     int32_t* __restrict__ run_pre, int32_t* __restrict__ row_list, uint32_t* status, int E, int R,
     int cap, int bn, int max_tiles, int tk, const int32_t* __restrict__ src_tok,
     int32_t* __restrict__ tok_list, int T, const int32_t* __restrict__ group_expert,
-    int32_t* __restrict__ grp_order) {
+    int32_t* __restrict__ grp_order, int32_t* __restrict__ n_tiles2, Tile* __restrict__ tiles2,
+    int max_tiles2) {
   __shared__ int warp_sums[33];
   __shared__ int rank_base[64];
   __shared__ int ord_g[kPlanThreads];   // group at each schedule position (then its expert)
@@ -213,6 +214,19 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     if (tiles_total > max_tiles) raise_status(status, MOE_DEV_BOUNDS);
     *n_tiles = min(tiles_total, max_tiles);
   }
+  // the same rows in tiles of 2 * bn
+  const int nt2 = (tile_rows + 2 * bn - 1) / (2 * bn);
+  int tiles_total2;
+  const int toff2 = block_exclusive_scan(nt2, &tiles_total2, warp_sums);
+  if (act)
+    for (int j = 0; j < nt2; ++j) {
+      const int ti = toff2 + j;
+      if (ti < max_tiles2) tiles2[ti] = Tile{g_i, j * 2 * bn, min(2 * bn, tile_rows - j * 2 * bn), nt2};
+    }
+  if (threadIdx.x == 0) {
+    if (tiles_total2 > max_tiles2) raise_status(status, MOE_DEV_BOUNDS);
+    *n_tiles2 = min(tiles_total2, max_tiles2);
+  }
 
   // per (source, expert) run: first receive row, rows from earlier sources
   int pre = 0;
@@ -287,6 +301,9 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
                          const __grid_constant__ CUtensorMap mapB,
                          const __grid_constant__ CUtensorMap mapBs) {
   using S = GemmShape<STAGE, BN, STAGES>;
+  // 256-row token tiles (down stage): the token rows come as two boxes of at most 128 rows
+  static_assert(BN <= 128 || STAGE == 1, "256-row token tiles: down stage only");
+  constexpr int kBoxRows = BN > 128 ? 128 : BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -387,12 +404,14 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
         if (__any_sync(0xffffffffu, nbad > 0) && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
         b_bytes = 512u * __popc(on);
       }
+      int nbox = 1;   // 256-row tiles: a second box when the tile has more than 128 rows
       if (STAGE == 1 || sh) {
         const int row0 = sh ? t.n0 : a.grp_off[t.g] + t.n0;
         const bool in = row0 >= 0 && row0 < (sh ? a.T : a.tk);
         if (!in && lane == 0) raise_status(a.status, MOE_DEV_BOUNDS);
         box_row = in ? row0 : -1;
-        b_bytes = in ? 128u * static_cast<uint32_t>(sh ? a.box_shared : a.box_routed) : 0u;
+        if (BN > kBoxRows && t.nlen > kBoxRows) nbox = 2;
+        b_bytes = in ? 128u * static_cast<uint32_t>(nbox * (sh ? a.box_shared : a.box_routed)) : 0u;
       }
       const uint32_t tx = S::NA * S::A_BYTES + b_bytes;
       for (int ks = 0; ks < a.k_steps; ++ks) {
@@ -406,7 +425,12 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
           mbar_arrive_expect_tx(&full[stage], tx);
           tma_load_2d(sa, amap, &full[stage], ks * 64, arow0, pol_w);
           if (S::NA == 2) tma_load_2d(sa + S::A_BYTES, amap, &full[stage], ks * 64, arow1, pol_w);
-          if (box_row >= 0) tma_load_2d(sb, bmap, &full[stage], ks * 64, box_row, pol_x);
+          if (box_row >= 0) {
+            tma_load_2d(sb, bmap, &full[stage], ks * 64, box_row, pol_x);
+            if (BN > kBoxRows && nbox == 2)
+              tma_load_2d(sb + kBoxRows * 128, bmap, &full[stage], ks * 64, box_row + kBoxRows,
+                          pol_x);
+          }
         }
         __syncwarp();
         if (g4_on)
@@ -428,7 +452,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
         const uint32_t n_pad = static_cast<uint32_t>(max(16, (t.nlen + 15) & ~15));
         const uint32_t idesc = idesc_bf16(128, n_pad);
@@ -462,6 +486,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
           }
         }
         if (ok) mma_commit(&tfull[b]);
+        ++it;
       }
     }
     __syncwarp();
@@ -523,7 +548,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
     const int rrow = quarter * 32 + lane;
     int it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
       const bool sh = t.g < 0;
       const int b = it & 1;
@@ -573,6 +598,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[b]);
+      ++it;
     }
   }
 
@@ -704,7 +730,9 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
       reinterpret_cast<int32_t*>(ws + L.run_start), reinterpret_cast<int32_t*>(ws + L.run_pre),
       reinterpret_cast<int32_t*>(ws + L.row_list), status, c.E, c.R, cap_of(c), L.bn,
       L.max_tiles, tk, src_tok, src_tok ? reinterpret_cast<int32_t*>(ws + L.tok_list) : nullptr,
-      c.T, group_expert, reinterpret_cast<int32_t*>(ws + L.grp_order));
+      c.T, group_expert, reinterpret_cast<int32_t*>(ws + L.grp_order),
+      reinterpret_cast<int32_t*>(ws + L.n_tiles2), reinterpret_cast<Tile*>(ws + L.tiles2),
+      L.max_tiles2);
   if (err != cudaSuccess) return err;
   if (tk <= kPlanFusedRows) return cudaSuccess;   // the plan CTA filled the row list
   const int blocks = (tk + 255) / 256 < 4 * 152 ? (tk + 255) / 256 : 4 * 152;
@@ -721,7 +749,7 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
 cudaError_t prepare_bf16_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                               const void* x, const moe_weights& w, void* ebuf, void* shared_out,
                               char* ws, const FfnPart& part, GemmArgs* args,
-                              CUtensorMap maps[4]) {
+                              CUtensorMap maps[4], bool wide) {
   const int cap = cap_of(c);
   const long long recv_rows = (long long)c.R * c.R * cap;
   const int F = c.d_ff, Fs = c.d_ff_shared, d = c.d, tk = c.T * c.k;
@@ -731,15 +759,17 @@ cudaError_t prepare_bf16_gemm(const moe_cfg& c, const WsLayout& L, int stage, co
   const bool gather = part.src_tok != nullptr && stage == 0;
 
   GemmArgs a{};
-  a.tiles = reinterpret_cast<const Tile*>(ws + L.tiles);
-  a.n_tiles = reinterpret_cast<const int32_t*>(ws + L.n_tiles);
+  wide = wide && stage == 1;
+  const int tbn = wide ? 2 * L.bn : L.bn;   // token-tile rows of this launch's schedule
+  a.tiles = reinterpret_cast<const Tile*>(ws + (wide ? L.tiles2 : L.tiles));
+  a.n_tiles = reinterpret_cast<const int32_t*>(ws + (wide ? L.n_tiles2 : L.n_tiles));
   a.grp_off = reinterpret_cast<const int32_t*>(ws + L.grp_off);
   a.row_list = reinterpret_cast<const int32_t*>(ws + L.row_list);
   a.tk = tk;
   a.recv_rows = recv_rows;
   a.T = c.T;
   a.status = reinterpret_cast<uint32_t*>(ws + L.status);
-  a.n_shared_tiles = has_shared ? (c.T + L.bn - 1) / L.bn : 0;
+  a.n_shared_tiles = has_shared ? (c.T + tbn - 1) / tbn : 0;
   a.group_expert = part.group_expert;
   const int n_w = part.weight_experts > 0 ? part.weight_experts : c.E;
   a.n_experts = n_w;
@@ -821,16 +851,20 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
   if (is_fp8(c))
     return launch_ffn_gemm_e4m3(c, L, stage, recv, recv_scales, w, ebuf, shared_out, ws, st, pdl,
                                 part);
+  // down, with a full 128-row token tile per expert on average: 256-row token tiles (M = 128
+  // weight rows, N up to 256), so each weight tile is read from L2 once per 256 rows
+  const bool wide = stage == 1 && L.bn == 128 && (long long)c.T * c.k >= 128ll * c.E;
   GemmArgs a{};
   CUtensorMap m[4];
   const cudaError_t err =
-      prepare_bf16_gemm(c, L, stage, recv, x, w, ebuf, shared_out, ws, part, &a, m);
+      prepare_bf16_gemm(c, L, stage, recv, x, w, ebuf, shared_out, ws, part, &a, m, wide);
   if (err != cudaSuccess) return err;
   if (L.bn == 64) {
     if (stage == 0) return run_gemm<0, 64, 5>(a, m[0], m[1], m[2], m[3], st, pdl, part.ctas);
     return run_gemm<1, 64, 8>(a, m[0], m[1], m[2], m[3], st, pdl, part.ctas);
   }
   if (stage == 0) return run_gemm<0, 128, 4>(a, m[0], m[1], m[2], m[3], st, pdl, part.ctas);
+  if (wide) return run_gemm<1, 256, 4>(a, m[0], m[1], m[2], m[3], st, pdl, part.ctas);
   return run_gemm<1, 128, 6>(a, m[0], m[1], m[2], m[3], st, pdl, part.ctas);
 }
 

@@ -143,9 +143,11 @@ struct GemmShape {
 
 // Host side: the arguments and TMA tensor maps of one bf16 GEMM stage (0 = gate/up with the
 // SwiGLU epilogue, 1 = down projection) for configuration c, as launch_ffn_gemm builds them.
-// maps: A (routed weights), A shared, B (routed token rows), B shared.
+// maps: A (routed weights), A shared, B (routed token rows), B shared. wide: the down stage on
+// the schedule's 2 * bn-row tiles (launch_ffn_gemm's 256-row kernel).
 cudaError_t prepare_bf16_gemm(const moe_cfg& c, const WsLayout& L, int stage, const void* recv,
                               const void* x, const moe_weights& w, void* ebuf, void* shared_out,
-                              char* ws, const FfnPart& part, GemmArgs* args, CUtensorMap maps[4]);
+                              char* ws, const FfnPart& part, GemmArgs* args, CUtensorMap maps[4],
+                              bool wide = false);
 
 }  // namespace moe

@@ -52,6 +52,11 @@ struct WsLayout {
   size_t sf_x;        // [T]: the shared expert's gate/up input rows (x quantised)
   size_t sf_h;        // [T*k]: routed down input rows (h)
   size_t sf_hs;       // [T]: the shared expert's down input rows (hs)
+  // the same schedule in tiles of 2 * bn rows (the bf16 down GEMM when experts average a full
+  // bn-row tile or more)
+  size_t n_tiles2;    // int32 [1]
+  size_t tiles2;      // Tile [max_tiles2]
+  int max_tiles2;
   int shared_tiles;   // token tiles of the shared expert (0: none)
   int fused_done_n;   // max_tiles + shared_tiles + 2
   size_t total;

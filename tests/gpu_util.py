@@ -86,7 +86,8 @@ def ws_offsets(cfg):
                        ("grp_order", 4 * cfg.E),
                        ("fused_done", 4 * (max_tiles + shared_tiles + 2)),
                        ("sf_gu", 64 * tk if p2 else 0), ("sf_x", 64 * cfg.T if p2 else 0),
-                       ("sf_h", 64 * tk if p2 else 0), ("sf_hs", 64 * cfg.T if p2 else 0)]:
+                       ("sf_h", 64 * tk if p2 else 0), ("sf_hs", 64 * cfg.T if p2 else 0),
+                       ("n_tiles2", 4), ("tiles2", 16 * (cfg.E + (tk + 2 * bn - 1) // (2 * bn)))]:
         o[name] = cur
         cur = up(cur + size)
     o["total"] = cur

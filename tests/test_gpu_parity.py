@@ -44,6 +44,12 @@ E192_R64 = synth.MoEConfig("e192_r64", T=128, d=256, E=192, k=4, n_group=4, topk
 # One expert receives every token (bias +10): several token tiles of one expert.
 HOT = synth.MoEConfig("hot", T=256, d=256, E=16, k=2, n_group=1, topk_group=1, d_ff=256,
                       d_ff_shared=256, R=2, route_scale=1.0, seed=5)
+# A full 128-row token tile per expert on average (T*k >= 128*E): the bf16 down GEMM takes two
+# token tiles of an expert per unit. Experts of 1, 2 and 3 ragged tiles; and the hot expert with
+# 8 tiles (and the shared expert's 8).
+PAIRED = synth.MoEConfig("paired", T=512, d=256, E=8, k=2, n_group=2, topk_group=2, d_ff=256,
+                         d_ff_shared=256, R=2, route_scale=1.0, seed=29)
+HOT_PAIRED = dataclasses.replace(HOT, name="hot_paired", T=1024)
 
 _cache = {}       # router inputs per workload
 _wcache = {}      # expert weights per (seed, shapes, format): sweep points share one set
@@ -385,8 +391,8 @@ def _layer_tokens_check(cfg, tokens, inp, W, y):
     return format_err(got, ref["y_exact"])
 
 
-@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, HOT, ER64, E192_R64],
-                         ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, HOT, ER64, E192_R64, PAIRED,
+                                 HOT_PAIRED], ids=lambda c: c.name)
 def test_layer_all_tokens(cfg):
     inp, W = inputs(cfg)
     lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
@@ -584,7 +590,7 @@ def _guarded(shape, dtype, store):
     return raw[GUARD:GUARD + n].view(dtype).view(shape)
 
 
-@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, FP8_SMALL, P2_SMALL],
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, FP8_SMALL, P2_SMALL, PAIRED],
                          ids=lambda c: c.name)
 def test_layer_writes_stay_inside_every_buffer(cfg):
     # Every buffer the layer writes (outputs, receive buffers, metadata, workspace) lies between
