@@ -44,9 +44,9 @@ E192_R64 = synth.MoEConfig("e192_r64", T=128, d=256, E=192, k=4, n_group=4, topk
 # One expert receives every token (bias +10): several token tiles of one expert.
 HOT = synth.MoEConfig("hot", T=256, d=256, E=16, k=2, n_group=1, topk_group=1, d_ff=256,
                       d_ff_shared=256, R=2, route_scale=1.0, seed=5)
-# A full 128-row token tile per expert on average (T*k >= 128*E): the bf16 down GEMM takes two
-# token tiles of an expert per unit. Experts of 1, 2 and 3 ragged tiles; and the hot expert with
-# 8 tiles (and the shared expert's 8).
+# A full 128-row token tile per expert on average (T*k >= 128*E): the bf16 GEMMs run on the
+# schedule's 256-row token tiles. Experts of 1, 2 and 3 ragged 128-row tiles; and the hot
+# expert with 1024 rows (and the shared expert's 1024).
 PAIRED = synth.MoEConfig("paired", T=512, d=256, E=8, k=2, n_group=2, topk_group=2, d_ff=256,
                          d_ff_shared=256, R=2, route_scale=1.0, seed=29)
 HOT_PAIRED = dataclasses.replace(HOT, name="hot_paired", T=1024)
@@ -921,8 +921,8 @@ VARIANTS = [dict(gather=True), dict(side_stream=True), dict(gather=True, side_st
             dict(side_stream=True, side_ctas=3)]
 
 
-@pytest.mark.parametrize("cfg", [SMALL, FP8_SMALL, HOT, FP8_HOT, synth.CONFIGS["dsv3_decode"]],
-                         ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [SMALL, FP8_SMALL, HOT, FP8_HOT, synth.CONFIGS["dsv3_decode"],
+                                 PAIRED], ids=lambda c: c.name)
 def test_layer_variants_equal_the_layer(cfg):
     """Every variant computes the same rows with the same kernels in the same K order, so its
     output equals moe_layer's bit for bit (and the gate weights, indices and counts too)."""
