@@ -853,7 +853,8 @@ cudaError_t launch_ffn_gemm(const moe_cfg& c, const WsLayout& L, int stage, cons
                                 part);
   // down, with a full 128-row token tile per expert on average: 256-row token tiles (M = 128
   // weight rows, N up to 256), so each weight tile is read from L2 once per 256 rows
-  const bool wide = stage == 1 && L.bn == 128 && (long long)c.T * c.k >= 128ll * c.E;
+  const int n_experts = part.weight_experts > 0 ? part.weight_experts : c.E;   // not slots
+  const bool wide = stage == 1 && L.bn == 128 && (long long)c.T * c.k >= 128ll * n_experts;
   GemmArgs a{};
   CUtensorMap m[4];
   const cudaError_t err =

@@ -1017,7 +1017,7 @@ def _placement_for(cfg, inp, spare_per_rank, seed):
 
 
 PLACED = [(SMALL, 2), (HOT, 3), (E192_R64, 1), (synth.CONFIGS["dsv3_decode"], 4),
-          (FP8_SMALL, 2)]
+          (FP8_SMALL, 2), (PAIRED, 2)]
 
 
 @pytest.mark.parametrize("cfg,spare", PLACED, ids=lambda v: getattr(v, "name", str(v)))
