@@ -50,6 +50,9 @@ HOT = synth.MoEConfig("hot", T=256, d=256, E=16, k=2, n_group=1, topk_group=1, d
 PAIRED = synth.MoEConfig("paired", T=512, d=256, E=8, k=2, n_group=2, topk_group=2, d_ff=256,
                          d_ff_shared=256, R=2, route_scale=1.0, seed=29)
 HOT_PAIRED = dataclasses.replace(HOT, name="hot_paired", T=1024)
+# ... with T = 700: the shared expert's last 256-row tile has 188 rows, its second 128-row box
+# runs past the last token (zero-filled)
+PAIRED_RAGGED = dataclasses.replace(PAIRED, name="paired_ragged", T=700, seed=31)
 
 _cache = {}       # router inputs per workload
 _wcache = {}      # expert weights per (seed, shapes, format): sweep points share one set
@@ -392,7 +395,7 @@ def _layer_tokens_check(cfg, tokens, inp, W, y):
 
 
 @pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], SMALL, HOT, ER64, E192_R64, PAIRED,
-                                 HOT_PAIRED], ids=lambda c: c.name)
+                                 HOT_PAIRED, PAIRED_RAGGED], ids=lambda c: c.name)
 def test_layer_all_tokens(cfg):
     inp, W = inputs(cfg)
     lay = moe().MoELayer(cfg, inp["w_gate"], inp["bias"], weight_dict(W))
