@@ -214,18 +214,21 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
     if (tiles_total > max_tiles) raise_status(status, MOE_DEV_BOUNDS);
     *n_tiles = min(tiles_total, max_tiles);
   }
-  // the same rows in tiles of 2 * bn
-  const int nt2 = (tile_rows + 2 * bn - 1) / (2 * bn);
-  int tiles_total2;
-  const int toff2 = block_exclusive_scan(nt2, &tiles_total2, warp_sums);
-  if (act)
-    for (int j = 0; j < nt2; ++j) {
-      const int ti = toff2 + j;
-      if (ti < max_tiles2) tiles2[ti] = Tile{g_i, j * 2 * bn, min(2 * bn, tile_rows - j * 2 * bn), nt2};
+  // the same rows in tiles of 2 * bn (max_tiles2 == 0: not needed by this layer's GEMMs)
+  if (max_tiles2 > 0) {
+    const int nt2 = (tile_rows + 2 * bn - 1) / (2 * bn);
+    int tiles_total2;
+    const int toff2 = block_exclusive_scan(nt2, &tiles_total2, warp_sums);
+    if (act)
+      for (int j = 0; j < nt2; ++j) {
+        const int ti = toff2 + j;
+        if (ti < max_tiles2)
+          tiles2[ti] = Tile{g_i, j * 2 * bn, min(2 * bn, tile_rows - j * 2 * bn), nt2};
+      }
+    if (threadIdx.x == 0) {
+      if (tiles_total2 > max_tiles2) raise_status(status, MOE_DEV_BOUNDS);
+      *n_tiles2 = min(tiles_total2, max_tiles2);
     }
-  if (threadIdx.x == 0) {
-    if (tiles_total2 > max_tiles2) raise_status(status, MOE_DEV_BOUNDS);
-    *n_tiles2 = min(tiles_total2, max_tiles2);
   }
 
   // per (source, expert) run: first receive row, rows from earlier sources
@@ -732,7 +735,7 @@ cudaError_t launch_ffn_setup(const moe_cfg& c, const WsLayout& L, const int32_t*
       L.max_tiles, tk, src_tok, src_tok ? reinterpret_cast<int32_t*>(ws + L.tok_list) : nullptr,
       c.T, group_expert, reinterpret_cast<int32_t*>(ws + L.grp_order),
       reinterpret_cast<int32_t*>(ws + L.n_tiles2), reinterpret_cast<Tile*>(ws + L.tiles2),
-      L.max_tiles2);
+      L.bn == 128 && !is_fp8(c) ? L.max_tiles2 : 0);   // the bf16 GEMMs' 256-row schedule
   if (err != cudaSuccess) return err;
   if (tk <= kPlanFusedRows) return cudaSuccess;   // the plan CTA filled the row list
   const int blocks = (tk + 255) / 256 < 4 * 152 ? (tk + 255) / 256 : 4 * 152;
