@@ -71,6 +71,9 @@ def parse():
     p.add_argument("--extra-steps", type=int, default=10, help="timed steps per extra workload")
     p.add_argument("--mode", default="layer", choices=sorted(MODES),
                    help="the layer variant of the main workload's timed steps")
+    p.add_argument("--route-only", action="store_true",
+                   help="time the router stage alone on the workload's shapes (router inputs "
+                        "and workspace only, no expert weights): for profiling its kernels")
     return p.parse_args()
 
 
@@ -582,6 +585,36 @@ def oracle_sample(cfg, inp, W, tokens):
     return sec
 
 
+def run_route_only(args, cfg):
+    """The router stage (moe_route) alone: W untimed calls, then K calls timed back to back with
+    CUDA events. The gate weight (7.3 MB for DSV3) stays in L2 between calls, unlike in the
+    layer, where the expert GEMMs stream gigabytes between router calls."""
+    import combine_grouped_gemm_gb300 as moe
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = synth.make_router_inputs(cfg, dev)
+    ws = torch.zeros(moe.query_sizes(cfg)["ws_bytes"], dtype=torch.uint8, device=dev)
+    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+    for _ in range(max(1, args.warmup)):
+        moe.route(cfg, inp["x"], inp["w_gate"], inp["bias"], idx, w, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        moe.route(cfg, inp["x"], inp["w_gate"], inp["bias"], idx, w, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    flops = 2.0 * cfg.T * cfg.d * cfg.E
+    print(json.dumps({"metric": "router stage us", "value": round(us, 2), "unit": "us",
+                      "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+                      "config": describe(cfg),
+                      "alu_frac": round(flops / (us * 1e-6) / (ALU_FP32_TFLOPS * 1e12), 4)}),
+          flush=True)
+    return 0
+
+
 def main():
     args = parse()
     cfg = workload(args)
@@ -594,6 +627,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, cfg, rank, world, local_rank)
+    if args.route_only:
+        return run_route_only(args, cfg)
 
     if world > 1:
         torch.cuda.set_device(local_rank)
