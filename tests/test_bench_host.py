@@ -153,3 +153,20 @@ def test_cpu_baseline_sizes_its_sample_from_the_probe():
     # a fixed size is taken as given, in batches of 8
     out = bench.cpu_baseline(cfg, inp, W, n_tokens=11)
     assert out["sample"].startswith(f"11 of {cfg.T} tokens")
+
+
+@pytest.mark.gpu
+def test_route_only_mode_times_the_router_and_prints_one_line():
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--workload", "tiny",
+                        "--route-only", "--steps", "3", "--warmup", "1"],
+                       cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    assert out["metric"] == "router stage us" and out["value"] > 0
+    assert out["config"]["workload"] == "tiny"
