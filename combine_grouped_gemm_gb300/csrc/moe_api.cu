@@ -95,7 +95,7 @@ WsLayout ws_layout(const moe_cfg& c) {
   L.partials = o;   o = up256(o + sizeof(float) * kRouteChunks * (size_t)c.T * c.E);
   L.grp_n = o;      o = up256(o + sizeof(int32_t) * c.E);
   L.grp_off = o;    o = up256(o + sizeof(int32_t) * c.E);
-  L.n_tiles = o;    o = up256(o + sizeof(int32_t));
+  L.n_tiles = o;    o = up256(o + 2 * sizeof(int32_t));   // tiles, of which hot (listed first)
   L.tiles = o;      o = up256(o + sizeof(Tile) * (size_t)L.max_tiles);
   L.row_list = o;   o = up256(o + sizeof(int32_t) * tk);
   L.h = o;          o = up256(o + ab * tk * c.d_ff);
@@ -118,7 +118,7 @@ WsLayout ws_layout(const moe_cfg& c) {
   L.sf_h = o;       o = up256(o + (p2 ? (size_t)kSfRowBytes * tk : 0));
   L.sf_hs = o;      o = up256(o + (p2 ? (size_t)kSfRowBytes * c.T : 0));
   L.max_tiles2 = c.E + (int)((tk + 2 * L.bn - 1) / (2 * L.bn));
-  L.n_tiles2 = o;   o = up256(o + sizeof(int32_t));
+  L.n_tiles2 = o;   o = up256(o + 2 * sizeof(int32_t));
   L.tiles2 = o;     o = up256(o + sizeof(Tile) * (size_t)L.max_tiles2);
   L.total = o;
   return L;

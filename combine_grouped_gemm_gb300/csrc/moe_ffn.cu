@@ -199,9 +199,16 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
         for (int q = threadIdx.x; q < E && ord_g[q] == eg; ++q) tile_rows += ord_n[q];
     }
   }
+  // The tile list holds the groups with two or more token tiles first (each of their weight
+  // tiles is read once per token tile, from L2 after the first: tensor-bound units), then the
+  // one-tile groups (every weight tile read once: HBM-bound units), each part in schedule
+  // order; n_tiles[1] counts the first part. The GEMMs interleave the two (interleave_unit).
   const int nt = (tile_rows + bn - 1) / bn;
-  int tiles_total;
-  const int toff = block_exclusive_scan(nt, &tiles_total, warp_sums);
+  int tiles_hot, tiles_cold;
+  const int toff_h = block_exclusive_scan(nt >= 2 ? nt : 0, &tiles_hot, warp_sums);
+  const int toff_c = block_exclusive_scan(nt >= 2 ? 0 : nt, &tiles_cold, warp_sums);
+  const int toff = nt >= 2 ? toff_h : tiles_hot + toff_c;
+  const int tiles_total = tiles_hot + tiles_cold;
   if (act) {
     grp_n[g_i] = n_i;
     grp_off[g_i] = off;
@@ -212,13 +219,17 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
   }
   if (threadIdx.x == 0) {
     if (tiles_total > max_tiles) raise_status(status, MOE_DEV_BOUNDS);
-    *n_tiles = min(tiles_total, max_tiles);
+    n_tiles[0] = min(tiles_total, max_tiles);
+    n_tiles[1] = min(tiles_hot, max_tiles);
   }
   // the same rows in tiles of 2 * bn (max_tiles2 == 0: not needed by this layer's GEMMs)
   if (max_tiles2 > 0) {
     const int nt2 = (tile_rows + 2 * bn - 1) / (2 * bn);
-    int tiles_total2;
-    const int toff2 = block_exclusive_scan(nt2, &tiles_total2, warp_sums);
+    int hot2, cold2;
+    const int toff2_h = block_exclusive_scan(nt2 >= 2 ? nt2 : 0, &hot2, warp_sums);
+    const int toff2_c = block_exclusive_scan(nt2 >= 2 ? 0 : nt2, &cold2, warp_sums);
+    const int toff2 = nt2 >= 2 ? toff2_h : hot2 + toff2_c;
+    const int tiles_total2 = hot2 + cold2;
     if (act)
       for (int j = 0; j < nt2; ++j) {
         const int ti = toff2 + j;
@@ -227,7 +238,8 @@ __global__ void __launch_bounds__(kPlanThreads) ffn_plan_kernel(
       }
     if (threadIdx.x == 0) {
       if (tiles_total2 > max_tiles2) raise_status(status, MOE_DEV_BOUNDS);
-      *n_tiles2 = min(tiles_total2, max_tiles2);
+      n_tiles2[0] = min(tiles_total2, max_tiles2);
+      n_tiles2[1] = min(hot2, max_tiles2);
     }
   }
 
@@ -353,6 +365,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
 
   const int n_tiles = *a.n_tiles;
   const int units = a.n_shared_tiles * a.mt_shared + n_tiles * a.mt_routed;
+  const int hot = hot_units(a, n_tiles);
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -362,7 +375,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    for (int sl = blockIdx.x; sl < units && ok; sl += gridDim.x) {
+      const int u = interleave_unit(sl, units, hot);
       const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
       const bool sh = t.g < 0;
       const uint64_t pol_w = weight_policy(t, pol_w1, pol_wk);
@@ -455,7 +469,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int sl = blockIdx.x; sl < units && ok; sl += gridDim.x) {
+        const int u = interleave_unit(sl, units, hot);
         const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
         const uint32_t n_pad = static_cast<uint32_t>(max(16, (t.nlen + 15) & ~15));
         const uint32_t idesc = idesc_bf16(128, n_pad);
@@ -507,7 +522,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    for (int sl = blockIdx.x; sl < units && ok; sl += gridDim.x) {
+      const int u = interleave_unit(sl, units, hot);
       const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
       const bool gather = STAGE == 0 && t.g >= 0 && t.nlen > kSmallTile;
       const uint8_t* src[kRowsPer];
@@ -551,7 +567,8 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
     const int rrow = quarter * 32 + lane;
     int it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    for (int sl = blockIdx.x; sl < units; sl += gridDim.x) {
+      const int u = interleave_unit(sl, units, hot);
       const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
       const bool sh = t.g < 0;
       const int b = it & 1;

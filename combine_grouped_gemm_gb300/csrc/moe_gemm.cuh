@@ -14,7 +14,8 @@ namespace moe {
 // ---------------------------------------------------------------------------------------
 struct GemmArgs {
   const Tile* tiles;
-  const int32_t* n_tiles;
+  const int32_t* n_tiles;  // [0]: tiles in the list; [1]: of those, the first ones, whose groups
+                           // have two or more token tiles
   const int32_t* grp_off;
   const int32_t* row_list;
   int tk;                 // compact rows (T*k)
@@ -103,6 +104,30 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u, int n_tile
     r.ti = ti;
   }
   return r;
+}
+
+// Schedule slot s -> unit. Units [0, hot) (the shared expert's and those of groups with two or
+// more token tiles: each weight tile is read once per token tile, from L2 after the first, so
+// they keep the tensor pipe busy) and units [hot, units) (one-tile groups: every weight tile is
+// read once, from HBM) are merged evenly, each in its own order, so that at any time about the
+// same share of the CTAs streams weights from HBM. Taken in list order, the two kinds ran one
+// after the other: on the skewed prefill each GEMM took about its HBM time plus its tensor time.
+__device__ __forceinline__ int interleave_unit(int s, int units, int hot) {
+  const int cold = units - hot;
+  if (hot <= 0 || cold <= 0) return s;
+  const long long c0 = static_cast<long long>(s) * cold / units;   // cold slots before s
+  const long long c1 = static_cast<long long>(s + 1) * cold / units;
+  return c1 > c0 ? hot + static_cast<int>(c0) : s - static_cast<int>(c0);
+}
+
+// Units of the tensor-bound part of a launch's list (see interleave_unit): the shared expert's
+// units, then those of the routed tiles listed first. 0 (the list order) unless the routed
+// groups are of both kinds: with one-tile routed groups only, spreading the shared expert's
+// units over the launch made the gate/up GEMM 2-3 % slower at 512 and 1024 tokens.
+__device__ __forceinline__ int hot_units(const GemmArgs& a, int n_tiles) {
+  const int hot_tiles = min(max(a.n_tiles[1], 0), n_tiles);
+  if (hot_tiles == 0 || hot_tiles == n_tiles) return 0;
+  return a.n_shared_tiles * a.mt_shared + hot_tiles * a.mt_routed;
 }
 
 // L2 policy of a unit's weight tiles. A group with one token tile reads each weight tile once:

@@ -30,7 +30,8 @@ struct WsLayout {
   size_t partials;    // router partial dot products: fp32 [16][T][E]
   size_t grp_n;       // int32 [E]: rows received by each routed expert
   size_t grp_off;     // int32 [E]: first compact row of each routed expert
-  size_t n_tiles;     // int32 [1]: routed tiles in the schedule
+  size_t n_tiles;     // int32 [2]: routed tiles in the schedule; of those, tiles of groups with
+                      // two or more (listed first)
   size_t tiles;       // Tile [max_tiles]
   size_t row_list;    // int32 [T*k]: receive row of each compact row
   size_t h;           // SwiGLU intermediate of routed rows: [T*k][d_ff] (bf16 or e4m3)
@@ -54,7 +55,7 @@ struct WsLayout {
   size_t sf_hs;       // [T]: the shared expert's down input rows (hs)
   // the same schedule in tiles of 2 * bn rows (the bf16 down GEMM when experts average a full
   // bn-row tile or more)
-  size_t n_tiles2;    // int32 [1]
+  size_t n_tiles2;    // int32 [2], as n_tiles
   size_t tiles2;      // Tile [max_tiles2]
   int max_tiles2;
   int shared_tiles;   // token tiles of the shared expert (0: none)

@@ -68,7 +68,7 @@ def ws_offsets(cfg):
     o = {}
     cur = 0
     for name, size in [("status", 16), ("partials", 4 * 16 * cfg.T * cfg.E), ("grp_n", 4 * cfg.E),
-                       ("grp_off", 4 * cfg.E), ("n_tiles", 4), ("tiles", 16 * max_tiles),
+                       ("grp_off", 4 * cfg.E), ("n_tiles", 8), ("tiles", 16 * max_tiles),
                        ("row_list", 4 * tk), ("h", ab * tk * cfg.d_ff)]:
         o[name] = cur
         cur = up(cur + size)
@@ -87,7 +87,7 @@ def ws_offsets(cfg):
                        ("fused_done", 4 * (max_tiles + shared_tiles + 2)),
                        ("sf_gu", 64 * tk if p2 else 0), ("sf_x", 64 * cfg.T if p2 else 0),
                        ("sf_h", 64 * tk if p2 else 0), ("sf_hs", 64 * cfg.T if p2 else 0),
-                       ("n_tiles2", 4), ("tiles2", 16 * (cfg.E + (tk + 2 * bn - 1) // (2 * bn)))]:
+                       ("n_tiles2", 8), ("tiles2", 16 * (cfg.E + (tk + 2 * bn - 1) // (2 * bn)))]:
         o[name] = cur
         cur = up(cur + size)
     o["total"] = cur
