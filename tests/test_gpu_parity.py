@@ -675,6 +675,41 @@ def test_gate_up_intermediate_and_schedule(cfg):
     assert n_off <= 0.01 * n_all, (n_off, n_all)
 
 
+@pytest.mark.parametrize("cfg", [SMALL, HOT, PAIRED, PAIRED_RAGGED], ids=lambda c: c.name)
+def test_schedule_lists_multi_tile_groups_first(cfg):
+    """The schedule's tile lists (bn-row tiles and, for bf16 layers with 128-row tiles, 2 bn-row
+    tiles): each group's rows in consecutive tiles of its own, the groups with two or more tiles
+    first and then the one-tile groups, each part in group order, and the word after each
+    list's tile count holding the size of its first part (which the GEMMs interleave with the
+    second)."""
+    from gpu_util import ws_offsets
+    inp, W = inputs(cfg)
+    r = _ffn(cfg, inp, W, run_stages(cfg, inp, W))
+    assert moe().read_status(r["ws"]) == 0
+    o = ws_offsets(cfg)
+    ws = r["ws"]
+    rows = r["counts"].cpu().numpy().sum(0)
+    lists = [("n_tiles", "tiles", o["bn"])]
+    if o["bn"] == 128 and cfg.act == "bf16":
+        lists.append(("n_tiles2", "tiles2", 2 * o["bn"]))
+    kinds = set()
+    for count_name, list_name, bn in lists:
+        head = ws[o[count_name]:o[count_name] + 8].view(torch.int32).cpu().numpy()
+        nt = [int((n + bn - 1) // bn) for n in rows]
+        multi = [g for g in range(cfg.E) if nt[g] >= 2]
+        single = [g for g in range(cfg.E) if nt[g] == 1]
+        expect = [(g, j * bn, min(bn, int(rows[g]) - j * bn), nt[g])
+                  for g in multi + single for j in range(nt[g])]
+        assert int(head[0]) == len(expect), (list_name, head, len(expect))
+        assert int(head[1]) == sum(nt[g] for g in multi), (list_name, head)
+        got = ws[o[list_name]:o[list_name] + 16 * len(expect)].view(torch.int32).view(-1, 4)
+        assert [tuple(int(v) for v in t) for t in got.cpu().numpy()] == expect, list_name
+        kinds.add((bool(multi), bool(single)))
+    # the configurations reach both kinds together in at least one list
+    if cfg.name in ("paired", "paired_ragged", "hot"):
+        assert (True, True) in kinds, kinds
+
+
 # ------------------------------------------------------------------------------------------
 # e4m3 path
 # ------------------------------------------------------------------------------------------
