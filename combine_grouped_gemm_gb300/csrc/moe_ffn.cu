@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     bool ok = true;
     for (int sl = blockIdx.x; sl < units && ok; sl += gridDim.x) {
       const int u = interleave_unit(sl, units, hot);
-      const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
+      const Unit t = decode_unit<BN, true>(a, u, n_tiles);
       const bool sh = t.g < 0;
       const uint64_t pol_w = weight_policy(t, pol_w1, pol_wk);
       const CUtensorMap* amap = sh ? &mapAs : &mapA;
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
       int it = 0;
       for (int sl = blockIdx.x; sl < units && ok; sl += gridDim.x) {
         const int u = interleave_unit(sl, units, hot);
-        const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
+        const Unit t = decode_unit<BN, true>(a, u, n_tiles);
         const uint32_t n_pad = static_cast<uint32_t>(max(16, (t.nlen + 15) & ~15));
         const uint32_t idesc = idesc_bf16(128, n_pad);
         const int b = it & 1;
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     bool ok = true;
     for (int sl = blockIdx.x; sl < units && ok; sl += gridDim.x) {
       const int u = interleave_unit(sl, units, hot);
-      const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
+      const Unit t = decode_unit<BN, true>(a, u, n_tiles);
       const bool gather = STAGE == 0 && t.g >= 0 && t.nlen > kSmallTile;
       const uint8_t* src[kRowsPer];
 #pragma unroll
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(GemmThreads<STAGE>::kAll, 1)
     int it = 0;
     for (int sl = blockIdx.x; sl < units; sl += gridDim.x) {
       const int u = interleave_unit(sl, units, hot);
-      const Unit t = decode_unit<BN, STAGE == 1>(a, u, n_tiles);
+      const Unit t = decode_unit<BN, true>(a, u, n_tiles);
       const bool sh = t.g < 0;
       const int b = it & 1;
       if (!mbar_wait(&tfull[b], (it >> 1) & 1, abort_flag, a.status)) break;

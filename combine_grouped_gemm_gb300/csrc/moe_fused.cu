@@ -15,7 +15,7 @@
 // start. Here a CTA that runs out of gate/up units takes down units at once; each down unit
 // waits only for the gate/up units of its own token tile.
 //
-// Unit list: the gate/up units (as in moe_ffn.cu: shared-expert tiles first, token-tile-major),
+// Unit list: the gate/up units (shared-expert tiles first, token-tile-major),
 // then the down units (weight-tile-major within a group); CTA c takes units c, c + grid, ...
 // so every CTA finishes its gate/up units before its down units. A down unit's producer waits
 // until the four epilogue warps of every gate/up unit of that token tile have published their
